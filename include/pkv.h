@@ -1,0 +1,211 @@
+/*
+ * pkv.h -- libpagedkv: attention over a paged KV cache on one GB300 (sm_103a).
+ *
+ * The problem these calls implement is stated on the pages this library
+ * follows:
+ *   [KV2] "LLM KV cache part 2: KV management in serving engines"
+ *         (ttlab.hopto.org), section 2 "PagedAttention: splitting KV into
+ *         blocks" (subsections "Blocks and block tables", "Sharing blocks"),
+ *         section 3 (continuous batching, chunked prefill).
+ *   [ENG] "How LLM inference engines work: from one token to agent caches"
+ *         (xiaohu-jiedu.pages.dev), sections "KV Cache", "PagedAttention",
+ *         "Chunked Prefill".
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Every array argument is a DEVICE pointer unless its name ends in
+ *    `_host`.  The caller owns every buffer; the library allocates no device
+ *    memory and keeps no state besides a per-device error word and cached
+ *    device properties.
+ *  - `stream` is a cudaStream_t passed as `void*` (NULL = legacy default
+ *    stream).  Every call only enqueues work: PKV_OK means the arguments
+ *    passed the host checks and the kernels were launched.  Errors found on
+ *    the device (an out-of-range block id, slot or length; a bounded wait
+ *    that expired) are recorded in the error word and read with
+ *    pkv_get_error().  No kernel traps, asserts or waits without a limit;
+ *    an invalid id is never dereferenced.
+ *  - bf16 is IEEE bfloat16; out is fp32.
+ *  - Device pointers must be 16-byte aligned.
+ *
+ * Cache layout ([KV2] section 2, "Blocks and block tables")
+ * ----------------------------------------------------------
+ * KV is cut into fixed blocks of 16 tokens that may sit anywhere in the pool;
+ * each sequence's block table maps its logical block i to a physical block.
+ * K and V are separate pools, each
+ *     bf16 [num_blocks][num_kv_heads][16][head_dim]
+ * so the 16 rows of one (block, kv head) are one contiguous run of
+ * 16*head_dim*2 bytes.  Token p of a sequence is row p % 16 of physical block
+ * block_table[p / 16].  A slot id is block * 16 + row.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pkv_status {
+    PKV_OK = 0,
+    PKV_ERR_NULL = 1,        /* a required pointer is NULL                                  */
+    PKV_ERR_SHAPE = 2,       /* a count or size is negative or inconsistent                 */
+    PKV_ERR_HEADS = 3,       /* num_q_heads / num_kv_heads is not one of 1, 2, 4, 8         */
+    PKV_ERR_HEADDIM = 4,     /* head_dim is not 64 or 128                                   */
+    PKV_ERR_BLOCKSIZE = 5,   /* block_size is not 16                                        */
+    PKV_ERR_ALIAS = 6,       /* copy_blocks: a dst repeats, or a dst is also a src          */
+    PKV_ERR_WORKSPACE = 7,   /* workspace NULL, too small or not 256-byte aligned           */
+    PKV_ERR_ALIGN = 8,       /* a device pointer is not 16-byte aligned                     */
+    PKV_ERR_RANGE = 9,       /* (device) block id, slot or context length out of range     */
+    PKV_ERR_TIMEOUT = 10,    /* (device) a bounded wait inside a kernel expired             */
+    PKV_ERR_CUDA = 11,       /* a CUDA runtime call failed (see pkv_last_cuda_error)        */
+    PKV_ERR_UNSUPPORTED = 12 /* the current device is not compute capability 10.3           */
+} pkv_status;
+
+typedef struct pkv_cache {
+    void* k_pool;         /* bf16 [num_blocks][num_kv_heads][16][head_dim], device        */
+    void* v_pool;         /* same layout                                                  */
+    int32_t num_blocks;   /* physical blocks in each pool, >= 0                           */
+    int32_t num_kv_heads; /* >= 1                                                         */
+    int32_t head_dim;     /* 64 or 128                                                    */
+    int32_t block_size;   /* tokens per block; must be 16 ([KV2] section 2 default)       */
+} pkv_cache_t;
+
+/*
+ * pkv_cache_write -- store this step's new K/V rows in their slots.
+ * [ENG] "KV Cache": each step computes only the new token's K/V column and
+ * keeps it, reading every past column from the cache; [KV2] section 2: the
+ * token lands in its sequence's current block.
+ *
+ *   k_new, v_new  bf16 [num_tokens][num_kv_heads][head_dim]
+ *   slot_mapping  int32 [num_tokens]; row t goes to slot slot_mapping[t]
+ *                 (block slot/16, row slot%16) for every kv head; a negative
+ *                 slot skips the row.  Slots within one call must be distinct.
+ *   A slot >= num_blocks*16 is not written and raises PKV_ERR_RANGE on the
+ *   device.  The copy is bit-exact.  num_tokens == 0 is a no-op.
+ */
+pkv_status pkv_cache_write(const pkv_cache_t* cache, const void* k_new, const void* v_new,
+                           const int32_t* slot_mapping, int32_t num_tokens, void* stream);
+
+/*
+ * pkv_copy_blocks -- copy-on-write of shared blocks.
+ * [KV2] section 2, "Sharing blocks": requests may point at the same physical
+ * block under a reference count; a block is copied only when someone must
+ * append to it.  For every i: K[dst[i]] <- K[src[i]] and V[dst[i]] <- V[src[i]],
+ * whole blocks (all kv heads, all 16 rows), bit-exact.
+ *
+ *   src, dst              int32 [num_pairs], device
+ *   src_host, dst_host    optional host copies of src/dst; when both are given
+ *                         the call checks that the dst ids are distinct and
+ *                         that no dst is also a src (PKV_ERR_ALIAS), and that
+ *                         ids are in range (PKV_ERR_RANGE) before launching.
+ *                         The same src may appear many times.
+ *   Ids out of range found on the device are skipped and raise PKV_ERR_RANGE.
+ */
+pkv_status pkv_copy_blocks(const pkv_cache_t* cache, const int32_t* src, const int32_t* dst, int32_t num_pairs,
+                           const int32_t* src_host, const int32_t* dst_host, void* stream);
+
+/*
+ * pkv_decode_workspace_size -- bytes of workspace pkv_decode_attention needs
+ * (a 256-byte header, one arrival counter per (sequence, kv head) and the
+ * split-KV partial results).  Depends on the current device's SM count.
+ * partition_blocks: 0 = automatic, else blocks per split-KV partition.
+ * Returns 0 for invalid arguments.
+ */
+size_t pkv_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                 int32_t max_context_len, int32_t partition_blocks);
+
+/*
+ * pkv_decode_attention -- one query token per sequence over its paged context.
+ * [KV2] section 2, "Blocks and block tables": the kernel follows the block
+ * table and reads K/V from scattered blocks; the result equals attention over
+ * one contiguous array.  [ENG] "Prefill/Decode": decode reads the whole
+ * context cache every step and is memory-bandwidth bound.
+ *
+ *   For sequence s with n = context_lens[s] (this step's token already
+ *   written, so it attends to itself) and q head h (kv head h / (Hq/Hkv)):
+ *       out[s][h] = softmax_j(scale * q[s][h] . K_j) V_j,   j = 0 .. n-1
+ *   with K_j, V_j row j % 16 of block block_tables[s][j / 16].
+ *
+ *   q              bf16 [num_seqs][num_q_heads][head_dim]
+ *   block_tables   int32 [num_seqs][max_blocks_per_seq]
+ *   context_lens   int32 [num_seqs]; 0 gives a zero output row; a value above
+ *                  max_blocks_per_seq*16 or max_context_len is clamped and
+ *                  raises PKV_ERR_RANGE
+ *   max_context_len host-side upper bound of context_lens (sizes the split)
+ *   out            fp32 [num_seqs][num_q_heads][head_dim]
+ *   workspace      device buffer of >= pkv_decode_workspace_size() bytes,
+ *                  256-byte aligned, ZERO-FILLED BEFORE ITS FIRST USE; every
+ *                  call leaves it zeroed again.  Calls that run concurrently
+ *                  need separate workspaces.
+ *   partition_blocks 0 = automatic split-KV partitioning; > 0 forces the
+ *                  blocks per partition (the workspace must be sized with the
+ *                  same value).
+ *   Long contexts are split into partitions whose partial results are merged
+ *   with the log-sum-exp rule inside the same launch.
+ */
+pkv_status pkv_decode_attention(const pkv_cache_t* cache, const void* q, int32_t num_q_heads,
+                                const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                int32_t num_seqs, int32_t max_context_len, float scale, float* out, void* workspace,
+                                size_t workspace_bytes, int32_t partition_blocks, void* stream);
+
+/*
+ * pkv_prefill_workspace_size -- bytes of workspace
+ * pkv_chunked_prefill_attention needs.  Returns 0 for invalid arguments.
+ */
+size_t pkv_prefill_workspace_size(int32_t num_seqs, int32_t num_tokens, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t max_context_len);
+
+/*
+ * pkv_chunked_prefill_attention -- attention of a mixed batch.
+ * [ENG] "Chunked Prefill": a long prompt is split into slices under a
+ * per-step token budget, and each slice shares its forward pass with the
+ * single decode tokens of the active users; [KV2] section 3 (chunks mixed
+ * with decode tokens).
+ *
+ *   Sequence s owns query rows query_start_loc[s] .. query_start_loc[s+1]-1
+ *   (query_len = their count).  Row i sits at absolute position
+ *   pos = context_lens[s] - query_len + i and attends keys 0..pos (causal),
+ *   read through the block table; the chunk's own K/V must already be in the
+ *   cache (pkv_cache_write first).  query_len == 1 rows are decode rows.
+ *
+ *   q                     bf16 [num_tokens][num_q_heads][head_dim]
+ *   query_start_loc       int32 [num_seqs+1], device
+ *   query_start_loc_host  the same values on the host (plans the launch)
+ *   context_lens          int32 [num_seqs], device, including this step's rows
+ *   out                   fp32 [num_tokens][num_q_heads][head_dim]
+ *   workspace             >= pkv_prefill_workspace_size() bytes, 256-byte
+ *                         aligned, zero-filled before first use (left zeroed)
+ *   Query rows are computed on tcgen05 tensor cores (P rounded to bf16 for
+ *   the P.V product); decode rows take the decode kernel.
+ */
+pkv_status pkv_chunked_prefill_attention(const pkv_cache_t* cache, const void* q, int32_t num_q_heads,
+                                         int32_t num_tokens, const int32_t* query_start_loc,
+                                         const int32_t* query_start_loc_host, const int32_t* context_lens,
+                                         int32_t num_seqs, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                         int32_t max_context_len, float scale, float* out, void* workspace,
+                                         size_t workspace_bytes, void* stream);
+
+/*
+ * pkv_get_error -- synchronise `stream`, then return (and clear) the first
+ * error a kernel recorded on the current device since the last call:
+ * PKV_OK, PKV_ERR_RANGE or PKV_ERR_TIMEOUT.  `detail` (optional) receives
+ * the offending index (a token, pair or sequence number) or wait site.
+ */
+pkv_status pkv_get_error(void* stream, int32_t* detail);
+
+/* Human-readable name of a status code (static storage). */
+const char* pkv_status_string(pkv_status status);
+
+/* Text of the last CUDA runtime error seen by this thread (static storage). */
+const char* pkv_last_cuda_error(void);
+
+/* Library version, "major.minor.patch". */
+const char* pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

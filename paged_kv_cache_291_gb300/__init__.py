@@ -1,0 +1,267 @@
+"""paged_kv_cache_291_gb300 -- Python binding of libpagedkv (GB300, sm_103a).
+
+A thin ctypes layer over the C-ABI declared in ``include/pkv.h``: it checks
+tensor dtypes, shapes and devices, passes ``data_ptr()`` values and the
+current CUDA stream, and raises :class:`PKVError` on a non-OK status.  Every
+step of the computation runs in the library's CUDA kernels; there is no
+fallback of any kind, and the binding refuses to work when ``libpagedkv.so``
+has not been built (build it with ``python -m paged_kv_cache_291_gb300.build``
+or ``__graft_entry__.build()``).
+
+Tensors: K/V pools are 2-byte (bf16) CUDA tensors
+``[num_blocks][num_kv_heads][16][head_dim]``; q/k_new/v_new bf16; index
+arrays int32; outputs float32.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+__all__ = [
+    "PKVError", "lib_path", "load", "version", "status_string", "cache_write", "copy_blocks",
+    "decode_workspace_size", "decode_attention", "prefill_workspace_size", "chunked_prefill_attention",
+    "get_error", "Cache",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libpagedkv.so")
+_lib = None
+
+PKV_OK = 0
+STATUS_NAMES = {
+    0: "PKV_OK", 1: "PKV_ERR_NULL", 2: "PKV_ERR_SHAPE", 3: "PKV_ERR_HEADS", 4: "PKV_ERR_HEADDIM",
+    5: "PKV_ERR_BLOCKSIZE", 6: "PKV_ERR_ALIAS", 7: "PKV_ERR_WORKSPACE", 8: "PKV_ERR_ALIGN", 9: "PKV_ERR_RANGE",
+    10: "PKV_ERR_TIMEOUT", 11: "PKV_ERR_CUDA", 12: "PKV_ERR_UNSUPPORTED",
+}
+
+
+class PKVError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = int(status)
+        msg = status_string(status) if _lib is not None else STATUS_NAMES.get(status, str(status))
+        if self.status == 11 and _lib is not None:
+            msg += f" ({_lib.pkv_last_cuda_error().decode()})"
+        super().__init__(f"{what}: {msg}" if what else msg)
+
+
+class Cache(ctypes.Structure):
+    """Mirror of ``pkv_cache_t``."""
+    _fields_ = [("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p), ("num_blocks", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32)]
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Load libpagedkv.so (raises if it is missing: there is no fallback)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(f"libpagedkv.so is not built ({_LIB_PATH}); run `python -m "
+                           "paged_kv_cache_291_gb300.build` or __graft_entry__.build() first")
+    lib = ctypes.CDLL(_LIB_PATH)
+    P, i32, sz, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.c_float
+    CP = ctypes.POINTER(Cache)
+    sigs = {
+        "pkv_cache_write": ([CP, P, P, P, i32, P], ctypes.c_int),
+        "pkv_copy_blocks": ([CP, P, P, i32, P, P, P], ctypes.c_int),
+        "pkv_decode_workspace_size": ([i32, i32, i32, i32, i32, i32], sz),
+        "pkv_decode_attention": ([CP, P, i32, P, i32, P, i32, i32, f32, P, P, sz, i32, P], ctypes.c_int),
+        "pkv_prefill_workspace_size": ([i32, i32, i32, i32, i32, i32], sz),
+        "pkv_chunked_prefill_attention": ([CP, P, i32, i32, P, P, P, i32, P, i32, i32, f32, P, P, sz, P],
+                                          ctypes.c_int),
+        "pkv_get_error": ([P, ctypes.POINTER(i32)], ctypes.c_int),
+        "pkv_status_string": ([ctypes.c_int], ctypes.c_char_p),
+        "pkv_last_cuda_error": ([], ctypes.c_char_p),
+        "pkv_version": ([], ctypes.c_char_p),
+    }
+    for name, (argt, rest) in sigs.items():
+        fn = getattr(lib, name)
+        fn.argtypes = argt
+        fn.restype = rest
+    _lib = lib
+    return lib
+
+
+def version() -> str:
+    return load().pkv_version().decode()
+
+
+def status_string(status: int) -> str:
+    return load().pkv_status_string(int(status)).decode()
+
+
+# ---------------------------------------------------------------- helpers
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dev(t, name, elem_size=None, dtype=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if elem_size is not None and t.element_size() != elem_size:
+        raise TypeError(f"{name} must have {elem_size}-byte elements")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _cache(k_pool, v_pool) -> Cache:
+    if k_pool.shape != v_pool.shape or k_pool.dim() != 4:
+        raise ValueError("k_pool and v_pool must both be [num_blocks][num_kv_heads][16][head_dim]")
+    nb, hkv, bs, d = k_pool.shape
+    return Cache(_dev(k_pool, "k_pool", 2).value, _dev(v_pool, "v_pool", 2).value, nb, hkv, d, bs)
+
+
+def _check(status, what):
+    if status != PKV_OK:
+        raise PKVError(status, what)
+
+
+def _host_i32(x):
+    import numpy as np
+    a = np.ascontiguousarray(x.cpu().numpy() if hasattr(x, "cpu") else x, dtype=np.int32)
+    return a, a.ctypes.data_as(ctypes.c_void_p)
+
+
+# ---------------------------------------------------------------- calls
+
+def cache_write(k_pool, v_pool, k_new, v_new, slot_mapping, stream=None) -> None:
+    """Store rows k_new/v_new [T][Hkv][d] at ``slot_mapping`` [T] (negative = skip)."""
+    torch = _torch()
+    lib = load()
+    c = _cache(k_pool, v_pool)
+    T = int(slot_mapping.shape[0])
+    if k_new.shape != (T, c.num_kv_heads, c.head_dim) or v_new.shape != k_new.shape:
+        raise ValueError("k_new/v_new must be [num_tokens][num_kv_heads][head_dim]")
+    st = lib.pkv_cache_write(ctypes.byref(c), _dev(k_new, "k_new", 2), _dev(v_new, "v_new", 2),
+                             _dev(slot_mapping, "slot_mapping", dtype=torch.int32), T, _stream_handle(stream))
+    _check(st, "pkv_cache_write")
+
+
+def copy_blocks(k_pool, v_pool, src, dst, check_host: bool = True, stream=None) -> None:
+    """Copy-on-write: pool[dst[i]] <- pool[src[i]] (K and V, whole blocks).
+
+    With ``check_host`` the int32 id lists are also copied to the host so the
+    library can reject aliasing destinations before launching.
+    """
+    torch = _torch()
+    lib = load()
+    c = _cache(k_pool, v_pool)
+    n = int(src.shape[0])
+    if dst.shape[0] != n:
+        raise ValueError("src and dst must have the same length")
+    sh = dh = None
+    sp = dp = None
+    if check_host:
+        sh, sp = _host_i32(src)
+        dh, dp = _host_i32(dst)
+    st = lib.pkv_copy_blocks(ctypes.byref(c), _dev(src, "src", dtype=torch.int32),
+                             _dev(dst, "dst", dtype=torch.int32), n, sp, dp, _stream_handle(stream))
+    _check(st, "pkv_copy_blocks")
+
+
+def decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len,
+                          partition_blocks=0) -> int:
+    n = load().pkv_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len,
+                                         partition_blocks)
+    if n == 0:
+        raise PKVError(2, "pkv_decode_workspace_size")
+    return int(n)
+
+
+def new_workspace(nbytes: int, device=None):
+    """A zero-filled, 256-byte aligned workspace (torch allocations are)."""
+    torch = _torch()
+    return torch.zeros(max(256, (nbytes + 255) // 256 * 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def decode_attention(k_pool, v_pool, q, block_tables, context_lens, max_context_len: int, scale: float,
+                     out=None, workspace=None, partition_blocks: int = 0, stream=None):
+    """Paged decode attention; returns ``out`` float32 [B][Hq][d]."""
+    torch = _torch()
+    lib = load()
+    c = _cache(k_pool, v_pool)
+    B, hq, d = q.shape
+    if d != c.head_dim:
+        raise ValueError("q head_dim does not match the pools")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.shape[0] != B:
+        raise ValueError("block_tables must be [B][max_blocks] and context_lens [B]")
+    if out is None:
+        out = torch.empty((B, hq, d), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        need = load().pkv_decode_workspace_size(B, hq, c.num_kv_heads, d, int(max_context_len),
+                                                int(partition_blocks))
+        workspace = new_workspace(need, q.device)  # a size of 0 means bad arguments: the call reports them
+    st = lib.pkv_decode_attention(ctypes.byref(c), _dev(q, "q", 2), hq,
+                                  _dev(block_tables, "block_tables", dtype=torch.int32), int(block_tables.shape[1]),
+                                  _dev(context_lens, "context_lens", dtype=torch.int32), B, int(max_context_len),
+                                  float(scale), _dev(out, "out", dtype=torch.float32),
+                                  _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+                                  int(partition_blocks), _stream_handle(stream))
+    _check(st, "pkv_decode_attention")
+    return out
+
+
+def prefill_workspace_size(num_seqs, num_tokens, num_q_heads, num_kv_heads, head_dim, max_context_len) -> int:
+    n = load().pkv_prefill_workspace_size(num_seqs, num_tokens, num_q_heads, num_kv_heads, head_dim,
+                                          max_context_len)
+    if n == 0:
+        raise PKVError(2, "pkv_prefill_workspace_size")
+    return int(n)
+
+
+def chunked_prefill_attention(k_pool, v_pool, q, query_start_loc, context_lens, block_tables,
+                              max_context_len: int, scale: float, out=None, workspace=None,
+                              query_start_loc_host=None, stream=None):
+    """Mixed batch of causal prefill chunks and decode rows; returns ``out``
+    float32 [Tq][Hq][d]."""
+    torch = _torch()
+    lib = load()
+    c = _cache(k_pool, v_pool)
+    T, hq, d = q.shape
+    S = int(context_lens.shape[0])
+    if query_start_loc.shape[0] != S + 1:
+        raise ValueError("query_start_loc must have num_seqs + 1 entries")
+    if query_start_loc_host is None:
+        query_start_loc_host = query_start_loc
+    qh, qhp = _host_i32(query_start_loc_host)
+    if out is None:
+        out = torch.empty((T, hq, d), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        need = load().pkv_prefill_workspace_size(S, T, hq, c.num_kv_heads, d, int(max_context_len))
+        workspace = new_workspace(need, q.device)
+    st = lib.pkv_chunked_prefill_attention(
+        ctypes.byref(c), _dev(q, "q", 2), hq, T, _dev(query_start_loc, "query_start_loc", dtype=torch.int32), qhp,
+        _dev(context_lens, "context_lens", dtype=torch.int32), S,
+        _dev(block_tables, "block_tables", dtype=torch.int32), int(block_tables.shape[1]), int(max_context_len),
+        float(scale), _dev(out, "out", dtype=torch.float32), _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _check(st, "pkv_chunked_prefill_attention")
+    return out
+
+
+def get_error(stream=None) -> Tuple[int, int]:
+    """Synchronise the stream and return (status, detail) of the first
+    device-side error since the last call, clearing it."""
+    detail = ctypes.c_int32(0)
+    st = load().pkv_get_error(_stream_handle(stream), ctypes.byref(detail))
+    return int(st), int(detail.value)

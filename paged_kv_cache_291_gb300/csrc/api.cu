@@ -1,0 +1,336 @@
+// api.cu -- the C-ABI of libpagedkv: argument checks, per-device state, the
+// device error word, workspace sizing and dispatch to the kernels.
+//
+// The calls and their contracts are declared (with the passages of the
+// pages that define each operation) in include/pkv.h.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <unordered_set>
+
+#include "pkv.h"
+#include "pkv_internal.h"
+
+#define PKV_API extern "C" __attribute__((visibility("default")))
+
+// First device-side error since the last pkv_get_error: (code << 32) | detail.
+__device__ unsigned long long g_pkv_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool ready = false;
+    int num_sms = 0;
+    int cc_major = 0, cc_minor = 0;
+    unsigned long long* err = nullptr;
+};
+
+DeviceState g_devices[kMaxDevices];
+std::mutex g_mutex;
+thread_local char g_cuda_error[256] = "no error";
+
+pkv_status cuda_fail(cudaError_t e) {
+    std::snprintf(g_cuda_error, sizeof g_cuda_error, "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+    return PKV_ERR_CUDA;
+}
+
+// Properties and the error-word address of the current device, looked up
+// once per device with that device current.
+pkv_status current_device(DeviceState** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return PKV_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState& d = g_devices[dev];
+    if (!d.ready) {
+        if ((e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return cuda_fail(e);
+        if ((e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
+            return cuda_fail(e);
+        if ((e = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+            return cuda_fail(e);
+        void* p = nullptr;
+        if ((e = cudaGetSymbolAddress(&p, g_pkv_error_word)) != cudaSuccess) return cuda_fail(e);
+        d.err = static_cast<unsigned long long*>(p);
+        d.ready = true;
+    }
+    if (d.cc_major != 10 || d.cc_minor != 3) return PKV_ERR_UNSUPPORTED;
+    *out = &d;
+    return PKV_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+pkv_status check_cache(const pkv_cache_t* c) {
+    if (c == nullptr || c->k_pool == nullptr || c->v_pool == nullptr) return PKV_ERR_NULL;
+    if (c->block_size != 16) return PKV_ERR_BLOCKSIZE;
+    if (c->num_blocks < 0 || c->num_kv_heads < 1) return PKV_ERR_SHAPE;
+    if (c->head_dim != 64 && c->head_dim != 128) return PKV_ERR_HEADDIM;
+    if (!aligned16(c->k_pool) || !aligned16(c->v_pool)) return PKV_ERR_ALIGN;
+    return PKV_OK;
+}
+
+pkv_status check_heads(int32_t hq, int32_t hkv) {
+    if (hq < 1 || hkv < 1 || hq % hkv != 0) return PKV_ERR_HEADS;
+    const int32_t g = hq / hkv;
+    if (g != 1 && g != 2 && g != 4 && g != 8) return PKV_ERR_HEADS;
+    return PKV_OK;
+}
+
+int32_t max_parts_for(int32_t max_context_len, int32_t part_blocks) {
+    const int64_t nblk = std::max<int64_t>(1, (static_cast<int64_t>(max_context_len) + 15) / 16);
+    return static_cast<int32_t>((nblk + part_blocks - 1) / part_blocks);
+}
+
+// Shared by the decode call and the decode rows of the mixed batch.
+pkv_status plan_decode(int32_t num_seqs, int32_t hq, int32_t hkv, int32_t head_dim, int32_t max_context_len,
+                       int32_t req_part_blocks, int num_sms, int32_t* part_blocks, int32_t* max_parts,
+                       size_t* ws_bytes) {
+    if (num_seqs < 0 || max_context_len < 0 || req_part_blocks < 0) return PKV_ERR_SHAPE;
+    *part_blocks = pkv::plan_part_blocks(num_seqs, hkv, max_context_len, num_sms, req_part_blocks);
+    *max_parts = max_parts_for(max_context_len, *part_blocks);
+    *ws_bytes = pkv::decode_ws_layout(num_seqs, hq, hkv, head_dim, *max_parts).total;
+    return PKV_OK;
+}
+
+}  // namespace
+
+PKV_API const char* pkv_version(void) { return "0.1.0"; }
+
+PKV_API const char* pkv_last_cuda_error(void) { return g_cuda_error; }
+
+PKV_API const char* pkv_status_string(pkv_status s) {
+    switch (s) {
+        case PKV_OK: return "PKV_OK";
+        case PKV_ERR_NULL: return "PKV_ERR_NULL: a required pointer is NULL";
+        case PKV_ERR_SHAPE: return "PKV_ERR_SHAPE: a count or size is negative or inconsistent";
+        case PKV_ERR_HEADS: return "PKV_ERR_HEADS: num_q_heads / num_kv_heads must be 1, 2, 4 or 8";
+        case PKV_ERR_HEADDIM: return "PKV_ERR_HEADDIM: head_dim must be 64 or 128";
+        case PKV_ERR_BLOCKSIZE: return "PKV_ERR_BLOCKSIZE: block_size must be 16";
+        case PKV_ERR_ALIAS: return "PKV_ERR_ALIAS: copy_blocks destinations repeat or overlap sources";
+        case PKV_ERR_WORKSPACE: return "PKV_ERR_WORKSPACE: workspace missing, too small or misaligned";
+        case PKV_ERR_ALIGN: return "PKV_ERR_ALIGN: a device pointer is not 16-byte aligned";
+        case PKV_ERR_RANGE: return "PKV_ERR_RANGE: a block id, slot or context length was out of range";
+        case PKV_ERR_TIMEOUT: return "PKV_ERR_TIMEOUT: a bounded wait inside a kernel expired";
+        case PKV_ERR_CUDA: return "PKV_ERR_CUDA: a CUDA runtime call failed";
+        case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED: the current device is not compute capability 10.3";
+    }
+    return "unknown pkv_status";
+}
+
+PKV_API pkv_status pkv_cache_write(const pkv_cache_t* cache, const void* k_new, const void* v_new,
+                                   const int32_t* slot_mapping, int32_t num_tokens, void* stream) {
+    pkv_status st = check_cache(cache);
+    if (st != PKV_OK) return st;
+    if (num_tokens < 0) return PKV_ERR_SHAPE;
+    if (num_tokens == 0) return PKV_OK;
+    if (k_new == nullptr || v_new == nullptr || slot_mapping == nullptr) return PKV_ERR_NULL;
+    if (!aligned16(k_new) || !aligned16(v_new)) return PKV_ERR_ALIGN;
+    DeviceState* dev = nullptr;
+    if ((st = current_device(&dev)) != PKV_OK) return st;
+    cudaError_t e = pkv::launch_cache_write(k_new, v_new, slot_mapping, num_tokens, cache->k_pool, cache->v_pool,
+                                            cache->num_blocks, cache->num_kv_heads, cache->head_dim, dev->err,
+                                            static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e);
+}
+
+PKV_API pkv_status pkv_copy_blocks(const pkv_cache_t* cache, const int32_t* src, const int32_t* dst,
+                                   int32_t num_pairs, const int32_t* src_host, const int32_t* dst_host,
+                                   void* stream) {
+    pkv_status st = check_cache(cache);
+    if (st != PKV_OK) return st;
+    if (num_pairs < 0) return PKV_ERR_SHAPE;
+    if (num_pairs == 0) return PKV_OK;
+    if (src == nullptr || dst == nullptr) return PKV_ERR_NULL;
+    if ((src_host == nullptr) != (dst_host == nullptr)) return PKV_ERR_NULL;
+    if (src_host != nullptr) {
+        std::unordered_set<int32_t> dsts, srcs;
+        for (int32_t i = 0; i < num_pairs; ++i) {
+            if (src_host[i] < 0 || src_host[i] >= cache->num_blocks || dst_host[i] < 0 ||
+                dst_host[i] >= cache->num_blocks)
+                return PKV_ERR_RANGE;
+            if (!dsts.insert(dst_host[i]).second) return PKV_ERR_ALIAS;
+            srcs.insert(src_host[i]);
+        }
+        for (int32_t d : dsts)
+            if (srcs.count(d)) return PKV_ERR_ALIAS;
+    }
+    DeviceState* dev = nullptr;
+    if ((st = current_device(&dev)) != PKV_OK) return st;
+    // grid.y is limited to 65,535 pairs per launch.
+    for (int32_t base = 0; base < num_pairs; base += 65535) {
+        const int32_t n = std::min<int32_t>(65535, num_pairs - base);
+        cudaError_t e = pkv::launch_copy_blocks(src + base, dst + base, n, cache->k_pool, cache->v_pool,
+                                                cache->num_blocks, cache->num_kv_heads, cache->head_dim, dev->err,
+                                                static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return PKV_OK;
+}
+
+PKV_API size_t pkv_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                         int32_t head_dim, int32_t max_context_len, int32_t partition_blocks) {
+    if (check_heads(num_q_heads, num_kv_heads) != PKV_OK) return 0;
+    if (head_dim != 64 && head_dim != 128) return 0;
+    DeviceState* dev = nullptr;
+    if (current_device(&dev) != PKV_OK) return 0;
+    int32_t pb = 0, mp = 0;
+    size_t bytes = 0;
+    if (plan_decode(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len, partition_blocks,
+                    dev->num_sms, &pb, &mp, &bytes) != PKV_OK)
+        return 0;
+    return bytes;
+}
+
+namespace {
+
+pkv_status decode_common(const pkv_cache_t* cache, const void* q, int32_t num_q_heads,
+                         const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* context_lens,
+                         const int32_t* query_start_loc, int32_t num_seqs, int32_t max_context_len, float scale,
+                         float* out, void* workspace, size_t workspace_bytes, int32_t partition_blocks,
+                         void* stream) {
+    pkv_status st = check_cache(cache);
+    if (st != PKV_OK) return st;
+    if ((st = check_heads(num_q_heads, cache->num_kv_heads)) != PKV_OK) return st;
+    if (num_seqs < 0 || max_blocks_per_seq < 0 || max_context_len < 0 || partition_blocks < 0)
+        return PKV_ERR_SHAPE;
+    if (num_seqs == 0) return PKV_OK;
+    if (q == nullptr || block_tables == nullptr || context_lens == nullptr || out == nullptr) return PKV_ERR_NULL;
+    if (!aligned16(q) || !aligned16(out)) return PKV_ERR_ALIGN;
+    DeviceState* dev = nullptr;
+    if ((st = current_device(&dev)) != PKV_OK) return st;
+    int32_t pb = 0, mp = 0;
+    size_t need = 0;
+    if ((st = plan_decode(num_seqs, num_q_heads, cache->num_kv_heads, cache->head_dim, max_context_len,
+                          partition_blocks, dev->num_sms, &pb, &mp, &need)) != PKV_OK)
+        return st;
+    if (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return PKV_ERR_WORKSPACE;
+    pkv::DecodeArgs a;
+    a.k_pool = cache->k_pool;
+    a.v_pool = cache->v_pool;
+    a.q = q;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.query_start_loc = query_start_loc;
+    a.out = out;
+    a.workspace = workspace;
+    a.err = dev->err;
+    a.num_blocks = cache->num_blocks;
+    a.num_kv_heads = cache->num_kv_heads;
+    a.num_q_heads = num_q_heads;
+    a.head_dim = cache->head_dim;
+    a.num_seqs = num_seqs;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.max_context_len = max_context_len;
+    a.part_blocks = pb;
+    a.max_parts = mp;
+    a.scale = scale;
+    const int64_t items_max = static_cast<int64_t>(num_seqs) * cache->num_kv_heads * mp;
+    a.grid = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(dev->num_sms, items_max)));
+    cudaError_t e = pkv::launch_decode(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+PKV_API pkv_status pkv_decode_attention(const pkv_cache_t* cache, const void* q, int32_t num_q_heads,
+                                        const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                        const int32_t* context_lens, int32_t num_seqs, int32_t max_context_len,
+                                        float scale, float* out, void* workspace, size_t workspace_bytes,
+                                        int32_t partition_blocks, void* stream) {
+    return decode_common(cache, q, num_q_heads, block_tables, max_blocks_per_seq, context_lens, nullptr, num_seqs,
+                         max_context_len, scale, out, workspace, workspace_bytes, partition_blocks, stream);
+}
+
+PKV_API size_t pkv_prefill_workspace_size(int32_t num_seqs, int32_t num_tokens, int32_t num_q_heads,
+                                          int32_t num_kv_heads, int32_t head_dim, int32_t max_context_len) {
+    if (num_tokens < 0) return 0;
+    return pkv_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len, 0);
+}
+
+PKV_API pkv_status pkv_chunked_prefill_attention(const pkv_cache_t* cache, const void* q, int32_t num_q_heads,
+                                                 int32_t num_tokens, const int32_t* query_start_loc,
+                                                 const int32_t* query_start_loc_host, const int32_t* context_lens,
+                                                 int32_t num_seqs, const int32_t* block_tables,
+                                                 int32_t max_blocks_per_seq, int32_t max_context_len, float scale,
+                                                 float* out, void* workspace, size_t workspace_bytes,
+                                                 void* stream) {
+    pkv_status st = check_cache(cache);
+    if (st != PKV_OK) return st;
+    if ((st = check_heads(num_q_heads, cache->num_kv_heads)) != PKV_OK) return st;
+    if (num_seqs < 0 || num_tokens < 0 || max_blocks_per_seq < 0 || max_context_len < 0) return PKV_ERR_SHAPE;
+    if (num_seqs == 0 || num_tokens == 0) return PKV_OK;
+    if (q == nullptr || query_start_loc == nullptr || query_start_loc_host == nullptr || context_lens == nullptr ||
+        block_tables == nullptr || out == nullptr)
+        return PKV_ERR_NULL;
+    if (!aligned16(q) || !aligned16(out)) return PKV_ERR_ALIGN;
+    if (query_start_loc_host[0] != 0 || query_start_loc_host[num_seqs] != num_tokens) return PKV_ERR_SHAPE;
+    int32_t tiles = 0, decode_rows = 0;
+    for (int32_t s = 0; s < num_seqs; ++s) {
+        const int32_t ql = query_start_loc_host[s + 1] - query_start_loc_host[s];
+        if (ql < 0) return PKV_ERR_SHAPE;
+        if (ql == 1) ++decode_rows;
+        if (ql > 1) tiles += (ql + 127) / 128;
+    }
+    DeviceState* dev = nullptr;
+    if ((st = current_device(&dev)) != PKV_OK) return st;
+    if (decode_rows > 0) {
+        st = decode_common(cache, q, num_q_heads, block_tables, max_blocks_per_seq, context_lens, query_start_loc,
+                           num_seqs, max_context_len, scale, out, workspace, workspace_bytes, 0, stream);
+        if (st != PKV_OK) return st;
+    }
+    if (tiles > 0) {
+        pkv::PrefillArgs a;
+        a.k_pool = cache->k_pool;
+        a.v_pool = cache->v_pool;
+        a.q = q;
+        a.block_tables = block_tables;
+        a.context_lens = context_lens;
+        a.query_start_loc = query_start_loc;
+        a.out = out;
+        a.err = dev->err;
+        a.num_blocks = cache->num_blocks;
+        a.num_kv_heads = cache->num_kv_heads;
+        a.num_q_heads = num_q_heads;
+        a.head_dim = cache->head_dim;
+        a.num_seqs = num_seqs;
+        a.num_tokens = num_tokens;
+        a.max_blocks_per_seq = max_blocks_per_seq;
+        a.max_context_len = max_context_len;
+        a.num_tiles = tiles;
+        a.scale = scale;
+        cudaError_t e = pkv::launch_prefill(a, static_cast<cudaStream_t>(stream));
+        if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return PKV_OK;
+}
+
+PKV_API pkv_status pkv_get_error(void* stream, int32_t* detail) {
+    DeviceState* dev = nullptr;
+    pkv_status st = current_device(&dev);
+    if (st != PKV_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned long long word = 0;
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaMemcpyAsync(&word, dev->err, sizeof word, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+        return cuda_fail(e);
+    if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e);
+    if (word == 0) {
+        if (detail) *detail = 0;
+        return PKV_OK;
+    }
+    if ((e = cudaMemsetAsync(dev->err, 0, sizeof word, s)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e);
+    if (detail) *detail = static_cast<int32_t>(word & 0xffffffffu);
+    return static_cast<pkv_status>(word >> 32);
+}

@@ -1,0 +1,113 @@
+// cache_ops.cu -- the two cache-maintenance kernels of libpagedkv.
+//
+//  cache_write: each step computes only the new token's K/V column and keeps
+//  it ("KV Cache" section of the inference-engine talk write-up); the row
+//  lands in slot (block = slot / 16, row = slot % 16) of the paged pool
+//  ("Blocks and block tables", section 2 of the serving-engine KV blog).
+//
+//  copy_blocks: copy-on-write of a shared, reference-counted block, done
+//  only when someone must append to it ("Sharing blocks", same section).
+//
+// Both are pure byte movement: 16-byte vector loads and stores, coalesced
+// along head_dim, bit-exact.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace {
+
+// One thread per 16-byte chunk of one (token, kv head) row; the same chunk
+// of K and of V.  Rows of k_new/v_new are [T][Hkv][d].
+__global__ void __launch_bounds__(256) cache_write_kernel(const uint4* __restrict__ k_new,
+                                                          const uint4* __restrict__ v_new,
+                                                          const int32_t* __restrict__ slot_mapping, int64_t total,
+                                                          int32_t chunks_per_row, int32_t num_kv_heads,
+                                                          int64_t num_slots, uint4* __restrict__ k_pool,
+                                                          uint4* __restrict__ v_pool, unsigned long long* err) {
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= total) return;
+    const int64_t row = i / chunks_per_row;          // (token, head)
+    const int32_t c = static_cast<int32_t>(i - row * chunks_per_row);
+    const int64_t t = row / num_kv_heads;
+    const int32_t h = static_cast<int32_t>(row - t * num_kv_heads);
+    const int64_t slot = __ldg(slot_mapping + t);
+    if (slot < 0) return;
+    if (slot >= num_slots) {
+        if (h == 0 && c == 0) record_error(err, kErrRange, static_cast<uint32_t>(t));
+        return;
+    }
+    const int64_t block = slot / kBlockSize;
+    const int64_t off = slot - block * kBlockSize;
+    // pool row index: ((block * Hkv + h) * 16 + off), each row chunks_per_row chunks
+    const int64_t dst = ((block * num_kv_heads + h) * kBlockSize + off) * chunks_per_row + c;
+    const uint4 kv = __ldg(k_new + i);
+    const uint4 vv = __ldg(v_new + i);
+    k_pool[dst] = kv;
+    v_pool[dst] = vv;
+}
+
+// Grid: x = chunk groups, y = pair.  Each pair copies the K slab then the V
+// slab of one block ([Hkv][16][d] bf16 each).
+__global__ void __launch_bounds__(256) copy_blocks_kernel(const int32_t* __restrict__ src,
+                                                          const int32_t* __restrict__ dst, int64_t block_chunks,
+                                                          int32_t num_blocks, uint4* __restrict__ k_pool,
+                                                          uint4* __restrict__ v_pool, unsigned long long* err) {
+    const int32_t pair = blockIdx.y;
+    const int32_t s = __ldg(src + pair);
+    const int32_t d = __ldg(dst + pair);
+    if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) record_error(err, kErrRange, static_cast<uint32_t>(pair));
+        return;
+    }
+    const uint4* ks = k_pool + static_cast<int64_t>(s) * block_chunks;
+    const uint4* vs = v_pool + static_cast<int64_t>(s) * block_chunks;
+    uint4* kd = k_pool + static_cast<int64_t>(d) * block_chunks;
+    uint4* vd = v_pool + static_cast<int64_t>(d) * block_chunks;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < 2 * block_chunks;
+         i += stride) {
+        if (i < block_chunks) {
+            kd[i] = ks[i];
+        } else {
+            vd[i - block_chunks] = vs[i - block_chunks];
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_cache_write(const void* k_new, const void* v_new, const int32_t* slot_mapping,
+                               int32_t num_tokens, void* k_pool, void* v_pool, int32_t num_blocks,
+                               int32_t num_kv_heads, int32_t head_dim, unsigned long long* err,
+                               cudaStream_t stream) {
+    if (num_tokens == 0) return cudaSuccess;
+    const int32_t chunks = head_dim * 2 / 16;
+    const int64_t total = static_cast<int64_t>(num_tokens) * num_kv_heads * chunks;
+    const int threads = 256;
+    const int64_t blocks = (total + threads - 1) / threads;
+    cache_write_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+        static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slot_mapping, total, chunks,
+        num_kv_heads, static_cast<int64_t>(num_blocks) * kBlockSize, static_cast<uint4*>(k_pool),
+        static_cast<uint4*>(v_pool), err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_copy_blocks(const int32_t* src, const int32_t* dst, int32_t num_pairs, void* k_pool,
+                               void* v_pool, int32_t num_blocks, int32_t num_kv_heads, int32_t head_dim,
+                               unsigned long long* err, cudaStream_t stream) {
+    if (num_pairs == 0) return cudaSuccess;
+    const int64_t block_chunks = static_cast<int64_t>(num_kv_heads) * kBlockSize * head_dim * 2 / 16;
+    const int threads = 256;
+    int64_t gx = (2 * block_chunks + threads - 1) / threads;
+    if (gx > 64) gx = 64;
+    dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(num_pairs));
+    copy_blocks_kernel<<<grid, threads, 0, stream>>>(src, dst, block_chunks, num_blocks,
+                                                     static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), err);
+    return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -1,0 +1,704 @@
+// decode.cu -- paged decode attention with split-KV and log-sum-exp merge.
+//
+// What it computes ("Blocks and block tables", section 2 of the
+// serving-engine KV blog): for each sequence s and q head h, attention of
+// one query over context_lens[s] keys that live in 16-token blocks scattered
+// through the pool; the kernel follows the block table and the result equals
+// attention over one contiguous array.  Decode reads the whole context every
+// step and is memory-bandwidth bound ("Prefill/Decode" section of the
+// inference-engine talk write-up), so the design is about keeping HBM busy:
+//
+//  * Work item = (sequence, kv head, partition of the context).  All G = Hq/Hkv
+//    query heads of a kv head are served by one item, so every K/V byte is
+//    read from HBM once.  Long contexts are cut into partitions (split-KV).
+//  * Persistent grid, one CTA per SM, items handed out by an atomic counter
+//    (the next index is fetched while the current item streams).
+//  * Warp 8 (producer) walks the block table and streams each (block, kv
+//    head) K slab and V slab -- 16 rows x d bf16, one contiguous 2-4 KB run
+//    each -- into a deep shared-memory ring with 1-D bulk (TMA) copies that
+//    complete on mbarriers, evict-first in L2.
+//  * Warps 0..7 (consumers) take an item's blocks round-robin, starting at
+//    a warp given by the item's global index.  A lane owns 4 dims of a row;
+//    q.K partial dots are summed across the lanes of a row by a
+//    transpose-reduce (16 values over 32 lanes in 16 shuffles), leaving one
+//    token score per lane pair.  Online
+//    softmax in the log2 domain, P.V on CUDA cores in fp32.  Rows past the
+//    context are never loaded, so whatever the unused tail of a block holds
+//    (NaN included) cannot reach the result.
+//  * Warp 9 (merger) combines the 8 warps' (m, l, o) states of an item with
+//    the log-sum-exp rule, off the consumers' critical path.  For a split
+//    context it stores the partition's (m, l, o) in the workspace; the last
+//    partition to arrive (atomic ticket) merges all of them and writes the
+//    output: one launch, no inter-CTA waiting.
+//  * Every wait is an mbarrier wait bounded by %globaltimer; on expiry the
+//    CTA records PKV_ERR_TIMEOUT and unwinds.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+
+namespace {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kProducerWarp = kConsumerWarps;
+constexpr int kMergerWarp = kConsumerWarps + 1;
+constexpr int kThreads = 32 * (kConsumerWarps + 2);
+constexpr int kItemRing = 8;
+constexpr int kMergeBufs = 2;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct __align__(16) ItemDesc {
+    int32_t s, g, p, nparts;
+    int32_t n, b0, b1, row;
+    int32_t rot, pad0, pad1, pad2;  // rot: warp that takes the item's first block
+};
+
+struct DecodeParams {
+    const uint8_t* k_pool;
+    const uint8_t* v_pool;
+    const uint8_t* q;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    const int32_t* qsl;
+    float* out;
+    float2* part_ml;
+    float* part_o;
+    uint32_t* counters;
+    uint32_t* work;  // work[0]: next item, work[1]: CTAs done
+    unsigned long long* err;
+    int32_t num_blocks, hkv, hq, num_seqs, max_blocks, ctx_cap, part_blocks, max_parts;
+    float scale_log2;
+};
+
+constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
+
+template <int D, int G>
+struct Cfg {
+    static constexpr int LPR = D / 4;                  // lanes per K/V row, 4 dims each
+    static constexpr int RPP = 32 / LPR;               // rows per warp pass
+    static constexpr int NV = kBlockSize / RPP;        // rows per lane per block
+    static constexpr int SLAB = kBlockSize * D * 2;    // bytes of one (block, kv head)
+    static constexpr int STAGE_BYTES = 2 * SLAB;       // K slab then V slab
+    static constexpr int QBYTES = G * D * 2;
+    static constexpr int HG = G < 4 ? G : 4;           // heads per pass over K
+    // Everything but the ring (offsets relative to the end of the ring).
+    static constexpr int R_ITEMQ = 0;
+    static constexpr int R_DESC = R_ITEMQ + kItemRing * QBYTES;
+    static constexpr int R_P = R_DESC + kItemRing * (int)sizeof(ItemDesc);
+    static constexpr int R_MO = R_P + kConsumerWarps * G * kBlockSize * 4;
+    static constexpr int R_ML = R_MO + kMergeBufs * kConsumerWarps * G * D * 4;
+    static constexpr int R_BAR = align_up(R_ML + kMergeBufs * kConsumerWarps * G * 8, 8);
+    static constexpr int STAGES_FIT = (220 * 1024 - R_BAR - 64 * 8 - 16) / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_FIT < 48 ? STAGES_FIT : 48;
+    static constexpr int NBAR = 2 * STAGES + 2 * kItemRing + 2 * kMergeBufs;
+    static constexpr int OFF_REST = STAGES * STAGE_BYTES;
+    static constexpr int OFF_ITEMQ = OFF_REST + R_ITEMQ;
+    static constexpr int OFF_DESC = OFF_REST + R_DESC;
+    static constexpr int OFF_P = OFF_REST + R_P;
+    static constexpr int OFF_MO = OFF_REST + R_MO;
+    static constexpr int OFF_ML = OFF_REST + R_ML;
+    static constexpr int OFF_BAR = OFF_REST + R_BAR;
+    static constexpr int OFF_FLAG = OFF_BAR + NBAR * 8;
+    static constexpr int SMEM = OFF_FLAG + 16;
+    static_assert(STAGES >= 8, "ring too shallow");
+    static_assert(SMEM <= 227 * 1024, "shared memory budget");
+    static_assert(NV * RPP == kBlockSize, "rows");
+};
+
+struct Bars {
+    uint64_t* full;    // [STAGES]   producer -> consumer (tx bytes)
+    uint64_t* empty;   // [STAGES]   consumer -> producer
+    uint64_t* ifull;   // [ITEMS]    item descriptor + q landed
+    uint64_t* iempty;  // [ITEMS]    consumers and merger read the descriptor
+    uint64_t* mfull;   // [MERGE]    8 consumer states published
+    uint64_t* mempty;  // [MERGE]    merger done with the buffer
+};
+
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Sum NV per-lane values over the LPR lanes that share a row group; on
+// return lane l holds the total of value index (l >> 1) & (NV - 1).
+template <int NV, int LPR>
+__device__ __forceinline__ float transpose_reduce(float (&v)[NV], int lane) {
+    int off = LPR / 2;
+#pragma unroll
+    for (int n = NV; n > 1; n >>= 1, off >>= 1) {
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            const float send = upper ? v[i] : v[i + n / 2];
+            const float keep = upper ? v[i + n / 2] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+    }
+#pragma unroll
+    for (; off >= 1; off >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
+    return v[0];
+}
+
+// Parts of sequence s (0 for rows that are not decode rows) and its context
+// length clamped to what the tables and the workspace can hold.
+__device__ __forceinline__ int seq_parts(const DecodeParams& P, int s, int& n_out, bool report) {
+    const int qlen = P.qsl ? (__ldg(P.qsl + s + 1) - __ldg(P.qsl + s)) : 1;
+    if (qlen != 1) {
+        n_out = 0;
+        return 0;
+    }
+    int n = __ldg(P.context_lens + s);
+    if (n < 0 || n > P.ctx_cap) {
+        if (report) record_error(P.err, kErrRange, static_cast<uint32_t>(s));
+        n = n < 0 ? 0 : P.ctx_cap;
+    }
+    n_out = n;
+    if (n == 0) return 1;
+    const int nblk = (n + kBlockSize - 1) / kBlockSize;
+    return (nblk + P.part_blocks - 1) / P.part_blocks;
+}
+
+template <int D, int G>
+__device__ __forceinline__ void compute_block(const uint8_t* kst, const uint8_t* vst, int valid,
+                                              const float (&qf)[G][4], float (&m)[G], float (&lsum)[G],
+                                              float (&o)[G][4], float* psm, int lane) {
+    using C = Cfg<D, G>;
+    const int sub = lane / C::LPR;
+    const int cl = lane % C::LPR;
+    const int myrow = ((lane >> 1) & (C::NV - 1)) * C::RPP + sub;
+#pragma unroll
+    for (int g0 = 0; g0 < G; g0 += C::HG) {
+        float acc[C::HG][C::NV];
+#pragma unroll
+        for (int i = 0; i < C::NV; ++i) {
+            const int row = i * C::RPP + sub;
+            float k0 = 0.f, k1 = 0.f, k2 = 0.f, k3 = 0.f;
+            if (row < valid) {
+                const uint2 u = lds64(kst + row * D * 2 + cl * 8);
+                k0 = bf16lo(u.x);
+                k1 = bf16hi(u.x);
+                k2 = bf16lo(u.y);
+                k3 = bf16hi(u.y);
+            }
+#pragma unroll
+            for (int g = 0; g < C::HG; ++g)
+                acc[g][i] = fmaf(qf[g0 + g][0], k0,
+                                 fmaf(qf[g0 + g][1], k1, fmaf(qf[g0 + g][2], k2, qf[g0 + g][3] * k3)));
+        }
+#pragma unroll
+        for (int g = 0; g < C::HG; ++g) {
+            float sc = transpose_reduce<C::NV, C::LPR>(acc[g], lane);
+            sc = (myrow < valid) ? sc : -INFINITY;
+            const float mb = warp_max(sc);
+            const float mn = fmaxf(m[g0 + g], mb);
+            const float alpha = fast_exp2(m[g0 + g] - mn);
+            const float p = fast_exp2(sc - mn);
+            lsum[g0 + g] = fmaf(lsum[g0 + g], alpha, (lane & 1) ? 0.f : p);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) o[g0 + g][j] *= alpha;
+            m[g0 + g] = mn;
+            if (!(lane & 1)) psm[(g0 + g) * kBlockSize + myrow] = p;
+        }
+    }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < C::NV; ++i) {
+        const int row = i * C::RPP + sub;
+        if (row < valid) {
+            const uint2 u = lds64(vst + row * D * 2 + cl * 8);
+            const float v0 = bf16lo(u.x), v1 = bf16hi(u.x), v2 = bf16lo(u.y), v3 = bf16hi(u.y);
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float pg = psm[g * kBlockSize + row];
+                o[g][0] = fmaf(pg, v0, o[g][0]);
+                o[g][1] = fmaf(pg, v1, o[g][1]);
+                o[g][2] = fmaf(pg, v2, o[g][2]);
+                o[g][3] = fmaf(pg, v3, o[g][3]);
+            }
+        }
+    }
+    __syncwarp();
+}
+
+template <int D, int G>
+__device__ void run_producer(const DecodeParams& P, uint8_t* smem, const Bars& B, volatile int* abort_flag,
+                             int lane) {
+    using C = Cfg<D, G>;
+    ItemDesc* descs = reinterpret_cast<ItemDesc*>(smem + C::OFF_DESC);
+    const unsigned FULL = 0xffffffffu;
+    // Total number of items (every CTA computes the same value).
+    int parts_here = 0;
+    for (int s0 = 0; s0 < P.num_seqs; s0 += 32) {
+        const int s = s0 + lane;
+        int n;
+        if (s < P.num_seqs) parts_here += seq_parts(P, s, n, blockIdx.x == 0);
+    }
+    long long total;
+    {
+        int t = parts_here;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(FULL, t, o);
+        total = static_cast<long long>(t) * P.hkv;
+    }
+    // Window of 32 sequences: lane j describes sequence win_s0 + j.
+    int win_s0 = 0, win_base = 0, w_np = 0, w_n = 0, w_incl = 0;
+    auto load_window = [&]() {
+        const int s = win_s0 + lane;
+        w_np = 0;
+        w_n = 0;
+        if (s < P.num_seqs) w_np = seq_parts(P, s, w_n, false);
+        w_incl = w_np;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(FULL, w_incl, o);
+            if (lane >= o) w_incl += t;
+        }
+    };
+    load_window();
+    const uint64_t policy = l2_policy_evict_first();
+    uint32_t stage_seq = 0;
+    uint32_t item_seq = 0;
+    bool aborted = false;
+    int it = 0;
+    if (lane == 0) it = static_cast<int>(atomicAdd(P.work, 1u));
+    it = __shfl_sync(FULL, it, 0);
+    while (true) {
+        // Fetch the next item index now; it is only needed an item later.
+        int nxt = 0;
+        if (lane == 0 && static_cast<long long>(it) < total) nxt = static_cast<int>(atomicAdd(P.work, 1u));
+        const uint32_t slot = item_seq % kItemRing;
+        if (!mbar_wait_warp(&B.iempty[slot], ((item_seq / kItemRing) & 1) ^ 1)) {
+            aborted = true;
+            break;
+        }
+        int j = -1;
+        if (static_cast<long long>(it) < total) {
+            // Locate the sequence holding item `it` (items are ordered (s, g, p);
+            // a CTA's item numbers only grow, so the window only moves forward).
+            while (true) {
+                const unsigned hit = __ballot_sync(
+                    FULL, static_cast<long long>(win_base + w_incl) * P.hkv > static_cast<long long>(it));
+                if (hit) {
+                    j = __ffs(hit) - 1;
+                    break;
+                }
+                if (win_s0 + 32 >= P.num_seqs) break;  // cannot happen for consistent inputs
+                win_base += __shfl_sync(FULL, w_incl, 31);
+                win_s0 += 32;
+                load_window();
+            }
+            if (j < 0) record_error(P.err, kErrRange, 0xFFFFFFFFu);
+        }
+        if (j < 0) {  // no more work: end marker
+            if (lane == 0) {
+                descs[slot].s = -1;
+                mbar_arrive(&B.ifull[slot]);
+            }
+            __syncwarp();
+            ++item_seq;
+            break;
+        }
+        const int s = win_s0 + j;
+        const int np = __shfl_sync(FULL, w_np, j);
+        const int n = __shfl_sync(FULL, w_n, j);
+        const int excl = win_base + __shfl_sync(FULL, w_incl, j) - np;
+        const int local = it - excl * P.hkv;
+        const int g = local / np;
+        const int p = local - g * np;
+        const int nblk = (n + kBlockSize - 1) / kBlockSize;
+        const int b0 = static_cast<int>(static_cast<long long>(p) * nblk / np);
+        const int b1 = static_cast<int>(static_cast<long long>(p + 1) * nblk / np);
+        const int row = P.qsl ? __ldg(P.qsl + s) : s;
+        const int32_t* trow = P.block_tables + static_cast<size_t>(s) * P.max_blocks;
+        // First chunk of table entries, requested before the descriptor work.
+        int e = 0;
+        if (lane < b1 - b0) e = __ldg(trow + b0 + lane);
+        if (lane == 0) {
+            ItemDesc d;
+            d.s = s; d.g = g; d.p = p; d.nparts = np; d.n = n; d.b0 = b0; d.b1 = b1; d.row = row;
+            d.rot = it % kConsumerWarps;
+            d.pad0 = d.pad1 = d.pad2 = 0;
+            descs[slot] = d;
+            mbar_arrive_expect_tx(&B.ifull[slot], C::QBYTES);
+            const uint8_t* qsrc = P.q + (static_cast<size_t>(row) * P.hq + static_cast<size_t>(g) * G) * D * 2;
+            bulk_g2s(smem + C::OFF_ITEMQ + slot * C::QBYTES, qsrc, C::QBYTES, &B.ifull[slot]);
+        }
+        __syncwarp();
+        ++item_seq;
+        // Stream the item's blocks, 32 table entries at a time (the next
+        // chunk's entries are requested before this chunk's copies).
+        for (int base = b0; base < b1 && !aborted; base += 32) {
+            const int cnt = min(32, b1 - base);
+            int e_next = 0;
+            if (base + 32 + lane < b1) e_next = __ldg(trow + base + 32 + lane);
+            if (lane < cnt && (e < 0 || e >= P.num_blocks)) {
+                record_error(P.err, kErrRange, static_cast<uint32_t>(s));
+                e = 0;  // never dereference an invalid id
+            }
+            for (int k = 0; k < cnt; ++k) {
+                const int phys = __shfl_sync(FULL, e, k);
+                const uint32_t st = stage_seq % C::STAGES;
+                int bad = 0;
+                if (lane == 0) {
+                    if (!mbar_wait(&B.empty[st], ((stage_seq / C::STAGES) & 1) ^ 1)) {
+                        bad = 1;
+                    } else {
+                        const size_t slab = (static_cast<size_t>(phys) * P.hkv + g) * C::SLAB;
+                        uint8_t* dst = smem + st * C::STAGE_BYTES;
+                        mbar_arrive_expect_tx(&B.full[st], 2 * C::SLAB);
+                        bulk_g2s_hint(dst, P.k_pool + slab, C::SLAB, &B.full[st], policy);
+                        bulk_g2s_hint(dst + C::SLAB, P.v_pool + slab, C::SLAB, &B.full[st], policy);
+                    }
+                }
+                if (__shfl_sync(FULL, bad, 0)) {
+                    aborted = true;
+                    break;
+                }
+                ++stage_seq;
+            }
+            e = e_next;
+        }
+        if (aborted) break;
+        it = __shfl_sync(FULL, nxt, 0);
+    }
+    if (aborted) {
+        *abort_flag = 1;
+        record_error(P.err, kErrTimeout, 1u);
+    }
+    // This CTA takes no more items.  The last CTA to get here resets the
+    // counters so the workspace is zero again for the next call.
+    if (lane == 0) {
+        __threadfence();
+        const uint32_t done = atomicAdd(P.work + 1, 1u);
+        if (done == gridDim.x - 1) {
+            atomicExch(P.work, 0u);
+            atomicExch(P.work + 1, 0u);
+        }
+    }
+    // Never leave with bulk copies still in flight (matters only after a
+    // timeout: normally the consumers have waited on every one).
+    if (aborted && lane == 0) {
+        for (uint32_t st = 0; st < C::STAGES; ++st)
+            if (st < stage_seq) mbar_wait(&B.full[st], ((stage_seq - 1 - st) / C::STAGES) & 1);
+        for (uint32_t sl = 0; sl < kItemRing; ++sl)
+            if (sl < item_seq) mbar_wait(&B.ifull[sl], ((item_seq - 1 - sl) / kItemRing) & 1);
+    }
+}
+
+template <int D, int G>
+__device__ void run_consumer(const DecodeParams& P, uint8_t* smem, const Bars& B, volatile int* abort_flag,
+                             int warp, int lane) {
+    using C = Cfg<D, G>;
+    const ItemDesc* descs = reinterpret_cast<const ItemDesc*>(smem + C::OFF_DESC);
+    float* psm = reinterpret_cast<float*>(smem + C::OFF_P) + warp * G * kBlockSize;
+    float* mo = reinterpret_cast<float*>(smem + C::OFF_MO);
+    float2* ml = reinterpret_cast<float2*>(smem + C::OFF_ML);
+    const int sub = lane / C::LPR;
+    const int cl = lane % C::LPR;
+    uint32_t stage_base = 0, item_seq = 0;
+    bool ok = true;
+    while (ok) {
+        const uint32_t slot = item_seq % kItemRing;
+        if (*abort_flag || !mbar_wait_warp(&B.ifull[slot], (item_seq / kItemRing) & 1)) {
+            ok = false;
+            break;
+        }
+        const ItemDesc d = descs[slot];
+        if (d.s < 0) break;
+        float qf[G][4];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const uint2 u = lds64(smem + C::OFF_ITEMQ + slot * C::QBYTES + (g * D + cl * 4) * 2);
+            qf[g][0] = bf16lo(u.x) * P.scale_log2;
+            qf[g][1] = bf16hi(u.x) * P.scale_log2;
+            qf[g][2] = bf16lo(u.y) * P.scale_log2;
+            qf[g][3] = bf16hi(u.y) * P.scale_log2;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&B.iempty[slot]);
+        float m[G], lsum[G], o[G][4];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            m[g] = -INFINITY;
+            lsum[g] = 0.f;
+            o[g][0] = o[g][1] = o[g][2] = o[g][3] = 0.f;
+        }
+        const int nb = d.b1 - d.b0;
+        // Block b of the item goes to warp (b + rot) % 8: the rotation comes
+        // from the item's global index, so the extra blocks of items whose
+        // length is not a multiple of 8 spread over the warps while every
+        // item is summed in an order that does not depend on which CTA took
+        // it (results are bitwise reproducible).
+        const int first = (warp - d.rot + kConsumerWarps) % kConsumerWarps;
+        for (int b = first; b < nb; b += kConsumerWarps) {
+            const uint32_t seqn = stage_base + b;
+            const uint32_t st = seqn % C::STAGES;
+            if (*abort_flag || !mbar_wait_warp(&B.full[st], (seqn / C::STAGES) & 1)) {
+                ok = false;
+                break;
+            }
+            const int blk = d.b0 + b;
+            const int valid = min(kBlockSize, d.n - blk * kBlockSize);
+            const uint8_t* kst = smem + st * C::STAGE_BYTES;
+            compute_block<D, G>(kst, kst + C::SLAB, valid, qf, m, lsum, o, psm, lane);
+            if (lane == 0) mbar_arrive(&B.empty[st]);
+        }
+        if (!ok) break;
+        stage_base += nb;
+        // Publish this warp's state for the merger.
+        const int buf = item_seq % kMergeBufs;
+        if (!mbar_wait_warp(&B.mempty[buf], ((item_seq / kMergeBufs) & 1) ^ 1)) {
+            ok = false;
+            break;
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const float lt = warp_sum(lsum[g]);
+            if (C::RPP == 2) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) o[g][j] += __shfl_xor_sync(0xffffffffu, o[g][j], 16);
+            }
+            if (lane == 0) ml[(buf * kConsumerWarps + warp) * G + g] = make_float2(m[g], lt);
+            if (sub == 0)
+                *reinterpret_cast<float4*>(mo + ((buf * kConsumerWarps + warp) * G + g) * D + cl * 4) =
+                    make_float4(o[g][0], o[g][1], o[g][2], o[g][3]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&B.mfull[buf]);
+        ++item_seq;
+    }
+    if (!ok) {
+        *abort_flag = 1;
+        record_error(P.err, kErrTimeout, 2u);
+    }
+}
+
+template <int D, int G>
+__device__ void run_merger(const DecodeParams& P, uint8_t* smem, const Bars& B, volatile int* abort_flag, int lane) {
+    using C = Cfg<D, G>;
+    const ItemDesc* descs = reinterpret_cast<const ItemDesc*>(smem + C::OFF_DESC);
+    const float* mo = reinterpret_cast<const float*>(smem + C::OFF_MO);
+    const float2* ml = reinterpret_cast<const float2*>(smem + C::OFF_ML);
+    uint32_t item_seq = 0;
+    bool ok = true;
+    while (true) {
+        const uint32_t slot = item_seq % kItemRing;
+        if (*abort_flag || !mbar_wait_warp(&B.ifull[slot], (item_seq / kItemRing) & 1)) {
+            ok = false;
+            break;
+        }
+        const ItemDesc d = descs[slot];
+        if (d.s < 0) break;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&B.iempty[slot]);
+        const int buf = item_seq % kMergeBufs;
+        if (!mbar_wait_warp(&B.mfull[buf], (item_seq / kMergeBufs) & 1)) {
+            ok = false;
+            break;
+        }
+        // Combine the consumer warps' states (log-sum-exp).
+        for (int idx = lane; idx < G * D; idx += 32) {
+            const int g = idx / D;
+            const int c = idx - g * D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, ml[(buf * kConsumerWarps + w) * G + g].x);
+            float L = 0.f, O = 0.f;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                const float2 e = ml[(buf * kConsumerWarps + w) * G + g];
+                const float wt = (e.x == -INFINITY) ? 0.f : fast_exp2(e.x - M);
+                L = fmaf(e.y, wt, L);
+                O = fmaf(mo[((buf * kConsumerWarps + w) * G + g) * D + c], wt, O);
+            }
+            const int h = d.g * G + g;
+            if (d.nparts == 1) {
+                P.out[(static_cast<size_t>(d.row) * P.hq + h) * D + c] = (L > 0.f) ? O / L : 0.f;
+            } else {
+                const size_t pi = (static_cast<size_t>(d.s) * P.hq + h) * P.max_parts + d.p;
+                P.part_o[pi * D + c] = O;
+                if (c == 0) P.part_ml[pi] = make_float2(M, L);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&B.mempty[buf]);
+        if (d.nparts > 1) {
+            __threadfence();
+            __syncwarp();
+            uint32_t ticket = 0;
+            uint32_t* ctr = P.counters + static_cast<size_t>(d.s) * P.hkv + d.g;
+            if (lane == 0) ticket = atomicAdd(ctr, 1u);
+            ticket = __shfl_sync(0xffffffffu, ticket, 0);
+            if (ticket == static_cast<uint32_t>(d.nparts - 1)) {
+                // Last partition in: merge all partitions of (s, kv head).
+                __threadfence();
+                for (int idx = lane; idx < G * D; idx += 32) {
+                    const int g = idx / D;
+                    const int c = idx - g * D;
+                    const int h = d.g * G + g;
+                    const size_t pb = (static_cast<size_t>(d.s) * P.hq + h) * P.max_parts;
+                    float M = -INFINITY;
+                    for (int pp = 0; pp < d.nparts; ++pp) M = fmaxf(M, __ldcg(P.part_ml + pb + pp).x);
+                    float L = 0.f, O = 0.f;
+                    for (int pp = 0; pp < d.nparts; ++pp) {
+                        const float2 e = __ldcg(P.part_ml + pb + pp);
+                        const float wt = (e.x == -INFINITY) ? 0.f : fast_exp2(e.x - M);
+                        L = fmaf(e.y, wt, L);
+                        O = fmaf(__ldcg(P.part_o + (pb + pp) * D + c), wt, O);
+                    }
+                    P.out[(static_cast<size_t>(d.row) * P.hq + h) * D + c] = (L > 0.f) ? O / L : 0.f;
+                }
+                if (lane == 0) atomicExch(ctr, 0u);
+            }
+        }
+        ++item_seq;
+    }
+    if (!ok) {
+        *abort_flag = 1;
+        record_error(P.err, kErrTimeout, 3u);
+    }
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams P) {
+    using C = Cfg<D, G>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+    Bars B;
+    B.full = bars;
+    B.empty = bars + C::STAGES;
+    B.ifull = bars + 2 * C::STAGES;
+    B.iempty = B.ifull + kItemRing;
+    B.mfull = B.iempty + kItemRing;
+    B.mempty = B.mfull + kMergeBufs;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_FLAG);
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::STAGES; ++i) {
+            mbar_init(&B.full[i], 1);
+            mbar_init(&B.empty[i], 1);
+        }
+        for (int i = 0; i < kItemRing; ++i) {
+            mbar_init(&B.ifull[i], 1);
+            mbar_init(&B.iempty[i], kConsumerWarps + 1);
+        }
+        for (int i = 0; i < kMergeBufs; ++i) {
+            mbar_init(&B.mfull[i], kConsumerWarps);
+            mbar_init(&B.mempty[i], 1);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (warp == kProducerWarp) {
+        run_producer<D, G>(P, smem, B, abort_flag, lane);
+    } else if (warp == kMergerWarp) {
+        run_merger<D, G>(P, smem, B, abort_flag, lane);
+    } else {
+        run_consumer<D, G>(P, smem, B, abort_flag, warp, lane);
+    }
+}
+
+template <int D, int G>
+cudaError_t launch_one(const DecodeParams& P, int grid, cudaStream_t stream) {
+    using C = Cfg<D, G>;
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::SMEM);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    decode_kernel<D, G><<<grid, kThreads, C::SMEM, stream>>>(P);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t dispatch_g(const DecodeParams& P, int G, int grid, cudaStream_t stream) {
+    switch (G) {
+        case 1: return launch_one<D, 1>(P, grid, stream);
+        case 2: return launch_one<D, 2>(P, grid, stream);
+        case 4: return launch_one<D, 4>(P, grid, stream);
+        case 8: return launch_one<D, 8>(P, grid, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+DecodeWsLayout decode_ws_layout(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                int32_t max_parts) {
+    DecodeWsLayout L;
+    L.header = 0;
+    L.counters = 256;
+    L.part_ml = L.counters + align256(static_cast<size_t>(num_seqs) * num_kv_heads * 4);
+    const size_t nparts = static_cast<size_t>(num_seqs) * num_q_heads * max_parts;
+    L.part_o = L.part_ml + align256(nparts * 8);
+    L.total = L.part_o + align256(nparts * head_dim * 4);
+    return L;
+}
+
+int32_t plan_part_blocks(int32_t num_seqs, int32_t num_kv_heads, int32_t max_context_len, int32_t num_sms,
+                         int32_t req) {
+    const int64_t nblk_max =
+        std::max<int64_t>(1, (static_cast<int64_t>(max_context_len) + kBlockSize - 1) / kBlockSize);
+    if (req > 0) return static_cast<int32_t>(std::min<int64_t>(req, nblk_max));
+    const int64_t pairs = std::max<int64_t>(1, static_cast<int64_t>(num_seqs) * num_kv_heads);
+    // Items of at most 128 blocks (2,048 tokens) so that no single item
+    // dominates the tail of the persistent grid; when there are fewer
+    // (sequence, kv head) pairs than two per SM, split further (down to 8
+    // blocks) so that every SM gets work.
+    int64_t pb = std::min<int64_t>(128, nblk_max);
+    if (pairs < 2LL * num_sms) {
+        const int64_t want = (pairs * nblk_max + 2LL * num_sms - 1) / (2LL * num_sms);
+        pb = std::min<int64_t>(pb, std::max<int64_t>(8, want));
+    }
+    return static_cast<int32_t>(std::max<int64_t>(1, pb));
+}
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
+    if (a.num_seqs == 0) return cudaSuccess;
+    const DecodeWsLayout L = decode_ws_layout(a.num_seqs, a.num_q_heads, a.num_kv_heads, a.head_dim, a.max_parts);
+    uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+    DecodeParams P;
+    P.k_pool = static_cast<const uint8_t*>(a.k_pool);
+    P.v_pool = static_cast<const uint8_t*>(a.v_pool);
+    P.q = static_cast<const uint8_t*>(a.q);
+    P.block_tables = a.block_tables;
+    P.context_lens = a.context_lens;
+    P.qsl = a.query_start_loc;
+    P.out = a.out;
+    P.part_ml = reinterpret_cast<float2*>(ws + L.part_ml);
+    P.part_o = reinterpret_cast<float*>(ws + L.part_o);
+    P.counters = reinterpret_cast<uint32_t*>(ws + L.counters);
+    P.work = reinterpret_cast<uint32_t*>(ws + L.header);
+    P.err = a.err;
+    P.num_blocks = a.num_blocks;
+    P.hkv = a.num_kv_heads;
+    P.hq = a.num_q_heads;
+    P.num_seqs = a.num_seqs;
+    P.max_blocks = a.max_blocks_per_seq;
+    P.ctx_cap = static_cast<int32_t>(
+        std::min<int64_t>(a.max_context_len, static_cast<int64_t>(a.max_blocks_per_seq) * kBlockSize));
+    P.part_blocks = a.part_blocks;
+    P.max_parts = a.max_parts;
+    P.scale_log2 = a.scale * kLog2e;
+    const int G = a.num_q_heads / a.num_kv_heads;
+    if (a.head_dim == 128) return dispatch_g<128>(P, G, a.grid, stream);
+    if (a.head_dim == 64) return dispatch_g<64>(P, G, a.grid, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace pkv

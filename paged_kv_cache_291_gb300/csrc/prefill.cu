@@ -1,0 +1,509 @@
+// prefill.cu -- causal chunked-prefill attention tiles on tcgen05 tensor cores.
+//
+// What it computes ("Chunked Prefill" section of the inference-engine talk
+// write-up; section 3 of the serving-engine KV blog): a long prompt is split
+// into slices that share a step with decode tokens.  Query row i of a
+// sequence with query_len rows and context_len keys (the chunk's own K/V are
+// already in the paged cache) sits at position context_len - query_len + i
+// and attends keys 0..pos, read through the sequence's block table
+// ("Blocks and block tables", section 2 of the blog).  The prefill part of
+// a step is a dense contraction ("Prefill/Decode" section of the talk
+// write-up), so these tiles run on the tensor cores:
+//
+//  * CTA = 128 query rows of one q head.  Warp 4 loads the Q tile and the
+//    K/V key tiles (128 keys = 8 paged blocks, each block a 16-row TMA box
+//    with 128-byte swizzle) into a 2-stage ring; warp 5 issues
+//    tcgen05.mma: S = Q K^T into TMEM (double-buffered), then O += P V with
+//    O resident in TMEM; warps 0-3 own one query row each (TMEM lane =
+//    row): causal mask, online softmax in the log2 domain, P rounded to bf16
+//    and written to shared memory in the MMA's K-major swizzled layout.
+//  * The running maximum is only moved (and O rescaled in TMEM) when it
+//    grows by more than 2^8; the final O / l uses the same reference, so the
+//    result is unchanged while most tiles skip the rescale.
+//  * l sums the bf16-rounded P actually fed to the MMA, so the normalisation
+//    matches the weights applied.
+//  * Keys past the last query position of the tile are masked; V rows past
+//    the context are zeroed in shared memory (a 0 weight times a NaN in an
+//    unused slot would otherwise poison the MMA).
+//  * Every wait is bounded; TMEM is freed on every exit path.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+#include "tcgen05.cuh"
+
+namespace pkv {
+
+namespace {
+
+constexpr int kTileM = 128;                  // query rows per CTA
+constexpr int kTileN = 128;                  // keys per key tile
+constexpr int kHeadDim = 128;                // head_dim of the tensor-core path
+constexpr int kBlocksPerTile = kTileN / kBlockSize;  // 8
+constexpr int kPanelBytes = 128 * 128;       // 128 rows x 128 B (64 bf16)
+constexpr int kTileBytes = 2 * kPanelBytes;  // [128][128] bf16 as two swizzled panels
+constexpr int kBoxBytes = kBlockSize * 128;  // one 16-row box of one panel
+
+constexpr int OFF_Q = 0;
+constexpr int OFF_K = OFF_Q + kTileBytes;          // 2 stages
+constexpr int OFF_V = OFF_K + 2 * kTileBytes;      // 2 stages
+constexpr int OFF_P = OFF_V + 2 * kTileBytes;
+constexpr int OFF_BAR = OFF_P + kTileBytes;
+constexpr int NBAR = 13;
+constexpr int OFF_INFO = OFF_BAR + NBAR * 8;       // tile info (ints)
+constexpr int OFF_TMEM = OFF_INFO + 16 * 4;
+constexpr int SMEM_USED = OFF_TMEM + 16;
+constexpr int SMEM_BYTES = SMEM_USED + 1024;       // slack to align the base to 1024 B
+
+constexpr int kSoftmaxWarps = 4;
+constexpr int kLoadWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kThreads = 32 * 6;
+
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColO = 256;  // O accumulator columns; S buffers at 0 and 128
+
+__host__ __device__ constexpr uint32_t col_s(int buf) { return static_cast<uint32_t>(buf) * 128u; }
+
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct PrefillParams {
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    const int32_t* qsl;
+    float* out;
+    unsigned long long* err;
+    int32_t num_blocks, hkv, hq, num_seqs, max_blocks, ctx_cap, num_tokens;
+    float scale_log2;
+};
+
+// Barrier indices.
+enum {
+    B_QFULL = 0,
+    B_KFULL = 1,   // +stage
+    B_KEMPTY = 3,  // +stage
+    B_VFULL = 5,   // +stage
+    B_VEMPTY = 7,  // +stage
+    B_SFULL = 9,   // +buffer
+    B_PFULL = 11,
+    B_ODONE = 12,
+};
+
+// Tile info slots (written by warp 0 before the CTA-wide sync).
+enum { I_S = 0, I_ROW0, I_ROWS, I_PMIN, I_PMAX, I_NT, I_KLAST, I_BAD, I_CTX };
+
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) { return mbar_wait_warp(bar, parity); }
+
+__device__ __forceinline__ uint32_t tmem_lane_addr(uint32_t base, int warp, uint32_t col) {
+    return base + (static_cast<uint32_t>(warp * 32) << 16) + col;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const PrefillParams P) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+    int* info = reinterpret_cast<int*>(smem + OFF_INFO);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_TMEM);
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const int h = blockIdx.y;
+    const int g = h / (P.hq / P.hkv);
+    const unsigned FULL = 0xffffffffu;
+
+    // ---------------------------------------------------------- setup
+    if (warp == 0) {
+        // Find the sequence and row tile of this CTA: tiles are numbered over
+        // the prefill sequences (query_len > 1) in order, ceil(qlen/128) each.
+        const int tile = blockIdx.x;
+        int base = 0, found = -1, tloc = 0;
+        for (int s0 = 0; s0 < P.num_seqs && found < 0; s0 += 32) {
+            const int s = s0 + lane;
+            int nt = 0;
+            if (s < P.num_seqs) {
+                const int ql = __ldg(P.qsl + s + 1) - __ldg(P.qsl + s);
+                nt = ql > 1 ? (ql + kTileM - 1) / kTileM : 0;
+            }
+            int incl = nt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int t = __shfl_up_sync(FULL, incl, o);
+                if (lane >= o) incl += t;
+            }
+            const unsigned hit = __ballot_sync(FULL, base + incl > tile);
+            if (hit) {
+                const int j = __ffs(hit) - 1;
+                found = s0 + j;
+                tloc = tile - (base + __shfl_sync(FULL, incl - nt, j));
+            } else {
+                base += __shfl_sync(FULL, incl, 31);
+            }
+        }
+        if (lane == 0) {
+            int bad = 0, s = found, row0 = 0, rows = 0, pmin = 0, pmax = 0, nt = 0, klast = 0, ctx = 0;
+            if (s < 0) {
+                bad = 1;
+            } else {
+                const int q0 = __ldg(P.qsl + s);
+                const int ql = __ldg(P.qsl + s + 1) - q0;
+                ctx = __ldg(P.context_lens + s);
+                if (ctx > P.ctx_cap || ql > ctx) {
+                    record_error(P.err, kErrRange, static_cast<uint32_t>(s));
+                    bad = 1;
+                }
+                row0 = q0 + tloc * kTileM;
+                rows = min(kTileM, ql - tloc * kTileM);
+                pmin = ctx - ql + tloc * kTileM;
+                pmax = pmin + rows - 1;
+                nt = pmax / kTileN + 1;
+                klast = pmax + 1 - (nt - 1) * kTileN;
+                if (bad) {
+                    nt = 0;
+                }
+            }
+            info[I_S] = s;
+            info[I_ROW0] = row0;
+            info[I_ROWS] = (s < 0) ? 0 : rows;
+            info[I_PMIN] = pmin;
+            info[I_PMAX] = pmax;
+            info[I_NT] = nt;
+            info[I_KLAST] = klast;
+            info[I_BAD] = bad;
+            info[I_CTX] = ctx;
+        }
+    }
+    if (threadIdx.x == 32 * kMmaWarp) {
+        for (int i = 0; i < NBAR; ++i) mbar_init(&bar[i], i == B_PFULL ? kSoftmaxWarps : 1);
+        fence_mbar_init();
+    }
+    if (warp == kLoadWarp) {
+        tc::tmem_alloc(tmem_slot, kTmemCols);
+        tc::tmem_relinquish();
+        if (lane == 0) {
+            tc::prefetch_tensormap(&tm_q);
+            tc::prefetch_tensormap(&tm_k);
+            tc::prefetch_tensormap(&tm_v);
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const int s = info[I_S];
+    const int row0 = info[I_ROW0];
+    const int rows = info[I_ROWS];
+    const int pmin = info[I_PMIN];
+    const int pmax = info[I_PMAX];
+    const int nt = info[I_NT];
+    const int klast = info[I_KLAST];
+    const int bad = info[I_BAD];
+    const int nblk = (pmax + 1 + kBlockSize - 1) / kBlockSize;  // blocks holding keys 0..pmax
+    bool ok = true;
+
+    if (warp == kLoadWarp && nt > 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&bar[B_QFULL], kTileBytes);
+            tc::tma_load_3d(smem + OFF_Q, &tm_q, 0, h, row0, &bar[B_QFULL]);
+            tc::tma_load_3d(smem + OFF_Q + kPanelBytes, &tm_q, 64, h, row0, &bar[B_QFULL]);
+        }
+        const int32_t* trow = P.block_tables + static_cast<size_t>(s) * P.max_blocks;
+        for (int j = 0; j < nt && ok; ++j) {
+            const int st = j & 1;
+            const uint32_t ph = (j >> 1) & 1;
+            const int nvb = min(kBlocksPerTile, nblk - j * kBlocksPerTile);
+            int e = 0;
+            if (lane < nvb) {
+                e = __ldg(trow + j * kBlocksPerTile + lane);
+                if (e < 0 || e >= P.num_blocks) {
+                    record_error(P.err, kErrRange, static_cast<uint32_t>(s));
+                    e = 0;
+                }
+            }
+            int rowsel[kBlocksPerTile];
+#pragma unroll
+            for (int b = 0; b < kBlocksPerTile; ++b) rowsel[b] = (__shfl_sync(FULL, e, b) * P.hkv + g) * kBlockSize;
+            const uint32_t bytes = static_cast<uint32_t>(nvb) * 2 * kBoxBytes;
+            if (!warp_wait(&bar[B_KEMPTY + st], ph ^ 1)) { ok = false; break; }
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&bar[B_KFULL + st], bytes);
+                uint8_t* dst = smem + OFF_K + st * kTileBytes;
+#pragma unroll
+                for (int b = 0; b < kBlocksPerTile; ++b) {
+                    if (b < nvb) {
+                        tc::tma_load_2d(dst + b * kBoxBytes, &tm_k, 0, rowsel[b], &bar[B_KFULL + st]);
+                        tc::tma_load_2d(dst + kPanelBytes + b * kBoxBytes, &tm_k, 64, rowsel[b], &bar[B_KFULL + st]);
+                    }
+                }
+            }
+            if (!warp_wait(&bar[B_VEMPTY + st], ph ^ 1)) { ok = false; break; }
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&bar[B_VFULL + st], bytes);
+                uint8_t* dst = smem + OFF_V + st * kTileBytes;
+#pragma unroll
+                for (int b = 0; b < kBlocksPerTile; ++b) {
+                    if (b < nvb) {
+                        tc::tma_load_2d(dst + b * kBoxBytes, &tm_v, 0, rowsel[b], &bar[B_VFULL + st]);
+                        tc::tma_load_2d(dst + kPanelBytes + b * kBoxBytes, &tm_v, 64, rowsel[b], &bar[B_VFULL + st]);
+                    }
+                }
+            }
+            __syncwarp();
+        }
+    } else if (warp == kMmaWarp && nt > 0) {
+        // ------------------------------------------------------ MMA issuer
+        constexpr uint32_t kIdescQK = tc::idesc_bf16_f32(kTileM, kTileN, 0, 0);
+        constexpr uint32_t kIdescPV = tc::idesc_bf16_f32(kTileM, kHeadDim, 0, 1);
+        const uint32_t sq = smem_addr(smem + OFF_Q);
+        const uint32_t sp = smem_addr(smem + OFF_P);
+        auto issue_qk = [&](int j) -> bool {
+            const int st = j & 1;
+            if (!warp_wait(&bar[B_KFULL + st], (j >> 1) & 1)) return false;
+            tc::fence_after_sync();
+            if (lane == 0) {
+                const uint32_t sk = smem_addr(smem + OFF_K + st * kTileBytes);
+#pragma unroll
+                for (int k = 0; k < kHeadDim / 16; ++k) {
+                    const uint32_t off = (k >> 2) * kPanelBytes + (k & 3) * 32;
+                    tc::mma_bf16_ss(tmem + col_s(j & 1), tc::smem_desc_sw128(sq + off, 16, 1024),
+                                    tc::smem_desc_sw128(sk + off, 16, 1024), kIdescQK, k > 0 ? 1u : 0u);
+                }
+                tc::mma_commit(&bar[B_SFULL + (j & 1)]);
+                tc::mma_commit(&bar[B_KEMPTY + st]);
+            }
+            __syncwarp();
+            return true;
+        };
+        ok = warp_wait(&bar[B_QFULL], 0);
+        if (ok) ok = issue_qk(0);
+        if (ok && nt > 1) ok = issue_qk(1);
+        for (int j = 0; j < nt && ok; ++j) {
+            const int st = j & 1;
+            if (!warp_wait(&bar[B_PFULL], j & 1)) { ok = false; break; }
+            if (!warp_wait(&bar[B_VFULL + st], (j >> 1) & 1)) { ok = false; break; }
+            uint8_t* sv = smem + OFF_V + st * kTileBytes;
+            if (j == nt - 1 && klast < kTileN) {
+                // Zero V rows of keys past the last visible position (unused
+                // slots of the last block and blocks never loaded).
+                const int nrows = kTileN - klast;
+                for (int i = lane; i < nrows * 16; i += 32) {
+                    const int r = klast + (i >> 4);
+                    const int panel = (i >> 3) & 1;
+                    const int chunk = i & 7;
+                    tc::sts128(smem_addr(sv + panel * kPanelBytes + r * 128 + chunk * 16), 0u, 0u, 0u, 0u);
+                }
+                tc::fence_proxy_async_smem();
+                __syncwarp();
+            }
+            tc::fence_after_sync();
+            if (lane == 0) {
+                const uint32_t svb = smem_addr(sv);
+#pragma unroll
+                for (int k = 0; k < kTileN / 16; ++k) {
+                    const uint32_t aoff = (k >> 2) * kPanelBytes + (k & 3) * 32;
+                    tc::mma_bf16_ss(tmem + kColO, tc::smem_desc_sw128(sp + aoff, 16, 1024),
+                                    tc::smem_desc_sw128(svb + k * 2048, kPanelBytes, 1024), kIdescPV,
+                                    (j > 0 || k > 0) ? 1u : 0u);
+                }
+                tc::mma_commit(&bar[B_ODONE]);
+                tc::mma_commit(&bar[B_VEMPTY + st]);
+            }
+            __syncwarp();
+            if (j + 2 < nt) ok = issue_qk(j + 2);
+        }
+    } else if (warp < kSoftmaxWarps) {
+        // ------------------------------------------------------ softmax rows
+        const int m = warp * 32 + lane;
+        const int pos = (m < rows) ? pmin + m : pmax;
+        float m_used = -INFINITY;
+        float l = 0.f;
+        const uint32_t sp = smem_addr(smem + OFF_P);
+        for (int j = 0; j < nt && ok; ++j) {
+            if (!warp_wait(&bar[B_SFULL + (j & 1)], (j >> 1) & 1)) { ok = false; break; }
+            tc::fence_after_sync();
+            float x[kTileN];
+#pragma unroll
+            for (int c = 0; c < kTileN / 32; ++c) {
+                uint32_t r[32];
+                tc::tmem_ld32(tmem_lane_addr(tmem, warp, col_s(j & 1) + 32 * c), r);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) x[32 * c + i] = __uint_as_float(r[i]);
+            }
+            const int kbase = j * kTileN;
+            float mt = -INFINITY;
+#pragma unroll
+            for (int n = 0; n < kTileN; ++n) {
+                x[n] = (kbase + n <= pos) ? x[n] * P.scale_log2 : -INFINITY;
+                mt = fmaxf(mt, x[n]);
+            }
+            // PV(j-1) must be complete before O is touched or P overwritten.
+            if (j > 0) {
+                if (!warp_wait(&bar[B_ODONE], (j - 1) & 1)) { ok = false; break; }
+                tc::fence_after_sync();
+            }
+            if (j == 0) {
+                m_used = mt;
+            } else {
+                const bool need = mt > m_used + kRescaleThreshold;
+                if (__any_sync(FULL, need)) {
+                    const float alpha = need ? fast_exp2(m_used - mt) : 1.f;
+#pragma unroll
+                    for (int c = 0; c < kHeadDim / 32; ++c) {
+                        uint32_t r[32];
+                        const uint32_t ta = tmem_lane_addr(tmem, warp, kColO + 32 * c);
+                        tc::tmem_ld32(ta, r);
+                        tc::tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                        tc::tmem_st32(ta, r);
+                    }
+                    tc::tmem_wait_st();
+                    l *= alpha;
+                    if (need) m_used = mt;
+                }
+            }
+            // P = exp2(x - m_used) in bf16, row m of the K-major swizzled tile.
+#pragma unroll
+            for (int c = 0; c < kTileN / 8; ++c) {
+                uint32_t w[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float p0 = fast_exp2(x[8 * c + 2 * i] - m_used);
+                    const float p1 = fast_exp2(x[8 * c + 2 * i + 1] - m_used);
+                    w[i] = tc::pack_bf16x2(p0, p1);
+                    l += bf16lo(w[i]) + bf16hi(w[i]);
+                }
+                const int panel = c >> 3;
+                const int chunk = (c & 7) ^ (m & 7);
+                tc::sts128(sp + panel * kPanelBytes + m * 128 + chunk * 16, w[0], w[1], w[2], w[3]);
+            }
+            tc::fence_proxy_async_smem();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[B_PFULL]);
+        }
+        if (ok && nt > 0) {
+            if (!warp_wait(&bar[B_ODONE], (nt - 1) & 1)) {
+                ok = false;
+            } else {
+                tc::fence_after_sync();
+                const float inv = 1.f / l;
+                float* orow = P.out + (static_cast<size_t>(row0 + m) * P.hq + h) * kHeadDim;
+#pragma unroll
+                for (int c = 0; c < kHeadDim / 32; ++c) {
+                    uint32_t r[32];
+                    tc::tmem_ld32(tmem_lane_addr(tmem, warp, kColO + 32 * c), r);
+                    tc::tmem_wait_ld();
+                    if (m < rows) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4)
+                            *reinterpret_cast<float4*>(orow + 32 * c + i) =
+                                make_float4(__uint_as_float(r[i]) * inv, __uint_as_float(r[i + 1]) * inv,
+                                            __uint_as_float(r[i + 2]) * inv, __uint_as_float(r[i + 3]) * inv);
+                    }
+                }
+            }
+        } else if (bad && s >= 0 && m < rows) {
+            float* orow = P.out + (static_cast<size_t>(row0 + m) * P.hq + h) * kHeadDim;
+            for (int c = 0; c < kHeadDim; c += 4) *reinterpret_cast<float4*>(orow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    if (!ok) record_error(P.err, kErrTimeout, 0x100u + static_cast<uint32_t>(warp));
+    // ---------------------------------------------------------- teardown
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (warp == kLoadWarp) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+bool make_map(CUtensorMap* map, const void* base, cuuint32_t rank, const cuuint64_t* dims,
+              const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint32_t elem_strides[3] = {1, 1, 1};
+    std::memset(map, 0, sizeof(*map));
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides_bytes,
+                          box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
+    if (a.head_dim != kHeadDim) return cudaErrorNotSupported;
+    if (a.num_tiles == 0) return cudaSuccess;
+    CUtensorMap tq, tk, tv;
+    {
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(a.head_dim), static_cast<cuuint64_t>(a.num_q_heads),
+                                    static_cast<cuuint64_t>(a.num_tokens)};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(a.head_dim) * 2,
+                                       static_cast<cuuint64_t>(a.num_q_heads) * a.head_dim * 2};
+        const cuuint32_t box[3] = {64, 1, kTileM};
+        if (!make_map(&tq, a.q, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t rows = static_cast<cuuint64_t>(a.num_blocks) * a.num_kv_heads * kBlockSize;
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.head_dim), rows > 0 ? rows : 1};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.head_dim) * 2};
+        const cuuint32_t box[2] = {64, kBlockSize};
+        if (!make_map(&tk, a.k_pool, 2, dims, strides, box)) return cudaErrorInvalidValue;
+        if (!make_map(&tv, a.v_pool, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    PrefillParams P;
+    P.block_tables = a.block_tables;
+    P.context_lens = a.context_lens;
+    P.qsl = a.query_start_loc;
+    P.out = a.out;
+    P.err = a.err;
+    P.num_blocks = a.num_blocks;
+    P.hkv = a.num_kv_heads;
+    P.hq = a.num_q_heads;
+    P.num_seqs = a.num_seqs;
+    P.max_blocks = a.max_blocks_per_seq;
+    P.ctx_cap = static_cast<int32_t>(
+        std::min<int64_t>(a.max_context_len, static_cast<int64_t>(a.max_blocks_per_seq) * kBlockSize));
+    P.num_tokens = a.num_tokens;
+    P.scale_log2 = a.scale * kLog2e;
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    dim3 grid(static_cast<unsigned>(a.num_tiles), static_cast<unsigned>(a.num_q_heads));
+    prefill_kernel<<<grid, kThreads, SMEM_BYTES, stream>>>(tq, tk, tv, P);
+    return cudaGetLastError();
+}
+
+}  // namespace pkv

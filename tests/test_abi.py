@@ -1,0 +1,92 @@
+"""CPU checks of the C-ABI boundary: the library builds, loads without a GPU,
+exports every call include/pkv.h declares, and the product path contains no
+route to the oracle or to any CPU fallback."""
+import ctypes
+import os
+import re
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pkv.h")
+PKG = os.path.join(ROOT, "paged_kv_cache_291_gb300")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z_0-9]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_cache_291_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_calls():
+    names = declared_functions()
+    for n in ["pkv_cache_write", "pkv_copy_blocks", "pkv_decode_attention", "pkv_decode_workspace_size",
+              "pkv_chunked_prefill_attention", "pkv_prefill_workspace_size", "pkv_get_error", "pkv_status_string"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/pkv.h but not exported"
+
+
+def test_only_pkv_symbols_are_exported(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", lib._name], capture_output=True, text=True).stdout
+    exported = [ln.split()[-1] for ln in out.splitlines() if " T " in ln]
+    extra = [s for s in exported if not s.startswith("pkv_")]
+    assert not extra, f"unexpected exported functions: {extra[:10]}"
+
+
+def test_status_strings_without_gpu(lib):
+    lib.pkv_status_string.restype = ctypes.c_char_p
+    lib.pkv_version.restype = ctypes.c_char_p
+    assert lib.pkv_status_string(0) == b"PKV_OK"
+    assert lib.pkv_status_string(6).startswith(b"PKV_ERR_ALIAS")
+    assert lib.pkv_version().count(b".") == 2
+
+
+def test_binding_status_table_matches_header():
+    import paged_kv_cache_291_gb300 as pkv
+    text = open(HEADER).read()
+    for name, val in re.findall(r"(PKV_(?:OK|ERR_[A-Z]+))\s*=\s*(\d+)", text):
+        assert pkv.STATUS_NAMES[int(val)] == name
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    code = ("import paged_kv_cache_291_gb300 as p; p._LIB_PATH = %r\n"
+            "try:\n    p.load()\nexcept RuntimeError as e:\n    print('RAISED', e)\n") % str(tmp_path / "none.so")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, cwd=ROOT)
+    assert "RAISED" in r.stdout and "not built" in r.stdout
+
+
+def test_product_path_never_touches_the_oracle():
+    offenders = []
+    for dirpath, _, files in os.walk(PKG):
+        if "_build" in dirpath:
+            continue
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                if re.search(r"\boracle\b", text) and re.search(r"import\s+oracle|from\s+oracle|oracle/|liboracle",
+                                                                text):
+                    offenders.append(f)
+    assert not offenders, offenders
+
+
+def test_sources_use_no_closed_copy_calls():
+    pat = re.compile("(cu|cuda)" + "Memcpy" + "(3D)?" + "Batch" + "Async")
+    for dirpath, _, files in os.walk(ROOT):
+        if any(x in dirpath for x in (".git", "_build", "gpurun_out", "_work")):
+            continue
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".c", ".cpp")):
+                assert not pat.search(open(os.path.join(dirpath, f), errors="ignore").read()), f
