@@ -503,29 +503,35 @@ __device__ void run_merger(const DecodeParams& P, uint8_t* smem, const Bars& B, 
             ok = false;
             break;
         }
-        // Combine the consumer warps' states (log-sum-exp).
-        for (int idx = lane; idx < G * D; idx += 32) {
-            const int g = idx / D;
-            const int c = idx - g * D;
-            float M = -INFINITY;
+        // Combine the consumer warps' states (log-sum-exp).  Per q head the
+        // warp weights are computed once: lane w < 8 holds warp w's.
+        const unsigned FULL = 0xffffffffu;
+        const int h0 = d.g * G;
 #pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, ml[(buf * kConsumerWarps + w) * G + g].x);
-            float L = 0.f, O = 0.f;
+        for (int g = 0; g < G; ++g) {
+            const float2 e = (lane < kConsumerWarps) ? ml[(buf * kConsumerWarps + lane) * G + g]
+                                                     : make_float2(-INFINITY, 0.f);
+            const float M = warp_max(e.x);
+            const float wt = (e.x == -INFINITY) ? 0.f : fast_exp2(e.x - M);
+            const float L = warp_sum(e.y * wt);
+            float wts[kConsumerWarps];
 #pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                const float2 e = ml[(buf * kConsumerWarps + w) * G + g];
-                const float wt = (e.x == -INFINITY) ? 0.f : fast_exp2(e.x - M);
-                L = fmaf(e.y, wt, L);
-                O = fmaf(mo[((buf * kConsumerWarps + w) * G + g) * D + c], wt, O);
+            for (int w = 0; w < kConsumerWarps; ++w) wts[w] = __shfl_sync(FULL, wt, w);
+            const int h = h0 + g;
+            const size_t pi = (static_cast<size_t>(d.s) * P.hq + h) * P.max_parts + d.p;
+#pragma unroll
+            for (int c = lane; c < D; c += 32) {
+                float O = 0.f;
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w)
+                    O = fmaf(mo[((buf * kConsumerWarps + w) * G + g) * D + c], wts[w], O);
+                if (d.nparts == 1) {
+                    P.out[(static_cast<size_t>(d.row) * P.hq + h) * D + c] = (L > 0.f) ? O / L : 0.f;
+                } else {
+                    P.part_o[pi * D + c] = O;
+                }
             }
-            const int h = d.g * G + g;
-            if (d.nparts == 1) {
-                P.out[(static_cast<size_t>(d.row) * P.hq + h) * D + c] = (L > 0.f) ? O / L : 0.f;
-            } else {
-                const size_t pi = (static_cast<size_t>(d.s) * P.hq + h) * P.max_parts + d.p;
-                P.part_o[pi * D + c] = O;
-                if (c == 0) P.part_ml[pi] = make_float2(M, L);
-            }
+            if (d.nparts > 1 && lane == 0) P.part_ml[pi] = make_float2(M, L);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&B.mempty[buf]);
@@ -535,25 +541,42 @@ __device__ void run_merger(const DecodeParams& P, uint8_t* smem, const Bars& B, 
             uint32_t ticket = 0;
             uint32_t* ctr = P.counters + static_cast<size_t>(d.s) * P.hkv + d.g;
             if (lane == 0) ticket = atomicAdd(ctr, 1u);
-            ticket = __shfl_sync(0xffffffffu, ticket, 0);
+            ticket = __shfl_sync(FULL, ticket, 0);
             if (ticket == static_cast<uint32_t>(d.nparts - 1)) {
                 // Last partition in: merge all partitions of (s, kv head).
+                // Lanes hold the partitions' weights, 32 at a time; the
+                // partitions' o rows are read with independent loads.
                 __threadfence();
-                for (int idx = lane; idx < G * D; idx += 32) {
-                    const int g = idx / D;
-                    const int c = idx - g * D;
-                    const int h = d.g * G + g;
+#pragma unroll 1
+                for (int g = 0; g < G; ++g) {
+                    const int h = h0 + g;
                     const size_t pb = (static_cast<size_t>(d.s) * P.hq + h) * P.max_parts;
                     float M = -INFINITY;
-                    for (int pp = 0; pp < d.nparts; ++pp) M = fmaxf(M, __ldcg(P.part_ml + pb + pp).x);
-                    float L = 0.f, O = 0.f;
-                    for (int pp = 0; pp < d.nparts; ++pp) {
-                        const float2 e = __ldcg(P.part_ml + pb + pp);
+                    for (int p0 = 0; p0 < d.nparts; p0 += 32)
+                        if (p0 + lane < d.nparts) M = fmaxf(M, __ldcg(P.part_ml + pb + p0 + lane).x);
+                    M = warp_max(M);
+                    float L = 0.f;
+                    float acc[D / 32];
+#pragma unroll
+                    for (int i = 0; i < D / 32; ++i) acc[i] = 0.f;
+                    for (int p0 = 0; p0 < d.nparts; p0 += 32) {
+                        const int pp = p0 + lane;
+                        const float2 e = (pp < d.nparts) ? __ldcg(P.part_ml + pb + pp) : make_float2(-INFINITY, 0.f);
                         const float wt = (e.x == -INFINITY) ? 0.f : fast_exp2(e.x - M);
                         L = fmaf(e.y, wt, L);
-                        O = fmaf(__ldcg(P.part_o + (pb + pp) * D + c), wt, O);
+                        const int cnt = min(32, d.nparts - p0);
+#pragma unroll 4
+                        for (int k = 0; k < cnt; ++k) {
+                            const float wk = __shfl_sync(FULL, wt, k);
+                            const float* orow = P.part_o + (pb + p0 + k) * D;
+#pragma unroll
+                            for (int i = 0; i < D / 32; ++i) acc[i] = fmaf(__ldcg(orow + lane + 32 * i), wk, acc[i]);
+                        }
                     }
-                    P.out[(static_cast<size_t>(d.row) * P.hq + h) * D + c] = (L > 0.f) ? O / L : 0.f;
+                    L = warp_sum(L);
+                    float* out = P.out + (static_cast<size_t>(d.row) * P.hq + h) * D;
+#pragma unroll
+                    for (int i = 0; i < D / 32; ++i) out[lane + 32 * i] = (L > 0.f) ? acc[i] / L : 0.f;
                 }
                 if (lane == 0) atomicExch(ctr, 0u);
             }

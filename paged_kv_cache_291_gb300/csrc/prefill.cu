@@ -20,8 +20,11 @@
 //  * The running maximum is only moved (and O rescaled in TMEM) when it
 //    grows by more than 2^8; the final O / l uses the same reference, so the
 //    result is unchanged while most tiles skip the rescale.
-//  * l sums the bf16-rounded P actually fed to the MMA, so the normalisation
-//    matches the weights applied.
+//  * P goes to the tensor cores as two bf16 matrices, its rounding and the
+//    rounding of the residual (P = P_hi + P_lo to about 2^-17 relative), and
+//    O += P_hi V + P_lo V: a single bf16 P (2^-9 relative) can miss a 2e-3
+//    absolute bound when a few keys carry all the weight.  l sums exactly
+//    the P_hi + P_lo fed to the MMA, so the normalisation matches.
 //  * Keys past the last query position of the tile are masked; V rows past
 //    the context are zeroed in shared memory (a 0 weight times a NaN in an
 //    unused slot would otherwise poison the MMA).
@@ -53,13 +56,15 @@ constexpr int kBoxBytes = kBlockSize * 128;  // one 16-row box of one panel
 constexpr int OFF_Q = 0;
 constexpr int OFF_K = OFF_Q + kTileBytes;          // 2 stages
 constexpr int OFF_V = OFF_K + 2 * kTileBytes;      // 2 stages
-constexpr int OFF_P = OFF_V + 2 * kTileBytes;
-constexpr int OFF_BAR = OFF_P + kTileBytes;
+constexpr int OFF_P = OFF_V + 2 * kTileBytes;      // P rounded to bf16 ("hi")
+constexpr int OFF_P2 = OFF_P + kTileBytes;         // bf16 of the rounding residual ("lo")
+constexpr int OFF_BAR = OFF_P2 + kTileBytes;
 constexpr int NBAR = 13;
 constexpr int OFF_INFO = OFF_BAR + NBAR * 8;       // tile info (ints)
 constexpr int OFF_TMEM = OFF_INFO + 16 * 4;
 constexpr int SMEM_USED = OFF_TMEM + 16;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;       // slack to align the base to 1024 B
+static_assert(SMEM_BYTES <= 232448, "shared memory budget (227 KB)");
 
 constexpr int kSoftmaxWarps = 4;
 constexpr int kLoadWarp = 4;
@@ -270,6 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr uint32_t kIdescPV = tc::idesc_bf16_f32(kTileM, kHeadDim, 0, 1);
         const uint32_t sq = smem_addr(smem + OFF_Q);
         const uint32_t sp = smem_addr(smem + OFF_P);
+        const uint32_t sp2 = smem_addr(smem + OFF_P2);
         auto issue_qk = [&](int j) -> bool {
             const int st = j & 1;
             if (!warp_wait(&bar[B_KFULL + st], (j >> 1) & 1)) return false;
@@ -315,9 +321,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int k = 0; k < kTileN / 16; ++k) {
                     const uint32_t aoff = (k >> 2) * kPanelBytes + (k & 3) * 32;
-                    tc::mma_bf16_ss(tmem + kColO, tc::smem_desc_sw128(sp + aoff, 16, 1024),
-                                    tc::smem_desc_sw128(svb + k * 2048, kPanelBytes, 1024), kIdescPV,
+                    const uint64_t vdesc = tc::smem_desc_sw128(svb + k * 2048, kPanelBytes, 1024);
+                    tc::mma_bf16_ss(tmem + kColO, tc::smem_desc_sw128(sp + aoff, 16, 1024), vdesc, kIdescPV,
                                     (j > 0 || k > 0) ? 1u : 0u);
+                    tc::mma_bf16_ss(tmem + kColO, tc::smem_desc_sw128(sp2 + aoff, 16, 1024), vdesc, kIdescPV, 1u);
                 }
                 tc::mma_commit(&bar[B_ODONE]);
                 tc::mma_commit(&bar[B_VEMPTY + st]);
@@ -332,6 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float m_used = -INFINITY;
         float l = 0.f;
         const uint32_t sp = smem_addr(smem + OFF_P);
+        const uint32_t sp2 = smem_addr(smem + OFF_P2);
         for (int j = 0; j < nt && ok; ++j) {
             if (!warp_wait(&bar[B_SFULL + (j & 1)], (j >> 1) & 1)) { ok = false; break; }
             tc::fence_after_sync();
@@ -377,20 +385,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (need) m_used = mt;
                 }
             }
-            // P = exp2(x - m_used) in bf16, row m of the K-major swizzled tile.
+            // P = exp2(x - m_used) as P_hi + P_lo in bf16, row m of the
+            // K-major swizzled tiles.
 #pragma unroll
             for (int c = 0; c < kTileN / 8; ++c) {
-                uint32_t w[4];
+                uint32_t whi[4], wlo[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const float p0 = fast_exp2(x[8 * c + 2 * i] - m_used);
                     const float p1 = fast_exp2(x[8 * c + 2 * i + 1] - m_used);
-                    w[i] = tc::pack_bf16x2(p0, p1);
-                    l += bf16lo(w[i]) + bf16hi(w[i]);
+                    whi[i] = tc::pack_bf16x2(p0, p1);
+                    const float h0 = bf16lo(whi[i]), h1 = bf16hi(whi[i]);
+                    wlo[i] = tc::pack_bf16x2(p0 - h0, p1 - h1);
+                    l += (h0 + bf16lo(wlo[i])) + (h1 + bf16hi(wlo[i]));
                 }
                 const int panel = c >> 3;
                 const int chunk = (c & 7) ^ (m & 7);
-                tc::sts128(sp + panel * kPanelBytes + m * 128 + chunk * 16, w[0], w[1], w[2], w[3]);
+                const uint32_t off = panel * kPanelBytes + m * 128 + chunk * 16;
+                tc::sts128(sp + off, whi[0], whi[1], whi[2], whi[3]);
+                tc::sts128(sp2 + off, wlo[0], wlo[1], wlo[2], wlo[3]);
             }
             tc::fence_proxy_async_smem();
             tc::fence_before_sync();
