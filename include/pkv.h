@@ -110,7 +110,8 @@ pkv_status pkv_copy_blocks(const pkv_cache_t* cache, const int32_t* src, const i
  * pkv_decode_workspace_size -- bytes of workspace pkv_decode_attention needs
  * (a 256-byte header, one arrival counter per (sequence, kv head) and the
  * split-KV partial results).  Depends on the current device's SM count.
- * partition_blocks: 0 = automatic, else blocks per split-KV partition.
+ * partition_blocks: 0 = automatic, else the number of (sequence, kv head,
+ * 16-token block) units per work range (see pkv_decode_attention).
  * Returns 0 for invalid arguments.
  */
 size_t pkv_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
@@ -139,11 +140,13 @@ size_t pkv_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t 
  *                  256-byte aligned, ZERO-FILLED BEFORE ITS FIRST USE; every
  *                  call leaves it zeroed again.  Calls that run concurrently
  *                  need separate workspaces.
- *   partition_blocks 0 = automatic split-KV partitioning; > 0 forces the
- *                  blocks per partition (the workspace must be sized with the
- *                  same value).
- *   Long contexts are split into partitions whose partial results are merged
- *   with the log-sum-exp rule inside the same launch.
+ *   partition_blocks 0 = automatic; > 0 forces the size of a work range in
+ *                  units (the workspace must be sized with the same value).
+ *   Work is the sequence of units (sequence, kv head, 16-token block) cut
+ *   into equal ranges, one per SM by default; a (sequence, kv head) whose
+ *   blocks straddle ranges is computed as split-KV partitions whose partial
+ *   results are merged with the log-sum-exp rule inside the same launch, in
+ *   a fixed order (results are bitwise reproducible).
  */
 pkv_status pkv_decode_attention(const pkv_cache_t* cache, const void* q, int32_t num_q_heads,
                                 const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* context_lens,

@@ -57,6 +57,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
                      "-Xcompiler", "-fPIC,-fvisibility=hidden", "-I", INCLUDE, "-I", CSRC]
     if ptxas_verbose:
         common += ["-Xptxas", "-v"]
+    common += os.environ.get("PKV_NVCC_FLAGS", "").split()  # extra flags for tuning builds
 
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.basename(src).replace(".cu", ".o"))

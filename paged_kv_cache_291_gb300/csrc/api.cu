@@ -84,19 +84,12 @@ pkv_status check_heads(int32_t hq, int32_t hkv) {
     return PKV_OK;
 }
 
-int32_t max_parts_for(int32_t max_context_len, int32_t part_blocks) {
-    const int64_t nblk = std::max<int64_t>(1, (static_cast<int64_t>(max_context_len) + 15) / 16);
-    return static_cast<int32_t>((nblk + part_blocks - 1) / part_blocks);
-}
-
 // Shared by the decode call and the decode rows of the mixed batch.
 pkv_status plan_decode(int32_t num_seqs, int32_t hq, int32_t hkv, int32_t head_dim, int32_t max_context_len,
-                       int32_t req_part_blocks, int num_sms, int32_t* part_blocks, int32_t* max_parts,
-                       size_t* ws_bytes) {
-    if (num_seqs < 0 || max_context_len < 0 || req_part_blocks < 0) return PKV_ERR_SHAPE;
-    *part_blocks = pkv::plan_part_blocks(num_seqs, hkv, max_context_len, num_sms, req_part_blocks);
-    *max_parts = max_parts_for(max_context_len, *part_blocks);
-    *ws_bytes = pkv::decode_ws_layout(num_seqs, hq, hkv, head_dim, *max_parts).total;
+                       int32_t req_range_units, int num_sms, pkv::DecodePlan* plan, size_t* ws_bytes) {
+    if (num_seqs < 0 || max_context_len < 0 || req_range_units < 0) return PKV_ERR_SHAPE;
+    *plan = pkv::plan_decode_ranges(num_seqs, hkv, max_context_len, num_sms, req_range_units);
+    *ws_bytes = pkv::decode_ws_layout(num_seqs, hq, hkv, head_dim, plan->max_ranges).total;
     return PKV_OK;
 }
 
@@ -181,10 +174,10 @@ PKV_API size_t pkv_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, 
     if (head_dim != 64 && head_dim != 128) return 0;
     DeviceState* dev = nullptr;
     if (current_device(&dev) != PKV_OK) return 0;
-    int32_t pb = 0, mp = 0;
+    pkv::DecodePlan plan;
     size_t bytes = 0;
     if (plan_decode(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len, partition_blocks,
-                    dev->num_sms, &pb, &mp, &bytes) != PKV_OK)
+                    dev->num_sms, &plan, &bytes) != PKV_OK)
         return 0;
     return bytes;
 }
@@ -206,10 +199,10 @@ pkv_status decode_common(const pkv_cache_t* cache, const void* q, int32_t num_q_
     if (!aligned16(q) || !aligned16(out)) return PKV_ERR_ALIGN;
     DeviceState* dev = nullptr;
     if ((st = current_device(&dev)) != PKV_OK) return st;
-    int32_t pb = 0, mp = 0;
+    pkv::DecodePlan plan;
     size_t need = 0;
     if ((st = plan_decode(num_seqs, num_q_heads, cache->num_kv_heads, cache->head_dim, max_context_len,
-                          partition_blocks, dev->num_sms, &pb, &mp, &need)) != PKV_OK)
+                          partition_blocks, dev->num_sms, &plan, &need)) != PKV_OK)
         return st;
     if (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return PKV_ERR_WORKSPACE;
@@ -230,11 +223,8 @@ pkv_status decode_common(const pkv_cache_t* cache, const void* q, int32_t num_q_
     a.num_seqs = num_seqs;
     a.max_blocks_per_seq = max_blocks_per_seq;
     a.max_context_len = max_context_len;
-    a.part_blocks = pb;
-    a.max_parts = mp;
+    a.plan = plan;
     a.scale = scale;
-    const int64_t items_max = static_cast<int64_t>(num_seqs) * cache->num_kv_heads * mp;
-    a.grid = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(dev->num_sms, items_max)));
     cudaError_t e = pkv::launch_decode(a, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PKV_OK : cuda_fail(e);
 }

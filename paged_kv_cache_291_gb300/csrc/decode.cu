@@ -8,15 +8,18 @@
 // step and is memory-bandwidth bound ("Prefill/Decode" section of the
 // inference-engine talk write-up), so the design is about keeping HBM busy:
 //
-//  * Work item = (sequence, kv head, partition of the context).  All G = Hq/Hkv
-//    query heads of a kv head are served by one item, so every K/V byte is
-//    read from HBM once.  Long contexts are cut into partitions (split-KV).
-//  * Persistent grid, one CTA per SM, items handed out by an atomic counter
-//    (the next index is fetched while the current item streams).
+//  * Work is measured in units = (sequence, kv head, 16-token block), all
+//    G = Hq/Hkv query heads of a kv head served together so that every K/V
+//    byte is read from HBM once.  The unit sequence is cut into equal
+//    contiguous ranges, one per CTA of a persistent grid (a stream-K style
+//    split: every CTA gets the same number of blocks whatever the mix of
+//    context lengths).  The part of a (sequence, kv head) pair inside one
+//    range is an item; a pair that straddles ranges is split-KV.
 //  * Warp 8 (producer) walks the block table and streams each (block, kv
 //    head) K slab and V slab -- 16 rows x d bf16, one contiguous 2-4 KB run
-//    each -- into a deep shared-memory ring with 1-D bulk (TMA) copies that
-//    complete on mbarriers, evict-first in L2.
+//    each -- with 1-D bulk (TMA) copies that complete on mbarriers,
+//    evict-first in L2, into a shared-memory ring split into one sub-ring
+//    per consumer warp (each warp consumes its stages strictly in order).
 //  * Warps 0..7 (consumers) take an item's blocks round-robin, starting at
 //    a warp given by the item's global index.  A lane owns 4 dims of a row;
 //    q.K partial dots are summed across the lanes of a row by a
@@ -27,9 +30,10 @@
 //    (NaN included) cannot reach the result.
 //  * Warp 9 (merger) combines the 8 warps' (m, l, o) states of an item with
 //    the log-sum-exp rule, off the consumers' critical path.  For a split
-//    context it stores the partition's (m, l, o) in the workspace; the last
-//    partition to arrive (atomic ticket) merges all of them and writes the
-//    output: one launch, no inter-CTA waiting.
+//    pair it stores the part's (m, l, o) in a per-range workspace slot; the
+//    last part to arrive (atomic ticket) merges all of them in part order
+//    and writes the output: one launch, no inter-CTA waiting, and results
+//    that do not depend on timing.
 //  * Every wait is an mbarrier wait bounded by %globaltimer; on expiry the
 //    CTA records PKV_ERR_TIMEOUT and unwinds.
 #include <cuda_runtime.h>
@@ -45,18 +49,27 @@ namespace pkv {
 
 namespace {
 
-constexpr int kConsumerWarps = 8;
+#ifndef PKV_DECODE_CONSUMER_WARPS
+#define PKV_DECODE_CONSUMER_WARPS 8
+#endif
+constexpr int kConsumerWarps = PKV_DECODE_CONSUMER_WARPS;
+static_assert(kConsumerWarps >= 1 && kConsumerWarps <= 24, "consumer warps");
 constexpr int kProducerWarp = kConsumerWarps;
 constexpr int kMergerWarp = kConsumerWarps + 1;
 constexpr int kThreads = 32 * (kConsumerWarps + 2);
 constexpr int kItemRing = 8;
 constexpr int kMergeBufs = 2;
+constexpr int kMinRangeUnits = 8;  // smallest automatic range (blocks per CTA)
 constexpr float kLog2e = 1.4426950408889634f;
 
+// One item = the part of one (sequence, kv head) pair that falls in one
+// range of units.  When the pair spans several ranges (nparts > 1) each part
+// leaves a partial result in slot `slot` of its range `r`; the pair's first
+// part is range r0, whose slot is slot0, and every later part uses slot 0.
 struct __align__(16) ItemDesc {
-    int32_t s, g, p, nparts;
+    int32_t s, g, r, nparts;
     int32_t n, b0, b1, row;
-    int32_t rot, pad0, pad1, pad2;  // rot: warp that takes the item's first block
+    int32_t rot, slot, r0, slot0;  // rot: warp that takes the item's first block
 };
 
 struct DecodeParams {
@@ -67,12 +80,13 @@ struct DecodeParams {
     const int32_t* context_lens;
     const int32_t* qsl;
     float* out;
-    float2* part_ml;
-    float* part_o;
-    uint32_t* counters;
-    uint32_t* work;  // work[0]: next item, work[1]: CTAs done
+    float2* part_ml;    // [max_ranges][2][G]      (m, l) of a partial result, log2 domain
+    float* part_o;      // [max_ranges][2][G][D]   its unnormalised o
+    uint32_t* counters; // [S][Hkv] arrival tickets of split pairs
     unsigned long long* err;
-    int32_t num_blocks, hkv, hq, num_seqs, max_blocks, ctx_cap, part_blocks, max_parts;
+    int32_t num_blocks, hkv, hq, num_seqs, max_blocks, ctx_cap;
+    int32_t range_units;  // units per range, 0 = automatic
+    int32_t max_ranges;   // ranges the workspace holds
     float scale_log2;
 };
 
@@ -95,7 +109,12 @@ struct Cfg {
     static constexpr int R_ML = R_MO + kMergeBufs * kConsumerWarps * G * D * 4;
     static constexpr int R_BAR = align_up(R_ML + kMergeBufs * kConsumerWarps * G * 8, 8);
     static constexpr int STAGES_FIT = (220 * 1024 - R_BAR - 64 * 8 - 16) / STAGE_BYTES;
-    static constexpr int STAGES = STAGES_FIT < 48 ? STAGES_FIT : 48;
+    // Each consumer warp owns SW consecutive stages that it consumes in
+    // order (an mbarrier parity wait is only exact when the waiter is at
+    // most one phase ahead of the barrier).
+    static constexpr int SW_FIT = STAGES_FIT / kConsumerWarps;
+    static constexpr int SW = SW_FIT < 6 ? SW_FIT : 6;
+    static constexpr int STAGES = SW * kConsumerWarps;
     static constexpr int NBAR = 2 * STAGES + 2 * kItemRing + 2 * kMergeBufs;
     static constexpr int OFF_REST = STAGES * STAGE_BYTES;
     static constexpr int OFF_ITEMQ = OFF_REST + R_ITEMQ;
@@ -106,7 +125,7 @@ struct Cfg {
     static constexpr int OFF_BAR = OFF_REST + R_BAR;
     static constexpr int OFF_FLAG = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_FLAG + 16;
-    static_assert(STAGES >= 8, "ring too shallow");
+    static_assert(SW >= 1, "ring too shallow");
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
     static_assert(NV * RPP == kBlockSize, "rows");
 };
@@ -146,9 +165,11 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[NV], int lane) {
     return v[0];
 }
 
-// Parts of sequence s (0 for rows that are not decode rows) and its context
-// length clamped to what the tables and the workspace can hold.
-__device__ __forceinline__ int seq_parts(const DecodeParams& P, int s, int& n_out, bool report) {
+// Units of work of one kv head of sequence s: one per 16-token block of its
+// context (at least one, so that an empty context still yields its zero
+// output row), 0 for rows that are not decode rows.  The context length is
+// clamped to what the block table can address.
+__device__ __forceinline__ int seq_units(const DecodeParams& P, int s, int& n_out, bool report) {
     const int qlen = P.qsl ? (__ldg(P.qsl + s + 1) - __ldg(P.qsl + s)) : 1;
     if (qlen != 1) {
         n_out = 0;
@@ -160,9 +181,7 @@ __device__ __forceinline__ int seq_parts(const DecodeParams& P, int s, int& n_ou
         n = n < 0 ? 0 : P.ctx_cap;
     }
     n_out = n;
-    if (n == 0) return 1;
-    const int nblk = (n + kBlockSize - 1) / kBlockSize;
-    return (nblk + P.part_blocks - 1) / P.part_blocks;
+    return max(1, (n + kBlockSize - 1) / kBlockSize);
 }
 
 template <int D, int G>
@@ -233,58 +252,58 @@ __device__ void run_producer(const DecodeParams& P, uint8_t* smem, const Bars& B
     using C = Cfg<D, G>;
     ItemDesc* descs = reinterpret_cast<ItemDesc*>(smem + C::OFF_DESC);
     const unsigned FULL = 0xffffffffu;
-    // Total number of items (every CTA computes the same value).
-    int parts_here = 0;
-    for (int s0 = 0; s0 < P.num_seqs; s0 += 32) {
-        const int s = s0 + lane;
-        int n;
-        if (s < P.num_seqs) parts_here += seq_parts(P, s, n, blockIdx.x == 0);
-    }
-    long long total;
-    {
-        int t = parts_here;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(FULL, t, o);
-        total = static_cast<long long>(t) * P.hkv;
-    }
-    // Window of 32 sequences: lane j describes sequence win_s0 + j.
-    int win_s0 = 0, win_base = 0, w_np = 0, w_n = 0, w_incl = 0;
-    auto load_window = [&]() {
+    // Work is the sequence of units (s, kv head, block), sequences in order,
+    // kv heads in order within a sequence, blocks in order within a head.
+    // It is cut into ranges of RU consecutive units; range r goes to CTA
+    // r % grid.  Every CTA derives the same cut from context_lens.
+    //
+    // Window of 32 sequences: lane j describes sequence win_s0 + j with its
+    // units per kv head (w_u), context (w_n) and the inclusive prefix of w_u
+    // over the window (w_incl); win_base = units per kv head before the window.
+    int win_s0 = 0, win_base = 0, w_u = 0, w_n = 0, w_incl = 0;
+    auto load_window = [&](bool report) {
         const int s = win_s0 + lane;
-        w_np = 0;
+        w_u = 0;
         w_n = 0;
-        if (s < P.num_seqs) w_np = seq_parts(P, s, w_n, false);
-        w_incl = w_np;
+        if (s < P.num_seqs) w_u = seq_units(P, s, w_n, report);
+        w_incl = w_u;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int t = __shfl_up_sync(FULL, w_incl, o);
             if (lane >= o) w_incl += t;
         }
     };
-    load_window();
+    load_window(blockIdx.x == 0);
+    long long per_head = __shfl_sync(FULL, w_incl, 31);
+    for (int s0 = 32; s0 < P.num_seqs; s0 += 32) {
+        int n, u = 0;
+        if (s0 + lane < P.num_seqs) u = seq_units(P, s0 + lane, n, blockIdx.x == 0);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) u += __shfl_xor_sync(FULL, u, o);
+        per_head += u;
+    }
+    const long long T = per_head * P.hkv;
+    long long RU = P.range_units;
+    if (RU <= 0) RU = max(static_cast<long long>(kMinRangeUnits), (T + gridDim.x - 1) / gridDim.x);
+    long long R = (T + RU - 1) / RU;
+    if (R > P.max_ranges) {  // cannot happen with a workspace sized by the library
+        record_error(P.err, kErrRange, 0xFFFFFFFEu);
+        R = P.max_ranges;
+    }
+
     const uint64_t policy = l2_policy_evict_first();
-    uint32_t stage_seq = 0;
+    uint32_t given = 0;  // lane w < W: blocks handed to consumer warp w so far
     uint32_t item_seq = 0;
     bool aborted = false;
-    int it = 0;
-    if (lane == 0) it = static_cast<int>(atomicAdd(P.work, 1u));
-    it = __shfl_sync(FULL, it, 0);
-    while (true) {
-        // Fetch the next item index now; it is only needed an item later.
-        int nxt = 0;
-        if (lane == 0 && static_cast<long long>(it) < total) nxt = static_cast<int>(atomicAdd(P.work, 1u));
-        const uint32_t slot = item_seq % kItemRing;
-        if (!mbar_wait_warp(&B.iempty[slot], ((item_seq / kItemRing) & 1) ^ 1)) {
-            aborted = true;
-            break;
-        }
-        int j = -1;
-        if (static_cast<long long>(it) < total) {
-            // Locate the sequence holding item `it` (items are ordered (s, g, p);
-            // a CTA's item numbers only grow, so the window only moves forward).
+    for (long long r = blockIdx.x; r < R && !aborted; r += gridDim.x) {
+        long long pos = r * RU;
+        const long long end = min(T, pos + RU);
+        while (pos < end && !aborted) {
+            // Locate the sequence holding unit `pos` (positions only grow, so
+            // the window only moves forward).
+            int j = -1;
             while (true) {
-                const unsigned hit = __ballot_sync(
-                    FULL, static_cast<long long>(win_base + w_incl) * P.hkv > static_cast<long long>(it));
+                const unsigned hit = __ballot_sync(FULL, static_cast<long long>(win_base + w_incl) * P.hkv > pos);
                 if (hit) {
                     j = __ffs(hit) - 1;
                     break;
@@ -292,62 +311,79 @@ __device__ void run_producer(const DecodeParams& P, uint8_t* smem, const Bars& B
                 if (win_s0 + 32 >= P.num_seqs) break;  // cannot happen for consistent inputs
                 win_base += __shfl_sync(FULL, w_incl, 31);
                 win_s0 += 32;
-                load_window();
+                load_window(false);
             }
-            if (j < 0) record_error(P.err, kErrRange, 0xFFFFFFFFu);
-        }
-        if (j < 0) {  // no more work: end marker
+            if (j < 0) {
+                record_error(P.err, kErrRange, 0xFFFFFFFFu);
+                pos = end;
+                break;
+            }
+            const int s = win_s0 + j;
+            const int u = __shfl_sync(FULL, w_u, j);
+            const int n = __shfl_sync(FULL, w_n, j);
+            const long long seq0 = static_cast<long long>(win_base + __shfl_sync(FULL, w_incl, j) - u) * P.hkv;
+            const int g = static_cast<int>((pos - seq0) / u);
+            const long long P0 = seq0 + static_cast<long long>(g) * u;  // the pair's units: [P0, P0 + u)
+            const long long u1 = min(P0 + u, end);
+            const int nblk = (n + kBlockSize - 1) / kBlockSize;
+            const int b0 = static_cast<int>(pos - P0);
+            const int b1 = min(static_cast<int>(u1 - P0), nblk);
+            const long long r0 = P0 / RU;
+            const int nparts = static_cast<int>((P0 + u - 1) / RU - r0 + 1);
+            const int rot = static_cast<int>(pos % kConsumerWarps);
+            const int row = P.qsl ? __ldg(P.qsl + s) : s;
+            const int32_t* trow = P.block_tables + static_cast<size_t>(s) * P.max_blocks;
+            // First batch of table entries, requested before the descriptor work.
+            int e = 0;
+            if (lane < b1 - b0) e = __ldg(trow + b0 + lane);
+            const uint32_t slot = item_seq % kItemRing;
+            if (!mbar_wait_warp(&B.iempty[slot], ((item_seq / kItemRing) & 1) ^ 1)) {
+                aborted = true;
+                break;
+            }
             if (lane == 0) {
-                descs[slot].s = -1;
-                mbar_arrive(&B.ifull[slot]);
+                ItemDesc d;
+                d.s = s; d.g = g; d.r = static_cast<int>(r); d.nparts = nparts;
+                d.n = n; d.b0 = b0; d.b1 = max(b0, b1); d.row = row;
+                d.rot = rot;
+                d.slot = (P0 <= r * RU) ? 0 : 1;
+                d.r0 = static_cast<int>(r0);
+                d.slot0 = (P0 == r0 * RU) ? 0 : 1;
+                descs[slot] = d;
+                mbar_arrive_expect_tx(&B.ifull[slot], C::QBYTES);
+                const uint8_t* qsrc = P.q + (static_cast<size_t>(row) * P.hq + static_cast<size_t>(g) * G) * D * 2;
+                bulk_g2s(smem + C::OFF_ITEMQ + slot * C::QBYTES, qsrc, C::QBYTES, &B.ifull[slot]);
             }
             __syncwarp();
             ++item_seq;
-            break;
-        }
-        const int s = win_s0 + j;
-        const int np = __shfl_sync(FULL, w_np, j);
-        const int n = __shfl_sync(FULL, w_n, j);
-        const int excl = win_base + __shfl_sync(FULL, w_incl, j) - np;
-        const int local = it - excl * P.hkv;
-        const int g = local / np;
-        const int p = local - g * np;
-        const int nblk = (n + kBlockSize - 1) / kBlockSize;
-        const int b0 = static_cast<int>(static_cast<long long>(p) * nblk / np);
-        const int b1 = static_cast<int>(static_cast<long long>(p + 1) * nblk / np);
-        const int row = P.qsl ? __ldg(P.qsl + s) : s;
-        const int32_t* trow = P.block_tables + static_cast<size_t>(s) * P.max_blocks;
-        // First chunk of table entries, requested before the descriptor work.
-        int e = 0;
-        if (lane < b1 - b0) e = __ldg(trow + b0 + lane);
-        if (lane == 0) {
-            ItemDesc d;
-            d.s = s; d.g = g; d.p = p; d.nparts = np; d.n = n; d.b0 = b0; d.b1 = b1; d.row = row;
-            d.rot = it % kConsumerWarps;
-            d.pad0 = d.pad1 = d.pad2 = 0;
-            descs[slot] = d;
-            mbar_arrive_expect_tx(&B.ifull[slot], C::QBYTES);
-            const uint8_t* qsrc = P.q + (static_cast<size_t>(row) * P.hq + static_cast<size_t>(g) * G) * D * 2;
-            bulk_g2s(smem + C::OFF_ITEMQ + slot * C::QBYTES, qsrc, C::QBYTES, &B.ifull[slot]);
-        }
-        __syncwarp();
-        ++item_seq;
-        // Stream the item's blocks, 32 table entries at a time (the next
-        // chunk's entries are requested before this chunk's copies).
-        for (int base = b0; base < b1 && !aborted; base += 32) {
-            const int cnt = min(32, b1 - base);
-            int e_next = 0;
-            if (base + 32 + lane < b1) e_next = __ldg(trow + base + 32 + lane);
-            if (lane < cnt && (e < 0 || e >= P.num_blocks)) {
-                record_error(P.err, kErrRange, static_cast<uint32_t>(s));
-                e = 0;  // never dereference an invalid id
-            }
-            for (int k = 0; k < cnt; ++k) {
-                const int phys = __shfl_sync(FULL, e, k);
-                const uint32_t st = stage_seq % C::STAGES;
+            // Stream the item's blocks.  Block b goes to consumer warp
+            // w = (b + rot) % W, into stage j % SW of w's sub-ring, where j
+            // counts the blocks w has been given so far (lane w keeps that
+            // count in `given`).  Blocks go out in batches of up to min(32,
+            // STAGES): lane k of a batch waits for its own stage and issues
+            // that block's two copies.  A batch holds at most SW blocks of any
+            // warp, so a lane's stage was last used by a block of an earlier
+            // batch and no lane waits on its own batch.  The next batch's
+            // table entries are requested before this batch's copies.
+            constexpr int kBatch = C::STAGES < 32 ? C::STAGES : 32;
+            for (int base = b0; base < b1; base += kBatch) {
+                const int cnt = min(kBatch, b1 - base);
+                int e_next = 0;
+                if (lane < kBatch && base + kBatch + lane < b1) e_next = __ldg(trow + base + kBatch + lane);
+                const int bl = base - b0 + lane;  // block index within the item
+                const int w = (bl + rot) % kConsumerWarps;
+                const int first_w = (w - rot + kConsumerWarps) % kConsumerWarps;
+                const uint32_t jw = static_cast<uint32_t>(__shfl_sync(FULL, static_cast<int>(given), w)) +
+                                    static_cast<uint32_t>((bl - first_w) / kConsumerWarps);
+                const uint32_t st = static_cast<uint32_t>(w * C::SW) + jw % C::SW;
                 int bad = 0;
-                if (lane == 0) {
-                    if (!mbar_wait(&B.empty[st], ((stage_seq / C::STAGES) & 1) ^ 1)) {
+                if (lane < cnt) {
+                    int phys = e;
+                    if (phys < 0 || phys >= P.num_blocks) {
+                        record_error(P.err, kErrRange, static_cast<uint32_t>(s));
+                        phys = 0;  // never dereference an invalid id
+                    }
+                    if (!mbar_wait(&B.empty[st], ((jw / C::SW) & 1) ^ 1)) {
                         bad = 1;
                     } else {
                         const size_t slab = (static_cast<size_t>(phys) * P.hkv + g) * C::SLAB;
@@ -357,38 +393,53 @@ __device__ void run_producer(const DecodeParams& P, uint8_t* smem, const Bars& B
                         bulk_g2s_hint(dst + C::SLAB, P.v_pool + slab, C::SLAB, &B.full[st], policy);
                     }
                 }
-                if (__shfl_sync(FULL, bad, 0)) {
+                if (__any_sync(FULL, bad)) {
+                    // Let this batch's issued copies land before unwinding.
+                    if (lane < cnt && !bad) mbar_wait(&B.full[st], (jw / C::SW) & 1);
                     aborted = true;
                     break;
                 }
-                ++stage_seq;
+                e = e_next;
             }
-            e = e_next;
+            // Blocks each warp received from this item.
+            if (lane < kConsumerWarps && !aborted) {
+                const int first_w = (lane - rot + kConsumerWarps) % kConsumerWarps;
+                const int nb = b1 - b0;
+                if (first_w < nb)
+                    given += static_cast<uint32_t>((nb - first_w + kConsumerWarps - 1) / kConsumerWarps);
+            }
+            pos = u1;
         }
-        if (aborted) break;
-        it = __shfl_sync(FULL, nxt, 0);
+    }
+    if (!aborted) {  // end marker
+        const uint32_t slot = item_seq % kItemRing;
+        if (mbar_wait_warp(&B.iempty[slot], ((item_seq / kItemRing) & 1) ^ 1)) {
+            if (lane == 0) {
+                descs[slot].s = -1;
+                mbar_arrive(&B.ifull[slot]);
+            }
+            __syncwarp();
+            ++item_seq;
+        } else {
+            aborted = true;
+        }
     }
     if (aborted) {
         *abort_flag = 1;
         record_error(P.err, kErrTimeout, 1u);
-    }
-    // This CTA takes no more items.  The last CTA to get here resets the
-    // counters so the workspace is zero again for the next call.
-    if (lane == 0) {
-        __threadfence();
-        const uint32_t done = atomicAdd(P.work + 1, 1u);
-        if (done == gridDim.x - 1) {
-            atomicExch(P.work, 0u);
-            atomicExch(P.work + 1, 0u);
+        // Never leave with bulk copies still in flight.
+        if (lane < kConsumerWarps) {
+            for (uint32_t k = 0; k < C::SW; ++k) {
+                if (k < given) {
+                    const uint32_t jl = given - 1 - ((given - 1 - k) % C::SW);  // last use of stage k
+                    mbar_wait(&B.full[lane * C::SW + k], (jl / C::SW) & 1);
+                }
+            }
         }
-    }
-    // Never leave with bulk copies still in flight (matters only after a
-    // timeout: normally the consumers have waited on every one).
-    if (aborted && lane == 0) {
-        for (uint32_t st = 0; st < C::STAGES; ++st)
-            if (st < stage_seq) mbar_wait(&B.full[st], ((stage_seq - 1 - st) / C::STAGES) & 1);
-        for (uint32_t sl = 0; sl < kItemRing; ++sl)
-            if (sl < item_seq) mbar_wait(&B.ifull[sl], ((item_seq - 1 - sl) / kItemRing) & 1);
+        if (lane == 0) {
+            for (uint32_t sl = 0; sl < kItemRing; ++sl)
+                if (sl < item_seq) mbar_wait(&B.ifull[sl], ((item_seq - 1 - sl) / kItemRing) & 1);
+        }
     }
 }
 
@@ -402,7 +453,7 @@ __device__ void run_consumer(const DecodeParams& P, uint8_t* smem, const Bars& B
     float2* ml = reinterpret_cast<float2*>(smem + C::OFF_ML);
     const int sub = lane / C::LPR;
     const int cl = lane % C::LPR;
-    uint32_t stage_base = 0, item_seq = 0;
+    uint32_t taken = 0, item_seq = 0;  // taken: blocks this warp consumed so far
     bool ok = true;
     while (ok) {
         const uint32_t slot = item_seq % kItemRing;
@@ -438,9 +489,8 @@ __device__ void run_consumer(const DecodeParams& P, uint8_t* smem, const Bars& B
         // it (results are bitwise reproducible).
         const int first = (warp - d.rot + kConsumerWarps) % kConsumerWarps;
         for (int b = first; b < nb; b += kConsumerWarps) {
-            const uint32_t seqn = stage_base + b;
-            const uint32_t st = seqn % C::STAGES;
-            if (*abort_flag || !mbar_wait_warp(&B.full[st], (seqn / C::STAGES) & 1)) {
+            const uint32_t st = static_cast<uint32_t>(warp * C::SW) + taken % C::SW;
+            if (*abort_flag || !mbar_wait_warp(&B.full[st], (taken / C::SW) & 1)) {
                 ok = false;
                 break;
             }
@@ -449,9 +499,9 @@ __device__ void run_consumer(const DecodeParams& P, uint8_t* smem, const Bars& B
             const uint8_t* kst = smem + st * C::STAGE_BYTES;
             compute_block<D, G>(kst, kst + C::SLAB, valid, qf, m, lsum, o, psm, lane);
             if (lane == 0) mbar_arrive(&B.empty[st]);
+            ++taken;
         }
         if (!ok) break;
-        stage_base += nb;
         // Publish this warp's state for the merger.
         const int buf = item_seq % kMergeBufs;
         if (!mbar_wait_warp(&B.mempty[buf], ((item_seq / kMergeBufs) & 1) ^ 1)) {
@@ -518,7 +568,7 @@ __device__ void run_merger(const DecodeParams& P, uint8_t* smem, const Bars& B, 
 #pragma unroll
             for (int w = 0; w < kConsumerWarps; ++w) wts[w] = __shfl_sync(FULL, wt, w);
             const int h = h0 + g;
-            const size_t pi = (static_cast<size_t>(d.s) * P.hq + h) * P.max_parts + d.p;
+            const size_t pi = (static_cast<size_t>(d.r) * 2 + d.slot) * G + g;  // this part's partial slot
 #pragma unroll
             for (int c = lane; c < D; c += 32) {
                 float O = 0.f;
@@ -550,10 +600,14 @@ __device__ void run_merger(const DecodeParams& P, uint8_t* smem, const Bars& B, 
 #pragma unroll 1
                 for (int g = 0; g < G; ++g) {
                     const int h = h0 + g;
-                    const size_t pb = (static_cast<size_t>(d.s) * P.hq + h) * P.max_parts;
+                    // Part k of the pair lives in range r0 + k, slot slot0 for
+                    // k = 0 and slot 0 after that.
+                    auto part_index = [&](int k) -> size_t {
+                        return (static_cast<size_t>(d.r0 + k) * 2 + (k == 0 ? d.slot0 : 0)) * G + g;
+                    };
                     float M = -INFINITY;
                     for (int p0 = 0; p0 < d.nparts; p0 += 32)
-                        if (p0 + lane < d.nparts) M = fmaxf(M, __ldcg(P.part_ml + pb + p0 + lane).x);
+                        if (p0 + lane < d.nparts) M = fmaxf(M, __ldcg(P.part_ml + part_index(p0 + lane)).x);
                     M = warp_max(M);
                     float L = 0.f;
                     float acc[D / 32];
@@ -561,14 +615,15 @@ __device__ void run_merger(const DecodeParams& P, uint8_t* smem, const Bars& B, 
                     for (int i = 0; i < D / 32; ++i) acc[i] = 0.f;
                     for (int p0 = 0; p0 < d.nparts; p0 += 32) {
                         const int pp = p0 + lane;
-                        const float2 e = (pp < d.nparts) ? __ldcg(P.part_ml + pb + pp) : make_float2(-INFINITY, 0.f);
+                        const float2 e =
+                            (pp < d.nparts) ? __ldcg(P.part_ml + part_index(pp)) : make_float2(-INFINITY, 0.f);
                         const float wt = (e.x == -INFINITY) ? 0.f : fast_exp2(e.x - M);
                         L = fmaf(e.y, wt, L);
                         const int cnt = min(32, d.nparts - p0);
 #pragma unroll 4
                         for (int k = 0; k < cnt; ++k) {
                             const float wk = __shfl_sync(FULL, wt, k);
-                            const float* orow = P.part_o + (pb + p0 + k) * D;
+                            const float* orow = P.part_o + part_index(p0 + k) * D;
 #pragma unroll
                             for (int i = 0; i < D / 32; ++i) acc[i] = fmaf(__ldcg(orow + lane + 32 * i), wk, acc[i]);
                         }
@@ -662,38 +717,42 @@ cudaError_t dispatch_g(const DecodeParams& P, int G, int grid, cudaStream_t stre
 static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 DecodeWsLayout decode_ws_layout(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                                int32_t max_parts) {
+                                int32_t max_ranges) {
+    const size_t G = static_cast<size_t>(num_q_heads / num_kv_heads);
     DecodeWsLayout L;
     L.header = 0;
     L.counters = 256;
     L.part_ml = L.counters + align256(static_cast<size_t>(num_seqs) * num_kv_heads * 4);
-    const size_t nparts = static_cast<size_t>(num_seqs) * num_q_heads * max_parts;
-    L.part_o = L.part_ml + align256(nparts * 8);
-    L.total = L.part_o + align256(nparts * head_dim * 4);
+    const size_t slots = static_cast<size_t>(max_ranges) * 2 * G;
+    L.part_o = L.part_ml + align256(slots * 8);
+    L.total = L.part_o + align256(slots * head_dim * 4);
     return L;
 }
 
-int32_t plan_part_blocks(int32_t num_seqs, int32_t num_kv_heads, int32_t max_context_len, int32_t num_sms,
-                         int32_t req) {
-    const int64_t nblk_max =
-        std::max<int64_t>(1, (static_cast<int64_t>(max_context_len) + kBlockSize - 1) / kBlockSize);
-    if (req > 0) return static_cast<int32_t>(std::min<int64_t>(req, nblk_max));
-    const int64_t pairs = std::max<int64_t>(1, static_cast<int64_t>(num_seqs) * num_kv_heads);
-    // Items of at most 128 blocks (2,048 tokens) so that no single item
-    // dominates the tail of the persistent grid; when there are fewer
-    // (sequence, kv head) pairs than two per SM, split further (down to 8
-    // blocks) so that every SM gets work.
-    int64_t pb = std::min<int64_t>(128, nblk_max);
-    if (pairs < 2LL * num_sms) {
-        const int64_t want = (pairs * nblk_max + 2LL * num_sms - 1) / (2LL * num_sms);
-        pb = std::min<int64_t>(pb, std::max<int64_t>(8, want));
+DecodePlan plan_decode_ranges(int32_t num_seqs, int32_t num_kv_heads, int32_t max_context_len, int32_t num_sms,
+                              int32_t req_range_units) {
+    DecodePlan pl;
+    const int64_t units_max = std::max<int64_t>(1, (static_cast<int64_t>(max_context_len) + kBlockSize - 1) / kBlockSize);
+    const int64_t total_max = std::max<int64_t>(1, static_cast<int64_t>(num_seqs) * num_kv_heads * units_max);
+    if (req_range_units > 0) {
+        // Fixed ranges: CTAs loop over them; the workspace holds them all.
+        pl.range_units = req_range_units;
+        pl.max_ranges = static_cast<int32_t>((total_max + req_range_units - 1) / req_range_units);
+        pl.grid = num_sms;
+    } else {
+        // One range per CTA, at least kMinRangeUnits blocks each.
+        pl.range_units = 0;
+        pl.grid = static_cast<int32_t>(
+            std::max<int64_t>(1, std::min<int64_t>(num_sms, (total_max + kMinRangeUnits - 1) / kMinRangeUnits)));
+        pl.max_ranges = pl.grid;
     }
-    return static_cast<int32_t>(std::max<int64_t>(1, pb));
+    return pl;
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     if (a.num_seqs == 0) return cudaSuccess;
-    const DecodeWsLayout L = decode_ws_layout(a.num_seqs, a.num_q_heads, a.num_kv_heads, a.head_dim, a.max_parts);
+    const DecodeWsLayout L =
+        decode_ws_layout(a.num_seqs, a.num_q_heads, a.num_kv_heads, a.head_dim, a.plan.max_ranges);
     uint8_t* ws = static_cast<uint8_t*>(a.workspace);
     DecodeParams P;
     P.k_pool = static_cast<const uint8_t*>(a.k_pool);
@@ -706,7 +765,6 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     P.part_ml = reinterpret_cast<float2*>(ws + L.part_ml);
     P.part_o = reinterpret_cast<float*>(ws + L.part_o);
     P.counters = reinterpret_cast<uint32_t*>(ws + L.counters);
-    P.work = reinterpret_cast<uint32_t*>(ws + L.header);
     P.err = a.err;
     P.num_blocks = a.num_blocks;
     P.hkv = a.num_kv_heads;
@@ -715,12 +773,12 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     P.max_blocks = a.max_blocks_per_seq;
     P.ctx_cap = static_cast<int32_t>(
         std::min<int64_t>(a.max_context_len, static_cast<int64_t>(a.max_blocks_per_seq) * kBlockSize));
-    P.part_blocks = a.part_blocks;
-    P.max_parts = a.max_parts;
+    P.range_units = a.plan.range_units;
+    P.max_ranges = a.plan.max_ranges;
     P.scale_log2 = a.scale * kLog2e;
     const int G = a.num_q_heads / a.num_kv_heads;
-    if (a.head_dim == 128) return dispatch_g<128>(P, G, a.grid, stream);
-    if (a.head_dim == 64) return dispatch_g<64>(P, G, a.grid, stream);
+    if (a.head_dim == 128) return dispatch_g<128>(P, G, a.plan.grid, stream);
+    if (a.head_dim == 64) return dispatch_g<64>(P, G, a.plan.grid, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -8,6 +8,18 @@
 
 namespace pkv {
 
+// How a decode launch cuts its work: the units (sequence, kv head, 16-token
+// block) are split into ranges of range_units consecutive units (0 = one
+// range per CTA, computed on the device from context_lens).
+struct DecodePlan {
+    int32_t range_units;
+    int32_t max_ranges;  // ranges the workspace must hold
+    int32_t grid;        // persistent CTAs
+};
+
+DecodePlan plan_decode_ranges(int32_t num_seqs, int32_t num_kv_heads, int32_t max_context_len, int32_t num_sms,
+                              int32_t req_range_units);
+
 // Split-KV decode launch description (everything already validated).
 struct DecodeArgs {
     const void* k_pool;
@@ -21,26 +33,20 @@ struct DecodeArgs {
     unsigned long long* err;       // device error word
     int32_t num_blocks, num_kv_heads, num_q_heads, head_dim;
     int32_t num_seqs, max_blocks_per_seq, max_context_len;
-    int32_t part_blocks;           // blocks per split-KV partition (>= 1)
-    int32_t max_parts;             // ceil(ceil(max_context_len/16) / part_blocks), >= 1
+    DecodePlan plan;
     float scale;
-    int32_t grid;                  // persistent CTAs
 };
 
 struct DecodeWsLayout {
-    size_t header;      // offset of the 256-byte header (work / done counters)
-    size_t counters;    // uint32 [S][Hkv]
-    size_t part_ml;     // float2 [S][Hq][max_parts]
-    size_t part_o;      // float [S][Hq][max_parts][d]
+    size_t header;      // 256 reserved bytes
+    size_t counters;    // uint32 [S][Hkv] arrival tickets
+    size_t part_ml;     // float2 [max_ranges][2][G]
+    size_t part_o;      // float [max_ranges][2][G][d]
     size_t total;
 };
 
 DecodeWsLayout decode_ws_layout(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                                int32_t max_parts);
-
-// Blocks per partition chosen for a launch (req > 0 forces it).
-int32_t plan_part_blocks(int32_t num_seqs, int32_t num_kv_heads, int32_t max_context_len, int32_t num_sms,
-                         int32_t req);
+                                int32_t max_ranges);
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 
