@@ -60,7 +60,8 @@ typedef enum pkv_status {
     PKV_ERR_RANGE = 9,       /* (device) block id, slot or context length out of range     */
     PKV_ERR_TIMEOUT = 10,    /* (device) a bounded wait inside a kernel expired             */
     PKV_ERR_CUDA = 11,       /* a CUDA runtime call failed (see pkv_last_cuda_error)        */
-    PKV_ERR_UNSUPPORTED = 12 /* the current device is not compute capability 10.3           */
+    PKV_ERR_UNSUPPORTED = 12, /* the current device is not compute capability 10.3          */
+    PKV_ERR_SCRATCH_LIMIT = 13 /* the problem needs more than the built-in scratch buffer   */
 } pkv_status;
 
 typedef struct pkv_cache {
@@ -189,6 +190,37 @@ pkv_status pkv_chunked_prefill_attention(const pkv_cache_t* cache, const void* q
                                          int32_t num_seqs, const int32_t* block_tables, int32_t max_blocks_per_seq,
                                          int32_t max_context_len, float scale, float* out, void* workspace,
                                          size_t workspace_bytes, void* stream);
+
+/*
+ * pkv_decode_attention_static -- pkv_decode_attention for callers that
+ * cannot allocate device memory.  The pages have no counterpart of this
+ * call; it exists for code that may not call cudaMalloc at the point where
+ * it decodes (host callbacks and other paths where allocation is forbidden,
+ * plug-ins that do not own the process's memory pool, runtimes that freeze
+ * device allocation after start-up).  It allocates nothing: its workspace is
+ * a fixed buffer of pkv_decode_static_scratch_bytes() bytes (4 MiB) that the
+ * library keeps on every GPU that loads it, until the process exits.  The
+ * caller still passes every input and the output, with the meaning they have
+ * in pkv_decode_attention (automatic partitioning).
+ *
+ *   - Returns PKV_ERR_SCRATCH_LIMIT, launching nothing, when the batch needs
+ *     more workspace than the buffer holds (pkv_decode_workspace_size with
+ *     partition_blocks = 0 tells the need).
+ *   - The first call on a device looks up the buffer's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - Each call clears the buffer's counters on `stream` before launching.
+ *   - All calls on a device share the one buffer: calls whose work overlaps
+ *     on the GPU (different streams, no ordering between them) race on it
+ *     and give wrong results.  Order them on one stream, or use
+ *     pkv_decode_attention with separate workspaces.
+ */
+pkv_status pkv_decode_attention_static(const pkv_cache_t* cache, const void* q, int32_t num_q_heads,
+                                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                       const int32_t* context_lens, int32_t num_seqs, int32_t max_context_len,
+                                       float scale, float* out, void* stream);
+
+/* Size in bytes of the built-in scratch buffer pkv_decode_attention_static uses. */
+size_t pkv_decode_static_scratch_bytes(void);
 
 /*
  * pkv_get_error -- synchronise `stream`, then return (and clear) the first

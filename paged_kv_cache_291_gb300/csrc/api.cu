@@ -114,6 +114,8 @@ PKV_API const char* pkv_status_string(pkv_status s) {
         case PKV_ERR_TIMEOUT: return "PKV_ERR_TIMEOUT: a bounded wait inside a kernel expired";
         case PKV_ERR_CUDA: return "PKV_ERR_CUDA: a CUDA runtime call failed";
         case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED: the current device is not compute capability 10.3";
+        case PKV_ERR_SCRATCH_LIMIT:
+            return "PKV_ERR_SCRATCH_LIMIT: the batch needs more workspace than the built-in 4 MiB scratch buffer";
     }
     return "unknown pkv_status";
 }
