@@ -64,8 +64,9 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 // One item = the part of one (sequence, kv head) pair that falls in one
 // range of units.  When the pair spans several ranges (nparts > 1) each part
-// leaves a partial result in slot `slot` of its range `r`; the pair's first
-// part is range r0, whose slot is slot0, and every later part uses slot 0.
+// leaves a partial result in slot `slot` of its range `r`: the pair's first
+// part, in range r0, ends its range and uses slot slot0 = 1; every later
+// part starts its range and uses slot 0.
 struct __align__(16) ItemDesc {
     int32_t s, g, r, nparts;
     int32_t n, b0, b1, row;
@@ -94,7 +95,7 @@ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
 template <int D, int G>
 struct Cfg {
-    static constexpr int LPR = D / 4;                  // lanes per K/V row, 4 dims each
+    static constexpr int LPR = D / 8;                  // lanes per K/V row, 8 dims (16 B) each
     static constexpr int RPP = 32 / LPR;               // rows per warp pass
     static constexpr int NV = kBlockSize / RPP;        // rows per lane per block
     static constexpr int SLAB = kBlockSize * D * 2;    // bytes of one (block, kv head)
@@ -105,7 +106,7 @@ struct Cfg {
     static constexpr int R_ITEMQ = 0;
     static constexpr int R_DESC = R_ITEMQ + kItemRing * QBYTES;
     static constexpr int R_P = R_DESC + kItemRing * (int)sizeof(ItemDesc);
-    static constexpr int R_MO = R_P + kConsumerWarps * G * kBlockSize * 4;
+    static constexpr int R_MO = R_P + kConsumerWarps * G * kBlockSize * 8;  // p stored as (p, p)
     static constexpr int R_ML = R_MO + kMergeBufs * kConsumerWarps * G * D * 4;
     static constexpr int R_BAR = align_up(R_ML + kMergeBufs * kConsumerWarps * G * 8, 8);
     static constexpr int STAGES_FIT = (220 * 1024 - R_BAR - 64 * 8 - 16) / STAGE_BYTES;
@@ -184,10 +185,24 @@ __device__ __forceinline__ int seq_units(const DecodeParams& P, int s, int& n_ou
     return max(1, (n + kBlockSize - 1) / kBlockSize);
 }
 
+__device__ __forceinline__ uint4 lds128(const void* p) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(smem_addr(p)));
+    return v;
+}
+
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t u) { return make_float2(bf16lo(u), bf16hi(u)); }
+
+// One 16-row block for one warp.  Lane (sub, cl) owns dims 8cl..8cl+7 of
+// rows i*RPP + sub.  q.K partial dots use packed fp32x2 FMAs; the row sums
+// come from a transpose-reduce over the LPR lanes of a row; P.V accumulates
+// with packed fp32x2 FMAs.  Rows >= valid are never loaded.
 template <int D, int G>
 __device__ __forceinline__ void compute_block(const uint8_t* kst, const uint8_t* vst, int valid,
-                                              const float (&qf)[G][4], float (&m)[G], float (&lsum)[G],
-                                              float (&o)[G][4], float* psm, int lane) {
+                                              const float2 (&q2)[G][4], float (&m)[G], float (&lsum)[G],
+                                              float2 (&o2)[G][4], float2* psm, int lane) {
     using C = Cfg<D, G>;
     const int sub = lane / C::LPR;
     const int cl = lane % C::LPR;
@@ -198,18 +213,18 @@ __device__ __forceinline__ void compute_block(const uint8_t* kst, const uint8_t*
 #pragma unroll
         for (int i = 0; i < C::NV; ++i) {
             const int row = i * C::RPP + sub;
-            float k0 = 0.f, k1 = 0.f, k2 = 0.f, k3 = 0.f;
-            if (row < valid) {
-                const uint2 u = lds64(kst + row * D * 2 + cl * 8);
-                k0 = bf16lo(u.x);
-                k1 = bf16hi(u.x);
-                k2 = bf16lo(u.y);
-                k3 = bf16hi(u.y);
-            }
+            uint4 u = make_uint4(0u, 0u, 0u, 0u);
+            if (row < valid) u = lds128(kst + row * D * 2 + cl * 16);
+            const float2 k0 = bf16x2_to_float2(u.x), k1 = bf16x2_to_float2(u.y);
+            const float2 k2 = bf16x2_to_float2(u.z), k3 = bf16x2_to_float2(u.w);
 #pragma unroll
-            for (int g = 0; g < C::HG; ++g)
-                acc[g][i] = fmaf(qf[g0 + g][0], k0,
-                                 fmaf(qf[g0 + g][1], k1, fmaf(qf[g0 + g][2], k2, qf[g0 + g][3] * k3)));
+            for (int g = 0; g < C::HG; ++g) {
+                float2 a = __fmul2_rn(q2[g0 + g][0], k0);
+                a = __ffma2_rn(q2[g0 + g][1], k1, a);
+                a = __ffma2_rn(q2[g0 + g][2], k2, a);
+                a = __ffma2_rn(q2[g0 + g][3], k3, a);
+                acc[g][i] = a.x + a.y;
+            }
         }
 #pragma unroll
         for (int g = 0; g < C::HG; ++g) {
@@ -220,10 +235,11 @@ __device__ __forceinline__ void compute_block(const uint8_t* kst, const uint8_t*
             const float alpha = fast_exp2(m[g0 + g] - mn);
             const float p = fast_exp2(sc - mn);
             lsum[g0 + g] = fmaf(lsum[g0 + g], alpha, (lane & 1) ? 0.f : p);
+            const float2 al = make_float2(alpha, alpha);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) o[g0 + g][j] *= alpha;
+            for (int j = 0; j < 4; ++j) o2[g0 + g][j] = __fmul2_rn(o2[g0 + g][j], al);
             m[g0 + g] = mn;
-            if (!(lane & 1)) psm[(g0 + g) * kBlockSize + myrow] = p;
+            if (!(lane & 1)) psm[(g0 + g) * kBlockSize + myrow] = make_float2(p, p);
         }
     }
     __syncwarp();
@@ -231,15 +247,16 @@ __device__ __forceinline__ void compute_block(const uint8_t* kst, const uint8_t*
     for (int i = 0; i < C::NV; ++i) {
         const int row = i * C::RPP + sub;
         if (row < valid) {
-            const uint2 u = lds64(vst + row * D * 2 + cl * 8);
-            const float v0 = bf16lo(u.x), v1 = bf16hi(u.x), v2 = bf16lo(u.y), v3 = bf16hi(u.y);
+            const uint4 u = lds128(vst + row * D * 2 + cl * 16);
+            const float2 v0 = bf16x2_to_float2(u.x), v1 = bf16x2_to_float2(u.y);
+            const float2 v2 = bf16x2_to_float2(u.z), v3 = bf16x2_to_float2(u.w);
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-                const float pg = psm[g * kBlockSize + row];
-                o[g][0] = fmaf(pg, v0, o[g][0]);
-                o[g][1] = fmaf(pg, v1, o[g][1]);
-                o[g][2] = fmaf(pg, v2, o[g][2]);
-                o[g][3] = fmaf(pg, v3, o[g][3]);
+                const float2 pp = psm[g * kBlockSize + row];
+                o2[g][0] = __ffma2_rn(pp, v0, o2[g][0]);
+                o2[g][1] = __ffma2_rn(pp, v1, o2[g][1]);
+                o2[g][2] = __ffma2_rn(pp, v2, o2[g][2]);
+                o2[g][3] = __ffma2_rn(pp, v3, o2[g][3]);
             }
         }
     }
@@ -257,24 +274,38 @@ __device__ void run_producer(const DecodeParams& P, uint8_t* smem, const Bars& B
     // It is cut into ranges of RU consecutive units; range r goes to CTA
     // r % grid.  Every CTA derives the same cut from context_lens.
     //
-    // Window of 32 sequences: lane j describes sequence win_s0 + j with its
-    // units per kv head (w_u), context (w_n) and the inclusive prefix of w_u
-    // over the window (w_incl); win_base = units per kv head before the window.
-    int win_s0 = 0, win_base = 0, w_u = 0, w_n = 0, w_incl = 0;
-    auto load_window = [&](bool report) {
-        const int s = win_s0 + lane;
-        w_u = 0;
-        w_n = 0;
-        if (s < P.num_seqs) w_u = seq_units(P, s, w_n, report);
-        w_incl = w_u;
+    // Window of 32 sequences: lane j describes sequence s0 + j with its units
+    // per kv head (u), context (n) and the inclusive prefix of u over the
+    // window (incl); base = units per kv head before the window.
+    struct Win {
+        int s0, base, u, n, incl;
+    };
+    auto load_window = [&](Win& W, bool report) {
+        const int s = W.s0 + lane;
+        W.u = 0;
+        W.n = 0;
+        if (s < P.num_seqs) W.u = seq_units(P, s, W.n, report);
+        W.incl = W.u;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int t = __shfl_up_sync(FULL, w_incl, o);
-            if (lane >= o) w_incl += t;
+            const int t = __shfl_up_sync(FULL, W.incl, o);
+            if (lane >= o) W.incl += t;
         }
     };
-    load_window(blockIdx.x == 0);
-    long long per_head = __shfl_sync(FULL, w_incl, 31);
+    // Move W forward to the sequence holding unit x; returns its lane or -1.
+    auto locate = [&](Win& W, long long x) -> int {
+        while (true) {
+            const unsigned hit = __ballot_sync(FULL, static_cast<long long>(W.base + W.incl) * P.hkv > x);
+            if (hit) return __ffs(hit) - 1;
+            if (W.s0 + 32 >= P.num_seqs) return -1;  // cannot happen for consistent inputs
+            W.base += __shfl_sync(FULL, W.incl, 31);
+            W.s0 += 32;
+            load_window(W, false);
+        }
+    };
+    Win win{0, 0, 0, 0, 0};
+    load_window(win, blockIdx.x == 0);
+    long long per_head = __shfl_sync(FULL, win.incl, 31);
     for (int s0 = 32; s0 < P.num_seqs; s0 += 32) {
         int n, u = 0;
         if (s0 + lane < P.num_seqs) u = seq_units(P, s0 + lane, n, blockIdx.x == 0);
@@ -295,121 +326,157 @@ __device__ void run_producer(const DecodeParams& P, uint8_t* smem, const Bars& B
     uint32_t given = 0;  // lane w < W: blocks handed to consumer warp w so far
     uint32_t item_seq = 0;
     bool aborted = false;
-    for (long long r = blockIdx.x; r < R && !aborted; r += gridDim.x) {
-        long long pos = r * RU;
-        const long long end = min(T, pos + RU);
-        while (pos < end && !aborted) {
-            // Locate the sequence holding unit `pos` (positions only grow, so
-            // the window only moves forward).
-            int j = -1;
-            while (true) {
-                const unsigned hit = __ballot_sync(FULL, static_cast<long long>(win_base + w_incl) * P.hkv > pos);
-                if (hit) {
-                    j = __ffs(hit) - 1;
-                    break;
+
+    // Emit the item of the pair holding unit `pos` (located in W), clipped to
+    // [pos, hi); returns the unit after it.
+    auto emit_item = [&](Win& W, long long pos, long long hi, long long lo, long long r) -> long long {
+        const int j = locate(W, pos);
+        if (j < 0) {
+            record_error(P.err, kErrRange, 0xFFFFFFFFu);
+            return hi;
+        }
+        const int win_s0 = W.s0, win_base = W.base, w_u = W.u, w_n = W.n, w_incl = W.incl;
+        const long long end = hi;
+        const int s = win_s0 + j;
+        const int u = __shfl_sync(FULL, w_u, j);
+        const int n = __shfl_sync(FULL, w_n, j);
+        const long long seq0 = static_cast<long long>(win_base + __shfl_sync(FULL, w_incl, j) - u) * P.hkv;
+        const int g = static_cast<int>((pos - seq0) / u);
+        const long long P0 = seq0 + static_cast<long long>(g) * u;  // the pair's units: [P0, P0 + u)
+        const long long u1 = min(P0 + u, end);
+        const int nblk = (n + kBlockSize - 1) / kBlockSize;
+        const int b0 = static_cast<int>(pos - P0);
+        const int b1 = min(static_cast<int>(u1 - P0), nblk);
+        const long long r0 = P0 / RU;
+        // Pairs no longer than a range are never split (boundaries snap
+        // around them); longer ones are split at every multiple of RU.
+        const int nparts = (u > RU) ? static_cast<int>((P0 + u - 1) / RU - r0 + 1) : 1;
+        const int rot = static_cast<int>(pos % kConsumerWarps);
+        const int row = P.qsl ? __ldg(P.qsl + s) : s;
+        const int32_t* trow = P.block_tables + static_cast<size_t>(s) * P.max_blocks;
+        // First batch of table entries, requested before the descriptor work.
+        int e = 0;
+        if (lane < b1 - b0) e = __ldg(trow + b0 + lane);
+        const uint32_t slot = item_seq % kItemRing;
+        if (!mbar_wait_warp(&B.iempty[slot], ((item_seq / kItemRing) & 1) ^ 1)) {
+            aborted = true;
+            return hi;
+        }
+        if (lane == 0) {
+            ItemDesc d;
+            d.s = s; d.g = g; d.r = static_cast<int>(r); d.nparts = nparts;
+            d.n = n; d.b0 = b0; d.b1 = max(b0, b1); d.row = row;
+            d.rot = rot;
+            // A split pair's first part ends its range (slot 1); every later
+            // part starts its range (slot 0).
+            d.slot = (nparts > 1 && P0 >= lo) ? 1 : 0;
+            d.r0 = static_cast<int>(r0);
+            d.slot0 = 1;
+            descs[slot] = d;
+            mbar_arrive_expect_tx(&B.ifull[slot], C::QBYTES);
+            const uint8_t* qsrc = P.q + (static_cast<size_t>(row) * P.hq + static_cast<size_t>(g) * G) * D * 2;
+            bulk_g2s(smem + C::OFF_ITEMQ + slot * C::QBYTES, qsrc, C::QBYTES, &B.ifull[slot]);
+        }
+        __syncwarp();
+        ++item_seq;
+        // Stream the item's blocks.  Block b goes to consumer warp
+        // w = (b + rot) % W, into stage j % SW of w's sub-ring, where j
+        // counts the blocks w has been given so far (lane w keeps that
+        // count in `given`).  Blocks go out in batches of up to min(32,
+        // STAGES): lane k of a batch waits for its own stage and issues
+        // that block's two copies.  A batch holds at most SW blocks of any
+        // warp, so a lane's stage was last used by a block of an earlier
+        // batch and no lane waits on its own batch.  The next batch's
+        // table entries are requested before this batch's copies.
+        constexpr int kBatch = C::STAGES < 32 ? C::STAGES : 32;
+        for (int base = b0; base < b1; base += kBatch) {
+            const int cnt = min(kBatch, b1 - base);
+            int e_next = 0;
+            if (lane < kBatch && base + kBatch + lane < b1) e_next = __ldg(trow + base + kBatch + lane);
+            const int bl = base - b0 + lane;  // block index within the item
+            const int w = (bl + rot) % kConsumerWarps;
+            const int first_w = (w - rot + kConsumerWarps) % kConsumerWarps;
+            const uint32_t jw = static_cast<uint32_t>(__shfl_sync(FULL, static_cast<int>(given), w)) +
+                                static_cast<uint32_t>((bl - first_w) / kConsumerWarps);
+            const uint32_t st = static_cast<uint32_t>(w * C::SW) + jw % C::SW;
+            int bad = 0;
+            if (lane < cnt) {
+                int phys = e;
+                if (phys < 0 || phys >= P.num_blocks) {
+                    record_error(P.err, kErrRange, static_cast<uint32_t>(s));
+                    phys = 0;  // never dereference an invalid id
                 }
-                if (win_s0 + 32 >= P.num_seqs) break;  // cannot happen for consistent inputs
-                win_base += __shfl_sync(FULL, w_incl, 31);
-                win_s0 += 32;
-                load_window(false);
+                if (!mbar_wait(&B.empty[st], ((jw / C::SW) & 1) ^ 1)) {
+                    bad = 1;
+                } else {
+                    const size_t slab = (static_cast<size_t>(phys) * P.hkv + g) * C::SLAB;
+                    uint8_t* dst = smem + st * C::STAGE_BYTES;
+                    mbar_arrive_expect_tx(&B.full[st], 2 * C::SLAB);
+                    bulk_g2s_hint(dst, P.k_pool + slab, C::SLAB, &B.full[st], policy);
+                    bulk_g2s_hint(dst + C::SLAB, P.v_pool + slab, C::SLAB, &B.full[st], policy);
+                }
             }
-            if (j < 0) {
-                record_error(P.err, kErrRange, 0xFFFFFFFFu);
-                pos = end;
-                break;
-            }
-            const int s = win_s0 + j;
-            const int u = __shfl_sync(FULL, w_u, j);
-            const int n = __shfl_sync(FULL, w_n, j);
-            const long long seq0 = static_cast<long long>(win_base + __shfl_sync(FULL, w_incl, j) - u) * P.hkv;
-            const int g = static_cast<int>((pos - seq0) / u);
-            const long long P0 = seq0 + static_cast<long long>(g) * u;  // the pair's units: [P0, P0 + u)
-            const long long u1 = min(P0 + u, end);
-            const int nblk = (n + kBlockSize - 1) / kBlockSize;
-            const int b0 = static_cast<int>(pos - P0);
-            const int b1 = min(static_cast<int>(u1 - P0), nblk);
-            const long long r0 = P0 / RU;
-            const int nparts = static_cast<int>((P0 + u - 1) / RU - r0 + 1);
-            const int rot = static_cast<int>(pos % kConsumerWarps);
-            const int row = P.qsl ? __ldg(P.qsl + s) : s;
-            const int32_t* trow = P.block_tables + static_cast<size_t>(s) * P.max_blocks;
-            // First batch of table entries, requested before the descriptor work.
-            int e = 0;
-            if (lane < b1 - b0) e = __ldg(trow + b0 + lane);
-            const uint32_t slot = item_seq % kItemRing;
-            if (!mbar_wait_warp(&B.iempty[slot], ((item_seq / kItemRing) & 1) ^ 1)) {
+            if (__any_sync(FULL, bad)) {
+                // Let this batch's issued copies land before unwinding.
+                if (lane < cnt && !bad) mbar_wait(&B.full[st], (jw / C::SW) & 1);
                 aborted = true;
                 break;
             }
-            if (lane == 0) {
-                ItemDesc d;
-                d.s = s; d.g = g; d.r = static_cast<int>(r); d.nparts = nparts;
-                d.n = n; d.b0 = b0; d.b1 = max(b0, b1); d.row = row;
-                d.rot = rot;
-                d.slot = (P0 <= r * RU) ? 0 : 1;
-                d.r0 = static_cast<int>(r0);
-                d.slot0 = (P0 == r0 * RU) ? 0 : 1;
-                descs[slot] = d;
-                mbar_arrive_expect_tx(&B.ifull[slot], C::QBYTES);
-                const uint8_t* qsrc = P.q + (static_cast<size_t>(row) * P.hq + static_cast<size_t>(g) * G) * D * 2;
-                bulk_g2s(smem + C::OFF_ITEMQ + slot * C::QBYTES, qsrc, C::QBYTES, &B.ifull[slot]);
-            }
-            __syncwarp();
-            ++item_seq;
-            // Stream the item's blocks.  Block b goes to consumer warp
-            // w = (b + rot) % W, into stage j % SW of w's sub-ring, where j
-            // counts the blocks w has been given so far (lane w keeps that
-            // count in `given`).  Blocks go out in batches of up to min(32,
-            // STAGES): lane k of a batch waits for its own stage and issues
-            // that block's two copies.  A batch holds at most SW blocks of any
-            // warp, so a lane's stage was last used by a block of an earlier
-            // batch and no lane waits on its own batch.  The next batch's
-            // table entries are requested before this batch's copies.
-            constexpr int kBatch = C::STAGES < 32 ? C::STAGES : 32;
-            for (int base = b0; base < b1; base += kBatch) {
-                const int cnt = min(kBatch, b1 - base);
-                int e_next = 0;
-                if (lane < kBatch && base + kBatch + lane < b1) e_next = __ldg(trow + base + kBatch + lane);
-                const int bl = base - b0 + lane;  // block index within the item
-                const int w = (bl + rot) % kConsumerWarps;
-                const int first_w = (w - rot + kConsumerWarps) % kConsumerWarps;
-                const uint32_t jw = static_cast<uint32_t>(__shfl_sync(FULL, static_cast<int>(given), w)) +
-                                    static_cast<uint32_t>((bl - first_w) / kConsumerWarps);
-                const uint32_t st = static_cast<uint32_t>(w * C::SW) + jw % C::SW;
-                int bad = 0;
-                if (lane < cnt) {
-                    int phys = e;
-                    if (phys < 0 || phys >= P.num_blocks) {
-                        record_error(P.err, kErrRange, static_cast<uint32_t>(s));
-                        phys = 0;  // never dereference an invalid id
-                    }
-                    if (!mbar_wait(&B.empty[st], ((jw / C::SW) & 1) ^ 1)) {
-                        bad = 1;
-                    } else {
-                        const size_t slab = (static_cast<size_t>(phys) * P.hkv + g) * C::SLAB;
-                        uint8_t* dst = smem + st * C::STAGE_BYTES;
-                        mbar_arrive_expect_tx(&B.full[st], 2 * C::SLAB);
-                        bulk_g2s_hint(dst, P.k_pool + slab, C::SLAB, &B.full[st], policy);
-                        bulk_g2s_hint(dst + C::SLAB, P.v_pool + slab, C::SLAB, &B.full[st], policy);
-                    }
-                }
-                if (__any_sync(FULL, bad)) {
-                    // Let this batch's issued copies land before unwinding.
-                    if (lane < cnt && !bad) mbar_wait(&B.full[st], (jw / C::SW) & 1);
-                    aborted = true;
-                    break;
-                }
-                e = e_next;
-            }
-            // Blocks each warp received from this item.
-            if (lane < kConsumerWarps && !aborted) {
-                const int first_w = (lane - rot + kConsumerWarps) % kConsumerWarps;
-                const int nb = b1 - b0;
-                if (first_w < nb)
-                    given += static_cast<uint32_t>((nb - first_w + kConsumerWarps - 1) / kConsumerWarps);
-            }
-            pos = u1;
+            e = e_next;
         }
+        // Blocks each warp received from this item.
+        if (lane < kConsumerWarps && !aborted) {
+            const int first_w = (lane - rot + kConsumerWarps) % kConsumerWarps;
+            const int nb = b1 - b0;
+            if (first_w < nb)
+                given += static_cast<uint32_t>((nb - first_w + kConsumerWarps - 1) / kConsumerWarps);
+        }
+        return u1;
+    };
+
+    // Range boundaries: nominally r * RU, but a boundary that falls inside a
+    // pair no longer than a range moves to the nearer edge of that pair, so
+    // such pairs are never split; only pairs longer than a range are, and
+    // their inner boundaries stay where they are.
+    auto snap = [&](Win& W, long long b) -> long long {
+        if (b <= 0) return 0;
+        if (b >= T) return T;
+        const int j = locate(W, b);
+        if (j < 0) return b;
+        const int u = __shfl_sync(FULL, W.u, j);
+        const long long seq0 = static_cast<long long>(W.base + __shfl_sync(FULL, W.incl, j) - u) * P.hkv;
+        const long long P0 = seq0 + (b - seq0) / u * u;
+        if (b == P0 || u > RU) return b;
+        return (b - P0 <= P0 + u - b) ? P0 : P0 + u;
+    };
+    for (long long r = blockIdx.x; r < R && !aborted; r += gridDim.x) {
+        const long long lo = snap(win, r * RU);
+        long long hi;
+        {
+            Win tw = win;
+            hi = snap(tw, (r + 1) * RU);
+        }
+        if (lo >= hi) continue;
+        // When the range's last item is the first part of a pair that goes
+        // on into the next range, stream it first: both parts of every split
+        // pair then run at the start of their CTAs, and their merge overlaps
+        // the rest of the work instead of trailing it.
+        long long stop = hi;
+        {
+            Win tw = win;
+            const int j = locate(tw, hi - 1);
+            if (j >= 0) {
+                const int u = __shfl_sync(FULL, tw.u, j);
+                const long long seq0 = static_cast<long long>(tw.base + __shfl_sync(FULL, tw.incl, j) - u) * P.hkv;
+                const long long P0 = seq0 + (hi - 1 - seq0) / u * u;
+                if (P0 > lo && P0 + u > hi) {
+                    emit_item(tw, P0, hi, lo, r);
+                    stop = P0;
+                }
+            }
+        }
+        long long pos = lo;
+        while (pos < stop && !aborted) pos = emit_item(win, pos, stop, lo, r);
     }
     if (!aborted) {  // end marker
         const uint32_t slot = item_seq % kItemRing;
@@ -448,7 +515,7 @@ __device__ void run_consumer(const DecodeParams& P, uint8_t* smem, const Bars& B
                              int warp, int lane) {
     using C = Cfg<D, G>;
     const ItemDesc* descs = reinterpret_cast<const ItemDesc*>(smem + C::OFF_DESC);
-    float* psm = reinterpret_cast<float*>(smem + C::OFF_P) + warp * G * kBlockSize;
+    float2* psm = reinterpret_cast<float2*>(smem + C::OFF_P) + warp * G * kBlockSize;
     float* mo = reinterpret_cast<float*>(smem + C::OFF_MO);
     float2* ml = reinterpret_cast<float2*>(smem + C::OFF_ML);
     const int sub = lane / C::LPR;
@@ -463,23 +530,26 @@ __device__ void run_consumer(const DecodeParams& P, uint8_t* smem, const Bars& B
         }
         const ItemDesc d = descs[slot];
         if (d.s < 0) break;
-        float qf[G][4];
+        float2 q2[G][4];
+        const float2 sc2 = make_float2(P.scale_log2, P.scale_log2);
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-            const uint2 u = lds64(smem + C::OFF_ITEMQ + slot * C::QBYTES + (g * D + cl * 4) * 2);
-            qf[g][0] = bf16lo(u.x) * P.scale_log2;
-            qf[g][1] = bf16hi(u.x) * P.scale_log2;
-            qf[g][2] = bf16lo(u.y) * P.scale_log2;
-            qf[g][3] = bf16hi(u.y) * P.scale_log2;
+            const uint4 u = lds128(smem + C::OFF_ITEMQ + slot * C::QBYTES + (g * D + cl * 8) * 2);
+            q2[g][0] = __fmul2_rn(bf16x2_to_float2(u.x), sc2);
+            q2[g][1] = __fmul2_rn(bf16x2_to_float2(u.y), sc2);
+            q2[g][2] = __fmul2_rn(bf16x2_to_float2(u.z), sc2);
+            q2[g][3] = __fmul2_rn(bf16x2_to_float2(u.w), sc2);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&B.iempty[slot]);
-        float m[G], lsum[G], o[G][4];
+        float m[G], lsum[G];
+        float2 o2[G][4];
 #pragma unroll
         for (int g = 0; g < G; ++g) {
             m[g] = -INFINITY;
             lsum[g] = 0.f;
-            o[g][0] = o[g][1] = o[g][2] = o[g][3] = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) o2[g][j] = make_float2(0.f, 0.f);
         }
         const int nb = d.b1 - d.b0;
         // Block b of the item goes to warp (b + rot) % 8: the rotation comes
@@ -497,7 +567,7 @@ __device__ void run_consumer(const DecodeParams& P, uint8_t* smem, const Bars& B
             const int blk = d.b0 + b;
             const int valid = min(kBlockSize, d.n - blk * kBlockSize);
             const uint8_t* kst = smem + st * C::STAGE_BYTES;
-            compute_block<D, G>(kst, kst + C::SLAB, valid, qf, m, lsum, o, psm, lane);
+            compute_block<D, G>(kst, kst + C::SLAB, valid, q2, m, lsum, o2, psm, lane);
             if (lane == 0) mbar_arrive(&B.empty[st]);
             ++taken;
         }
@@ -511,14 +581,21 @@ __device__ void run_consumer(const DecodeParams& P, uint8_t* smem, const Bars& B
 #pragma unroll
         for (int g = 0; g < G; ++g) {
             const float lt = warp_sum(lsum[g]);
-            if (C::RPP == 2) {
+            // Lanes with the same dims but different rows hold partial o.
 #pragma unroll
-                for (int j = 0; j < 4; ++j) o[g][j] += __shfl_xor_sync(0xffffffffu, o[g][j], 16);
+            for (int off = C::LPR; off < 32; off <<= 1) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    o2[g][j].x += __shfl_xor_sync(0xffffffffu, o2[g][j].x, off);
+                    o2[g][j].y += __shfl_xor_sync(0xffffffffu, o2[g][j].y, off);
+                }
             }
             if (lane == 0) ml[(buf * kConsumerWarps + warp) * G + g] = make_float2(m[g], lt);
-            if (sub == 0)
-                *reinterpret_cast<float4*>(mo + ((buf * kConsumerWarps + warp) * G + g) * D + cl * 4) =
-                    make_float4(o[g][0], o[g][1], o[g][2], o[g][3]);
+            if (sub == 0) {
+                float4* dst = reinterpret_cast<float4*>(mo + ((buf * kConsumerWarps + warp) * G + g) * D + cl * 8);
+                dst[0] = make_float4(o2[g][0].x, o2[g][0].y, o2[g][1].x, o2[g][1].y);
+                dst[1] = make_float4(o2[g][2].x, o2[g][2].y, o2[g][3].x, o2[g][3].y);
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&B.mfull[buf]);
@@ -600,8 +677,8 @@ __device__ void run_merger(const DecodeParams& P, uint8_t* smem, const Bars& B, 
 #pragma unroll 1
                 for (int g = 0; g < G; ++g) {
                     const int h = h0 + g;
-                    // Part k of the pair lives in range r0 + k, slot slot0 for
-                    // k = 0 and slot 0 after that.
+                    // Part k of the pair lives in range r0 + k, in slot slot0
+                    // for k = 0 and slot 0 after that.
                     auto part_index = [&](int k) -> size_t {
                         return (static_cast<size_t>(d.r0 + k) * 2 + (k == 0 ? d.slot0 : 0)) * G + g;
                     };
