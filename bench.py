@@ -36,13 +36,13 @@ if ROOT not in sys.path:
 
 METRIC = "paged decode attention: achieved HBM GB/s vs GB300 peak; sequences/s per layer"
 UNIT = "seqs/s"
-CONFIG_ID = 2
-WORKLOAD = "qwen3-1.7b paged decode: 34 seqs x 640 ctx, 16q/8kv heads, d128, block 16, pool 22048 tokens"
+CONFIG_ID = 2  # the Qwen3-1.7B decode step (34 sequences x 640 tokens)
 
 # DRAM traffic of one decode launch on this workload from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), and the hash of the kernel
 # sources it was taken on; reported only while the sources still match.
-NCU_TRAFFIC = {"bytes": None, "sources_sha": None, "capture": None}
+NCU_TRAFFIC = {"bytes": 91587840, "sources_sha": "fa11fe4caa9cd027",
+               "capture": "profiles/decode_kernel_qwen3_1p7b_decode.md"}
 KERNEL_SOURCES = ["paged_kv_cache_291_gb300/csrc/decode.cu", "paged_kv_cache_291_gb300/csrc/pkv_device.cuh"]
 
 
@@ -152,12 +152,34 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def measured_tensor_peak():
+    """Dense bf16 tensor peak: the measured burst figure (a kernel timed alone)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, cuBLAS burst)"
+    return 1900.0, "fallback"
+
+
+def decode_rows(w):
+    """Indices of the sequences that are decode rows (query_len == 1)."""
+    import numpy as np
+    return np.nonzero(w.query_lens == 1)[0]
+
+
+def prefill_rows(w):
+    import numpy as np
+    return np.nonzero(w.query_lens > 1)[0]
+
+
 def decode_bytes(w) -> int:
     """Algorithmic bytes of one decode launch: Q + gathered K/V (once per kv
-    head) + block-table entries read + fp32 output."""
+    head) + block-table entries read + fp32 output, over the decode rows."""
     hq, hkv, d = w.num_q_heads, w.num_kv_heads, w.head_dim
     total = 0
-    for n in w.context_lens.tolist():
+    for s in decode_rows(w).tolist():
+        n = int(w.context_lens[s])
         total += hq * d * 2                     # q
         total += n * hkv * d * 2 * 2            # K and V rows
         total += -(-n // 16) * 4                # block-table entries
@@ -165,45 +187,91 @@ def decode_bytes(w) -> int:
     return total
 
 
+def prefill_flops(w) -> int:
+    """Algorithmic flops of the prefill rows: causal (query, key) pairs x
+    4 d (q.k and p.v, multiply-add = 2) x q heads."""
+    total = 0
+    for s in prefill_rows(w).tolist():
+        n, ql = int(w.context_lens[s]), int(w.query_lens[s])
+        total += ql * (n - ql) + ql * (ql + 1) // 2
+    return total * 4 * w.head_dim * w.num_q_heads
+
+
 def cache_write_bytes(w) -> int:
     T = w.slot_mapping.shape[0]
     return T * (w.num_kv_heads * w.head_dim * 2 * 2 * 2 + 4)  # read + write of K and V rows, slot ids
+
+
+def subset(w, seqs):
+    """The same step restricted to the sequences `seqs` (their q rows, tables
+    and contexts; the pools are shared)."""
+    import numpy as np
+    seqs = np.asarray(seqs, dtype=np.int64)
+    qsl = w.query_start_loc
+    rows = np.concatenate([np.arange(qsl[s], qsl[s + 1]) for s in seqs]) if len(seqs) else np.zeros(0, np.int64)
+    ql = (qsl[seqs + 1] - qsl[seqs]).astype(np.int32)
+    nqsl = np.zeros(len(seqs) + 1, dtype=np.int32)
+    nqsl[1:] = np.cumsum(ql)
+    return dict(q=np.ascontiguousarray(w.q[rows]), tables=np.ascontiguousarray(w.block_tables[seqs]),
+                ctx=np.ascontiguousarray(w.context_lens[seqs]), qsl=nqsl, decode=bool(np.all(ql == 1)),
+                max_ctx=int(w.context_lens[seqs].max()) if len(seqs) else 0)
 
 
 _ORACLE_POOLS = {}
 
 
 def oracle_step_seconds(w, seqs, threads):
-    """Run the oracle's whole step (cache_write of the new rows, then
-    attention) on the first `seqs` sequences; returns seconds.  The pools are
-    copied once, outside the timing (cache_write is idempotent)."""
+    """Run the oracle's whole step (copy-on-write copies, cache_write of the
+    new rows, then attention) on the sequences `seqs`; returns seconds.  The
+    pools are copied once, outside the timing (the step is idempotent)."""
     import numpy as np
     import oracle
     if id(w) not in _ORACLE_POOLS:
         _ORACLE_POOLS[id(w)] = (w.k_pool.copy(), w.v_pool.copy())
     k, v = _ORACLE_POOLS[id(w)]
-    sm = w.slot_mapping.copy()
-    sm[seqs:] = -1
+    sub = subset(w, seqs)
     t0 = time.perf_counter()
-    oracle.cache_write(k, v, w.k_new, w.v_new, sm)
-    qsl = np.arange(seqs + 1, dtype=np.int32)
-    oracle.paged_attention(k, v, w.q[:seqs], qsl, w.context_lens[:seqs], w.block_tables[:seqs], w.scale,
-                           threads=threads)
+    if w.copy_src is not None:
+        oracle.copy_blocks(k, v, w.copy_src, w.copy_dst)
+    oracle.cache_write(k, v, w.k_new, w.v_new, w.slot_mapping)
+    oracle.paged_attention(k, v, sub["q"], sub["qsl"], sub["ctx"], sub["tables"], w.scale, threads=threads)
     return time.perf_counter() - t0
 
 
+def oracle_sample(w, threads, budget_s):
+    """Sequences per oracle step so that one step takes about budget_s."""
+    B = w.num_seqs
+    n = 1
+    while True:
+        t = oracle_step_seconds(w, list(range(n)), threads)
+        if t > 0.2 * budget_s or n >= B:
+            break
+        n = min(B, n * 4)
+    per_seq = t / n
+    return max(1, min(B, int(budget_s / max(per_seq, 1e-9))))
+
+
 def cpu_baseline(w, budget_s=12.0):
-    """The oracle on the host cores: whole steps repeated for about budget_s."""
+    """The oracle on the host cores, repeated steps for about budget_s."""
     threads = os.cpu_count() or 1
     B = w.num_seqs
-    oracle_step_seconds(w, B, threads)  # warm (compiles/loads the oracle)
+    n = oracle_sample(w, threads, budget_s / 4)
+    seqs = list(range(n))
     reps, spent = 0, 0.0
     while spent < budget_s and reps < 1000:
-        spent += oracle_step_seconds(w, B, threads)
+        spent += oracle_step_seconds(w, seqs, threads)
         reps += 1
-    return {"value": reps * B / spent, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"{reps} full steps (cache_write + attention of all {B} sequences), {spent:.1f} s, "
-                      f"{threads} threads"}
+    what = "all" if n == B else f"the first {n} of"
+    return {"value": reps * n / spent, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{reps} steps over {what} {B} sequences (copy-on-write, cache_write and attention), "
+                      f"{spent:.1f} s, {threads} threads"}
+
+
+def build_workload(config, rank=0, threads=None):
+    import pkv_workloads as W
+    if rank == 0:
+        return W.build_config(config, threads=threads)
+    return W.build_config(config, seed=W.default_seed(config) + 7919 * rank, threads=threads)
 
 
 # ----------------------------------------------------------- reference arm
@@ -212,25 +280,23 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    import pkv_workloads as W
-    w = W.build_config(CONFIG_ID)
+    w = build_workload(args.config)
     threads = os.cpu_count() or 1
     B = w.num_seqs
-    full = oracle_step_seconds(w, B, threads)
-    # bounded per-step sample so that warmup + steps take about a minute
     per_step_budget = 60.0 / max(1, args.steps + args.warmup)
-    seqs = max(1, min(B, int(B * per_step_budget / max(full, 1e-9))))
+    n = oracle_sample(w, threads, per_step_budget)
+    seqs = list(range(n))
     for _ in range(args.warmup):
         oracle_step_seconds(w, seqs, threads)
     t = 0.0
     for _ in range(args.steps):
         t += oracle_step_seconds(w, seqs, threads)
-    value = args.steps * seqs / t
-    sample = f"first {seqs} of {B} sequences per step (cache_write + attention), {threads} threads"
+    value = args.steps * n / t
+    sample = f"first {n} of {B} sequences per step (copy-on-write, cache_write and attention), {threads} threads"
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "sample": sample},
+            "config": {"workload": w.name, "sample": sample},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -244,7 +310,6 @@ def run_ours(args):
     import torch
 
     import paged_kv_cache_291_gb300 as pkv
-    import pkv_workloads as W
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -259,10 +324,11 @@ def run_ours(args):
     dev = torch.device("cuda", torch.cuda.current_device())
     pkv.load()
 
-    # Each rank builds its own batch (weak scaling); seed by rank.
-    base = W.build_config(CONFIG_ID)
-    w = base if rank == 0 else W.build_config(CONFIG_ID, seed=W.default_seed(CONFIG_ID) + 7919 * rank)
-    R = args.replicas
+    # Each rank builds its own batch (weak scaling: sequences are independent
+    # units, every rank owns its own pool, tables and sequences).
+    w = build_workload(args.config, rank)
+    pool_bytes = 2 * w.k_pool.nbytes
+    R = args.replicas or int(min(256, max(2, -(-512 * 2 ** 20 // pool_bytes))))
 
     def td(a):
         x = torch.from_numpy(np.ascontiguousarray(a))
@@ -270,28 +336,47 @@ def run_ours(args):
             x = x.view(torch.int16).view(torch.bfloat16)
         return x.to(dev)
 
+    maxctx, scale = w.max_context_len, w.scale
+    Tq = w.num_tokens
     reps = []
-    for r in range(R):
-        reps.append(dict(k=td(w.k_pool), v=td(w.v_pool), q=td(w.q), kn=td(w.k_new), vn=td(w.v_new),
-                         slots=td(w.slot_mapping), tables=td(w.block_tables), ctx=td(w.context_lens),
-                         out=torch.empty((w.num_seqs, w.num_q_heads, w.head_dim), dtype=torch.float32, device=dev)))
+    for _ in range(R):
+        r = dict(k=td(w.k_pool), v=td(w.v_pool), q=td(w.q), kn=td(w.k_new), vn=td(w.v_new),
+                 slots=td(w.slot_mapping), tables=td(w.block_tables), ctx=td(w.context_lens),
+                 qsl=td(w.query_start_loc),
+                 out=torch.empty((Tq, w.num_q_heads, w.head_dim), dtype=torch.float32, device=dev))
+        if w.copy_src is not None:
+            r["src"], r["dst"] = td(w.copy_src), td(w.copy_dst)
+        reps.append(r)
     pb = args.partition_blocks
-    need = pkv.decode_workspace_size(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim, w.max_context_len, pb)
+    if w.is_decode:
+        need = pkv.decode_workspace_size(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim, maxctx, pb)
+    else:
+        need = pkv.prefill_workspace_size(w.num_seqs, Tq, w.num_q_heads, w.num_kv_heads, w.head_dim, maxctx)
     for r in reps:
         r["ws"] = pkv.new_workspace(need, dev)
     stream = torch.cuda.Stream(device=dev)
-    maxctx, scale = w.max_context_len, w.scale
+    qsl_host = w.query_start_loc
+
+    def attention(r):
+        if w.is_decode:
+            pkv.decode_attention(r["k"], r["v"], r["q"], r["tables"], r["ctx"], maxctx, scale, out=r["out"],
+                                 workspace=r["ws"], partition_blocks=pb, stream=stream)
+        else:
+            pkv.chunked_prefill_attention(r["k"], r["v"], r["q"], r["qsl"], r["ctx"], r["tables"], maxctx, scale,
+                                          out=r["out"], workspace=r["ws"], query_start_loc_host=qsl_host,
+                                          stream=stream)
 
     def step(r):
+        if w.copy_src is not None:
+            pkv.copy_blocks(r["k"], r["v"], r["src"], r["dst"], src_host=w.copy_src, dst_host=w.copy_dst,
+                            stream=stream)
         pkv.cache_write(r["k"], r["v"], r["kn"], r["vn"], r["slots"], stream=stream)
-        pkv.decode_attention(r["k"], r["v"], r["q"], r["tables"], r["ctx"], maxctx, scale, out=r["out"],
-                             workspace=r["ws"], partition_blocks=pb, stream=stream)
+        attention(r)
 
-    def decode_only(r):
-        pkv.decode_attention(r["k"], r["v"], r["q"], r["tables"], r["ctx"], maxctx, scale, out=r["out"],
-                             workspace=r["ws"], partition_blocks=pb, stream=stream)
+    launches_per_step = (1 if w.copy_src is not None else 0) + 1 + (1 if w.is_decode else 0)
+    if not w.is_decode:
+        launches_per_step += (1 if len(decode_rows(w)) else 0) + (1 if len(prefill_rows(w)) else 0)
 
-    # Graphs: one cycle through the R replicas (2R launches / R launches).
     with torch.cuda.stream(stream):
         for r in reps:  # eager once (also loads kernels)
             step(r)
@@ -300,21 +385,15 @@ def run_ours(args):
     if status[0] != 0:
         raise RuntimeError(f"device error during eager step: {status}")
 
-    def capture(fn):
+    def capture(fn, items):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            for r in reps:
-                fn(r)
+            for it in items:
+                fn(it)
         return g
 
-    g_step = capture(step)
-    g_dec = capture(decode_only)
-    g_single = []
-    for r in reps:
-        g1 = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g1, stream=stream):
-            step(r)
-        g_single.append(g1)
+    g_step = capture(step, reps)
+    g_single = [capture(step, [r]) for r in reps]
 
     def run_steps(n):
         cycles, rem = divmod(n, R)
@@ -328,7 +407,6 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize()
 
-    # warmup
     with torch.cuda.stream(stream):
         run_steps(max(args.warmup, 3))
     barrier()
@@ -348,42 +426,70 @@ def run_ours(args):
     step_ms = e0.elapsed_time(e1) / args.steps
     step_ms_max = reduce_max(step_ms, dist)
 
-    # The dominant kernel alone: decode launches replayed back to back.
-    dec_cycles = max(1, args.steps // R)
-    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        g_dec.replay()
-        d0.record(stream)
-        for _ in range(dec_cycles):
-            g_dec.replay()
-        d1.record(stream)
-    barrier()
+    # Kernel-alone timings: decode rows and prefill rows as separate batches
+    # over the same pools, replayed back to back from graphs.
+    def kernel_time(seqs):
+        sub = subset(w, seqs)
+        items = []
+        for r in reps:
+            it = dict(k=r["k"], v=r["v"], q=td(sub["q"]), tables=td(sub["tables"]), ctx=td(sub["ctx"]),
+                      qsl=td(sub["qsl"]), out=torch.empty((sub["q"].shape[0], w.num_q_heads, w.head_dim),
+                                                           dtype=torch.float32, device=dev))
+            if sub["decode"]:
+                n = pkv.decode_workspace_size(len(seqs), w.num_q_heads, w.num_kv_heads, w.head_dim, sub["max_ctx"], pb)
+            else:
+                n = pkv.prefill_workspace_size(len(seqs), sub["q"].shape[0], w.num_q_heads, w.num_kv_heads,
+                                               w.head_dim, sub["max_ctx"])
+            it["ws"] = pkv.new_workspace(n, dev)
+            items.append(it)
+
+        def f(it):
+            if sub["decode"]:
+                pkv.decode_attention(it["k"], it["v"], it["q"], it["tables"], it["ctx"], sub["max_ctx"], scale,
+                                     out=it["out"], workspace=it["ws"], partition_blocks=pb, stream=stream)
+            else:
+                pkv.chunked_prefill_attention(it["k"], it["v"], it["q"], it["qsl"], it["ctx"], it["tables"],
+                                              sub["max_ctx"], scale, out=it["out"], workspace=it["ws"],
+                                              query_start_loc_host=sub["qsl"], stream=stream)
+        with torch.cuda.stream(stream):
+            for it in items:
+                f(it)
+        stream.synchronize()
+        g = capture(f, items)
+        cycles = max(1, min(args.steps // R, 2000))
+        d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            g.replay()
+            d0.record(stream)
+            for _ in range(cycles):
+                g.replay()
+            d1.record(stream)
+        barrier()
+        return d0.elapsed_time(d1) / (cycles * R)
+
+    dec_ms = kernel_time(decode_rows(w)) if len(decode_rows(w)) else None
+    pre_ms = kernel_time(prefill_rows(w)) if len(prefill_rows(w)) else None
     if clocks:
         clocks.stop()
-    dec_ms = d0.elapsed_time(d1) / (dec_cycles * R)
     st = pkv.get_error(stream)
     if st[0] != 0:
         raise RuntimeError(f"device error during timing: {st}")
 
     # End to end through the public API with pinned host buffers.
     e2e_steps = min(args.steps, args.e2e_steps)
-    host_in = dict(q=torch.from_numpy(w.q.view(np.int16)).pin_memory(),
-                   kn=torch.from_numpy(w.k_new.view(np.int16)).pin_memory(),
-                   vn=torch.from_numpy(w.v_new.view(np.int16)).pin_memory(),
-                   slots=torch.from_numpy(w.slot_mapping).pin_memory(),
-                   tables=torch.from_numpy(w.block_tables).pin_memory(),
-                   ctx=torch.from_numpy(w.context_lens).pin_memory())
-    host_out = torch.empty((w.num_seqs, w.num_q_heads, w.head_dim), dtype=torch.float32).pin_memory()
+    host_in = dict(q=w.q.view(np.int16), kn=w.k_new.view(np.int16), vn=w.v_new.view(np.int16),
+                   slots=w.slot_mapping, tables=w.block_tables, ctx=w.context_lens, qsl=w.query_start_loc)
+    if w.copy_src is not None:
+        host_in.update(src=w.copy_src, dst=w.copy_dst)
+    host_in = {k: torch.from_numpy(np.ascontiguousarray(a)).pin_memory() for k, a in host_in.items()}
+    host_out = torch.empty((Tq, w.num_q_heads, w.head_dim), dtype=torch.float32).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = host_out.numel() * host_out.element_size()
 
     def e2e_step(r):
-        r["q"].view(torch.int16).copy_(host_in["q"], non_blocking=True)
-        r["kn"].view(torch.int16).copy_(host_in["kn"], non_blocking=True)
-        r["vn"].view(torch.int16).copy_(host_in["vn"], non_blocking=True)
-        r["slots"].copy_(host_in["slots"], non_blocking=True)
-        r["tables"].copy_(host_in["tables"], non_blocking=True)
-        r["ctx"].copy_(host_in["ctx"], non_blocking=True)
+        for key, t in host_in.items():
+            dst = r[key].view(torch.int16) if r[key].dtype == torch.bfloat16 else r[key]
+            dst.copy_(t, non_blocking=True)
         step(r)
         host_out.copy_(r["out"], non_blocking=True)
 
@@ -406,12 +512,9 @@ def run_ours(args):
         return 0
 
     B = w.num_seqs
-    peak, peak_kind = measured_peaks()
+    hbm, hbm_kind = measured_peaks()
+    tflops_peak, tf_kind = measured_tensor_peak()
     dbytes = decode_bytes(w)
-    achieved = dbytes / (dec_ms * 1e-3) / 1e9
-    traffic = NCU_TRAFFIC["bytes"] if NCU_TRAFFIC["sources_sha"] == sources_sha() else None
-    step_bytes = dbytes + cache_write_bytes(w)
-    ck = clocks.summary(t_wall0, t_wall1) if clocks else {}
     line = {
         "metric": METRIC,
         "value": world * B / (step_ms_max * 1e-3),
@@ -425,21 +528,41 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "global_batch": world * B, "seq_len": int(w.context_lens.max()),
+        "config": {"workload": w.name, "global_batch": world * B, "seq_len": int(w.context_lens.max()),
                    "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
-                   "l2": f"{R} rotated input replicas of {step_bytes / 1e6:.0f} MB each (> 129 MB L2)",
+                   "l2": f"{R} rotated input replicas of {pool_bytes / 1e6:.0f} MB pools (> 129 MB L2 in total)",
                    "graph": "CUDA graph per cycle of replicas"},
-        "step_gbs": step_bytes / (step_ms_max * 1e-3) / 1e9,
-        "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": achieved, "peak": peak,
-                     "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy)" if peak_kind == "measured"
-                     else "fallback", "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
-                     "algorithmic_bytes": dbytes, "avg_launch_us": dec_ms * 1e3},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": launches_per_step * args.steps,
         "e2e": {"value": world * B / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps, "ms_per_step": e2e_ms},
-        "clocks": {"sm_mhz": ck.get("sm_mhz"), "sm_max_mhz": ck.get("sm_max_mhz"), "reasons": ck.get("reasons", []),
-                   "samples": ck.get("samples", 0)},
     }
+    decode_roof = None
+    if dec_ms is not None:
+        achieved = dbytes / (dec_ms * 1e-3) / 1e9
+        traffic = (NCU_TRAFFIC["bytes"] if NCU_TRAFFIC["sources_sha"] == sources_sha() and args.config == CONFIG_ID
+                   else None)
+        decode_roof = {"bound": "hbm", "kernel": "decode_kernel", "achieved": achieved, "peak": hbm,
+                       "peak_kind": f"{hbm_kind} (MEASURED_PEAKS.json hbm_gbs, copy)" if hbm_kind == "measured"
+                       else "fallback", "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
+                       "algorithmic_bytes": dbytes, "avg_launch_us": dec_ms * 1e3}
+    prefill_roof = None
+    if pre_ms is not None:
+        fl = prefill_flops(w)
+        achieved = fl / (pre_ms * 1e-3) / 1e12
+        prefill_roof = {"bound": "tensor", "kernel": "prefill_kernel", "achieved": achieved, "peak": tflops_peak,
+                        "peak_kind": tf_kind, "unit": "TFLOP/s", "frac": achieved / tflops_peak, "traffic": None,
+                        "algorithmic_flops": fl, "avg_launch_us": pre_ms * 1e3}
+    if prefill_roof is not None and (decode_roof is None or pre_ms > dec_ms):
+        line["roofline"] = prefill_roof
+        if decode_roof is not None:
+            line["decode_roofline"] = decode_roof
+    else:
+        line["roofline"] = decode_roof
+        if prefill_roof is not None:
+            line["prefill_roofline"] = prefill_roof
+    ck = clocks.summary(t_wall0, t_wall1) if clocks else {}
+    line["clocks"] = {"sm_mhz": ck.get("sm_mhz"), "sm_max_mhz": ck.get("sm_max_mhz"),
+                      "reasons": ck.get("reasons", []), "samples": ck.get("samples", 0)}
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_budget)
     print(json.dumps(line), flush=True)
@@ -454,7 +577,9 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=40000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--replicas", type=int, default=8)
+    ap.add_argument("--replicas", type=int, default=0, help="0 = enough pool replicas to exceed 512 MB")
+    ap.add_argument("--config", type=int, default=CONFIG_ID, choices=[1, 2, 3, 4, 5],
+                    help="workload (default: the Qwen3-1.7B decode step the metric is quoted on)")
     ap.add_argument("--e2e-steps", type=int, default=4000)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -157,11 +157,14 @@ def cache_write(k_pool, v_pool, k_new, v_new, slot_mapping, stream=None) -> None
     _check(st, "pkv_cache_write")
 
 
-def copy_blocks(k_pool, v_pool, src, dst, check_host: bool = True, stream=None) -> None:
+def copy_blocks(k_pool, v_pool, src, dst, check_host: bool = True, src_host=None, dst_host=None,
+                stream=None) -> None:
     """Copy-on-write: pool[dst[i]] <- pool[src[i]] (K and V, whole blocks).
 
-    With ``check_host`` the int32 id lists are also copied to the host so the
-    library can reject aliasing destinations before launching.
+    The library rejects aliasing destinations before launching when it gets
+    host copies of the id lists: pass them as ``src_host``/``dst_host``, or
+    leave ``check_host`` on to have them copied from the device tensors
+    (which synchronises).
     """
     torch = _torch()
     lib = load()
@@ -171,7 +174,12 @@ def copy_blocks(k_pool, v_pool, src, dst, check_host: bool = True, stream=None) 
         raise ValueError("src and dst must have the same length")
     sh = dh = None
     sp = dp = None
-    if check_host:
+    if src_host is not None and dst_host is not None:
+        sh, sp = _host_i32(src_host)
+        dh, dp = _host_i32(dst_host)
+        if sh.shape[0] != n or dh.shape[0] != n:
+            raise ValueError("host id lists must match the device ones")
+    elif check_host:
         sh, sp = _host_i32(src)
         dh, dp = _host_i32(dst)
     st = lib.pkv_copy_blocks(ctypes.byref(c), _dev(src, "src", dtype=torch.int32),

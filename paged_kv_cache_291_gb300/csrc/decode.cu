@@ -316,6 +316,7 @@ __device__ void run_producer(const DecodeParams& P, uint8_t* smem, const Bars& B
     const long long T = per_head * P.hkv;
     long long RU = P.range_units;
     if (RU <= 0) RU = max(static_cast<long long>(kMinRangeUnits), (T + gridDim.x - 1) / gridDim.x);
+    const long long shift_max = max(8LL, RU / 8);  // largest move of a range boundary (see snap)
     long long R = (T + RU - 1) / RU;
     if (R > P.max_ranges) {  // cannot happen with a workspace sized by the library
         record_error(P.err, kErrRange, 0xFFFFFFFEu);
@@ -348,9 +349,18 @@ __device__ void run_producer(const DecodeParams& P, uint8_t* smem, const Bars& B
         const int b0 = static_cast<int>(pos - P0);
         const int b1 = min(static_cast<int>(u1 - P0), nblk);
         const long long r0 = P0 / RU;
-        // Pairs no longer than a range are never split (boundaries snap
-        // around them); longer ones are split at every multiple of RU.
-        const int nparts = (u > RU) ? static_cast<int>((P0 + u - 1) / RU - r0 + 1) : 1;
+        // A pair is split by every boundary strictly inside it: for a pair
+        // longer than a range these are the multiples of RU; a shorter pair
+        // holds at most one, which stays only when it did not snap to an
+        // edge.  The parts are ranges r0, r0 + 1, ... (r0 = P0 / RU).
+        int nparts;
+        if (u > RU) {
+            nparts = static_cast<int>((P0 + u - 1) / RU - r0 + 1);
+        } else {
+            const long long b = (r0 + 1) * RU;  // the only nominal boundary that can fall inside
+            const long long down = b - P0, up = P0 + u - b;
+            nparts = (b > P0 && b < P0 + u && min(down, up) > shift_max) ? 2 : 1;
+        }
         const int rot = static_cast<int>(pos % kConsumerWarps);
         const int row = P.qsl ? __ldg(P.qsl + s) : s;
         const int32_t* trow = P.block_tables + static_cast<size_t>(s) * P.max_blocks;
@@ -434,10 +444,11 @@ __device__ void run_producer(const DecodeParams& P, uint8_t* smem, const Bars& B
         return u1;
     };
 
-    // Range boundaries: nominally r * RU, but a boundary that falls inside a
-    // pair no longer than a range moves to the nearer edge of that pair, so
-    // such pairs are never split; only pairs longer than a range are, and
-    // their inner boundaries stay where they are.
+    // Range boundaries: nominally r * RU.  A boundary that falls within
+    // `shift_max` units of an edge of the pair it cuts moves to that edge
+    // (the pair is not split and the range sizes change by little); other
+    // boundaries split their pair.  Only pairs no longer than a range move:
+    // boundaries inside longer pairs stay at multiples of RU.
     auto snap = [&](Win& W, long long b) -> long long {
         if (b <= 0) return 0;
         if (b >= T) return T;
@@ -447,7 +458,9 @@ __device__ void run_producer(const DecodeParams& P, uint8_t* smem, const Bars& B
         const long long seq0 = static_cast<long long>(W.base + __shfl_sync(FULL, W.incl, j) - u) * P.hkv;
         const long long P0 = seq0 + (b - seq0) / u * u;
         if (b == P0 || u > RU) return b;
-        return (b - P0 <= P0 + u - b) ? P0 : P0 + u;
+        const long long down = b - P0, up = P0 + u - b;
+        if (min(down, up) > shift_max) return b;
+        return (down <= up) ? P0 : P0 + u;
     };
     for (long long r = blockIdx.x; r < R && !aborted; r += gridDim.x) {
         const long long lo = snap(win, r * RU);
