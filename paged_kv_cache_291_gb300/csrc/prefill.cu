@@ -10,29 +10,35 @@
 // a step is a dense contraction ("Prefill/Decode" section of the talk
 // write-up), so these tiles run on the tensor cores:
 //
-//  * CTA = 128 query rows of one q head.  Warp 4 loads the Q tile and the
-//    K/V key tiles (128 keys = 8 paged blocks, each block a 16-row TMA box
-//    with 128-byte swizzle) into a 2-stage ring; warp 5 issues
-//    tcgen05.mma: S = Q K^T into TMEM (double-buffered), then O += P V with
-//    O resident in TMEM; warps 0-3 own one query row each (TMEM lane =
-//    row): causal mask, online softmax in the log2 domain, P rounded to bf16
-//    and written to shared memory in the MMA's K-major swizzled layout.
-//  * The running maximum is only moved (and O rescaled in TMEM) when it
-//    grows by more than 2^8; the final O / l uses the same reference, so the
-//    result is unchanged while most tiles skip the rescale.
-//  * P goes to the tensor cores as two bf16 matrices, its rounding and the
-//    rounding of the residual (P = P_hi + P_lo to about 2^-17 relative), and
-//    O += P_hi V + P_lo V: a single bf16 P (2^-9 relative) can miss a 2e-3
-//    absolute bound when a few keys carry all the weight.  l sums exactly
-//    the P_hi + P_lo fed to the MMA, so the normalisation matches.
+//  * A CTA owns 128 query rows of the two q heads of a GQA group ("units";
+//    one unit when Hq/Hkv is odd).  Both units read the same K/V tiles, so a
+//    tile is loaded once for two heads.  Warp 8 loads the two Q tiles and
+//    the K/V key tiles (128 keys = 8 paged blocks, each block a 16-row TMA
+//    box with 128-byte swizzle) into a 2-stage ring.  Warp 9 issues
+//    tcgen05.mma.  Warps 0-3 and 4-7 are the softmax warpgroups of units 0
+//    and 1 (TMEM lane = query row), so one unit's softmax overlaps the
+//    other unit's MMAs.
+//  * Per unit, TMEM holds S (128 fp32 columns) and O (128 columns).  S =
+//    Q K^T is written there; the softmax reads it, then writes P into the
+//    same columns as bf16, and O += P V takes P straight from TMEM (the A
+//    operand of the MMA) with V from shared memory (MN-major operand).
+//  * P goes in as two bf16 matrices, its rounding and the rounding of the
+//    residual (P = P_hi + P_lo to about 2^-17 relative), and O += P_hi V +
+//    P_lo V: a single bf16 P (2^-9 relative) can miss a 2e-3 absolute bound
+//    when a few keys carry all the weight.  l sums P in fp32 (it differs
+//    from P_hi + P_lo by about 2^-17 relative).
+//  * Online softmax in the log2 domain; the running maximum is only moved
+//    (and O rescaled in TMEM) when it grows by more than 2^8; the final
+//    O / l uses the same reference, so the result is unchanged.
 //  * Keys past the last query position of the tile are masked; V rows past
-//    the context are zeroed in shared memory (a 0 weight times a NaN in an
-//    unused slot would otherwise poison the MMA).
+//    it are zeroed in shared memory (a 0 weight times a NaN in an unused
+//    slot would otherwise poison the MMA).
 //  * Every wait is bounded; TMEM is freed on every exit path.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -45,36 +51,35 @@ namespace pkv {
 
 namespace {
 
-constexpr int kTileM = 128;                  // query rows per CTA
-constexpr int kTileN = 128;                  // keys per key tile
-constexpr int kHeadDim = 128;                // head_dim of the tensor-core path
+constexpr int kTileM = 128;                          // query rows per unit
+constexpr int kTileN = 128;                          // keys per key tile
+constexpr int kHeadDim = 128;                        // head_dim of the tensor-core path
+constexpr int kUnits = 2;                            // q heads per CTA (max)
 constexpr int kBlocksPerTile = kTileN / kBlockSize;  // 8
-constexpr int kPanelBytes = 128 * 128;       // 128 rows x 128 B (64 bf16)
-constexpr int kTileBytes = 2 * kPanelBytes;  // [128][128] bf16 as two swizzled panels
-constexpr int kBoxBytes = kBlockSize * 128;  // one 16-row box of one panel
+constexpr int kPanelBytes = 128 * 128;               // 128 rows x 128 B (64 bf16)
+constexpr int kTileBytes = 2 * kPanelBytes;          // [128][128] bf16 as two swizzled panels
+constexpr int kBoxBytes = kBlockSize * 128;          // one 16-row box of one panel
 
-constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + kTileBytes;          // 2 stages
-constexpr int OFF_V = OFF_K + 2 * kTileBytes;      // 2 stages
-constexpr int OFF_P = OFF_V + 2 * kTileBytes;      // P rounded to bf16 ("hi")
-constexpr int OFF_P2 = OFF_P + kTileBytes;         // bf16 of the rounding residual ("lo")
-constexpr int OFF_BAR = OFF_P2 + kTileBytes;
-constexpr int NBAR = 13;
-constexpr int OFF_INFO = OFF_BAR + NBAR * 8;       // tile info (ints)
+constexpr int OFF_Q = 0;                             // kUnits Q tiles
+constexpr int OFF_K = OFF_Q + kUnits * kTileBytes;   // 2 stages
+constexpr int OFF_V = OFF_K + 2 * kTileBytes;        // 2 stages
+constexpr int OFF_BAR = OFF_V + 2 * kTileBytes;
+constexpr int NBAR = 15;
+constexpr int OFF_INFO = OFF_BAR + NBAR * 8;         // tile info (ints)
 constexpr int OFF_TMEM = OFF_INFO + 16 * 4;
 constexpr int SMEM_USED = OFF_TMEM + 16;
-constexpr int SMEM_BYTES = SMEM_USED + 1024;       // slack to align the base to 1024 B
+constexpr int SMEM_BYTES = SMEM_USED + 1024;         // slack to align the base to 1024 B
 static_assert(SMEM_BYTES <= 232448, "shared memory budget (227 KB)");
 
-constexpr int kSoftmaxWarps = 4;
-constexpr int kLoadWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kThreads = 32 * 6;
+constexpr int kSoftmaxWarps = 4;                     // per unit
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 32 * 10;
 
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 256;  // O accumulator columns; S buffers at 0 and 128
-
-__host__ __device__ constexpr uint32_t col_s(int buf) { return static_cast<uint32_t>(buf) * 128u; }
+// Unit u: S/P at columns [256u, 256u + 128), O at [256u + 128, 256u + 256).
+__host__ __device__ constexpr uint32_t col_s(int u) { return static_cast<uint32_t>(u) * 256u; }
+__host__ __device__ constexpr uint32_t col_o(int u) { return static_cast<uint32_t>(u) * 256u + 128u; }
 
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLog2e = 1.4426950408889634f;
@@ -85,7 +90,7 @@ struct PrefillParams {
     const int32_t* qsl;
     float* out;
     unsigned long long* err;
-    int32_t num_blocks, hkv, hq, num_seqs, max_blocks, ctx_cap, num_tokens;
+    int32_t num_blocks, hkv, hq, num_seqs, max_blocks, ctx_cap, num_tokens, units;
     float scale_log2;
 };
 
@@ -96,9 +101,9 @@ enum {
     B_KEMPTY = 3,  // +stage
     B_VFULL = 5,   // +stage
     B_VEMPTY = 7,  // +stage
-    B_SFULL = 9,   // +buffer
-    B_PFULL = 11,
-    B_ODONE = 12,
+    B_SFULL = 9,   // +unit
+    B_PFULL = 11,  // +unit (4 arrivals)
+    B_ODONE = 13,  // +unit
 };
 
 // Tile info slots (written by warp 0 before the CTA-wide sync).
@@ -113,7 +118,7 @@ __device__ __forceinline__ float fast_exp2(float x) {
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) { return mbar_wait_warp(bar, parity); }
 
 __device__ __forceinline__ uint32_t tmem_lane_addr(uint32_t base, int warp, uint32_t col) {
-    return base + (static_cast<uint32_t>(warp * 32) << 16) + col;
+    return base + (static_cast<uint32_t>((warp & 3) * 32) << 16) + col;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -126,8 +131,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_TMEM);
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-    const int h = blockIdx.y;
-    const int g = h / (P.hq / P.hkv);
+    const int units = P.units;
+    const int h0 = blockIdx.y * units;           // q head of unit 0 (unit 1 is h0 + 1)
+    const int g = h0 / (P.hq / P.hkv);           // the kv head both units read
     const unsigned FULL = 0xffffffffu;
 
     // ---------------------------------------------------------- setup
@@ -176,9 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pmax = pmin + rows - 1;
                 nt = pmax / kTileN + 1;
                 klast = pmax + 1 - (nt - 1) * kTileN;
-                if (bad) {
-                    nt = 0;
-                }
+                if (bad) nt = 0;
             }
             info[I_S] = s;
             info[I_ROW0] = row0;
@@ -192,7 +196,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     if (threadIdx.x == 32 * kMmaWarp) {
-        for (int i = 0; i < NBAR; ++i) mbar_init(&bar[i], i == B_PFULL ? kSoftmaxWarps : 1);
+        for (int i = 0; i < NBAR; ++i)
+            mbar_init(&bar[i], (i == B_PFULL || i == B_PFULL + 1) ? kSoftmaxWarps : 1);
         fence_mbar_init();
     }
     if (warp == kLoadWarp) {
@@ -222,9 +227,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kLoadWarp && nt > 0) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
-            mbar_arrive_expect_tx(&bar[B_QFULL], kTileBytes);
-            tc::tma_load_3d(smem + OFF_Q, &tm_q, 0, h, row0, &bar[B_QFULL]);
-            tc::tma_load_3d(smem + OFF_Q + kPanelBytes, &tm_q, 64, h, row0, &bar[B_QFULL]);
+            mbar_arrive_expect_tx(&bar[B_QFULL], static_cast<uint32_t>(units) * kTileBytes);
+            for (int u = 0; u < units; ++u) {
+                uint8_t* dq = smem + OFF_Q + u * kTileBytes;
+                tc::tma_load_3d(dq, &tm_q, 0, h0 + u, row0, &bar[B_QFULL]);
+                tc::tma_load_3d(dq + kPanelBytes, &tm_q, 64, h0 + u, row0, &bar[B_QFULL]);
+            }
         }
         const int32_t* trow = P.block_tables + static_cast<size_t>(s) * P.max_blocks;
         for (int j = 0; j < nt && ok; ++j) {
@@ -273,33 +281,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------ MMA issuer
         constexpr uint32_t kIdescQK = tc::idesc_bf16_f32(kTileM, kTileN, 0, 0);
         constexpr uint32_t kIdescPV = tc::idesc_bf16_f32(kTileM, kHeadDim, 0, 1);
-        const uint32_t sq = smem_addr(smem + OFF_Q);
-        const uint32_t sp = smem_addr(smem + OFF_P);
-        const uint32_t sp2 = smem_addr(smem + OFF_P2);
-        auto issue_qk = [&](int j) -> bool {
-            const int st = j & 1;
-            if (!warp_wait(&bar[B_KFULL + st], (j >> 1) & 1)) return false;
+        // S_u = Q_u K^T for K tile j into the unit's S/P columns.
+        auto qk = [&](int u, int j) {
+            const uint32_t sq = smem_addr(smem + OFF_Q + u * kTileBytes);
+            const uint32_t sk = smem_addr(smem + OFF_K + (j & 1) * kTileBytes);
+#pragma unroll
+            for (int k = 0; k < kHeadDim / 16; ++k) {
+                const uint32_t off = (k >> 2) * kPanelBytes + (k & 3) * 32;
+                tc::mma_bf16_ss(tmem + col_s(u), tc::smem_desc_sw128(sq + off, 16, 1024),
+                                tc::smem_desc_sw128(sk + off, 16, 1024), kIdescQK, k > 0 ? 1u : 0u);
+            }
+            tc::mma_commit(&bar[B_SFULL + u]);
+        };
+        // O_u += P_u V for V tile j.  Key step k covers keys 16k..16k+15:
+        // P_hi in columns [16k, 16k+8) of the unit's S/P block, P_lo in
+        // [16k+8, 16k+16).
+        auto pv = [&](int u, int j) {
+            const uint32_t svb = smem_addr(smem + OFF_V + (j & 1) * kTileBytes);
+#pragma unroll
+            for (int k = 0; k < kTileN / 16; ++k) {
+                const uint64_t vdesc = tc::smem_desc_sw128(svb + k * 2048, kPanelBytes, 1024);
+                tc::mma_bf16_ts(tmem + col_o(u), tmem + col_s(u) + 16 * k, vdesc, kIdescPV,
+                                (j > 0 || k > 0) ? 1u : 0u);
+                tc::mma_bf16_ts(tmem + col_o(u), tmem + col_s(u) + 16 * k + 8, vdesc, kIdescPV, 1u);
+            }
+            tc::mma_commit(&bar[B_ODONE + u]);
+        };
+        ok = warp_wait(&bar[B_QFULL], 0) && warp_wait(&bar[B_KFULL], 0);
+        if (ok) {
             tc::fence_after_sync();
             if (lane == 0) {
-                const uint32_t sk = smem_addr(smem + OFF_K + st * kTileBytes);
-#pragma unroll
-                for (int k = 0; k < kHeadDim / 16; ++k) {
-                    const uint32_t off = (k >> 2) * kPanelBytes + (k & 3) * 32;
-                    tc::mma_bf16_ss(tmem + col_s(j & 1), tc::smem_desc_sw128(sq + off, 16, 1024),
-                                    tc::smem_desc_sw128(sk + off, 16, 1024), kIdescQK, k > 0 ? 1u : 0u);
-                }
-                tc::mma_commit(&bar[B_SFULL + (j & 1)]);
-                tc::mma_commit(&bar[B_KEMPTY + st]);
+                for (int u = 0; u < units; ++u) qk(u, 0);
+                tc::mma_commit(&bar[B_KEMPTY]);
             }
             __syncwarp();
-            return true;
-        };
-        ok = warp_wait(&bar[B_QFULL], 0);
-        if (ok) ok = issue_qk(0);
-        if (ok && nt > 1) ok = issue_qk(1);
+        }
+        // Per tile, unit by unit: P_u V, then (once P_u has been read) the
+        // next tile's S_u.  Unit 1's softmax then runs while unit 0's MMAs
+        // execute and the other way round.
         for (int j = 0; j < nt && ok; ++j) {
             const int st = j & 1;
-            if (!warp_wait(&bar[B_PFULL], j & 1)) { ok = false; break; }
             if (!warp_wait(&bar[B_VFULL + st], (j >> 1) & 1)) { ok = false; break; }
             uint8_t* sv = smem + OFF_V + st * kTileBytes;
             if (j == nt - 1 && klast < kTileN) {
@@ -315,55 +336,63 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::fence_proxy_async_smem();
                 __syncwarp();
             }
-            tc::fence_after_sync();
-            if (lane == 0) {
-                const uint32_t svb = smem_addr(sv);
-#pragma unroll
-                for (int k = 0; k < kTileN / 16; ++k) {
-                    const uint32_t aoff = (k >> 2) * kPanelBytes + (k & 3) * 32;
-                    const uint64_t vdesc = tc::smem_desc_sw128(svb + k * 2048, kPanelBytes, 1024);
-                    tc::mma_bf16_ss(tmem + kColO, tc::smem_desc_sw128(sp + aoff, 16, 1024), vdesc, kIdescPV,
-                                    (j > 0 || k > 0) ? 1u : 0u);
-                    tc::mma_bf16_ss(tmem + kColO, tc::smem_desc_sw128(sp2 + aoff, 16, 1024), vdesc, kIdescPV, 1u);
+            const bool next = j + 1 < nt;
+            if (next && !warp_wait(&bar[B_KFULL + ((j + 1) & 1)], ((j + 1) >> 1) & 1)) { ok = false; break; }
+            for (int u = 0; u < units && ok; ++u) {
+                if (!warp_wait(&bar[B_PFULL + u], j & 1)) { ok = false; break; }
+                tc::fence_after_sync();
+                if (lane == 0) pv(u, j);
+                __syncwarp();
+                if (next) {
+                    if (!warp_wait(&bar[B_ODONE + u], j & 1)) { ok = false; break; }  // P_u(j) consumed
+                    tc::fence_after_sync();
+                    if (lane == 0) qk(u, j + 1);
+                    __syncwarp();
                 }
-                tc::mma_commit(&bar[B_ODONE]);
+            }
+            if (!ok) break;
+            if (lane == 0) {
                 tc::mma_commit(&bar[B_VEMPTY + st]);
+                if (next) tc::mma_commit(&bar[B_KEMPTY + ((j + 1) & 1)]);
             }
             __syncwarp();
-            if (j + 2 < nt) ok = issue_qk(j + 2);
         }
-    } else if (warp < kSoftmaxWarps) {
+    } else if (warp < kSoftmaxWarps * units) {
         // ------------------------------------------------------ softmax rows
-        const int m = warp * 32 + lane;
+        const int u = warp / kSoftmaxWarps;
+        const int m = (warp % kSoftmaxWarps) * 32 + lane;
+        const int h = h0 + u;
         const int pos = (m < rows) ? pmin + m : pmax;
         float m_used = -INFINITY;
-        float l = 0.f;
-        const uint32_t sp = smem_addr(smem + OFF_P);
-        const uint32_t sp2 = smem_addr(smem + OFF_P2);
+        float2 l2 = make_float2(0.f, 0.f);  // row sum of P (two interleaved halves)
         for (int j = 0; j < nt && ok; ++j) {
-            if (!warp_wait(&bar[B_SFULL + (j & 1)], (j >> 1) & 1)) { ok = false; break; }
+            if (!warp_wait(&bar[B_SFULL + u], j & 1)) { ok = false; break; }
             tc::fence_after_sync();
-            float x[kTileN];
-#pragma unroll
-            for (int c = 0; c < kTileN / 32; ++c) {
-                uint32_t r[32];
-                tc::tmem_ld32(tmem_lane_addr(tmem, warp, col_s(j & 1) + 32 * c), r);
-                tc::tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) x[32 * c + i] = __uint_as_float(r[i]);
-            }
             const int kbase = j * kTileN;
-            float mt = -INFINITY;
+            // Rows grow down the warp, so the tile is fully visible to the
+            // warp when its last key is visible to the warp's first row.
+            const bool full = kbase + kTileN - 1 <= __shfl_sync(FULL, pos, 0);
+            // Pass 1: the tile's row maximum (of the raw scores; the scale is
+            // positive, so it is applied afterwards).
+            float mraw = -INFINITY;
 #pragma unroll
-            for (int n = 0; n < kTileN; ++n) {
-                x[n] = (kbase + n <= pos) ? x[n] * P.scale_log2 : -INFINITY;
-                mt = fmaxf(mt, x[n]);
+            for (int c = 0; c < kTileN / 32; c += 2) {
+                uint32_t r0[32], r1[32];
+                tc::tmem_ld32(tmem_lane_addr(tmem, warp, col_s(u) + 32 * c), r0);
+                tc::tmem_ld32(tmem_lane_addr(tmem, warp, col_s(u) + 32 * c + 32), r1);
+                tc::tmem_wait_ld();
+                if (full) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) mraw = fmaxf(mraw, fmaxf(__uint_as_float(r0[i]), __uint_as_float(r1[i])));
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        if (kbase + 32 * c + i <= pos) mraw = fmaxf(mraw, __uint_as_float(r0[i]));
+                        if (kbase + 32 * c + 32 + i <= pos) mraw = fmaxf(mraw, __uint_as_float(r1[i]));
+                    }
+                }
             }
-            // PV(j-1) must be complete before O is touched or P overwritten.
-            if (j > 0) {
-                if (!warp_wait(&bar[B_ODONE], (j - 1) & 1)) { ok = false; break; }
-                tc::fence_after_sync();
-            }
+            const float mt = mraw * P.scale_log2;
             if (j == 0) {
                 m_used = mt;
             } else {
@@ -373,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int c = 0; c < kHeadDim / 32; ++c) {
                         uint32_t r[32];
-                        const uint32_t ta = tmem_lane_addr(tmem, warp, kColO + 32 * c);
+                        const uint32_t ta = tmem_lane_addr(tmem, warp, col_o(u) + 32 * c);
                         tc::tmem_ld32(ta, r);
                         tc::tmem_wait_ld();
 #pragma unroll
@@ -381,46 +410,61 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc::tmem_st32(ta, r);
                     }
                     tc::tmem_wait_st();
-                    l *= alpha;
+                    l2.x *= alpha;
+                    l2.y *= alpha;
                     if (need) m_used = mt;
                 }
             }
-            // P = exp2(x - m_used) as P_hi + P_lo in bf16, row m of the
-            // K-major swizzled tiles.
+            // Pass 2: P = exp2(scale * s - m_used) as bf16 P_hi + P_lo,
+            // written over the S columns just read: 32 keys -> 16 hi words +
+            // 16 lo words, laid out per 16-key step as [8 hi | 8 lo].
+            const float2 sc2 = make_float2(P.scale_log2, P.scale_log2);
+            const float2 nm2 = make_float2(-m_used, -m_used);
 #pragma unroll
-            for (int c = 0; c < kTileN / 8; ++c) {
-                uint32_t whi[4], wlo[4];
+            for (int c = 0; c < kTileN / 32; ++c) {
+                uint32_t r[32];
+                const uint32_t ta = tmem_lane_addr(tmem, warp, col_s(u) + 32 * c);
+                tc::tmem_ld32(ta, r);
+                tc::tmem_wait_ld();
+                uint32_t w[32];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float p0 = fast_exp2(x[8 * c + 2 * i] - m_used);
-                    const float p1 = fast_exp2(x[8 * c + 2 * i + 1] - m_used);
-                    whi[i] = tc::pack_bf16x2(p0, p1);
-                    const float h0 = bf16lo(whi[i]), h1 = bf16hi(whi[i]);
-                    wlo[i] = tc::pack_bf16x2(p0 - h0, p1 - h1);
-                    l += (h0 + bf16lo(wlo[i])) + (h1 + bf16hi(wlo[i]));
+                for (int t = 0; t < 2; ++t) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int k0 = 32 * c + 16 * t + 2 * i;
+                        float2 x = __ffma2_rn(make_float2(__uint_as_float(r[16 * t + 2 * i]),
+                                                          __uint_as_float(r[16 * t + 2 * i + 1])),
+                                              sc2, nm2);
+                        if (!full) {
+                            if (kbase + k0 > pos) x.x = -INFINITY;
+                            if (kbase + k0 + 1 > pos) x.y = -INFINITY;
+                        }
+                        const float2 p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                        const uint32_t hi = tc::pack_bf16x2(p.x, p.y);
+                        const float2 res = __fadd2_rn(p, make_float2(-bf16lo(hi), -bf16hi(hi)));
+                        w[16 * t + i] = hi;
+                        w[16 * t + 8 + i] = tc::pack_bf16x2(res.x, res.y);
+                        l2 = __fadd2_rn(l2, p);
+                    }
                 }
-                const int panel = c >> 3;
-                const int chunk = (c & 7) ^ (m & 7);
-                const uint32_t off = panel * kPanelBytes + m * 128 + chunk * 16;
-                tc::sts128(sp + off, whi[0], whi[1], whi[2], whi[3]);
-                tc::sts128(sp2 + off, wlo[0], wlo[1], wlo[2], wlo[3]);
+                tc::tmem_st32(ta, w);
             }
-            tc::fence_proxy_async_smem();
+            tc::tmem_wait_st();
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bar[B_PFULL]);
+            if (lane == 0) mbar_arrive(&bar[B_PFULL + u]);
         }
         if (ok && nt > 0) {
-            if (!warp_wait(&bar[B_ODONE], (nt - 1) & 1)) {
+            if (!warp_wait(&bar[B_ODONE + u], (nt - 1) & 1)) {
                 ok = false;
             } else {
                 tc::fence_after_sync();
-                const float inv = 1.f / l;
+                const float inv = 1.f / (l2.x + l2.y);
                 float* orow = P.out + (static_cast<size_t>(row0 + m) * P.hq + h) * kHeadDim;
 #pragma unroll
                 for (int c = 0; c < kHeadDim / 32; ++c) {
                     uint32_t r[32];
-                    tc::tmem_ld32(tmem_lane_addr(tmem, warp, kColO + 32 * c), r);
+                    tc::tmem_ld32(tmem_lane_addr(tmem, warp, col_o(u) + 32 * c), r);
                     tc::tmem_wait_ld();
                     if (m < rows) {
 #pragma unroll
@@ -505,6 +549,8 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
     P.ctx_cap = static_cast<int32_t>(
         std::min<int64_t>(a.max_context_len, static_cast<int64_t>(a.max_blocks_per_seq) * kBlockSize));
     P.num_tokens = a.num_tokens;
+    // Two q heads per CTA when a GQA group holds an even number of them.
+    P.units = ((a.num_q_heads / a.num_kv_heads) % 2 == 0) ? 2 : 1;
     P.scale_log2 = a.scale * kLog2e;
     static bool configured[64] = {};
     int dev = 0;
@@ -514,7 +560,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    dim3 grid(static_cast<unsigned>(a.num_tiles), static_cast<unsigned>(a.num_q_heads));
+    dim3 grid(static_cast<unsigned>(a.num_tiles), static_cast<unsigned>(a.num_q_heads / P.units));
     prefill_kernel<<<grid, kThreads, SMEM_BYTES, stream>>>(tq, tk, tv, P);
     return cudaGetLastError();
 }
