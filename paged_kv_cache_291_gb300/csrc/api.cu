@@ -8,6 +8,7 @@
 #include <algorithm>
 #include <cstdint>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <unordered_set>
@@ -19,6 +20,17 @@
 
 // First device-side error since the last pkv_get_error: (code << 32) | detail.
 __device__ unsigned long long g_pkv_error_word;
+
+namespace pkv {
+// Overlapped launches are on unless PKV_OVERLAP=0 (read once per process).
+bool overlap_enabled() {
+    static const bool on = [] {
+        const char* v = std::getenv("PKV_OVERLAP");
+        return !(v != nullptr && v[0] == '0' && v[1] == '\0');
+    }();
+    return on;
+}
+}  // namespace pkv
 
 namespace {
 

@@ -9,7 +9,8 @@
 //  only when someone must append to it ("Sharing blocks", same section).
 //
 // Both are pure byte movement: 16-byte vector loads and stores, coalesced
-// along head_dim, bit-exact.
+// along head_dim, bit-exact.  Both wait for the previous kernel on the
+// stream before their first access (overlapped launch, pkv_device.cuh).
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -28,6 +29,8 @@ __global__ void __launch_bounds__(256) cache_write_kernel(const uint4* __restric
                                                           int32_t chunks_per_row, int32_t num_kv_heads,
                                                           int64_t num_slots, uint4* __restrict__ k_pool,
                                                           uint4* __restrict__ v_pool, unsigned long long* err) {
+    griddep_launch_dependents();
+    griddep_wait();
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i >= total) return;
     const int64_t row = i / chunks_per_row;          // (token, head)
@@ -56,6 +59,8 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(const int32_t* __restr
                                                           const int32_t* __restrict__ dst, int64_t block_chunks,
                                                           int32_t num_blocks, uint4* __restrict__ k_pool,
                                                           uint4* __restrict__ v_pool, unsigned long long* err) {
+    griddep_launch_dependents();
+    griddep_wait();
     const int32_t pair = blockIdx.y;
     const int32_t s = __ldg(src + pair);
     const int32_t d = __ldg(dst + pair);
@@ -89,11 +94,10 @@ cudaError_t launch_cache_write(const void* k_new, const void* v_new, const int32
     const int64_t total = static_cast<int64_t>(num_tokens) * num_kv_heads * chunks;
     const int threads = 256;
     const int64_t blocks = (total + threads - 1) / threads;
-    cache_write_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-        static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slot_mapping, total, chunks,
-        num_kv_heads, static_cast<int64_t>(num_blocks) * kBlockSize, static_cast<uint4*>(k_pool),
-        static_cast<uint4*>(v_pool), err);
-    return cudaGetLastError();
+    return launch_overlapped(cache_write_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, stream,
+                             static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slot_mapping, total,
+                             chunks, num_kv_heads, static_cast<int64_t>(num_blocks) * kBlockSize,
+                             static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), err);
 }
 
 cudaError_t launch_copy_blocks(const int32_t* src, const int32_t* dst, int32_t num_pairs, void* k_pool,
@@ -105,9 +109,8 @@ cudaError_t launch_copy_blocks(const int32_t* src, const int32_t* dst, int32_t n
     int64_t gx = (2 * block_chunks + threads - 1) / threads;
     if (gx > 64) gx = 64;
     dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(num_pairs));
-    copy_blocks_kernel<<<grid, threads, 0, stream>>>(src, dst, block_chunks, num_blocks,
-                                                     static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), err);
-    return cudaGetLastError();
+    return launch_overlapped(copy_blocks_kernel, grid, dim3(threads), 0, stream, src, dst, block_chunks, num_blocks,
+                             static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), err);
 }
 
 }  // namespace pkv

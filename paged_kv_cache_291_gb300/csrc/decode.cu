@@ -21,10 +21,10 @@
 //    evict-first in L2, into a shared-memory ring split into one sub-ring
 //    per consumer warp (each warp consumes its stages strictly in order).
 //  * Warps 0..7 (consumers) take an item's blocks round-robin, starting at
-//    a warp given by the item's global index.  A lane owns 4 dims of a row;
-//    q.K partial dots are summed across the lanes of a row by a
-//    transpose-reduce (16 values over 32 lanes in 16 shuffles), leaving one
-//    token score per lane pair.  Online
+//    a warp given by the item's global index.  A lane owns 8 dims of a row
+//    (one 16-byte shared load); q.K partial dots are summed across the
+//    lanes of a row by a transpose-reduce, leaving one token score per lane
+//    pair.  Online
 //    softmax in the log2 domain, P.V on CUDA cores in fp32.  Rows past the
 //    context are never loaded, so whatever the unused tail of a block holds
 //    (NaN included) cannot reach the result.
@@ -36,6 +36,10 @@
 //    that do not depend on timing.
 //  * Every wait is an mbarrier wait bounded by %globaltimer; on expiry the
 //    CTA records PKV_ERR_TIMEOUT and unwinds.
+//  * Start-up: the launch may overlap the previous kernel on the stream.
+//    Until that kernel has finished, the CTA only prefetches context_lens,
+//    the block tables and q into L2, so its first reads after the wait hit
+//    L2.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -53,7 +57,8 @@ namespace {
 #define PKV_DECODE_CONSUMER_WARPS 8
 #endif
 constexpr int kConsumerWarps = PKV_DECODE_CONSUMER_WARPS;
-static_assert(kConsumerWarps >= 1 && kConsumerWarps <= 24, "consumer warps");
+static_assert(kConsumerWarps >= 1 && kConsumerWarps <= 32 && (kConsumerWarps & (kConsumerWarps - 1)) == 0,
+              "consumer warps: a power of two up to 32 (the merger reduces over aligned lane groups)");
 constexpr int kProducerWarp = kConsumerWarps;
 constexpr int kMergerWarp = kConsumerWarps + 1;
 constexpr int kThreads = 32 * (kConsumerWarps + 2);
@@ -108,7 +113,8 @@ struct Cfg {
     static constexpr int R_P = R_DESC + kItemRing * (int)sizeof(ItemDesc);
     static constexpr int R_MO = R_P + kConsumerWarps * G * kBlockSize * 8;  // p stored as (p, p)
     static constexpr int R_ML = R_MO + kMergeBufs * kConsumerWarps * G * D * 4;
-    static constexpr int R_BAR = align_up(R_ML + kMergeBufs * kConsumerWarps * G * 8, 8);
+    static constexpr int R_WT = R_ML + kMergeBufs * kConsumerWarps * G * 8;  // merger: [G][W] weights, [G] (M, L)
+    static constexpr int R_BAR = align_up(R_WT + G * kConsumerWarps * 4 + G * 8, 8);
     static constexpr int STAGES_FIT = (220 * 1024 - R_BAR - 64 * 8 - 16) / STAGE_BYTES;
     // Each consumer warp owns SW consecutive stages that it consumes in
     // order (an mbarrier parity wait is only exact when the waiter is at
@@ -123,6 +129,7 @@ struct Cfg {
     static constexpr int OFF_P = OFF_REST + R_P;
     static constexpr int OFF_MO = OFF_REST + R_MO;
     static constexpr int OFF_ML = OFF_REST + R_ML;
+    static constexpr int OFF_WT = OFF_REST + R_WT;
     static constexpr int OFF_BAR = OFF_REST + R_BAR;
     static constexpr int OFF_FLAG = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_FLAG + 16;
@@ -626,6 +633,8 @@ __device__ void run_merger(const DecodeParams& P, uint8_t* smem, const Bars& B, 
     const ItemDesc* descs = reinterpret_cast<const ItemDesc*>(smem + C::OFF_DESC);
     const float* mo = reinterpret_cast<const float*>(smem + C::OFF_MO);
     const float2* ml = reinterpret_cast<const float2*>(smem + C::OFF_ML);
+    float* wsm = reinterpret_cast<float*>(smem + C::OFF_WT);
+    float2* msm = reinterpret_cast<float2*>(smem + C::OFF_WT + G * kConsumerWarps * 4);
     uint32_t item_seq = 0;
     bool ok = true;
     while (true) {
@@ -643,36 +652,63 @@ __device__ void run_merger(const DecodeParams& P, uint8_t* smem, const Bars& B, 
             ok = false;
             break;
         }
-        // Combine the consumer warps' states (log-sum-exp).  Per q head the
-        // warp weights are computed once: lane w < 8 holds warp w's.
+        // Combine the consumer warps' states (log-sum-exp).  First the
+        // weights of all (q head g, warp w) pairs at once: lane g * W + w,
+        // W lanes per head; then each lane combines whole float4 chunks of
+        // the item's G output rows (contiguous in out and in part_o), with
+        // the W chunk loads issued together.
         const unsigned FULL = 0xffffffffu;
-        const int h0 = d.g * G;
+        constexpr int W = kConsumerWarps;
+        constexpr int CH = G * D / 4;
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-            const float2 e = (lane < kConsumerWarps) ? ml[(buf * kConsumerWarps + lane) * G + g]
-                                                     : make_float2(-INFINITY, 0.f);
-            const float M = warp_max(e.x);
+        for (int i0 = 0; i0 < G * W; i0 += 32) {
+            const int i = i0 + lane;
+            const int w = i % W;
+            const float2 e = (i < G * W) ? ml[(buf * W + w) * G + i / W] : make_float2(-INFINITY, 0.f);
+            float M = e.x;
+#pragma unroll
+            for (int o = 1; o < W; o <<= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, o));
             const float wt = (e.x == -INFINITY) ? 0.f : fast_exp2(e.x - M);
-            const float L = warp_sum(e.y * wt);
-            float wts[kConsumerWarps];
+            float L = e.y * wt;
 #pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) wts[w] = __shfl_sync(FULL, wt, w);
-            const int h = h0 + g;
-            const size_t pi = (static_cast<size_t>(d.r) * 2 + d.slot) * G + g;  // this part's partial slot
-#pragma unroll
-            for (int c = lane; c < D; c += 32) {
-                float O = 0.f;
-#pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w)
-                    O = fmaf(mo[((buf * kConsumerWarps + w) * G + g) * D + c], wts[w], O);
-                if (d.nparts == 1) {
-                    P.out[(static_cast<size_t>(d.row) * P.hq + h) * D + c] = (L > 0.f) ? O / L : 0.f;
-                } else {
-                    P.part_o[pi * D + c] = O;
-                }
+            for (int o = 1; o < W; o <<= 1) L += __shfl_xor_sync(FULL, L, o);
+            if (i < G * W) {
+                wsm[i] = wt;
+                if (w == 0) msm[i / W] = make_float2(M, L);
             }
-            if (d.nparts > 1 && lane == 0) P.part_ml[pi] = make_float2(M, L);
         }
+        __syncwarp();
+        const int h0 = d.g * G;
+        const size_t pi0 = (static_cast<size_t>(d.r) * 2 + d.slot) * G;  // this part's partial slots, one per head
+        const float4* mo4 = reinterpret_cast<const float4*>(mo) + static_cast<size_t>(buf) * W * CH;
+        float4* dst = (d.nparts == 1)
+                          ? reinterpret_cast<float4*>(P.out + (static_cast<size_t>(d.row) * P.hq + h0) * D)
+                          : reinterpret_cast<float4*>(P.part_o + pi0 * D);
+#pragma unroll
+        for (int j = 0; j < (CH + 31) / 32; ++j) {
+            const int k = lane + 32 * j;
+            if (k < CH) {
+                const int g = k / (D / 4);
+                float4 v[W];
+#pragma unroll
+                for (int w = 0; w < W; ++w) v[w] = mo4[w * CH + k];
+                float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int w = 0; w < W; ++w) {
+                    const float wt = wsm[g * W + w];
+                    a.x = fmaf(v[w].x, wt, a.x);
+                    a.y = fmaf(v[w].y, wt, a.y);
+                    a.z = fmaf(v[w].z, wt, a.z);
+                    a.w = fmaf(v[w].w, wt, a.w);
+                }
+                if (d.nparts == 1) {
+                    const float L = msm[g].y;
+                    a = (L > 0.f) ? make_float4(a.x / L, a.y / L, a.z / L, a.w / L) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+                dst[k] = a;
+            }
+        }
+        if (d.nparts > 1 && lane < G) P.part_ml[pi0 + lane] = msm[lane];
         __syncwarp();
         if (lane == 0) mbar_arrive(&B.mempty[buf]);
         if (d.nparts > 1) {
@@ -683,45 +719,82 @@ __device__ void run_merger(const DecodeParams& P, uint8_t* smem, const Bars& B, 
             if (lane == 0) ticket = atomicAdd(ctr, 1u);
             ticket = __shfl_sync(FULL, ticket, 0);
             if (ticket == static_cast<uint32_t>(d.nparts - 1)) {
-                // Last partition in: merge all partitions of (s, kv head).
-                // Lanes hold the partitions' weights, 32 at a time; the
-                // partitions' o rows are read with independent loads.
+                // Last part in: merge all parts of (s, kv head), in part
+                // order.  Part k of the pair lives in range r0 + k, in slot
+                // slot0 for k = 0 and slot 0 after that; its G heads' (m, l)
+                // and o rows are contiguous.  Lanes hold the parts' weights
+                // for every head, 32 parts at a time.
                 __threadfence();
-#pragma unroll 1
+                auto part_base = [&](int k) -> size_t {
+                    return (static_cast<size_t>(d.r0 + k) * 2 + (k == 0 ? d.slot0 : 0)) * G;
+                };
+                auto pick = [](const float (&x)[G], int g) {
+                    float r = x[0];
+#pragma unroll
+                    for (int i = 1; i < G; ++i) r = (g == i) ? x[i] : r;
+                    return r;
+                };
+                float M[G], L[G];
+#pragma unroll
                 for (int g = 0; g < G; ++g) {
-                    const int h = h0 + g;
-                    // Part k of the pair lives in range r0 + k, in slot slot0
-                    // for k = 0 and slot 0 after that.
-                    auto part_index = [&](int k) -> size_t {
-                        return (static_cast<size_t>(d.r0 + k) * 2 + (k == 0 ? d.slot0 : 0)) * G + g;
-                    };
-                    float M = -INFINITY;
-                    for (int p0 = 0; p0 < d.nparts; p0 += 32)
-                        if (p0 + lane < d.nparts) M = fmaxf(M, __ldcg(P.part_ml + part_index(p0 + lane)).x);
-                    M = warp_max(M);
-                    float L = 0.f;
-                    float acc[D / 32];
+                    M[g] = -INFINITY;
+                    L[g] = 0.f;
+                }
+                for (int p0 = 0; p0 < d.nparts; p0 += 32) {
+                    if (p0 + lane < d.nparts) {
+                        const float2* pm = P.part_ml + part_base(p0 + lane);
 #pragma unroll
-                    for (int i = 0; i < D / 32; ++i) acc[i] = 0.f;
-                    for (int p0 = 0; p0 < d.nparts; p0 += 32) {
-                        const int pp = p0 + lane;
-                        const float2 e =
-                            (pp < d.nparts) ? __ldcg(P.part_ml + part_index(pp)) : make_float2(-INFINITY, 0.f);
-                        const float wt = (e.x == -INFINITY) ? 0.f : fast_exp2(e.x - M);
-                        L = fmaf(e.y, wt, L);
-                        const int cnt = min(32, d.nparts - p0);
-#pragma unroll 4
-                        for (int k = 0; k < cnt; ++k) {
-                            const float wk = __shfl_sync(FULL, wt, k);
-                            const float* orow = P.part_o + part_index(p0 + k) * D;
+                        for (int g = 0; g < G; ++g) M[g] = fmaxf(M[g], __ldcg(pm + g).x);
+                    }
+                }
 #pragma unroll
-                            for (int i = 0; i < D / 32; ++i) acc[i] = fmaf(__ldcg(orow + lane + 32 * i), wk, acc[i]);
+                for (int g = 0; g < G; ++g) M[g] = warp_max(M[g]);
+                constexpr int NJ = (CH + 31) / 32;
+                float4 acc[NJ];
+#pragma unroll
+                for (int j = 0; j < NJ; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int p0 = 0; p0 < d.nparts; p0 += 32) {
+                    const int pp = p0 + lane;
+                    float wt[G];
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        const float2 e = (pp < d.nparts) ? __ldcg(P.part_ml + part_base(pp) + g)
+                                                         : make_float2(-INFINITY, 0.f);
+                        wt[g] = (e.x == -INFINITY) ? 0.f : fast_exp2(e.x - M[g]);
+                        L[g] = fmaf(e.y, wt[g], L[g]);
+                    }
+                    const int cnt = min(32, d.nparts - p0);
+#pragma unroll 2
+                    for (int k = 0; k < cnt; ++k) {
+                        float wk[G];
+#pragma unroll
+                        for (int g = 0; g < G; ++g) wk[g] = __shfl_sync(FULL, wt[g], k);
+                        const float4* orow = reinterpret_cast<const float4*>(P.part_o + part_base(p0 + k) * D);
+#pragma unroll
+                        for (int j = 0; j < NJ; ++j) {
+                            const int c = lane + 32 * j;
+                            if (c < CH) {
+                                const float4 o = __ldcg(orow + c);
+                                const float w = pick(wk, c / (D / 4));
+                                acc[j].x = fmaf(o.x, w, acc[j].x);
+                                acc[j].y = fmaf(o.y, w, acc[j].y);
+                                acc[j].z = fmaf(o.z, w, acc[j].z);
+                                acc[j].w = fmaf(o.w, w, acc[j].w);
+                            }
                         }
                     }
-                    L = warp_sum(L);
-                    float* out = P.out + (static_cast<size_t>(d.row) * P.hq + h) * D;
+                }
 #pragma unroll
-                    for (int i = 0; i < D / 32; ++i) out[lane + 32 * i] = (L > 0.f) ? acc[i] / L : 0.f;
+                for (int g = 0; g < G; ++g) L[g] = warp_sum(L[g]);
+                float4* out4 = reinterpret_cast<float4*>(P.out + (static_cast<size_t>(d.row) * P.hq + h0) * D);
+#pragma unroll
+                for (int j = 0; j < NJ; ++j) {
+                    const int c = lane + 32 * j;
+                    if (c < CH) {
+                        const float Lg = pick(L, c / (D / 4));
+                        out4[c] = (Lg > 0.f) ? make_float4(acc[j].x / Lg, acc[j].y / Lg, acc[j].z / Lg, acc[j].w / Lg)
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
                 }
                 if (lane == 0) atomicExch(ctr, 0u);
             }
@@ -731,6 +804,112 @@ __device__ void run_merger(const DecodeParams& P, uint8_t* smem, const Bars& B, 
     if (!ok) {
         *abort_flag = 1;
         record_error(P.err, kErrTimeout, 3u);
+    }
+}
+
+// Warm L2 with what every CTA reads first: context_lens (and
+// query_start_loc), the used part of every block-table row and, for a pure
+// decode batch, the query rows.  Runs before griddep_wait(), so the chain
+// context_lens -> table -> K/V that opens each CTA starts from L2 rather than
+// from DRAM.  Thread t of CTA c takes lines c * nthr + t + k * gridDim.x * nthr.
+// A region past kPrefetchCap bytes is left to the regular loads.
+template <int D>
+__device__ void prefetch_inputs(const DecodeParams& P, int t, int nthr) {
+    constexpr long long kPrefetchCap = 16ll << 20;
+    const long long S = P.num_seqs;
+    const long long nb = min(static_cast<long long>(P.max_blocks),
+                             static_cast<long long>(P.ctx_cap + kBlockSize - 1) / kBlockSize);
+    const long long n_ctx = range_lines(S * 4);
+    const long long n_qsl = P.qsl ? range_lines((S + 1) * 4) : 0;
+    const long long lpr = range_lines(nb * 4);
+    const long long n_tab = (S * nb * 4 <= kPrefetchCap) ? S * lpr : 0;
+    const long long q_bytes = S * P.hq * D * 2;
+    const long long n_q = (P.qsl == nullptr && q_bytes <= kPrefetchCap) ? range_lines(q_bytes) : 0;
+    const long long total = n_ctx + n_qsl + n_tab + n_q;
+    const long long step = static_cast<long long>(gridDim.x) * nthr;
+    for (long long k = static_cast<long long>(blockIdx.x) * nthr + t; k < total; k += step) {
+        const void* a;
+        if (k < n_ctx) {
+            a = range_line(P.context_lens, S * 4, k);
+        } else if (k < n_ctx + n_qsl) {
+            a = range_line(P.qsl, (S + 1) * 4, k - n_ctx);
+        } else if (k < n_ctx + n_qsl + n_tab) {
+            const long long j = k - n_ctx - n_qsl;
+            a = range_line(P.block_tables + (j / lpr) * P.max_blocks, nb * 4, j % lpr);
+        } else {
+            a = range_line(P.q, q_bytes, k - n_ctx - n_qsl - n_tab);
+        }
+        if (a != nullptr) prefetch_l2(a);
+    }
+}
+
+// Guess this CTA's first blocks and prefetch their K and V slabs into L2,
+// before the previous kernel on the stream has finished.  The reads here
+// may see values that kernel is still writing (they bypass L1, so no stale
+// copy outlives the wait); they only choose what to prefetch, and every
+// address is checked against the pool first.  The guess is the nominal
+// range start (no boundary snapping); the producer recomputes everything
+// after the wait.  Up to kSpecWindows * 32 sequences; larger batches skip
+// the guess.
+constexpr int kSpecWindows = 8;
+
+template <int D, int G>
+__device__ void prefetch_first_blocks(const DecodeParams& P, int lane, int max_units) {
+    using C = Cfg<D, G>;
+    const unsigned FULL = 0xffffffffu;
+    if (P.num_seqs > kSpecWindows * 32) return;
+    int u[kSpecWindows], incl[kSpecWindows];
+#pragma unroll
+    for (int w = 0; w < kSpecWindows; ++w) {
+        const int s = w * 32 + lane;
+        u[w] = 0;
+        if (s < P.num_seqs) {
+            const bool dec = P.qsl == nullptr || ld_l2_only(P.qsl + s + 1) - ld_l2_only(P.qsl + s) == 1;
+            const int n = min(max(ld_l2_only(P.context_lens + s), 0), P.ctx_cap);
+            u[w] = dec ? max(1, (n + kBlockSize - 1) / kBlockSize) : 0;
+        }
+    }
+    long long per_head = 0;
+#pragma unroll
+    for (int w = 0; w < kSpecWindows; ++w) {
+        incl[w] = u[w];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(FULL, incl[w], o);
+            if (lane >= o) incl[w] += t;
+        }
+        per_head += __shfl_sync(FULL, incl[w], 31);
+    }
+    const long long T = per_head * P.hkv;
+    long long RU = P.range_units;
+    if (RU <= 0) RU = max(static_cast<long long>(kMinRangeUnits), (T + gridDim.x - 1) / gridDim.x);
+    long long x = static_cast<long long>(blockIdx.x) * RU;
+    const long long hi = min(T, x + min(RU, static_cast<long long>(max_units)));
+    // Walk the pairs from x: find the sequence (window w, lane j) holding x.
+    long long base = 0;  // units per kv head before window w
+#pragma unroll
+    for (int w = 0; w < kSpecWindows; ++w) {
+        while (x < hi) {
+            const unsigned hit = __ballot_sync(FULL, (base + incl[w]) * P.hkv > x);
+            if (!hit) break;
+            const int j = __ffs(hit) - 1;
+            const int us = __shfl_sync(FULL, u[w], j);
+            const long long seq0 = (base + __shfl_sync(FULL, incl[w], j) - us) * P.hkv;
+            const int g = static_cast<int>((x - seq0) / us);
+            const int b0 = static_cast<int>(x - seq0 - static_cast<long long>(g) * us);
+            const int cnt = static_cast<int>(min(static_cast<long long>(us - b0), hi - x));
+            const int32_t* trow = P.block_tables + static_cast<size_t>(w * 32 + j) * P.max_blocks;
+            for (int b = lane; b < cnt; b += 32) {
+                const int phys = ld_l2_only(trow + b0 + b);
+                if (phys >= 0 && phys < P.num_blocks) {
+                    const size_t slab = (static_cast<size_t>(phys) * P.hkv + g) * C::SLAB;
+                    bulk_prefetch_l2(P.k_pool + slab, C::SLAB);
+                    bulk_prefetch_l2(P.v_pool + slab, C::SLAB);
+                }
+            }
+            x += cnt;
+        }
+        base += __shfl_sync(FULL, incl[w], 31);
     }
 }
 
@@ -765,12 +944,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
         *abort_flag = 0;
         fence_mbar_init();
     }
+    griddep_launch_dependents();
     __syncthreads();
+    // Until griddep_wait() returns, only L2 prefetches touch global memory.
+    // Consumer warps read shared memory only and need no wait.
     if (warp == kProducerWarp) {
+        griddep_wait();
         run_producer<D, G>(P, smem, B, abort_flag, lane);
     } else if (warp == kMergerWarp) {
+        prefetch_first_blocks<D, G>(P, lane, C::STAGES);
+        griddep_wait();
         run_merger<D, G>(P, smem, B, abort_flag, lane);
     } else {
+        prefetch_inputs<D>(P, threadIdx.x, kConsumerWarps * 32);
         run_consumer<D, G>(P, smem, B, abort_flag, warp, lane);
     }
 }
@@ -787,8 +973,7 @@ cudaError_t launch_one(const DecodeParams& P, int grid, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    decode_kernel<D, G><<<grid, kThreads, C::SMEM, stream>>>(P);
-    return cudaGetLastError();
+    return launch_overlapped(decode_kernel<D, G>, dim3(grid), dim3(kThreads), C::SMEM, stream, P);
 }
 
 template <int D>

@@ -32,6 +32,45 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
+// ---------------------------------------------------------------- launch overlap
+// Every libpagedkv kernel is launched with programmatic stream
+// serialization (launch_overlapped below): it may start while the kernel
+// before it on the stream is still running.  Before griddep_wait() returns,
+// a kernel touches global memory only through L2 prefetches (which cannot
+// make it read stale data: L2 is where every write lands); griddep_wait()
+// returns once the previous kernel has completed and its writes are
+// visible.  launch_dependents lets the next overlapped launch start early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+__device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
+
+// Load that bypasses L1 (cached in L2 only): for values read before
+// griddep_wait() that must not leave a stale copy in L1.
+__device__ __forceinline__ int32_t ld_l2_only(const int32_t* p) {
+    int32_t v;
+    asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+// Prefetch [p, p + bytes) into L2 with one bulk request (p and bytes
+// multiples of 16).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Item k of the 128-byte lines that overlap [base, base + bytes): returns
+// an address inside the range on that line, or nullptr past the end.
+__device__ __forceinline__ const void* range_line(const void* base, long long bytes, long long k) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(base);
+    const uintptr_t line = (a & ~static_cast<uintptr_t>(127)) + static_cast<uintptr_t>(k) * 128u;
+    if (line >= a + static_cast<uintptr_t>(bytes)) return nullptr;
+    return reinterpret_cast<const void*>(line < a ? a : line);
+}
+
+// Upper bound on the 128-byte lines that overlap a range of `bytes` bytes.
+__host__ __device__ __forceinline__ long long range_lines(long long bytes) { return bytes > 0 ? bytes / 128 + 2 : 0; }
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
@@ -127,6 +166,26 @@ __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
+}
+
+// Host: launch `kernel` with programmatic stream serialization unless the
+// PKV_OVERLAP environment variable is "0" (then a plain launch).
+bool overlap_enabled();
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_overlapped(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = overlap_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 
 }  // namespace pkv

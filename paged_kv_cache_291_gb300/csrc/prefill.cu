@@ -137,7 +137,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const unsigned FULL = 0xffffffffu;
 
     // ---------------------------------------------------------- setup
+    // The launch may overlap the previous kernel on the stream: barrier and
+    // TMEM set-up go first, every global access after griddep_wait().
+    griddep_launch_dependents();
     if (warp == 0) {
+        griddep_wait();
         // Find the sequence and row tile of this CTA: tiles are numbered over
         // the prefill sequences (query_len > 1) in order, ceil(qlen/128) each.
         const int tile = blockIdx.x;
@@ -209,6 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::prefetch_tensormap(&tm_v);
         }
     }
+    griddep_wait();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
@@ -561,8 +566,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
         configured[dev] = true;
     }
     dim3 grid(static_cast<unsigned>(a.num_tiles), static_cast<unsigned>(a.num_q_heads / P.units));
-    prefill_kernel<<<grid, kThreads, SMEM_BYTES, stream>>>(tq, tk, tv, P);
-    return cudaGetLastError();
+    return launch_overlapped(prefill_kernel, grid, dim3(kThreads), SMEM_BYTES, stream, tq, tk, tv, P);
 }
 
 }  // namespace pkv
