@@ -41,7 +41,7 @@ CONFIG_ID = 2  # the Qwen3-1.7B decode step (34 sequences x 640 tokens)
 # DRAM traffic of one decode launch on this workload from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), and the hash of the kernel
 # sources it was taken on; reported only while the sources still match.
-NCU_TRAFFIC = {"bytes": 91587840, "sources_sha": "fa11fe4caa9cd027",
+NCU_TRAFFIC = {"bytes": 91950336, "sources_sha": "ea2e77710bb1e74b",
                "capture": "profiles/decode_kernel_qwen3_1p7b_decode.md"}
 KERNEL_SOURCES = ["paged_kv_cache_291_gb300/csrc/decode.cu", "paged_kv_cache_291_gb300/csrc/pkv_device.cuh"]
 
@@ -139,6 +139,78 @@ class ClockSampler:
                     reasons.add(name)
         return {"sm_mhz": statistics.median(r["sm"] for r in rows), "sm_max_mhz": max(r["smmax"] for r in rows),
                 "reasons": sorted(reasons), "samples": len(rows)}
+
+
+class NvmlClockSampler:
+    """SM clock and clock-event reasons polled through NVML (read-only
+    queries: nvmlDeviceGetClockInfo, nvmlDeviceGetMaxClockInfo,
+    nvmlDeviceGetCurrentClocksEventReasons) every half millisecond while the
+    timed region runs, so that even a region of a few milliseconds has
+    samples.  The device is matched by PCI bus id.  Falls back to
+    nvidia-smi sampling when NVML cannot be loaded."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device: int):
+        import ctypes
+
+        import torch
+        self.samples = []
+        self._stop = threading.Event()
+        self._thr = None
+        self.fallback = None
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            pr = torch.cuda.get_device_properties(device)
+            bus = f"{pr.pci_domain_id:08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0".encode()
+            h = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByPciBusId_v2(bus, ctypes.byref(h)) != 0:
+                raise OSError("no NVML handle for " + bus.decode())
+            self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                lib.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.lib, self.h, self.ct = lib, h, ctypes
+            mx = ctypes.c_uint()
+            lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))  # 1 = NVML_CLOCK_SM
+            self.max_mhz = float(mx.value)
+        except (OSError, AttributeError, RuntimeError):
+            self.lib = None
+            self.fallback = ClockSampler(device)
+
+    def _poll(self):
+        ct, lib, h = self.ct, self.lib, self.h
+        clk, rs = ct.c_uint(), ct.c_ulonglong()
+        while not self._stop.is_set():
+            ok = lib.nvmlDeviceGetClockInfo(h, 1, ct.byref(clk)) == 0 and self.reasons_fn(h, ct.byref(rs)) == 0
+            if ok:
+                self.samples.append((time.time(), float(clk.value), int(rs.value)))
+            time.sleep(0.0005)
+
+    def start(self):
+        if self.lib is None:
+            self.fallback.start()
+            return
+        self._thr = threading.Thread(target=self._poll, daemon=True)
+        self._thr.start()
+        time.sleep(0.01)
+
+    def stop(self):
+        if self.lib is None:
+            self.fallback.stop()
+            return
+        self._stop.set()
+        self._thr.join(timeout=2)
+
+    def summary(self, t0: float, t1: float):
+        if self.lib is None:
+            return self.fallback.summary(t0, t1)
+        rows = [(mhz, rs) for ts, mhz, rs in self.samples if t0 <= ts <= t1]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0}
+        reasons = sorted({name for _, rs in rows for bit, name in self.REASONS.items() if rs & bit})
+        return {"sm_mhz": statistics.median(m for m, _ in rows), "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(rows)}
 
 
 # ----------------------------------------------------------- helpers
@@ -411,7 +483,7 @@ def run_ours(args):
         run_steps(max(args.warmup, 3))
     barrier()
 
-    clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    clocks = NvmlClockSampler(torch.cuda.current_device()) if rank == 0 else None
     if clocks:
         clocks.start()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

@@ -161,3 +161,60 @@ def test_decode_rows_through_mixed_batch_api(pkv):
     assert pkv.get_error() == (0, 0)
     _, _, ref = oracle.run_step(w)
     assert_close(out.cpu().numpy(), ref, "mixed decode rows")
+
+
+def _lengths_from_previous_kernel(pkv, fresh: list, stale_value: int):
+    """A fake two-block pool whose block 0 holds stale int32 values and block 1
+    the fresh ones; returns (k_fake, v_fake, view of block 0, launch) where
+    launch() rewrites block 0 from block 1 with pkv_copy_blocks.  The decode
+    call made right after may start before that copy ends (both launch
+    overlapped), so it can see the stale values before its wait."""
+    n = len(fresh)
+    fk = torch.zeros((2, 1, 16, 128), dtype=torch.bfloat16, device="cuda")
+    fv = torch.zeros_like(fk)
+    flat = fk.view(torch.int32).view(-1)  # 1,024 int32 per block
+    assert n <= 1024
+    flat[1024:1024 + n] = torch.tensor(fresh, dtype=torch.int32, device="cuda")
+    src = torch.tensor([1], dtype=torch.int32, device="cuda")
+    dst = torch.tensor([0], dtype=torch.int32, device="cuda")
+    one, zero = np.array([1], dtype=np.int32), np.array([0], dtype=np.int32)
+
+    def launch():
+        flat[0:n] = stale_value
+        pkv.copy_blocks(fk, fv, src, dst, src_host=one, dst_host=zero)
+
+    return flat[0:n], launch
+
+
+def test_lengths_written_by_the_previous_kernel(pkv):
+    """context_lens produced by the kernel launched just before decode: the
+    decode plan may be worked out from stale lengths before the wait, and must
+    be redone from the fresh ones after it."""
+    w = W.make_paged("prev-kernel lengths", 21, 16, 8, 128, [640] * 20 + [37, 1000, 3, 129], [1] * 24)
+    ds = DeviceStep(w)
+    pkv.cache_write(ds.k, ds.v, ds.k_new, ds.v_new, ds.slots)
+    _, _, ref = oracle.run_step(w)
+    ctx_view, launch = _lengths_from_previous_kernel(pkv, w.context_lens.tolist(), 1)
+    for _ in range(6):
+        launch()
+        out = pkv.decode_attention(ds.k, ds.v, ds.q, ds.tables, ctx_view, w.max_context_len, w.scale)
+        torch.cuda.synchronize()
+        assert pkv.get_error() == (0, 0)
+        assert_close(out.cpu().numpy(), ref, "lengths from the previous kernel")
+
+
+def test_row_offsets_written_by_the_previous_kernel(pkv):
+    """The same through the mixed-batch call: query_start_loc (which decides
+    which rows are decode rows) comes from the kernel launched just before."""
+    w = W.make_paged("prev-kernel qsl", 22, 16, 8, 128, [300, 2000, 90, 640], [1, 1, 1, 1])
+    ds = DeviceStep(w)
+    pkv.cache_write(ds.k, ds.v, ds.k_new, ds.v_new, ds.slots)
+    _, _, ref = oracle.run_step(w)
+    qsl_view, launch = _lengths_from_previous_kernel(pkv, w.query_start_loc.tolist(), 0)
+    for _ in range(6):
+        launch()
+        out = pkv.chunked_prefill_attention(ds.k, ds.v, ds.q, qsl_view, ds.ctx, ds.tables, w.max_context_len,
+                                            w.scale, query_start_loc_host=w.query_start_loc)
+        torch.cuda.synchronize()
+        assert pkv.get_error() == (0, 0)
+        assert_close(out.cpu().numpy(), ref, "row offsets from the previous kernel")
