@@ -22,11 +22,10 @@
 //    Q K^T is written there; the softmax reads it, then writes P into the
 //    same columns as bf16, and O += P V takes P straight from TMEM (the A
 //    operand of the MMA) with V from shared memory (MN-major operand).
-//  * P goes in as two bf16 matrices, its rounding and the rounding of the
-//    residual (P = P_hi + P_lo to about 2^-17 relative), and O += P_hi V +
-//    P_lo V: a single bf16 P (2^-9 relative) can miss a 2e-3 absolute bound
-//    when a few keys carry all the weight.  l sums P in fp32 (it differs
-//    from P_hi + P_lo by about 2^-17 relative).
+//  * P goes in as two bf16 matrices, its truncation and the truncation of
+//    the (exact) residual, so P = P_hi + P_lo to within 2^-14 relative, and
+//    O += P_hi V + P_lo V: a single bf16 P (2^-9 relative) can miss a 2e-3
+//    absolute bound when a few keys carry all the weight.  l sums P in fp32.
 //  * Online softmax in the log2 domain; the running maximum is only moved
 //    (and O rescaled in TMEM) when it grows by more than 2^8; the final
 //    O / l uses the same reference, so the result is unchanged.
@@ -369,7 +368,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int h = h0 + u;
         const int pos = (m < rows) ? pmin + m : pmax;
         float m_used = -INFINITY;
-        float2 l2 = make_float2(0.f, 0.f);  // row sum of P (two interleaved halves)
+        float2 l2[4];  // row sum of P (8 interleaved partial sums)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) l2[k] = make_float2(0.f, 0.f);
         for (int j = 0; j < nt && ok; ++j) {
             if (!warp_wait(&bar[B_SFULL + u], j & 1)) { ok = false; break; }
             tc::fence_after_sync();
@@ -377,82 +378,97 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Rows grow down the warp, so the tile is fully visible to the
             // warp when its last key is visible to the warp's first row.
             const bool full = kbase + kTileN - 1 <= __shfl_sync(FULL, pos, 0);
+            // The row's 128 scores, loaded once behind a single wait and kept
+            // in registers for both passes.
+            uint32_t sr[kTileN];
+#pragma unroll
+            for (int c = 0; c < kTileN / 32; ++c)
+                tc::tmem_ld32(tmem_lane_addr(tmem, warp, col_s(u) + 32 * c),
+                              *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
+            tc::tmem_wait_ld();
             // Pass 1: the tile's row maximum (of the raw scores; the scale is
-            // positive, so it is applied afterwards).
-            float mraw = -INFINITY;
+            // positive, so it is applied afterwards), as 8 independent
+            // partial maxima.
+            float mp[8];
 #pragma unroll
-            for (int c = 0; c < kTileN / 32; c += 2) {
-                uint32_t r0[32], r1[32];
-                tc::tmem_ld32(tmem_lane_addr(tmem, warp, col_s(u) + 32 * c), r0);
-                tc::tmem_ld32(tmem_lane_addr(tmem, warp, col_s(u) + 32 * c + 32), r1);
-                tc::tmem_wait_ld();
-                if (full) {
+            for (int k = 0; k < 8; ++k) mp[k] = -INFINITY;
+            if (full) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) mraw = fmaxf(mraw, fmaxf(__uint_as_float(r0[i]), __uint_as_float(r1[i])));
-                } else {
+                for (int i = 0; i < kTileN; ++i) mp[i % 8] = fmaxf(mp[i % 8], __uint_as_float(sr[i]));
+            } else {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        if (kbase + 32 * c + i <= pos) mraw = fmaxf(mraw, __uint_as_float(r0[i]));
-                        if (kbase + 32 * c + 32 + i <= pos) mraw = fmaxf(mraw, __uint_as_float(r1[i]));
-                    }
-                }
+                for (int i = 0; i < kTileN; ++i)
+                    if (kbase + i <= pos) mp[i % 8] = fmaxf(mp[i % 8], __uint_as_float(sr[i]));
             }
+            const float mraw = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                                     fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
             const float mt = mraw * P.scale_log2;
+            // A new reference only when the maximum grew by more than 2^8;
+            // O is then rescaled by alpha after pass 2 (before P is handed
+            // to the MMA warp), l now.
+            float alpha = 1.f;
+            bool rescale = false;
             if (j == 0) {
                 m_used = mt;
             } else {
                 const bool need = mt > m_used + kRescaleThreshold;
-                if (__any_sync(FULL, need)) {
-                    const float alpha = need ? fast_exp2(m_used - mt) : 1.f;
+                rescale = __any_sync(FULL, need);
+                if (need) {
+                    alpha = fast_exp2(m_used - mt);
+                    m_used = mt;
 #pragma unroll
-                    for (int c = 0; c < kHeadDim / 32; ++c) {
-                        uint32_t r[32];
-                        const uint32_t ta = tmem_lane_addr(tmem, warp, col_o(u) + 32 * c);
-                        tc::tmem_ld32(ta, r);
-                        tc::tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                        tc::tmem_st32(ta, r);
+                    for (int k = 0; k < 4; ++k) {
+                        l2[k].x *= alpha;
+                        l2[k].y *= alpha;
                     }
-                    tc::tmem_wait_st();
-                    l2.x *= alpha;
-                    l2.y *= alpha;
-                    if (need) m_used = mt;
                 }
             }
             // Pass 2: P = exp2(scale * s - m_used) as bf16 P_hi + P_lo,
-            // written over the S columns just read: 32 keys -> 16 hi words +
-            // 16 lo words, laid out per 16-key step as [8 hi | 8 lo].
+            // written over the S columns: 32 keys -> 16 hi words + 16 lo
+            // words, laid out per 16-key step as [8 hi | 8 lo].  The row sum
+            // goes to 4 independent fp32x2 accumulators.
             const float2 sc2 = make_float2(P.scale_log2, P.scale_log2);
             const float2 nm2 = make_float2(-m_used, -m_used);
 #pragma unroll
             for (int c = 0; c < kTileN / 32; ++c) {
-                uint32_t r[32];
-                const uint32_t ta = tmem_lane_addr(tmem, warp, col_s(u) + 32 * c);
-                tc::tmem_ld32(ta, r);
-                tc::tmem_wait_ld();
                 uint32_t w[32];
 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const int k0 = 32 * c + 16 * t + 2 * i;
-                        float2 x = __ffma2_rn(make_float2(__uint_as_float(r[16 * t + 2 * i]),
-                                                          __uint_as_float(r[16 * t + 2 * i + 1])),
-                                              sc2, nm2);
-                        if (!full) {
-                            if (kbase + k0 > pos) x.x = -INFINITY;
-                            if (kbase + k0 + 1 > pos) x.y = -INFINITY;
+                        const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[k0]), __uint_as_float(sr[k0 + 1])),
+                                                    sc2, nm2);
+                        float2 p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                        if (!full) {  // keys past the row's position (NaN in unused slots included)
+                            if (kbase + k0 > pos) p.x = 0.f;
+                            if (kbase + k0 + 1 > pos) p.y = 0.f;
                         }
-                        const float2 p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-                        const uint32_t hi = tc::pack_bf16x2(p.x, p.y);
-                        const float2 res = __fadd2_rn(p, make_float2(-bf16lo(hi), -bf16hi(hi)));
-                        w[16 * t + i] = hi;
-                        w[16 * t + 8 + i] = tc::pack_bf16x2(res.x, res.y);
-                        l2 = __fadd2_rn(l2, p);
+                        // P_hi: p truncated to bf16 (its high 16 bits), P_lo:
+                        // the exact residual truncated likewise.  Byte
+                        // permutes instead of conversions keep the special
+                        // function unit free for ex2.
+                        const uint32_t ux = __float_as_uint(p.x), uy = __float_as_uint(p.y);
+                        const float2 res = __fadd2_rn(p, make_float2(-__uint_as_float(ux & 0xFFFF0000u),
+                                                                     -__uint_as_float(uy & 0xFFFF0000u)));
+                        w[16 * t + i] = __byte_perm(ux, uy, 0x7632);
+                        w[16 * t + 8 + i] = __byte_perm(__float_as_uint(res.x), __float_as_uint(res.y), 0x7632);
+                        l2[i % 4] = __fadd2_rn(l2[i % 4], p);
                     }
                 }
-                tc::tmem_st32(ta, w);
+                tc::tmem_st32(tmem_lane_addr(tmem, warp, col_s(u) + 32 * c), w);
+            }
+            if (rescale) {
+#pragma unroll
+                for (int c = 0; c < kHeadDim / 32; ++c) {
+                    uint32_t r[32];
+                    const uint32_t ta = tmem_lane_addr(tmem, warp, col_o(u) + 32 * c);
+                    tc::tmem_ld32(ta, r);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                    tc::tmem_st32(ta, r);
+                }
             }
             tc::tmem_wait_st();
             tc::fence_before_sync();
@@ -464,7 +480,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = false;
             } else {
                 tc::fence_after_sync();
-                const float inv = 1.f / (l2.x + l2.y);
+                const float inv = 1.f / (((l2[0].x + l2[0].y) + (l2[1].x + l2[1].y)) +
+                                         ((l2[2].x + l2[2].y) + (l2[3].x + l2[3].y)));
                 float* orow = P.out + (static_cast<size_t>(row0 + m) * P.hq + h) * kHeadDim;
 #pragma unroll
                 for (int c = 0; c < kHeadDim / 32; ++c) {
