@@ -53,17 +53,20 @@ namespace pkv {
 
 namespace {
 
-#ifndef PKV_DECODE_CONSUMER_WARPS
-#define PKV_DECODE_CONSUMER_WARPS 8
+// Consumer warps per CTA: 12 for head groups of 1 or 2 (their per-lane state
+// is small, and a fourth warp per scheduler hides more of the latency of the
+// dependent shuffle and FMA chains), 8 for groups of 4 and 8 (which need
+// more than the 128 registers a thread that 14 warps leave).  A build can
+// force one count for every group with PKV_DECODE_CONSUMER_WARPS.
+template <int G>
+constexpr int consumer_warps() {
+#ifdef PKV_DECODE_CONSUMER_WARPS
+    return PKV_DECODE_CONSUMER_WARPS;
+#else
+    return G <= 2 ? 12 : 8;
 #endif
-constexpr int kConsumerWarps = PKV_DECODE_CONSUMER_WARPS;
-static_assert(kConsumerWarps >= 1 && kConsumerWarps <= 32 && (kConsumerWarps & (kConsumerWarps - 1)) == 0,
-              "consumer warps: a power of two up to 32 (the merger reduces over aligned lane groups)");
-constexpr int kProducerWarp = kConsumerWarps;
-constexpr int kMergerWarp = kConsumerWarps + 1;
-constexpr int kThreads = 32 * (kConsumerWarps + 2);
+}
 constexpr int kItemRing = 8;
-constexpr int kMergeBufs = 2;
 constexpr int kMinRangeUnits = 8;  // smallest automatic range (blocks per CTA)
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -100,6 +103,15 @@ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
 template <int D, int G>
 struct Cfg {
+    static constexpr int W = consumer_warps<G>();     // consumer warps
+    static_assert(W >= 1 && W <= 16, "consumer warps");
+    // Lanes per q head in the merger's weight reduction: W rounded up to a
+    // power of two (the extra lanes carry empty states).
+    static constexpr int MERGE_LANES = W <= 1 ? 1 : W <= 2 ? 2 : W <= 4 ? 4 : W <= 8 ? 8 : 16;
+    static constexpr int MERGE_BUFS = W > 8 ? 1 : 2;  // consumer states the merger can lag by
+    static constexpr int PRODUCER_WARP = W;
+    static constexpr int MERGER_WARP = W + 1;
+    static constexpr int THREADS = 32 * (W + 2);
     static constexpr int LPR = D / 8;                  // lanes per K/V row, 8 dims (16 B) each
     static constexpr int RPP = 32 / LPR;               // rows per warp pass
     static constexpr int NV = kBlockSize / RPP;        // rows per lane per block
@@ -111,18 +123,18 @@ struct Cfg {
     static constexpr int R_ITEMQ = 0;
     static constexpr int R_DESC = R_ITEMQ + kItemRing * QBYTES;
     static constexpr int R_P = R_DESC + kItemRing * (int)sizeof(ItemDesc);
-    static constexpr int R_MO = R_P + kConsumerWarps * G * kBlockSize * 8;  // p stored as (p, p)
-    static constexpr int R_ML = R_MO + kMergeBufs * kConsumerWarps * G * D * 4;
-    static constexpr int R_WT = R_ML + kMergeBufs * kConsumerWarps * G * 8;  // merger: [G][W] weights, [G] (M, L)
-    static constexpr int R_BAR = align_up(R_WT + G * kConsumerWarps * 4 + G * 8, 8);
+    static constexpr int R_MO = R_P + W * G * kBlockSize * 8;  // p stored as (p, p)
+    static constexpr int R_ML = R_MO + MERGE_BUFS * W * G * D * 4;
+    static constexpr int R_WT = R_ML + MERGE_BUFS * W * G * 8;  // merger: [G][W] weights, [G] (M, L)
+    static constexpr int R_BAR = align_up(R_WT + G * W * 4 + G * 8, 8);
     static constexpr int STAGES_FIT = (220 * 1024 - R_BAR - 64 * 8 - 16) / STAGE_BYTES;
     // Each consumer warp owns SW consecutive stages that it consumes in
     // order (an mbarrier parity wait is only exact when the waiter is at
     // most one phase ahead of the barrier).
-    static constexpr int SW_FIT = STAGES_FIT / kConsumerWarps;
+    static constexpr int SW_FIT = STAGES_FIT / W;
     static constexpr int SW = SW_FIT < 6 ? SW_FIT : 6;
-    static constexpr int STAGES = SW * kConsumerWarps;
-    static constexpr int NBAR = 2 * STAGES + 2 * kItemRing + 2 * kMergeBufs;
+    static constexpr int STAGES = SW * W;
+    static constexpr int NBAR = 2 * STAGES + 2 * kItemRing + 2 * MERGE_BUFS;
     static constexpr int OFF_REST = STAGES * STAGE_BYTES;
     static constexpr int OFF_ITEMQ = OFF_REST + R_ITEMQ;
     static constexpr int OFF_DESC = OFF_REST + R_DESC;
@@ -368,7 +380,7 @@ __device__ void run_producer(const DecodeParams& P, uint8_t* smem, const Bars& B
             const long long down = b - P0, up = P0 + u - b;
             nparts = (b > P0 && b < P0 + u && min(down, up) > shift_max) ? 2 : 1;
         }
-        const int rot = static_cast<int>(pos % kConsumerWarps);
+        const int rot = static_cast<int>(pos % C::W);
         const int row = P.qsl ? __ldg(P.qsl + s) : s;
         const int32_t* trow = P.block_tables + static_cast<size_t>(s) * P.max_blocks;
         // First batch of table entries, requested before the descriptor work.
@@ -411,10 +423,10 @@ __device__ void run_producer(const DecodeParams& P, uint8_t* smem, const Bars& B
             int e_next = 0;
             if (lane < kBatch && base + kBatch + lane < b1) e_next = __ldg(trow + base + kBatch + lane);
             const int bl = base - b0 + lane;  // block index within the item
-            const int w = (bl + rot) % kConsumerWarps;
-            const int first_w = (w - rot + kConsumerWarps) % kConsumerWarps;
+            const int w = (bl + rot) % C::W;
+            const int first_w = (w - rot + C::W) % C::W;
             const uint32_t jw = static_cast<uint32_t>(__shfl_sync(FULL, static_cast<int>(given), w)) +
-                                static_cast<uint32_t>((bl - first_w) / kConsumerWarps);
+                                static_cast<uint32_t>((bl - first_w) / C::W);
             const uint32_t st = static_cast<uint32_t>(w * C::SW) + jw % C::SW;
             int bad = 0;
             if (lane < cnt) {
@@ -442,11 +454,11 @@ __device__ void run_producer(const DecodeParams& P, uint8_t* smem, const Bars& B
             e = e_next;
         }
         // Blocks each warp received from this item.
-        if (lane < kConsumerWarps && !aborted) {
-            const int first_w = (lane - rot + kConsumerWarps) % kConsumerWarps;
+        if (lane < C::W && !aborted) {
+            const int first_w = (lane - rot + C::W) % C::W;
             const int nb = b1 - b0;
             if (first_w < nb)
-                given += static_cast<uint32_t>((nb - first_w + kConsumerWarps - 1) / kConsumerWarps);
+                given += static_cast<uint32_t>((nb - first_w + C::W - 1) / C::W);
         }
         return u1;
     };
@@ -515,7 +527,7 @@ __device__ void run_producer(const DecodeParams& P, uint8_t* smem, const Bars& B
         *abort_flag = 1;
         record_error(P.err, kErrTimeout, 1u);
         // Never leave with bulk copies still in flight.
-        if (lane < kConsumerWarps) {
+        if (lane < C::W) {
             for (uint32_t k = 0; k < C::SW; ++k) {
                 if (k < given) {
                     const uint32_t jl = given - 1 - ((given - 1 - k) % C::SW);  // last use of stage k
@@ -577,8 +589,8 @@ __device__ void run_consumer(const DecodeParams& P, uint8_t* smem, const Bars& B
         // length is not a multiple of 8 spread over the warps while every
         // item is summed in an order that does not depend on which CTA took
         // it (results are bitwise reproducible).
-        const int first = (warp - d.rot + kConsumerWarps) % kConsumerWarps;
-        for (int b = first; b < nb; b += kConsumerWarps) {
+        const int first = (warp - d.rot + C::W) % C::W;
+        for (int b = first; b < nb; b += C::W) {
             const uint32_t st = static_cast<uint32_t>(warp * C::SW) + taken % C::SW;
             if (*abort_flag || !mbar_wait_warp(&B.full[st], (taken / C::SW) & 1)) {
                 ok = false;
@@ -593,8 +605,8 @@ __device__ void run_consumer(const DecodeParams& P, uint8_t* smem, const Bars& B
         }
         if (!ok) break;
         // Publish this warp's state for the merger.
-        const int buf = item_seq % kMergeBufs;
-        if (!mbar_wait_warp(&B.mempty[buf], ((item_seq / kMergeBufs) & 1) ^ 1)) {
+        const int buf = item_seq % C::MERGE_BUFS;
+        if (!mbar_wait_warp(&B.mempty[buf], ((item_seq / C::MERGE_BUFS) & 1) ^ 1)) {
             ok = false;
             break;
         }
@@ -610,9 +622,9 @@ __device__ void run_consumer(const DecodeParams& P, uint8_t* smem, const Bars& B
                     o2[g][j].y += __shfl_xor_sync(0xffffffffu, o2[g][j].y, off);
                 }
             }
-            if (lane == 0) ml[(buf * kConsumerWarps + warp) * G + g] = make_float2(m[g], lt);
+            if (lane == 0) ml[(buf * C::W + warp) * G + g] = make_float2(m[g], lt);
             if (sub == 0) {
-                float4* dst = reinterpret_cast<float4*>(mo + ((buf * kConsumerWarps + warp) * G + g) * D + cl * 8);
+                float4* dst = reinterpret_cast<float4*>(mo + ((buf * C::W + warp) * G + g) * D + cl * 8);
                 dst[0] = make_float4(o2[g][0].x, o2[g][0].y, o2[g][1].x, o2[g][1].y);
                 dst[1] = make_float4(o2[g][2].x, o2[g][2].y, o2[g][3].x, o2[g][3].y);
             }
@@ -634,7 +646,7 @@ __device__ void run_merger(const DecodeParams& P, uint8_t* smem, const Bars& B, 
     const float* mo = reinterpret_cast<const float*>(smem + C::OFF_MO);
     const float2* ml = reinterpret_cast<const float2*>(smem + C::OFF_ML);
     float* wsm = reinterpret_cast<float*>(smem + C::OFF_WT);
-    float2* msm = reinterpret_cast<float2*>(smem + C::OFF_WT + G * kConsumerWarps * 4);
+    float2* msm = reinterpret_cast<float2*>(smem + C::OFF_WT + G * C::W * 4);
     uint32_t item_seq = 0;
     bool ok = true;
     while (true) {
@@ -647,8 +659,8 @@ __device__ void run_merger(const DecodeParams& P, uint8_t* smem, const Bars& B, 
         if (d.s < 0) break;
         __syncwarp();
         if (lane == 0) mbar_arrive(&B.iempty[slot]);
-        const int buf = item_seq % kMergeBufs;
-        if (!mbar_wait_warp(&B.mfull[buf], (item_seq / kMergeBufs) & 1)) {
+        const int buf = item_seq % C::MERGE_BUFS;
+        if (!mbar_wait_warp(&B.mfull[buf], (item_seq / C::MERGE_BUFS) & 1)) {
             ok = false;
             break;
         }
@@ -658,23 +670,25 @@ __device__ void run_merger(const DecodeParams& P, uint8_t* smem, const Bars& B, 
         // the item's G output rows (contiguous in out and in part_o), with
         // the W chunk loads issued together.
         const unsigned FULL = 0xffffffffu;
-        constexpr int W = kConsumerWarps;
+        constexpr int W = C::W;
         constexpr int CH = G * D / 4;
+        constexpr int WL = C::MERGE_LANES;
 #pragma unroll
-        for (int i0 = 0; i0 < G * W; i0 += 32) {
+        for (int i0 = 0; i0 < G * WL; i0 += 32) {
             const int i = i0 + lane;
-            const int w = i % W;
-            const float2 e = (i < G * W) ? ml[(buf * W + w) * G + i / W] : make_float2(-INFINITY, 0.f);
+            const int w = i % WL, gi = i / WL;
+            const bool live = gi < G && w < W;
+            const float2 e = live ? ml[(buf * W + w) * G + gi] : make_float2(-INFINITY, 0.f);
             float M = e.x;
 #pragma unroll
-            for (int o = 1; o < W; o <<= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, o));
+            for (int o = 1; o < WL; o <<= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, o));
             const float wt = (e.x == -INFINITY) ? 0.f : fast_exp2(e.x - M);
             float L = e.y * wt;
 #pragma unroll
-            for (int o = 1; o < W; o <<= 1) L += __shfl_xor_sync(FULL, L, o);
-            if (i < G * W) {
-                wsm[i] = wt;
-                if (w == 0) msm[i / W] = make_float2(M, L);
+            for (int o = 1; o < WL; o <<= 1) L += __shfl_xor_sync(FULL, L, o);
+            if (live) {
+                wsm[gi * W + w] = wt;
+                if (w == 0) msm[gi] = make_float2(M, L);
             }
         }
         __syncwarp();
@@ -914,7 +928,7 @@ __device__ void prefetch_first_blocks(const DecodeParams& P, int lane, int max_u
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams P) {
+__global__ void __launch_bounds__(Cfg<D, G>::THREADS, 1) decode_kernel(const DecodeParams P) {
     using C = Cfg<D, G>;
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
@@ -924,7 +938,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
     B.ifull = bars + 2 * C::STAGES;
     B.iempty = B.ifull + kItemRing;
     B.mfull = B.iempty + kItemRing;
-    B.mempty = B.mfull + kMergeBufs;
+    B.mempty = B.mfull + C::MERGE_BUFS;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_FLAG);
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
@@ -935,10 +949,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
         }
         for (int i = 0; i < kItemRing; ++i) {
             mbar_init(&B.ifull[i], 1);
-            mbar_init(&B.iempty[i], kConsumerWarps + 1);
+            mbar_init(&B.iempty[i], C::W + 1);
         }
-        for (int i = 0; i < kMergeBufs; ++i) {
-            mbar_init(&B.mfull[i], kConsumerWarps);
+        for (int i = 0; i < C::MERGE_BUFS; ++i) {
+            mbar_init(&B.mfull[i], C::W);
             mbar_init(&B.mempty[i], 1);
         }
         *abort_flag = 0;
@@ -948,15 +962,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
     __syncthreads();
     // Until griddep_wait() returns, only L2 prefetches touch global memory.
     // Consumer warps read shared memory only and need no wait.
-    if (warp == kProducerWarp) {
+    if (warp == C::PRODUCER_WARP) {
         griddep_wait();
         run_producer<D, G>(P, smem, B, abort_flag, lane);
-    } else if (warp == kMergerWarp) {
+    } else if (warp == C::MERGER_WARP) {
         prefetch_first_blocks<D, G>(P, lane, C::STAGES);
         griddep_wait();
         run_merger<D, G>(P, smem, B, abort_flag, lane);
     } else {
-        prefetch_inputs<D>(P, threadIdx.x, kConsumerWarps * 32);
+        prefetch_inputs<D>(P, threadIdx.x, C::W * 32);
         run_consumer<D, G>(P, smem, B, abort_flag, warp, lane);
     }
 }
@@ -973,7 +987,7 @@ cudaError_t launch_one(const DecodeParams& P, int grid, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    return launch_overlapped(decode_kernel<D, G>, dim3(grid), dim3(kThreads), C::SMEM, stream, P);
+    return launch_overlapped(decode_kernel<D, G>, dim3(grid), dim3(C::THREADS), C::SMEM, stream, P);
 }
 
 template <int D>
