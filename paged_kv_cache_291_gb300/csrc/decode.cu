@@ -69,6 +69,7 @@ constexpr int consumer_warps() {
 constexpr int kItemRing = 8;
 constexpr int kMinRangeUnits = 8;  // smallest automatic range (blocks per CTA)
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 // One item = the part of one (sequence, kv head) pair that falls in one
 // range of units.  When the pair spans several ranges (nparts > 1) each part
@@ -250,14 +251,20 @@ __device__ __forceinline__ void compute_block(const uint8_t* kst, const uint8_t*
             float sc = transpose_reduce<C::NV, C::LPR>(acc[g], lane);
             sc = (myrow < valid) ? sc : -INFINITY;
             const float mb = warp_max(sc);
-            const float mn = fmaxf(m[g0 + g], mb);
-            const float alpha = fast_exp2(m[g0 + g] - mn);
-            const float p = fast_exp2(sc - mn);
-            lsum[g0 + g] = fmaf(lsum[g0 + g], alpha, (lane & 1) ? 0.f : p);
-            const float2 al = make_float2(alpha, alpha);
+            // The reference m moves only when a block's maximum exceeds it by
+            // more than 2^8 (log2 units; the condition is warp-uniform): p
+            // stays below 256 and O and l are rescaled on few blocks.  The
+            // merge divides by l taken against the same reference.
+            if (mb > m[g0 + g] + kRescaleThreshold) {
+                const float alpha = fast_exp2(m[g0 + g] - mb);
+                lsum[g0 + g] *= alpha;
+                const float2 al = make_float2(alpha, alpha);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) o2[g0 + g][j] = __fmul2_rn(o2[g0 + g][j], al);
-            m[g0 + g] = mn;
+                for (int j = 0; j < 4; ++j) o2[g0 + g][j] = __fmul2_rn(o2[g0 + g][j], al);
+                m[g0 + g] = mb;
+            }
+            const float p = fast_exp2(sc - m[g0 + g]);
+            lsum[g0 + g] += (lane & 1) ? 0.f : p;
             if (!(lane & 1)) psm[(g0 + g) * kBlockSize + myrow] = make_float2(p, p);
         }
     }
