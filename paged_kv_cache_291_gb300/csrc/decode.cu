@@ -265,7 +265,7 @@ __device__ __forceinline__ void compute_block(const uint8_t* kst, const uint8_t*
             }
             const float p = fast_exp2(sc - m[g0 + g]);
             lsum[g0 + g] += (lane & 1) ? 0.f : p;
-            if (!(lane & 1)) psm[(g0 + g) * kBlockSize + myrow] = make_float2(p, p);
+            if (!(lane & 1)) psm[myrow * G + g0 + g] = make_float2(p, p);
         }
     }
     __syncwarp();
@@ -276,13 +276,26 @@ __device__ __forceinline__ void compute_block(const uint8_t* kst, const uint8_t*
             const uint4 u = lds128(vst + row * D * 2 + cl * 16);
             const float2 v0 = bf16x2_to_float2(u.x), v1 = bf16x2_to_float2(u.y);
             const float2 v2 = bf16x2_to_float2(u.z), v3 = bf16x2_to_float2(u.w);
+            // p of this row for every head: psm is [row][head] (p, p) pairs,
+            // read two heads per 16-byte load.
+            float2 pr[G];
+            if constexpr (G % 2 == 0) {
+#pragma unroll
+                for (int g = 0; g < G; g += 2) {
+                    const float4 q4 = *reinterpret_cast<const float4*>(&psm[row * G + g]);
+                    pr[g] = make_float2(q4.x, q4.y);
+                    pr[g + 1] = make_float2(q4.z, q4.w);
+                }
+            } else {
+#pragma unroll
+                for (int g = 0; g < G; ++g) pr[g] = psm[row * G + g];
+            }
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-                const float2 pp = psm[g * kBlockSize + row];
-                o2[g][0] = __ffma2_rn(pp, v0, o2[g][0]);
-                o2[g][1] = __ffma2_rn(pp, v1, o2[g][1]);
-                o2[g][2] = __ffma2_rn(pp, v2, o2[g][2]);
-                o2[g][3] = __ffma2_rn(pp, v3, o2[g][3]);
+                o2[g][0] = __ffma2_rn(pr[g], v0, o2[g][0]);
+                o2[g][1] = __ffma2_rn(pr[g], v1, o2[g][1]);
+                o2[g][2] = __ffma2_rn(pr[g], v2, o2[g][2]);
+                o2[g][3] = __ffma2_rn(pr[g], v3, o2[g][3]);
             }
         }
     }
