@@ -250,7 +250,7 @@ __device__ __forceinline__ void compute_block(const uint8_t* kst, const uint8_t*
         for (int g = 0; g < C::HG; ++g) {
             float sc = transpose_reduce<C::NV, C::LPR>(acc[g], lane);
             sc = (myrow < valid) ? sc : -INFINITY;
-            const float mb = warp_max(sc);
+            const float mb = warp_max_redux(sc);
             // The reference m moves only when a block's maximum exceeds it by
             // more than 2^8 (log2 units; the condition is warp-uniform): p
             // stays below 256 and O and l are rescaled on few blocks.  The

@@ -162,6 +162,14 @@ __device__ __forceinline__ float warp_max(float v) {
     return v;
 }
 
+// Maximum over the full warp in one instruction (sm_100 family); inputs are
+// finite or -inf.
+__device__ __forceinline__ float warp_max_redux(float v) {
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
