@@ -26,6 +26,11 @@
  *    an invalid id is never dereferenced.
  *  - bf16 is IEEE bfloat16; out is fp32.
  *  - Device pointers must be 16-byte aligned.
+ *  - Kernels are launched with programmatic stream serialization: one may
+ *    start while the previous kernel on the stream finishes, but it reads and
+ *    writes nothing in global memory (other than L2 prefetches) before that
+ *    kernel has completed, so results are those of serialised launches.  The
+ *    environment variable PKV_OVERLAP=0 turns this off.
  *
  * Cache layout ([KV2] section 2, "Blocks and block tables")
  * ----------------------------------------------------------
