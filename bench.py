@@ -627,6 +627,8 @@ def run_ours(args):
                    "l2": f"{R} rotated input replicas of {pool_bytes / 1e6:.0f} MB pools (> 129 MB L2 in total)",
                    "graph": "CUDA graph per cycle of replicas"},
         "gpu_launches": launches_per_step * args.steps,
+        # query rows (decode rows and prefill tokens) per second over the whole step
+        "tokens_per_s": world * Tq / (step_ms_max * 1e-3),
         "e2e": {"value": world * B / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps, "ms_per_step": e2e_ms},
     }
