@@ -62,7 +62,7 @@ typedef enum pkv_status {
     PKV_ERR_ALIAS = 6,       /* copy_blocks: a dst repeats, or a dst is also a src          */
     PKV_ERR_WORKSPACE = 7,   /* workspace NULL, too small or not 256-byte aligned           */
     PKV_ERR_ALIGN = 8,       /* a device pointer is not 16-byte aligned                     */
-    PKV_ERR_RANGE = 9,       /* (device) block id, slot or context length out of range     */
+    PKV_ERR_RANGE = 9,       /* (device) block id, slot, length or V value out of range     */
     PKV_ERR_TIMEOUT = 10,    /* (device) a bounded wait inside a kernel expired             */
     PKV_ERR_CUDA = 11,       /* a CUDA runtime call failed (see pkv_last_cuda_error)        */
     PKV_ERR_UNSUPPORTED = 12, /* the current device is not compute capability 10.3          */
@@ -186,8 +186,12 @@ size_t pkv_prefill_workspace_size(int32_t num_seqs, int32_t num_tokens, int32_t 
  *   out                   fp32 [num_tokens][num_q_heads][head_dim]
  *   workspace             >= pkv_prefill_workspace_size() bytes, 256-byte
  *                         aligned, zero-filled before first use (left zeroed)
- *   Query rows are computed on tcgen05 tensor cores (P rounded to bf16 for
- *   the P.V product); decode rows take the decode kernel.
+ *   Query rows are computed on tcgen05 tensor cores: Q.K^T in bf16, P.V in
+ *   fp16 (P rounded to fp16, V converted from bf16 exactly for
+ *   2^-14 <= |v| <= 65504); decode rows take the decode kernel.  A V entry
+ *   of a visible key that fp16 cannot hold (|v| > 65504, inf or NaN) raises
+ *   PKV_ERR_RANGE (detail: the sequence); the output of that call is then
+ *   unspecified.
  */
 pkv_status pkv_chunked_prefill_attention(const pkv_cache_t* cache, const void* q, int32_t num_q_heads,
                                          int32_t num_tokens, const int32_t* query_start_loc,

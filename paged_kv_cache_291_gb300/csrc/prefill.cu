@@ -14,24 +14,28 @@
 //    one unit when Hq/Hkv is odd).  Both units read the same K/V tiles, so a
 //    tile is loaded once for two heads.  Warp 8 loads the two Q tiles and
 //    the K/V key tiles (128 keys = 8 paged blocks, each block a 16-row TMA
-//    box with 128-byte swizzle) into a 2-stage ring.  Warp 9 issues
-//    tcgen05.mma.  Warps 0-3 and 4-7 are the softmax warpgroups of units 0
-//    and 1 (TMEM lane = query row), so one unit's softmax overlaps the
-//    other unit's MMAs.
+//    box with 128-byte swizzle) into rings of 2 (K) and 3 (V) stages.
+//    Warp 9 issues tcgen05.mma.  Warps 0-3 and 4-7 are the softmax
+//    warpgroups of units 0 and 1 (TMEM lane = query row), so one unit's
+//    softmax overlaps the other unit's MMAs.
 //  * Per unit, TMEM holds S (128 fp32 columns) and O (128 columns).  S =
 //    Q K^T is written there; the softmax reads it, then writes P into the
-//    same columns as bf16, and O += P V takes P straight from TMEM (the A
-//    operand of the MMA) with V from shared memory (MN-major operand).
-//  * P goes in as two bf16 matrices, its truncation and the truncation of
-//    the (exact) residual, so P = P_hi + P_lo to within 2^-14 relative, and
-//    O += P_hi V + P_lo V: a single bf16 P (2^-9 relative) can miss a 2e-3
-//    absolute bound when a few keys carry all the weight.  l sums P in fp32.
+//    first 64 of the same columns as fp16 pairs, and O += P V takes P
+//    straight from TMEM (the A operand of the MMA) with V from shared
+//    memory (MN-major operand).
+//  * P V runs in fp16: P (in [0, 256]) is rounded to fp16, 2^-11 relative,
+//    where a bf16 P (2^-9) can miss a 2e-3 absolute bound when a few keys
+//    carry all the weight.  The MMA needs V in the same type, so warps 0-7
+//    rewrite each V tile in shared memory from bf16 to fp16 in place, an
+//    eighth each, between their softmax passes (exact for 2^-14 <= |v| <=
+//    65504, absolute error at most 2^-25 below; a larger |v| becomes inf
+//    and is reported as PKV_ERR_RANGE).  l sums P in fp32.
 //  * Online softmax in the log2 domain; the running maximum is only moved
 //    (and O rescaled in TMEM) when it grows by more than 2^8; the final
 //    O / l uses the same reference, so the result is unchanged.
 //  * Keys past the last query position of the tile are masked; V rows past
-//    it are zeroed in shared memory (a 0 weight times a NaN in an unused
-//    slot would otherwise poison the MMA).
+//    it are zeroed in shared memory during the conversion (a 0 weight
+//    times a NaN in an unused slot would otherwise poison the MMA).
 //  * Every wait is bounded; TMEM is freed on every exit path.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -59,11 +63,12 @@ constexpr int kPanelBytes = 128 * 128;               // 128 rows x 128 B (64 bf1
 constexpr int kTileBytes = 2 * kPanelBytes;          // [128][128] bf16 as two swizzled panels
 constexpr int kBoxBytes = kBlockSize * 128;          // one 16-row box of one panel
 
+constexpr int kVStages = 3;                          // V waits longest (load + fp16 conversion)
 constexpr int OFF_Q = 0;                             // kUnits Q tiles
 constexpr int OFF_K = OFF_Q + kUnits * kTileBytes;   // 2 stages
-constexpr int OFF_V = OFF_K + 2 * kTileBytes;        // 2 stages
-constexpr int OFF_BAR = OFF_V + 2 * kTileBytes;
-constexpr int NBAR = 15;
+constexpr int OFF_V = OFF_K + 2 * kTileBytes;        // kVStages stages
+constexpr int OFF_BAR = OFF_V + kVStages * kTileBytes;
+constexpr int NBAR = 20;
 constexpr int OFF_INFO = OFF_BAR + NBAR * 8;         // tile info (ints)
 constexpr int OFF_TMEM = OFF_INFO + 16 * 4;
 constexpr int SMEM_USED = OFF_TMEM + 16;
@@ -74,6 +79,7 @@ constexpr int kSoftmaxWarps = 4;                     // per unit
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kThreads = 32 * 10;
+constexpr int kConvWarps = kSoftmaxWarps * kUnits;   // warps 0-7 also convert V tiles
 
 constexpr uint32_t kTmemCols = 512;
 // Unit u: S/P at columns [256u, 256u + 128), O at [256u + 128, 256u + 256).
@@ -98,11 +104,12 @@ enum {
     B_QFULL = 0,
     B_KFULL = 1,   // +stage
     B_KEMPTY = 3,  // +stage
-    B_VFULL = 5,   // +stage
-    B_VEMPTY = 7,  // +stage
-    B_SFULL = 9,   // +unit
-    B_PFULL = 11,  // +unit (4 arrivals)
-    B_ODONE = 13,  // +unit
+    B_VFULL = 5,   // +V stage
+    B_VEMPTY = 8,  // +V stage
+    B_SFULL = 11,  // +unit
+    B_PFULL = 13,  // +unit (4 arrivals)
+    B_ODONE = 15,  // +unit
+    B_VCONV = 17,  // +V stage (8 arrivals): V tile converted to fp16
 };
 
 // Tile info slots (written by warp 0 before the CTA-wide sync).
@@ -112,6 +119,20 @@ __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// bf16 pair -> fp16 pair (round to nearest even: exact for 2^-14 <= |v| <=
+// 65504); `vmax` tracks the largest magnitude seen.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x, float& vmax) {
+    const float lo = __uint_as_float(x << 16), hi = __uint_as_float(x & 0xFFFF0000u);
+    vmax = fmax3(vmax, fabsf(lo), fabsf(hi));
+    return tc::pack_f16x2(lo, hi);
 }
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) { return mbar_wait_warp(bar, parity); }
@@ -200,7 +221,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (threadIdx.x == 32 * kMmaWarp) {
         for (int i = 0; i < NBAR; ++i)
-            mbar_init(&bar[i], (i == B_PFULL || i == B_PFULL + 1) ? kSoftmaxWarps : 1);
+            mbar_init(&bar[i], (i == B_PFULL || i == B_PFULL + 1) ? kSoftmaxWarps
+                                : (i >= B_VCONV && i < B_VCONV + kVStages) ? kConvWarps : 1u);
         fence_mbar_init();
     }
     if (warp == kLoadWarp) {
@@ -267,15 +289,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (!warp_wait(&bar[B_VEMPTY + st], ph ^ 1)) { ok = false; break; }
+            const int sv = j % kVStages;
+            if (!warp_wait(&bar[B_VEMPTY + sv], ((j / kVStages) & 1) ^ 1)) { ok = false; break; }
             if (lane == 0) {
-                mbar_arrive_expect_tx(&bar[B_VFULL + st], bytes);
-                uint8_t* dst = smem + OFF_V + st * kTileBytes;
+                mbar_arrive_expect_tx(&bar[B_VFULL + sv], bytes);
+                uint8_t* dst = smem + OFF_V + sv * kTileBytes;
 #pragma unroll
                 for (int b = 0; b < kBlocksPerTile; ++b) {
                     if (b < nvb) {
-                        tc::tma_load_2d(dst + b * kBoxBytes, &tm_v, 0, rowsel[b], &bar[B_VFULL + st]);
-                        tc::tma_load_2d(dst + kPanelBytes + b * kBoxBytes, &tm_v, 64, rowsel[b], &bar[B_VFULL + st]);
+                        tc::tma_load_2d(dst + b * kBoxBytes, &tm_v, 0, rowsel[b], &bar[B_VFULL + sv]);
+                        tc::tma_load_2d(dst + kPanelBytes + b * kBoxBytes, &tm_v, 64, rowsel[b], &bar[B_VFULL + sv]);
                     }
                 }
             }
@@ -284,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kMmaWarp && nt > 0) {
         // ------------------------------------------------------ MMA issuer
         constexpr uint32_t kIdescQK = tc::idesc_bf16_f32(kTileM, kTileN, 0, 0);
-        constexpr uint32_t kIdescPV = tc::idesc_bf16_f32(kTileM, kHeadDim, 0, 1);
+        constexpr uint32_t kIdescPV = tc::idesc_f16_f32(kTileM, kHeadDim, 0, 1);
         // S_u = Q_u K^T for K tile j into the unit's S/P columns.
         auto qk = [&](int u, int j) {
             const uint32_t sq = smem_addr(smem + OFF_Q + u * kTileBytes);
@@ -297,17 +320,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc::mma_commit(&bar[B_SFULL + u]);
         };
-        // O_u += P_u V for V tile j.  Key step k covers keys 16k..16k+15:
-        // P_hi in columns [16k, 16k+8) of the unit's S/P block, P_lo in
-        // [16k+8, 16k+16).
+        // O_u += P_u V for V tile j, both in fp16.  Key step k covers keys
+        // 16k..16k+15, held as P in columns [8k, 8k+8) of the unit's S/P
+        // block.
         auto pv = [&](int u, int j) {
-            const uint32_t svb = smem_addr(smem + OFF_V + (j & 1) * kTileBytes);
+            const uint32_t svb = smem_addr(smem + OFF_V + (j % kVStages) * kTileBytes);
 #pragma unroll
             for (int k = 0; k < kTileN / 16; ++k) {
                 const uint64_t vdesc = tc::smem_desc_sw128(svb + k * 2048, kPanelBytes, 1024);
-                tc::mma_bf16_ts(tmem + col_o(u), tmem + col_s(u) + 16 * k, vdesc, kIdescPV,
+                tc::mma_bf16_ts(tmem + col_o(u), tmem + col_s(u) + 8 * k, vdesc, kIdescPV,
                                 (j > 0 || k > 0) ? 1u : 0u);
-                tc::mma_bf16_ts(tmem + col_o(u), tmem + col_s(u) + 16 * k + 8, vdesc, kIdescPV, 1u);
             }
             tc::mma_commit(&bar[B_ODONE + u]);
         };
@@ -324,28 +346,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // next tile's S_u.  Unit 1's softmax then runs while unit 0's MMAs
         // execute and the other way round.
         for (int j = 0; j < nt && ok; ++j) {
-            const int st = j & 1;
-            if (!warp_wait(&bar[B_VFULL + st], (j >> 1) & 1)) { ok = false; break; }
-            uint8_t* sv = smem + OFF_V + st * kTileBytes;
-            if (j == nt - 1 && klast < kTileN) {
-                // Zero V rows of keys past the last visible position (unused
-                // slots of the last block and blocks never loaded).
-                const int nrows = kTileN - klast;
-                for (int i = lane; i < nrows * 16; i += 32) {
-                    const int r = klast + (i >> 4);
-                    const int panel = (i >> 3) & 1;
-                    const int chunk = i & 7;
-                    tc::sts128(smem_addr(sv + panel * kPanelBytes + r * 128 + chunk * 16), 0u, 0u, 0u, 0u);
-                }
-                tc::fence_proxy_async_smem();
-                __syncwarp();
-            }
+            const int sv = j % kVStages;
+            if (!warp_wait(&bar[B_VCONV + sv], (j / kVStages) & 1)) { ok = false; break; }
             const bool next = j + 1 < nt;
             if (next && !warp_wait(&bar[B_KFULL + ((j + 1) & 1)], ((j + 1) >> 1) & 1)) { ok = false; break; }
             for (int u = 0; u < units && ok; ++u) {
                 if (!warp_wait(&bar[B_PFULL + u], j & 1)) { ok = false; break; }
                 tc::fence_after_sync();
-                if (lane == 0) pv(u, j);
+                if (lane == 0) {
+                    pv(u, j);
+                    if (u == units - 1) tc::mma_commit(&bar[B_VEMPTY + sv]);  // V tile j read
+                }
                 __syncwarp();
                 if (next) {
                     if (!warp_wait(&bar[B_ODONE + u], j & 1)) { ok = false; break; }  // P_u(j) consumed
@@ -355,15 +366,49 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (!ok) break;
-            if (lane == 0) {
-                tc::mma_commit(&bar[B_VEMPTY + st]);
-                if (next) tc::mma_commit(&bar[B_KEMPTY + ((j + 1) & 1)]);
-            }
+            if (lane == 0 && next) tc::mma_commit(&bar[B_KEMPTY + ((j + 1) & 1)]);
             __syncwarp();
         }
-    } else if (warp < kSoftmaxWarps * units) {
-        // ------------------------------------------------------ softmax rows
+    } else if (warp < kConvWarps) {
+        // ------------------------------------------------------ V to fp16
+        // Warps 0-7 convert each V tile in place, an eighth (256 16-byte
+        // chunks, contiguous) each; the map is elementwise, so the 128-byte
+        // swizzle is irrelevant.  On the last tile, rows of keys past the last
+        // visible position (unused slots of the last block, blocks never
+        // loaded) are zeroed instead: a 0 weight times a NaN would poison
+        // the MMA.  A softmax warp converts tile j right before it waits for
+        // S of tile j, while the MMAs run.  Spread over eight warps (all four
+        // SM sub-partitions), the work stays off the softmax's critical
+        // path; two dedicated warps on two sub-partitions slowed it down.
+        float vmax = 0.f;
+        auto convert_v = [&](int j) -> bool {
+            const int sv = j % kVStages;
+            if (!warp_wait(&bar[B_VFULL + sv], (j / kVStages) & 1)) return false;
+            const uint32_t base = smem_addr(smem + OFF_V + sv * kTileBytes) + static_cast<uint32_t>(warp) * 4096u;
+            const int nrows = (j == nt - 1) ? klast : kTileN;
+#pragma unroll
+            for (int n = 0; n < 8; ++n) {
+                const int i = warp * 256 + n * 32 + lane;  // chunk of the tile
+                const uint32_t a = base + static_cast<uint32_t>(n * 32 + lane) * 16u;
+                if (((i >> 3) & (kTileN - 1)) < nrows) {
+                    uint32_t x[4];
+                    tc::lds128(a, x);
+                    tc::sts128(a, bf16x2_to_f16x2(x[0], vmax), bf16x2_to_f16x2(x[1], vmax),
+                               bf16x2_to_f16x2(x[2], vmax), bf16x2_to_f16x2(x[3], vmax));
+                } else {
+                    tc::sts128(a, 0u, 0u, 0u, 0u);
+                }
+            }
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[B_VCONV + sv]);
+            return true;
+        };
         const int u = warp / kSoftmaxWarps;
+        if (u >= units) {
+            for (int j = 0; j < nt && ok; ++j) ok = convert_v(j);
+        } else {
+        // ------------------------------------------------------ softmax rows
         const int m = (warp % kSoftmaxWarps) * 32 + lane;
         const int h = h0 + u;
         const int pos = (m < rows) ? pmin + m : pmax;
@@ -372,7 +417,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < 4; ++k) l2[k] = make_float2(0.f, 0.f);
         for (int j = 0; j < nt && ok; ++j) {
-            if (!warp_wait(&bar[B_SFULL + u], j & 1)) { ok = false; break; }
+            // V tile j first (unit 1 gets here while unit 0 still works on
+            // tile j), then S of tile j.
+            if (!convert_v(j) || !warp_wait(&bar[B_SFULL + u], j & 1)) { ok = false; break; }
             tc::fence_after_sync();
             const int kbase = j * kTileN;
             // Rows grow down the warp, so the tile is fully visible to the
@@ -394,7 +441,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k = 0; k < 8; ++k) mp[k] = -INFINITY;
             if (full) {
 #pragma unroll
-                for (int i = 0; i < kTileN; ++i) mp[i % 8] = fmaxf(mp[i % 8], __uint_as_float(sr[i]));
+                for (int i = 0; i < kTileN; i += 2)
+                    mp[(i / 2) % 8] = fmax3(mp[(i / 2) % 8], __uint_as_float(sr[i]), __uint_as_float(sr[i + 1]));
             } else {
 #pragma unroll
                 for (int i = 0; i < kTileN; ++i)
@@ -423,38 +471,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            // Pass 2: P = exp2(scale * s - m_used) as bf16 P_hi + P_lo,
-            // written over the S columns: 32 keys -> 16 hi words + 16 lo
-            // words, laid out per 16-key step as [8 hi | 8 lo].  The row sum
+            // Pass 2: P = exp2(scale * s - m_used) as fp16, written over the
+            // S columns: keys 2i, 2i+1 of the tile in column i.  The row sum
             // goes to 4 independent fp32x2 accumulators.
             const float2 sc2 = make_float2(P.scale_log2, P.scale_log2);
             const float2 nm2 = make_float2(-m_used, -m_used);
 #pragma unroll
-            for (int c = 0; c < kTileN / 32; ++c) {
+            for (int c = 0; c < kTileN / 64; ++c) {
                 uint32_t w[32];
 #pragma unroll
-                for (int t = 0; t < 2; ++t) {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int k0 = 32 * c + 16 * t + 2 * i;
-                        const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[k0]), __uint_as_float(sr[k0 + 1])),
-                                                    sc2, nm2);
-                        float2 p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-                        if (!full) {  // keys past the row's position (NaN in unused slots included)
-                            if (kbase + k0 > pos) p.x = 0.f;
-                            if (kbase + k0 + 1 > pos) p.y = 0.f;
-                        }
-                        // P_hi: p truncated to bf16 (its high 16 bits), P_lo:
-                        // the exact residual truncated likewise.  Byte
-                        // permutes instead of conversions keep the special
-                        // function unit free for ex2.
-                        const uint32_t ux = __float_as_uint(p.x), uy = __float_as_uint(p.y);
-                        const float2 res = __fadd2_rn(p, make_float2(-__uint_as_float(ux & 0xFFFF0000u),
-                                                                     -__uint_as_float(uy & 0xFFFF0000u)));
-                        w[16 * t + i] = __byte_perm(ux, uy, 0x7632);
-                        w[16 * t + 8 + i] = __byte_perm(__float_as_uint(res.x), __float_as_uint(res.y), 0x7632);
-                        l2[i % 4] = __fadd2_rn(l2[i % 4], p);
+                for (int i = 0; i < 32; ++i) {
+                    const int k0 = 64 * c + 2 * i;
+                    const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[k0]), __uint_as_float(sr[k0 + 1])),
+                                                sc2, nm2);
+                    float2 p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                    if (!full) {  // keys past the row's position (NaN in unused slots included)
+                        if (kbase + k0 > pos) p.x = 0.f;
+                        if (kbase + k0 + 1 > pos) p.y = 0.f;
                     }
+                    w[i] = tc::pack_f16x2(p.x, p.y);
+                    l2[i % 4] = __fadd2_rn(l2[i % 4], p);
                 }
                 tc::tmem_st32(tmem_lane_addr(tmem, warp, col_s(u) + 32 * c), w);
             }
@@ -501,6 +537,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             float* orow = P.out + (static_cast<size_t>(row0 + m) * P.hq + h) * kHeadDim;
             for (int c = 0; c < kHeadDim; c += 4) *reinterpret_cast<float4*>(orow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
+        }
+        // A V entry beyond the fp16 range (inf included) became inf.
+        if (vmax > 65504.f) record_error(P.err, kErrRange, static_cast<uint32_t>(s));
     }
     if (!ok) record_error(P.err, kErrTimeout, 0x100u + static_cast<uint32_t>(warp));
     // ---------------------------------------------------------- teardown

@@ -91,3 +91,54 @@ def test_prefill_head_dim_64_is_rejected_cleanly(pkv):
     with pytest.raises(pkv.PKVError) as e:
         ds.run(pkv)
     assert e.value.status == 12
+
+
+def _bf16(x):
+    return W._f32_to_bf16_bits(np.asarray(x, dtype=np.float32))
+
+
+def _pool_index(w, s, pos):
+    blk = int(w.block_tables[s][pos // W.BLOCK_SIZE])
+    return blk, pos % W.BLOCK_SIZE
+
+
+def test_prefill_dominant_keys_and_tiny_weights(pkv):
+    """P V runs with P in fp16.  Scores are built so that two keys carry
+    most of the weight (the second at 2^0.51 times the first, so its P is
+    not a power of two, with V = +3 and -3) while the ~2,100 others sit 14-15
+    binary orders below: under the fp16 normal range once P is formed, yet
+    about 4% of the row sum, with V near 1.  Flushing those weights to zero
+    moves the output by ~4e-2; P rounded to bf16 by ~2.7e-3 (both beyond
+    the tolerance); fp16 P by ~3.5e-4."""
+    prefix, ql, d = 2048, 128, 128
+    w = W.make_paged("tiny-p", 31, 16, 8, d, [prefix + ql], [ql])
+    rng = np.random.default_rng(7)
+    # q = (8, 0, ...), k = (beta, 0, ...): log2-domain score 8*beta*scale*log2(e)
+    w.q[:] = 0
+    w.q[:, :, 0] = _bf16(8.0)
+    beta = rng.uniform(5.4, 6.3, size=prefix + ql)
+    vals = 1.0 + 0.1 * rng.standard_normal((prefix + ql, w.num_kv_heads, d))
+    for pos, b, v in ((0, 20.0, 3.0), (700, 20.5, -3.0)):
+        beta[pos], vals[pos] = b, v
+    for pos in range(prefix):
+        blk, row = _pool_index(w, 0, pos)
+        w.k_pool[blk, :, row, :] = 0
+        w.k_pool[blk, :, row, 0] = _bf16(beta[pos])
+        w.v_pool[blk, :, row, :] = _bf16(vals[pos])
+    w.k_new[:] = 0
+    w.k_new[:, :, 0] = _bf16(beta[prefix:])[:, None]
+    w.v_new[:] = _bf16(vals[prefix:])
+    run_and_check(pkv, w)
+
+
+def test_prefill_v_beyond_fp16_range_reports_range_error(pkv):
+    """A V entry of a visible key that fp16 cannot hold (|v| > 65504) is
+    reported as PKV_ERR_RANGE (detail: the sequence), without a fault."""
+    w = W.make_paged("v-range", 32, 16, 8, 128, [300], [200])
+    blk, row = _pool_index(w, 0, 5)
+    w.v_pool[blk, 3, row, 7] = _bf16(70000.0)
+    ds = DeviceStep(w)
+    ds.run(pkv)
+    torch.cuda.synchronize()
+    assert pkv.get_error() == (9, 0)
+    assert pkv.get_error() == (0, 0)
