@@ -66,7 +66,8 @@ typedef enum pkv_status {
     PKV_ERR_TIMEOUT = 10,    /* (device) a bounded wait inside a kernel expired             */
     PKV_ERR_CUDA = 11,       /* a CUDA runtime call failed (see pkv_last_cuda_error)        */
     PKV_ERR_UNSUPPORTED = 12, /* the current device is not compute capability 10.3          */
-    PKV_ERR_SCRATCH_LIMIT = 13 /* the problem needs more than the built-in scratch buffer   */
+    PKV_ERR_SCRATCH_LIMIT = 13, /* the problem needs more than the built-in scratch buffer  */
+    PKV_ERR_NO_BLOCKS = 14   /* (device) the free queue cannot supply the blocks an append needs */
 } pkv_status;
 
 typedef struct pkv_cache {
@@ -101,13 +102,16 @@ pkv_status pkv_cache_write(const pkv_cache_t* cache, const void* k_new, const vo
  * append to it.  For every i: K[dst[i]] <- K[src[i]] and V[dst[i]] <- V[src[i]],
  * whole blocks (all kv heads, all 16 rows), bit-exact.
  *
- *   src, dst              int32 [num_pairs], device
+ *   src, dst              int32 [num_pairs], device.  A pair whose src is
+ *                         negative is skipped without error (the unused
+ *                         entries pkv_blocks_append leaves are -1).
  *   src_host, dst_host    optional host copies of src/dst; when both are given
  *                         the call checks that the dst ids are distinct and
  *                         that no dst is also a src (PKV_ERR_ALIAS), and that
  *                         ids are in range (PKV_ERR_RANGE) before launching.
  *                         The same src may appear many times.
- *   Ids out of range found on the device are skipped and raise PKV_ERR_RANGE.
+ *   Other ids out of range found on the device are skipped and raise
+ *   PKV_ERR_RANGE.
  */
 pkv_status pkv_copy_blocks(const pkv_cache_t* cache, const int32_t* src, const int32_t* dst, int32_t num_pairs,
                            const int32_t* src_host, const int32_t* dst_host, void* stream);
@@ -232,9 +236,98 @@ pkv_status pkv_decode_attention_static(const pkv_cache_t* cache, const void* q, 
 size_t pkv_decode_static_scratch_bytes(void);
 
 /*
+ * Block bookkeeping on the device.
+ * [KV2] section 2, "Blocks and block tables": a request's KV is cut into
+ * 16-token blocks that may sit anywhere in free memory; its block table maps
+ * logical to physical blocks, and a block is allocated at the moment the
+ * tokens fill the last one (nothing is reserved ahead).  "Sharing blocks":
+ * requests may point at one block under a reference count, and a shared block
+ * is copied only when a holder must append to it (copy-on-write).  [KV2]
+ * section 4: a finished request's blocks return to the free queue tail block
+ * first.
+ *
+ * The state is caller-owned device memory; rows of the tables are sequences.
+ * block_tables and context_lens are the arrays the attention calls read, so
+ * a step is: pkv_blocks_append -> pkv_copy_blocks (its pairs) ->
+ * pkv_cache_write (its slot mapping) -> attention, with no host round trip.
+ * Every call is one launch on `stream`; device-side failures are recorded in
+ * the error word (pkv_get_error) and leave the state unchanged.
+ */
+typedef struct pkv_blocks {
+    int32_t* block_tables;   /* int32 [max_seqs][max_blocks_per_seq]; -1 = no block        */
+    int32_t* context_lens;   /* int32 [max_seqs]: tokens each row holds                    */
+    int32_t* ref_counts;     /* int32 [num_blocks]: rows holding each block                */
+    int32_t* free_ids;       /* int32 [num_blocks]: ring of free block ids (FIFO)           */
+    int32_t* free_state;     /* int32 [2]: {head, count} of the ring                        */
+    int32_t* scratch;        /* int32 [2 * num_blocks]: zero between calls (reset zeroes it) */
+    int32_t num_blocks;      /* >= 0                                                        */
+    int32_t max_seqs;        /* rows, >= 0                                                  */
+    int32_t max_blocks_per_seq; /* >= 1                                                     */
+} pkv_blocks_t;
+
+/*
+ * pkv_blocks_reset -- every row empty (tables -1, lengths 0), every count 0,
+ * the ring holding blocks 0, 1, ..., num_blocks-1 in that order, scratch 0.
+ */
+pkv_status pkv_blocks_reset(const pkv_blocks_t* blocks, void* stream);
+
+/*
+ * pkv_blocks_append -- row s (0 <= s < num_seqs) gains
+ * query_start_loc[s+1] - query_start_loc[s] tokens (0 = untouched).
+ *
+ *   query_start_loc  int32 [num_seqs+1], device; [0] must be 0 and
+ *                    [num_seqs] == num_tokens (host value), non-decreasing
+ *   slot_mapping     int32 [num_tokens] out: slot (block*16 + row) of each new
+ *                    token, the input of pkv_cache_write
+ *   cow_src, cow_dst int32 [num_seqs] out: copy-on-write pairs in sequence
+ *                    order, then -1 (pkv_copy_blocks with num_pairs = num_seqs
+ *                    copies exactly these)
+ *   cow_count        int32 [1] out: number of pairs
+ *
+ *   Sequences are processed as if one after another in index order:
+ *   - a row whose last block is partly filled and held by others copies it
+ *     into a new block (the pair is emitted and the old block loses a
+ *     holder); when every holder appends in the same call, the last one
+ *     writes in place;
+ *   - new blocks (one per 16 tokens crossing a block boundary) and the
+ *     copy-on-write blocks come from the ring's head in that order.
+ *   Errors, found on the device, change no state; slot_mapping is then all
+ *   -1 and the pairs all -1 (so the cache write and copies that follow do
+ *   nothing):
+ *   - PKV_ERR_RANGE: query_start_loc malformed, a length beyond
+ *     max_blocks_per_seq*16, a partly filled last block not held, or more
+ *     appenders than holders;
+ *   - PKV_ERR_NO_BLOCKS: the ring holds fewer blocks than the call needs.
+ *   num_seqs <= max_seqs (else PKV_ERR_SHAPE).
+ */
+pkv_status pkv_blocks_append(const pkv_blocks_t* blocks, const int32_t* query_start_loc, int32_t num_seqs,
+                             int32_t num_tokens, int32_t* slot_mapping, int32_t* cow_src, int32_t* cow_dst,
+                             int32_t* cow_count, void* stream);
+
+/*
+ * pkv_blocks_fork -- row children[i] takes row parents[i]'s blocks and
+ * length (parallel sampling, beam search: [KV2] "Sharing blocks"); each
+ * shared block gains a holder.  n <= 4096 (else PKV_ERR_SHAPE).  Device
+ * errors: PKV_ERR_RANGE (a row out of range, a child not empty, a parent's
+ * block not held), PKV_ERR_ALIAS (children repeat, or a child is a parent).
+ */
+pkv_status pkv_blocks_fork(const pkv_blocks_t* blocks, const int32_t* parents, const int32_t* children, int32_t n,
+                           void* stream);
+
+/*
+ * pkv_blocks_release -- rows[i] (in order) drop their blocks, each row's
+ * last block first; a block whose count reaches 0 joins the ring's tail.
+ * The rows end empty.  n <= 4096 (else PKV_ERR_SHAPE).  Device errors:
+ * PKV_ERR_RANGE (a row out of range, a block not held, more releases than
+ * holders), PKV_ERR_ALIAS (a row repeats).
+ */
+pkv_status pkv_blocks_release(const pkv_blocks_t* blocks, const int32_t* rows, int32_t n, void* stream);
+
+/*
  * pkv_get_error -- synchronise `stream`, then return (and clear) the first
  * error a kernel recorded on the current device since the last call:
- * PKV_OK, PKV_ERR_RANGE or PKV_ERR_TIMEOUT.  `detail` (optional) receives
+ * PKV_OK, PKV_ERR_RANGE, PKV_ERR_ALIAS, PKV_ERR_NO_BLOCKS or PKV_ERR_TIMEOUT.
+ * `detail` (optional) receives
  * the offending index (a token, pair or sequence number) or wait site.
  */
 pkv_status pkv_get_error(void* stream, int32_t* detail);

@@ -102,14 +102,16 @@ int oracle_cache_write(uint16_t* k_pool, uint16_t* v_pool, int64_t num_blocks, i
 }
 
 /* ------------------------------------------------------------------------ */
-/* copy_blocks: pool[dst[i]] <- pool[src[i]], whole blocks, K and V.         */
+/* copy_blocks: pool[dst[i]] <- pool[src[i]], whole blocks, K and V; a pair  */
+/* with a negative src is skipped.                                           */
 /* ------------------------------------------------------------------------ */
 int oracle_copy_blocks(uint16_t* k_pool, uint16_t* v_pool, int64_t num_blocks, int32_t num_kv_heads,
                        int32_t head_dim, int32_t block_size, const int32_t* src, const int32_t* dst, int64_t n) {
     if (num_blocks < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || n < 0) return ORACLE_ERR_ARG;
     const int64_t block_elems = (int64_t)num_kv_heads * block_size * head_dim;
     for (int64_t i = 0; i < n; ++i) {
-        if (src[i] < 0 || src[i] >= num_blocks || dst[i] < 0 || dst[i] >= num_blocks) return ORACLE_ERR_RANGE;
+        if (src[i] < 0) continue;                       /* unused pair entry: skipped */
+        if (src[i] >= num_blocks || dst[i] < 0 || dst[i] >= num_blocks) return ORACLE_ERR_RANGE;
         memmove(k_pool + (int64_t)dst[i] * block_elems, k_pool + (int64_t)src[i] * block_elems,
                 (size_t)block_elems * sizeof(uint16_t));
         memmove(v_pool + (int64_t)dst[i] * block_elems, v_pool + (int64_t)src[i] * block_elems,

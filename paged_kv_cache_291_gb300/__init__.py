@@ -21,7 +21,7 @@ from typing import Optional, Tuple
 __all__ = [
     "PKVError", "lib_path", "load", "version", "status_string", "cache_write", "copy_blocks",
     "decode_workspace_size", "decode_attention", "prefill_workspace_size", "chunked_prefill_attention",
-    "get_error", "Cache",
+    "get_error", "Cache", "Blocks",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -33,6 +33,7 @@ STATUS_NAMES = {
     0: "PKV_OK", 1: "PKV_ERR_NULL", 2: "PKV_ERR_SHAPE", 3: "PKV_ERR_HEADS", 4: "PKV_ERR_HEADDIM",
     5: "PKV_ERR_BLOCKSIZE", 6: "PKV_ERR_ALIAS", 7: "PKV_ERR_WORKSPACE", 8: "PKV_ERR_ALIGN", 9: "PKV_ERR_RANGE",
     10: "PKV_ERR_TIMEOUT", 11: "PKV_ERR_CUDA", 12: "PKV_ERR_UNSUPPORTED", 13: "PKV_ERR_SCRATCH_LIMIT",
+    14: "PKV_ERR_NO_BLOCKS",
 }
 
 
@@ -49,6 +50,14 @@ class Cache(ctypes.Structure):
     """Mirror of ``pkv_cache_t``."""
     _fields_ = [("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p), ("num_blocks", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32)]
+
+
+class BlocksState(ctypes.Structure):
+    """Mirror of ``pkv_blocks_t``."""
+    _fields_ = [("block_tables", ctypes.c_void_p), ("context_lens", ctypes.c_void_p),
+                ("ref_counts", ctypes.c_void_p), ("free_ids", ctypes.c_void_p), ("free_state", ctypes.c_void_p),
+                ("scratch", ctypes.c_void_p), ("num_blocks", ctypes.c_int32), ("max_seqs", ctypes.c_int32),
+                ("max_blocks_per_seq", ctypes.c_int32)]
 
 
 def lib_path() -> str:
@@ -74,6 +83,10 @@ def load():
         "pkv_prefill_workspace_size": ([i32, i32, i32, i32, i32, i32], sz),
         "pkv_chunked_prefill_attention": ([CP, P, i32, i32, P, P, P, i32, P, i32, i32, f32, P, P, sz, P],
                                           ctypes.c_int),
+        "pkv_blocks_reset": ([ctypes.POINTER(BlocksState), P], ctypes.c_int),
+        "pkv_blocks_append": ([ctypes.POINTER(BlocksState), P, i32, i32, P, P, P, P, P], ctypes.c_int),
+        "pkv_blocks_fork": ([ctypes.POINTER(BlocksState), P, P, i32, P], ctypes.c_int),
+        "pkv_blocks_release": ([ctypes.POINTER(BlocksState), P, i32, P], ctypes.c_int),
         "pkv_get_error": ([P, ctypes.POINTER(i32)], ctypes.c_int),
         "pkv_status_string": ([ctypes.c_int], ctypes.c_char_p),
         "pkv_last_cuda_error": ([], ctypes.c_char_p),
@@ -265,6 +278,78 @@ def chunked_prefill_attention(k_pool, v_pool, q, query_start_loc, context_lens, 
         workspace.numel() * workspace.element_size(), _stream_handle(stream))
     _check(st, "pkv_chunked_prefill_attention")
     return out
+
+
+class Blocks:
+    """Block bookkeeping state on one GPU (``pkv_blocks_t``): block tables,
+    context lengths, reference counts and the ring of free blocks, as int32
+    CUDA tensors owned by this object.  ``block_tables`` and ``context_lens``
+    are the arrays the attention calls read.  Every method is one launch on
+    the current stream; device-side errors are read with :func:`get_error`."""
+
+    def __init__(self, num_blocks: int, max_seqs: int, max_blocks_per_seq: int, device=None):
+        torch = _torch()
+        device = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+        i32 = dict(dtype=torch.int32, device=device)
+        self.num_blocks, self.max_seqs, self.max_blocks_per_seq = num_blocks, max_seqs, max_blocks_per_seq
+        self.block_tables = torch.empty((max_seqs, max_blocks_per_seq), **i32)
+        self.context_lens = torch.empty((max_seqs,), **i32)
+        self.ref_counts = torch.empty((max(num_blocks, 1),), **i32)
+        self.free_ids = torch.empty((max(num_blocks, 1),), **i32)
+        self.free_state = torch.empty((2,), **i32)
+        self.scratch = torch.empty((max(2 * num_blocks, 1),), **i32)
+        self.reset()
+
+    def _state(self) -> BlocksState:
+        return BlocksState(self.block_tables.data_ptr(), self.context_lens.data_ptr(), self.ref_counts.data_ptr(),
+                           self.free_ids.data_ptr(), self.free_state.data_ptr(), self.scratch.data_ptr(),
+                           self.num_blocks, self.max_seqs, self.max_blocks_per_seq)
+
+    def reset(self, stream=None) -> None:
+        """Every row empty, every block free (queued 0, 1, 2, ...)."""
+        _check(load().pkv_blocks_reset(ctypes.byref(self._state()), _stream_handle(stream)), "pkv_blocks_reset")
+
+    def append(self, query_start_loc, num_tokens: int, slot_mapping=None, cow_src=None, cow_dst=None,
+               cow_count=None, stream=None):
+        """Row s gains query_start_loc[s+1] - query_start_loc[s] tokens.
+
+        Returns (slot_mapping [num_tokens], cow_src [S], cow_dst [S],
+        cow_count [1]) as int32 CUDA tensors (allocated when not given)."""
+        torch = _torch()
+        S = int(query_start_loc.shape[0]) - 1
+        dev = self.block_tables.device
+        i32 = dict(dtype=torch.int32, device=dev)
+        slot_mapping = slot_mapping if slot_mapping is not None else torch.empty((num_tokens,), **i32)
+        cow_src = cow_src if cow_src is not None else torch.empty((max(S, 1),), **i32)
+        cow_dst = cow_dst if cow_dst is not None else torch.empty((max(S, 1),), **i32)
+        cow_count = cow_count if cow_count is not None else torch.empty((1,), **i32)
+        if slot_mapping.shape[0] < num_tokens or cow_src.shape[0] < S or cow_dst.shape[0] < S:
+            raise ValueError("output tensors are too small")
+        sp = _dev(slot_mapping, "slot_mapping", dtype=torch.int32) if num_tokens > 0 else None
+        st = load().pkv_blocks_append(ctypes.byref(self._state()),
+                                      _dev(query_start_loc, "query_start_loc", dtype=torch.int32), S,
+                                      int(num_tokens), sp, _dev(cow_src, "cow_src", dtype=torch.int32),
+                                      _dev(cow_dst, "cow_dst", dtype=torch.int32),
+                                      _dev(cow_count, "cow_count", dtype=torch.int32), _stream_handle(stream))
+        _check(st, "pkv_blocks_append")
+        return slot_mapping, cow_src, cow_dst, cow_count
+
+    def fork(self, parents, children, stream=None) -> None:
+        """Row children[i] takes row parents[i]'s blocks and length."""
+        torch = _torch()
+        n = int(parents.shape[0])
+        if children.shape[0] != n:
+            raise ValueError("parents and children must have the same length")
+        st = load().pkv_blocks_fork(ctypes.byref(self._state()), _dev(parents, "parents", dtype=torch.int32),
+                                    _dev(children, "children", dtype=torch.int32), n, _stream_handle(stream))
+        _check(st, "pkv_blocks_fork")
+
+    def release(self, rows, stream=None) -> None:
+        """Rows drop their blocks (each row last block first) and end empty."""
+        torch = _torch()
+        st = load().pkv_blocks_release(ctypes.byref(self._state()), _dev(rows, "rows", dtype=torch.int32),
+                                       int(rows.shape[0]), _stream_handle(stream))
+        _check(st, "pkv_blocks_release")
 
 
 def get_error(stream=None) -> Tuple[int, int]:

@@ -128,6 +128,7 @@ PKV_API const char* pkv_status_string(pkv_status s) {
         case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED: the current device is not compute capability 10.3";
         case PKV_ERR_SCRATCH_LIMIT:
             return "PKV_ERR_SCRATCH_LIMIT: the batch needs more workspace than the built-in 4 MiB scratch buffer";
+        case PKV_ERR_NO_BLOCKS: return "PKV_ERR_NO_BLOCKS: the free queue holds fewer blocks than the append needs";
     }
     return "unknown pkv_status";
 }
@@ -160,7 +161,8 @@ PKV_API pkv_status pkv_copy_blocks(const pkv_cache_t* cache, const int32_t* src,
     if (src_host != nullptr) {
         std::unordered_set<int32_t> dsts, srcs;
         for (int32_t i = 0; i < num_pairs; ++i) {
-            if (src_host[i] < 0 || src_host[i] >= cache->num_blocks || dst_host[i] < 0 ||
+            if (src_host[i] < 0) continue;  // skipped pair
+            if (src_host[i] >= cache->num_blocks || dst_host[i] < 0 ||
                 dst_host[i] >= cache->num_blocks)
                 return PKV_ERR_RANGE;
             if (!dsts.insert(dst_host[i]).second) return PKV_ERR_ALIAS;
@@ -180,6 +182,76 @@ PKV_API pkv_status pkv_copy_blocks(const pkv_cache_t* cache, const int32_t* src,
         if (e != cudaSuccess) return cuda_fail(e);
     }
     return PKV_OK;
+}
+
+namespace {
+
+pkv_status check_blocks(const pkv_blocks_t* b, pkv::BlocksArgs* a) {
+    if (b == nullptr || b->block_tables == nullptr || b->context_lens == nullptr || b->ref_counts == nullptr ||
+        b->free_ids == nullptr || b->free_state == nullptr || b->scratch == nullptr)
+        return PKV_ERR_NULL;
+    if (b->num_blocks < 0 || b->max_seqs < 0 || b->max_blocks_per_seq < 1) return PKV_ERR_SHAPE;
+    if (static_cast<int64_t>(b->max_blocks_per_seq) * 16 > INT32_MAX) return PKV_ERR_SHAPE;
+    *a = pkv::BlocksArgs{b->block_tables, b->context_lens, b->ref_counts, b->free_ids, b->free_state,
+                         b->scratch,      b->num_blocks,   b->max_seqs,   b->max_blocks_per_seq};
+    return PKV_OK;
+}
+
+}  // namespace
+
+PKV_API pkv_status pkv_blocks_reset(const pkv_blocks_t* blocks, void* stream) {
+    pkv::BlocksArgs a;
+    pkv_status st = check_blocks(blocks, &a);
+    if (st != PKV_OK) return st;
+    DeviceState* dev = nullptr;
+    if ((st = current_device(&dev)) != PKV_OK) return st;
+    cudaError_t e = pkv::launch_blocks_reset(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e);
+}
+
+PKV_API pkv_status pkv_blocks_append(const pkv_blocks_t* blocks, const int32_t* query_start_loc, int32_t num_seqs,
+                                     int32_t num_tokens, int32_t* slot_mapping, int32_t* cow_src, int32_t* cow_dst,
+                                     int32_t* cow_count, void* stream) {
+    pkv::BlocksArgs a;
+    pkv_status st = check_blocks(blocks, &a);
+    if (st != PKV_OK) return st;
+    if (num_seqs < 0 || num_tokens < 0 || num_seqs > blocks->max_seqs) return PKV_ERR_SHAPE;
+    if (num_seqs == 0) return num_tokens == 0 ? PKV_OK : PKV_ERR_SHAPE;
+    if (query_start_loc == nullptr || cow_src == nullptr || cow_dst == nullptr || cow_count == nullptr)
+        return PKV_ERR_NULL;
+    if (num_tokens > 0 && slot_mapping == nullptr) return PKV_ERR_NULL;
+    DeviceState* dev = nullptr;
+    if ((st = current_device(&dev)) != PKV_OK) return st;
+    cudaError_t e = pkv::launch_blocks_append(a, query_start_loc, num_seqs, num_tokens, slot_mapping, cow_src,
+                                              cow_dst, cow_count, dev->err, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e);
+}
+
+PKV_API pkv_status pkv_blocks_fork(const pkv_blocks_t* blocks, const int32_t* parents, const int32_t* children,
+                                   int32_t n, void* stream) {
+    pkv::BlocksArgs a;
+    pkv_status st = check_blocks(blocks, &a);
+    if (st != PKV_OK) return st;
+    if (n < 0 || n > pkv::kBlocksMaxRows) return PKV_ERR_SHAPE;
+    if (n == 0) return PKV_OK;
+    if (parents == nullptr || children == nullptr) return PKV_ERR_NULL;
+    DeviceState* dev = nullptr;
+    if ((st = current_device(&dev)) != PKV_OK) return st;
+    cudaError_t e = pkv::launch_blocks_fork(a, parents, children, n, dev->err, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e);
+}
+
+PKV_API pkv_status pkv_blocks_release(const pkv_blocks_t* blocks, const int32_t* rows, int32_t n, void* stream) {
+    pkv::BlocksArgs a;
+    pkv_status st = check_blocks(blocks, &a);
+    if (st != PKV_OK) return st;
+    if (n < 0 || n > pkv::kBlocksMaxRows) return PKV_ERR_SHAPE;
+    if (n == 0) return PKV_OK;
+    if (rows == nullptr) return PKV_ERR_NULL;
+    DeviceState* dev = nullptr;
+    if ((st = current_device(&dev)) != PKV_OK) return st;
+    cudaError_t e = pkv::launch_blocks_release(a, rows, n, dev->err, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e);
 }
 
 PKV_API size_t pkv_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,

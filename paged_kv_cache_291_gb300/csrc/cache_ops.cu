@@ -64,7 +64,8 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(const int32_t* __restr
     const int32_t pair = blockIdx.y;
     const int32_t s = __ldg(src + pair);
     const int32_t d = __ldg(dst + pair);
-    if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks) {
+    if (s < 0) return;  // unused pair entry
+    if (s >= num_blocks || d < 0 || d >= num_blocks) {
         if (blockIdx.x == 0 && threadIdx.x == 0) record_error(err, kErrRange, static_cast<uint32_t>(pair));
         return;
     }

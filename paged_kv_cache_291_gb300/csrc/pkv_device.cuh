@@ -14,6 +14,8 @@ constexpr int kBlockSize = 16;  // tokens per KV block
 // Error word layout: (code << 32) | detail; the first error wins.
 constexpr uint32_t kErrRange = 9;    // PKV_ERR_RANGE
 constexpr uint32_t kErrTimeout = 10; // PKV_ERR_TIMEOUT
+constexpr uint32_t kErrAlias = 6;    // PKV_ERR_ALIAS
+constexpr uint32_t kErrNoBlocks = 14; // PKV_ERR_NO_BLOCKS
 
 // Upper bound on any wait inside a kernel (nanoseconds of %globaltimer).
 constexpr uint64_t kWaitLimitNs = 2000000000ull;

@@ -76,4 +76,27 @@ struct PrefillArgs {
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
 
+// Block bookkeeping state (pkv_blocks_t), all device memory.
+struct BlocksArgs {
+    int32_t* tables;      // [max_seqs][max_blocks]
+    int32_t* lens;        // [max_seqs]
+    int32_t* refs;        // [num_blocks]
+    int32_t* free_ids;    // [num_blocks] ring
+    int32_t* free_state;  // [2] {head, count}
+    int32_t* scratch;     // [2 * num_blocks], zero between calls
+    int32_t num_blocks, max_seqs, max_blocks;
+};
+
+// Rows per fork or release call (the kernels keep per-row offsets on chip).
+constexpr int32_t kBlocksMaxRows = 4096;
+
+cudaError_t launch_blocks_reset(const BlocksArgs& st, cudaStream_t stream);
+cudaError_t launch_blocks_append(const BlocksArgs& st, const int32_t* query_start_loc, int32_t num_seqs,
+                                 int32_t num_tokens, int32_t* slot_mapping, int32_t* cow_src, int32_t* cow_dst,
+                                 int32_t* cow_count, unsigned long long* err, cudaStream_t stream);
+cudaError_t launch_blocks_fork(const BlocksArgs& st, const int32_t* parents, const int32_t* children, int32_t n,
+                               unsigned long long* err, cudaStream_t stream);
+cudaError_t launch_blocks_release(const BlocksArgs& st, const int32_t* rows, int32_t n, unsigned long long* err,
+                                  cudaStream_t stream);
+
 }  // namespace pkv
