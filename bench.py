@@ -377,6 +377,53 @@ def run_reference(args):
 
 # ----------------------------------------------------------- our arm
 
+def block_manager_timing(w, pkv, torch, dev, stream, iters=200, warm=10):
+    """Device time of one pkv_blocks_append for this batch's rows: every row
+    first holds its context minus this step's rows, then appends this step's
+    rows again and again (the decode loop), replayed from a CUDA graph of
+    `iters` appends and timed with events on the launching stream."""
+    import numpy as np
+    ql = np.diff(w.query_start_loc).astype(np.int64)
+    prefix = w.context_lens.astype(np.int64) - ql
+    S = w.num_seqs
+    final = prefix + ql * (warm + iters)
+    MB = int(-(-final.max() // 16)) + 1
+    NB = int(np.sum(-(-final // 16))) + S
+    blocks = pkv.Blocks(NB, S, MB, device=dev)
+    torch.cuda.synchronize(dev)
+
+    def i32(a):
+        return torch.tensor(np.asarray(a, dtype=np.int32), device=dev)
+
+    qsl0 = np.concatenate([[0], np.cumsum(prefix)])
+    qsl = i32(w.query_start_loc)
+    T = int(w.query_start_loc[-1])
+    outs = [torch.empty((max(T, 1),), dtype=torch.int32, device=dev)] + \
+           [torch.empty((max(S, 1),), dtype=torch.int32, device=dev) for _ in range(2)] + \
+           [torch.empty((1,), dtype=torch.int32, device=dev)]
+    with torch.cuda.stream(stream):
+        blocks.append(i32(qsl0), int(qsl0[-1]), stream=stream)
+        for _ in range(warm):
+            blocks.append(qsl, T, *outs, stream=stream)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(iters):
+            blocks.append(qsl, T, *outs, stream=stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    g.replay()
+    e1.record(stream)
+    stream.synchronize()
+    status = pkv.get_error(stream)
+    if status[0] != 0:
+        raise RuntimeError(f"device error in the block-manager timing: {status}")
+    us = e0.elapsed_time(e1) * 1e3 / iters
+    return {"call": "pkv_blocks_append", "workload": f"{S} rows, {T} new tokens per call, "
+            f"{int(prefix.sum())} tokens held at the start", "us_per_call": us, "rows_per_s": S / (us * 1e-6),
+            "launches_per_call": 1, "bound": "latency (one CTA of 1,024 threads)"}
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -659,6 +706,7 @@ def run_ours(args):
     ck = clocks.summary(t_wall0, t_wall1) if clocks else {}
     line["clocks"] = {"sm_mhz": ck.get("sm_mhz"), "sm_max_mhz": ck.get("sm_max_mhz"),
                       "reasons": ck.get("reasons", []), "samples": ck.get("samples", 0)}
+    line["block_manager"] = block_manager_timing(w, pkv, torch, dev, stream)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_budget)
     print(json.dumps(line), flush=True)
