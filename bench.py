@@ -424,6 +424,40 @@ def block_manager_timing(w, pkv, torch, dev, stream, iters=200, warm=10):
             "launches_per_call": 1, "bound": "latency (one CTA of 1,024 threads)"}
 
 
+def prefix_keys_timing(w, pkv, torch, dev, stream, iters=5):
+    """Device time of pkv_prefix_keys over every row's whole context (one
+    synthetic, seeded token id per cached token), as a prefix cache keys a
+    batch of prompts: the SHA-256 chain over the rows' full blocks."""
+    import numpy as np
+    import pkv_workloads as W
+    lens = w.context_lens.astype(np.int64)
+    S = len(lens)
+    qsl = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    toks = (W.uniform_u64(w.seed, 77, int(qsl[-1])) % 151936).astype(np.int32)  # Qwen3 vocabulary size
+    MB = max(1, int(lens.max()) // 16)
+    tt = torch.tensor(toks, device=dev)
+    qq = torch.tensor(qsl, device=dev)
+    keys = torch.zeros((S, MB, 32), dtype=torch.uint8, device=dev)
+    with torch.cuda.stream(stream):
+        pkv.prefix_keys(tt, qq, MB, keys=keys, stream=stream)
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(iters):
+            pkv.prefix_keys(tt, qq, MB, keys=keys, stream=stream)
+        e1.record(stream)
+    stream.synchronize()
+    status = pkv.get_error(stream)
+    if status[0] != 0:
+        raise RuntimeError(f"device error in the prefix-key timing: {status}")
+    us = e0.elapsed_time(e1) * 1e3 / iters
+    nkeys = int(np.sum(lens // 16))
+    return {"call": "pkv_prefix_keys", "workload": f"{S} rows, {int(qsl[-1])} tokens, {nkeys} full blocks, "
+            f"longest chain {int(lens.max()) // 16}", "us_per_call": us, "keys_per_s": nkeys / (us * 1e-6),
+            "launches_per_call": 1, "bound": "latency (one thread per chain, SHA-256 rounds in sequence)"}
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -707,6 +741,7 @@ def run_ours(args):
     line["clocks"] = {"sm_mhz": ck.get("sm_mhz"), "sm_max_mhz": ck.get("sm_max_mhz"),
                       "reasons": ck.get("reasons", []), "samples": ck.get("samples", 0)}
     line["block_manager"] = block_manager_timing(w, pkv, torch, dev, stream)
+    line["prefix_keys"] = prefix_keys_timing(w, pkv, torch, dev, stream)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_budget)
     print(json.dumps(line), flush=True)

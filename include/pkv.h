@@ -324,6 +324,32 @@ pkv_status pkv_blocks_fork(const pkv_blocks_t* blocks, const int32_t* parents, c
 pkv_status pkv_blocks_release(const pkv_blocks_t* blocks, const int32_t* rows, int32_t n, void* stream);
 
 /*
+ * pkv_prefix_keys -- prefix-cache keys of the full blocks of a batch of
+ * token lists.  [KV2] section 4, "Prefix cache": a block's key hashes the
+ * previous block's key, the block's token ids and extra information (adapter,
+ * multimodal hashes, a per-user cache salt), so a key stands for the whole
+ * prefix up to its block; only full blocks are keyed; SHA-256 by default.
+ *
+ *   key_i = SHA-256(key_{i-1} || the block's 16 token ids as little-endian
+ *           int32 || extra[s] as little-endian int64)   (104-byte message)
+ *   key_{-1} = parent_keys[s] (continuing a chain), or 32 zero bytes.
+ *
+ *   token_ids        int32 [T], device
+ *   token_start_loc  int32 [num_seqs+1], device: sequence s owns
+ *                    token_ids[token_start_loc[s] .. token_start_loc[s+1])
+ *   extra            int64 [num_seqs], device, or NULL (all 0)
+ *   parent_keys      uint8 [num_seqs][32], device, or NULL; 16-byte aligned
+ *   keys             uint8 [num_seqs][max_blocks][32] out, 16-byte aligned:
+ *                    the key of full block i of sequence s at [s][i] (the
+ *                    32-byte digest); entries past its full blocks untouched
+ *   A sequence with a decreasing range or more than max_blocks full blocks
+ *   writes no key and raises PKV_ERR_RANGE (detail: the sequence).  Keys
+ *   depend on each other along a sequence: one thread hashes one sequence.
+ */
+pkv_status pkv_prefix_keys(const int32_t* token_ids, const int32_t* token_start_loc, const int64_t* extra,
+                           const void* parent_keys, int32_t num_seqs, int32_t max_blocks, void* keys, void* stream);
+
+/*
  * pkv_get_error -- synchronise `stream`, then return (and clear) the first
  * error a kernel recorded on the current device since the last call:
  * PKV_OK, PKV_ERR_RANGE, PKV_ERR_ALIAS, PKV_ERR_NO_BLOCKS or PKV_ERR_TIMEOUT.

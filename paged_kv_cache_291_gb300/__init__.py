@@ -21,7 +21,7 @@ from typing import Optional, Tuple
 __all__ = [
     "PKVError", "lib_path", "load", "version", "status_string", "cache_write", "copy_blocks",
     "decode_workspace_size", "decode_attention", "prefill_workspace_size", "chunked_prefill_attention",
-    "get_error", "Cache", "Blocks",
+    "get_error", "Cache", "Blocks", "prefix_keys",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -87,6 +87,7 @@ def load():
         "pkv_blocks_append": ([ctypes.POINTER(BlocksState), P, i32, i32, P, P, P, P, P], ctypes.c_int),
         "pkv_blocks_fork": ([ctypes.POINTER(BlocksState), P, P, i32, P], ctypes.c_int),
         "pkv_blocks_release": ([ctypes.POINTER(BlocksState), P, i32, P], ctypes.c_int),
+        "pkv_prefix_keys": ([P, P, P, P, i32, i32, P, P], ctypes.c_int),
         "pkv_get_error": ([P, ctypes.POINTER(i32)], ctypes.c_int),
         "pkv_status_string": ([ctypes.c_int], ctypes.c_char_p),
         "pkv_last_cuda_error": ([], ctypes.c_char_p),
@@ -278,6 +279,23 @@ def chunked_prefill_attention(k_pool, v_pool, q, query_start_loc, context_lens, 
         workspace.numel() * workspace.element_size(), _stream_handle(stream))
     _check(st, "pkv_chunked_prefill_attention")
     return out
+
+
+def prefix_keys(token_ids, token_start_loc, max_blocks: int, extra=None, parent_keys=None, keys=None,
+                stream=None):
+    """Prefix-cache keys (uint8 [S][max_blocks][32]) of the full blocks of each
+    token list: key_i = SHA-256(key_{i-1} || 16 token ids (<i4) || extra (<i8))."""
+    torch = _torch()
+    S = int(token_start_loc.shape[0]) - 1
+    if keys is None:
+        keys = torch.zeros((max(S, 1), max(max_blocks, 1), 32), dtype=torch.uint8, device=token_ids.device)
+    ep = _dev(extra, "extra", dtype=torch.int64) if extra is not None else None
+    pp = _dev(parent_keys, "parent_keys", dtype=torch.uint8) if parent_keys is not None else None
+    st = load().pkv_prefix_keys(_dev(token_ids, "token_ids", dtype=torch.int32),
+                                _dev(token_start_loc, "token_start_loc", dtype=torch.int32), ep, pp, S,
+                                int(max_blocks), _dev(keys, "keys", dtype=torch.uint8), _stream_handle(stream))
+    _check(st, "pkv_prefix_keys")
+    return keys
 
 
 class Blocks:

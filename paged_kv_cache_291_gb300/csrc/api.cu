@@ -254,6 +254,22 @@ PKV_API pkv_status pkv_blocks_release(const pkv_blocks_t* blocks, const int32_t*
     return e == cudaSuccess ? PKV_OK : cuda_fail(e);
 }
 
+PKV_API pkv_status pkv_prefix_keys(const int32_t* token_ids, const int32_t* token_start_loc, const int64_t* extra,
+                                   const void* parent_keys, int32_t num_seqs, int32_t max_blocks, void* keys,
+                                   void* stream) {
+    if (num_seqs < 0 || max_blocks < 0) return PKV_ERR_SHAPE;
+    if (num_seqs == 0) return PKV_OK;
+    if (token_ids == nullptr || token_start_loc == nullptr || keys == nullptr) return PKV_ERR_NULL;
+    if (!aligned16(keys) || (parent_keys != nullptr && !aligned16(parent_keys))) return PKV_ERR_ALIGN;
+    pkv_status st;
+    DeviceState* dev = nullptr;
+    if ((st = current_device(&dev)) != PKV_OK) return st;
+    cudaError_t e = pkv::launch_prefix_keys(token_ids, token_start_loc, extra,
+                                            static_cast<const uint8_t*>(parent_keys), num_seqs, max_blocks,
+                                            static_cast<uint8_t*>(keys), dev->err, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e);
+}
+
 PKV_API size_t pkv_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                          int32_t head_dim, int32_t max_context_len, int32_t partition_blocks) {
     if (check_heads(num_q_heads, num_kv_heads) != PKV_OK) return 0;

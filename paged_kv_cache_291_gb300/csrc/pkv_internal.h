@@ -96,6 +96,9 @@ cudaError_t launch_blocks_append(const BlocksArgs& st, const int32_t* query_star
                                  int32_t* cow_count, unsigned long long* err, cudaStream_t stream);
 cudaError_t launch_blocks_fork(const BlocksArgs& st, const int32_t* parents, const int32_t* children, int32_t n,
                                unsigned long long* err, cudaStream_t stream);
+cudaError_t launch_prefix_keys(const int32_t* token_ids, const int32_t* token_start_loc, const int64_t* extra,
+                               const uint8_t* parent_keys, int32_t num_seqs, int32_t max_blocks, uint8_t* keys,
+                               unsigned long long* err, cudaStream_t stream);
 cudaError_t launch_blocks_release(const BlocksArgs& st, const int32_t* rows, int32_t n, unsigned long long* err,
                                   cudaStream_t stream);
 
