@@ -458,6 +458,51 @@ def prefix_keys_timing(w, pkv, torch, dev, stream, iters=5):
             "launches_per_call": 1, "bound": "latency (one thread per chain, SHA-256 rounds in sequence)"}
 
 
+def prefix_cache_timing(w, pkv, torch, dev, stream):
+    """Device time of pkv_blocks_register (every row's full blocks, all new
+    keys) and of pkv_blocks_match (every row's full prefix cached, the blocks
+    free again) for the workload's rows, one call each after a warm-up
+    cycle, with keys from pkv_prefix_keys over seeded synthetic token ids."""
+    import numpy as np
+    import pkv_workloads as W
+    lens = w.context_lens.astype(np.int64)
+    S = len(lens)
+    qsl = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    toks = (W.uniform_u64(w.seed, 77, int(qsl[-1])) % 151936).astype(np.int32)
+    MB = int(-(-lens.max() // 16))
+    NB = int(np.sum(-(-lens // 16)))
+    blocks = pkv.Blocks(NB, S, MB, device=dev, prefix_cache=True)
+    keys = pkv.prefix_keys(torch.tensor(toks, device=dev), torch.tensor(qsl, device=dev), MB)
+    nk = torch.tensor(lens // 16, dtype=torch.int32, device=dev)
+    qsl_d = torch.tensor(qsl, device=dev)
+    rows = torch.arange(S, dtype=torch.int32, device=dev)
+    times = {}
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        for it in range(2):
+            blocks.reset(stream=stream)
+            blocks.append(qsl_d, int(qsl[-1]), stream=stream)
+            e0.record(stream)
+            blocks.register(keys, nk, stream=stream)
+            e1.record(stream)
+            stream.synchronize()
+            times["register_us"] = e0.elapsed_time(e1) * 1e3
+            blocks.release(rows, stream=stream)
+            e0.record(stream)
+            m = blocks.match(keys, nk, stream=stream)
+            e1.record(stream)
+            stream.synchronize()
+            times["match_us"] = e0.elapsed_time(e1) * 1e3
+    status = pkv.get_error(stream)
+    if status[0] != 0 or int(m[:S].sum().item()) != int(np.sum(lens // 16)):
+        raise RuntimeError(f"prefix-cache timing went wrong: {status}")
+    return {"calls": "pkv_blocks_register, pkv_blocks_match",
+            "workload": f"{S} rows, {int(np.sum(lens // 16))} full blocks, all new (register) / all hits (match)",
+            **times, "launches_per_call": 1,
+            "bound": "latency (one CTA; register inserts from one thread, in order)"}
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -742,6 +787,7 @@ def run_ours(args):
                       "reasons": ck.get("reasons", []), "samples": ck.get("samples", 0)}
     line["block_manager"] = block_manager_timing(w, pkv, torch, dev, stream)
     line["prefix_keys"] = prefix_keys_timing(w, pkv, torch, dev, stream)
+    line["prefix_cache"] = prefix_cache_timing(w, pkv, torch, dev, stream)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_budget)
     print(json.dumps(line), flush=True)

@@ -252,22 +252,42 @@ size_t pkv_decode_static_scratch_bytes(void);
  * pkv_cache_write (its slot mapping) -> attention, with no host round trip.
  * Every call is one launch on `stream`; device-side failures are recorded in
  * the error word (pkv_get_error) and leave the state unchanged.
+ *
+ * Prefix cache ([KV2] section 4), when block_keys/key_table/cached are given:
+ * a block registered with its key (pkv_blocks_register) keeps its content and
+ * key after its last holder releases it ("empty but content kept"), waiting
+ * in the free queue in least-recently-freed order; a new row whose leading
+ * keys are cached takes those blocks (pkv_blocks_match), taking a free one
+ * back out of the queue; an append that takes a cached block from the queue
+ * drops its key.  The free queue is a ring of 2 * num_blocks entries: a block
+ * taken back by a match leaves a stale entry (ring_pos no longer points at
+ * it), which pops skip and a release compacts away when the ring would
+ * overflow.  Keys come from pkv_prefix_keys.
  */
 typedef struct pkv_blocks {
-    int32_t* block_tables;   /* int32 [max_seqs][max_blocks_per_seq]; -1 = no block        */
-    int32_t* context_lens;   /* int32 [max_seqs]: tokens each row holds                    */
-    int32_t* ref_counts;     /* int32 [num_blocks]: rows holding each block                */
-    int32_t* free_ids;       /* int32 [num_blocks]: ring of free block ids (FIFO)           */
-    int32_t* free_state;     /* int32 [2]: {head, count} of the ring                        */
-    int32_t* scratch;        /* int32 [2 * num_blocks]: zero between calls (reset zeroes it) */
-    int32_t num_blocks;      /* >= 0                                                        */
-    int32_t max_seqs;        /* rows, >= 0                                                  */
-    int32_t max_blocks_per_seq; /* >= 1                                                     */
+    int32_t* block_tables;   /* int32 [max_seqs][max_blocks_per_seq]; -1 = no block          */
+    int32_t* context_lens;   /* int32 [max_seqs]: tokens each row holds                      */
+    int32_t* ref_counts;     /* int32 [num_blocks]: rows holding each block                  */
+    int32_t* free_ring;      /* int32 [2 * num_blocks]: the free queue, least recently freed
+                                first (a ring that may hold stale entries, see below)         */
+    int32_t* ring_pos;       /* int32 [num_blocks]: ring index of a free block, -1 if held    */
+    int32_t* free_state;     /* int32 [3]: {head, ring entries, free blocks}                  */
+    int32_t* scratch;        /* int32 [3 * num_blocks]; the first 2 * num_blocks are zero
+                                between calls (pkv_blocks_reset zeroes them)                  */
+    uint8_t* block_keys;     /* uint8 [num_blocks][32] prefix-cache keys, 16-byte aligned,
+                                or NULL: no prefix cache                                      */
+    int32_t* key_table;      /* int32 [table_size]: cached blocks by key, or NULL             */
+    int32_t* cached;         /* int32 [num_blocks]: 1 = the block's key is in key_table, or NULL */
+    int32_t num_blocks;      /* >= 0                                                          */
+    int32_t max_seqs;        /* rows, >= 0                                                    */
+    int32_t max_blocks_per_seq; /* >= 1                                                       */
+    int32_t table_size;      /* power of two >= 2 * num_blocks, or 0 without a prefix cache  */
 } pkv_blocks_t;
 
 /*
  * pkv_blocks_reset -- every row empty (tables -1, lengths 0), every count 0,
- * the ring holding blocks 0, 1, ..., num_blocks-1 in that order, scratch 0.
+ * the free queue holding blocks 0, 1, ..., num_blocks-1 in that order,
+ * scratch 0, the prefix cache empty.
  */
 pkv_status pkv_blocks_reset(const pkv_blocks_t* blocks, void* stream);
 
@@ -290,14 +310,15 @@ pkv_status pkv_blocks_reset(const pkv_blocks_t* blocks, void* stream);
  *     holder); when every holder appends in the same call, the last one
  *     writes in place;
  *   - new blocks (one per 16 tokens crossing a block boundary) and the
- *     copy-on-write blocks come from the ring's head in that order.
+ *     copy-on-write blocks come from the free queue's head in that order; a
+ *     cached block taken this way loses its key.
  *   Errors, found on the device, change no state; slot_mapping is then all
  *   -1 and the pairs all -1 (so the cache write and copies that follow do
  *   nothing):
  *   - PKV_ERR_RANGE: query_start_loc malformed, a length beyond
  *     max_blocks_per_seq*16, a partly filled last block not held, or more
  *     appenders than holders;
- *   - PKV_ERR_NO_BLOCKS: the ring holds fewer blocks than the call needs.
+ *   - PKV_ERR_NO_BLOCKS: the free queue holds fewer blocks than the call needs.
  *   num_seqs <= max_seqs (else PKV_ERR_SHAPE).
  */
 pkv_status pkv_blocks_append(const pkv_blocks_t* blocks, const int32_t* query_start_loc, int32_t num_seqs,
@@ -315,8 +336,37 @@ pkv_status pkv_blocks_fork(const pkv_blocks_t* blocks, const int32_t* parents, c
                            void* stream);
 
 /*
+ * pkv_blocks_match -- prefix-cache hits.  Rows s < num_seqs with
+ * num_keys[s] > 0 (each must be empty) take the cached blocks of their
+ * leading keys keys[s][0 .. matched[s]), stopping at the first key not
+ * cached; a block nobody holds leaves the free queue; the row's length
+ * becomes 16 * matched[s].  Rows with num_keys[s] == 0 are untouched.
+ *
+ *   keys       uint8 [num_seqs][key_stride][32], device, 16-byte aligned
+ *              (the layout pkv_prefix_keys writes, key_stride = its max_blocks)
+ *   num_keys   int32 [num_seqs], device
+ *   matched    int32 [num_seqs] out
+ *   num_seqs <= min(max_seqs, 4096).  Device errors (PKV_ERR_RANGE): a row with
+ *   keys that is not empty, or num_keys beyond key_stride or the table width.
+ */
+pkv_status pkv_blocks_match(const pkv_blocks_t* blocks, const void* keys, int32_t key_stride,
+                            const int32_t* num_keys, int32_t num_seqs, int32_t* matched, void* stream);
+
+/*
+ * pkv_blocks_register -- rows s < num_seqs give their first num_keys[s]
+ * blocks (full ones) the keys keys[s][0 .. num_keys[s]), in (row, block)
+ * order: a block that already has a key keeps it, and a key already cached
+ * (or given to an earlier row or block of the call) keeps its block.
+ * num_seqs <= min(max_seqs, 4096).  Device errors (PKV_ERR_RANGE):
+ * num_keys beyond the row's full blocks or key_stride, a block not held.
+ */
+pkv_status pkv_blocks_register(const pkv_blocks_t* blocks, const void* keys, int32_t key_stride,
+                               const int32_t* num_keys, int32_t num_seqs, void* stream);
+
+/*
  * pkv_blocks_release -- rows[i] (in order) drop their blocks, each row's
- * last block first; a block whose count reaches 0 joins the ring's tail.
+ * last block first; a block whose count reaches 0 joins the free queue's
+ * tail, keeping its content and (if registered) its key.
  * The rows end empty.  n <= 4096 (else PKV_ERR_SHAPE).  Device errors:
  * PKV_ERR_RANGE (a row out of range, a block not held, more releases than
  * holders), PKV_ERR_ALIAS (a row repeats).

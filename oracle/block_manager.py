@@ -33,6 +33,14 @@ notes):
   logical block to its first; a block is queued when its count reaches 0.
 - Fork gives a child row all of its parent's blocks (the partly filled last
   block included), each block's count going up by one.
+- Prefix cache (section 4): a freed block keeps its content and its key
+  ("empty but content kept") and stays in the free queue in LRU order; a
+  new row whose leading block keys are cached takes those blocks (a block
+  with no holder leaves the free queue); allocation takes the least recently
+  freed block first and drops its key.  Match is per row, in row order, and
+  stops at the first key not cached.  Register gives a row's full blocks their
+  keys in (row, block) order; a block that already has a key keeps it, and a
+  key that is already cached keeps its first block.
 - A call that cannot be completed (too few free blocks, a length beyond the
   table, an inconsistent table or count, a repeated row) changes nothing and
   returns its error code.
@@ -69,27 +77,29 @@ class BlockState:
         self.tables = np.full((max_seqs, max_blocks_per_seq), -1, dtype=np.int32)
         self.context_lens = np.zeros(max_seqs, dtype=np.int32)
         self.ref_counts = np.zeros(num_blocks, dtype=np.int32)
-        self.free_ids = np.arange(num_blocks, dtype=np.int32)
-        self.free_head = 0
-        self.free_count = int(num_blocks)
+        self.queue = list(range(num_blocks))   # free blocks, least recently freed first
+        self.cache = {}                        # key (bytes) -> block
+        self.block_key = {}                    # block -> its key, for cached blocks
+
+    @property
+    def free_count(self) -> int:
+        return len(self.queue)
 
     def clone(self) -> "BlockState":
         return copy.deepcopy(self)
 
     def free_queue(self) -> list:
-        """The free block ids from head to tail."""
-        n = self.num_blocks
-        return [int(self.free_ids[(self.free_head + i) % n]) for i in range(self.free_count)]
+        """The free block ids, least recently freed first."""
+        return list(self.queue)
 
     def _pop(self) -> int:
-        b = int(self.free_ids[self.free_head])
-        self.free_head = (self.free_head + 1) % self.num_blocks
-        self.free_count -= 1
+        b = self.queue.pop(0)
+        if b in self.block_key:                # reused: its cached content is gone
+            del self.cache[self.block_key.pop(b)]
         return b
 
     def _push(self, b: int) -> None:
-        self.free_ids[(self.free_head + self.free_count) % self.num_blocks] = b
-        self.free_count += 1
+        self.queue.append(b)
 
 
 def _row_blocks_valid(st: BlockState, r: int) -> bool:
@@ -223,4 +233,56 @@ def release(st: BlockState, rows) -> int:
                 st._push(b)
             st.tables[r, li] = -1
         st.context_lens[r] = 0
+    return OK
+
+
+def match(st: BlockState, keys, num_keys):
+    """Rows s = 0 .. S-1 with num_keys[s] > 0 (each empty) take the cached
+    blocks of their leading keys keys[s][0 .. m_s) (m_s <= num_keys[s],
+    stopping at the first key that is not cached); a block with no holder
+    leaves the free queue.  Rows with num_keys[s] == 0 are untouched.
+    Returns (status, m)."""
+    num_keys = [int(n) for n in num_keys]
+    S = len(num_keys)
+    if S > st.tables.shape[0]:
+        return ERR_SHAPE, None
+    for s in range(S):
+        if num_keys[s] < 0 or num_keys[s] > st.tables.shape[1] or (num_keys[s] > 0 and st.context_lens[s] != 0):
+            return ERR_RANGE, None
+    m = np.zeros(S, dtype=np.int32)
+    for s in range(S):
+        if num_keys[s] == 0:
+            continue
+        for i in range(num_keys[s]):
+            b = st.cache.get(bytes(np.asarray(keys[s][i], dtype=np.uint8)))
+            if b is None:
+                break
+            if st.ref_counts[b] == 0:
+                st.queue.remove(b)
+            st.ref_counts[b] += 1
+            st.tables[s, i] = b
+            m[s] = i + 1
+        st.context_lens[s] = m[s] * BLOCK_SIZE
+    return OK, m
+
+
+def register(st: BlockState, keys, num_keys) -> int:
+    """Give the full blocks of rows s = 0 .. S-1 their keys keys[s][0 ..
+    num_keys[s]), in (row, block) order: a block that already has a key keeps
+    it, and a key already cached keeps its block."""
+    num_keys = [int(n) for n in num_keys]
+    S = len(num_keys)
+    if S > st.tables.shape[0]:
+        return ERR_SHAPE
+    for s in range(S):
+        if num_keys[s] < 0 or num_keys[s] > int(st.context_lens[s]) // BLOCK_SIZE:
+            return ERR_RANGE
+    for s in range(S):
+        for i in range(num_keys[s]):
+            b = int(st.tables[s, i])
+            k = bytes(np.asarray(keys[s][i], dtype=np.uint8))
+            if b in st.block_key or k in st.cache:
+                continue
+            st.cache[k] = b
+            st.block_key[b] = k
     return OK

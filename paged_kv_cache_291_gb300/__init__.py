@@ -55,9 +55,10 @@ class Cache(ctypes.Structure):
 class BlocksState(ctypes.Structure):
     """Mirror of ``pkv_blocks_t``."""
     _fields_ = [("block_tables", ctypes.c_void_p), ("context_lens", ctypes.c_void_p),
-                ("ref_counts", ctypes.c_void_p), ("free_ids", ctypes.c_void_p), ("free_state", ctypes.c_void_p),
-                ("scratch", ctypes.c_void_p), ("num_blocks", ctypes.c_int32), ("max_seqs", ctypes.c_int32),
-                ("max_blocks_per_seq", ctypes.c_int32)]
+                ("ref_counts", ctypes.c_void_p), ("free_ring", ctypes.c_void_p), ("ring_pos", ctypes.c_void_p),
+                ("free_state", ctypes.c_void_p), ("scratch", ctypes.c_void_p), ("block_keys", ctypes.c_void_p),
+                ("key_table", ctypes.c_void_p), ("cached", ctypes.c_void_p), ("num_blocks", ctypes.c_int32),
+                ("max_seqs", ctypes.c_int32), ("max_blocks_per_seq", ctypes.c_int32), ("table_size", ctypes.c_int32)]
 
 
 def lib_path() -> str:
@@ -87,6 +88,8 @@ def load():
         "pkv_blocks_append": ([ctypes.POINTER(BlocksState), P, i32, i32, P, P, P, P, P], ctypes.c_int),
         "pkv_blocks_fork": ([ctypes.POINTER(BlocksState), P, P, i32, P], ctypes.c_int),
         "pkv_blocks_release": ([ctypes.POINTER(BlocksState), P, i32, P], ctypes.c_int),
+        "pkv_blocks_match": ([ctypes.POINTER(BlocksState), P, i32, P, i32, P, P], ctypes.c_int),
+        "pkv_blocks_register": ([ctypes.POINTER(BlocksState), P, i32, P, i32, P], ctypes.c_int),
         "pkv_prefix_keys": ([P, P, P, P, i32, i32, P, P], ctypes.c_int),
         "pkv_get_error": ([P, ctypes.POINTER(i32)], ctypes.c_int),
         "pkv_status_string": ([ctypes.c_int], ctypes.c_char_p),
@@ -305,23 +308,68 @@ class Blocks:
     are the arrays the attention calls read.  Every method is one launch on
     the current stream; device-side errors are read with :func:`get_error`."""
 
-    def __init__(self, num_blocks: int, max_seqs: int, max_blocks_per_seq: int, device=None):
+    def __init__(self, num_blocks: int, max_seqs: int, max_blocks_per_seq: int, device=None,
+                 prefix_cache: bool = False):
         torch = _torch()
         device = device if device is not None else torch.device("cuda", torch.cuda.current_device())
         i32 = dict(dtype=torch.int32, device=device)
         self.num_blocks, self.max_seqs, self.max_blocks_per_seq = num_blocks, max_seqs, max_blocks_per_seq
+        n1 = max(num_blocks, 1)
         self.block_tables = torch.empty((max_seqs, max_blocks_per_seq), **i32)
         self.context_lens = torch.empty((max_seqs,), **i32)
-        self.ref_counts = torch.empty((max(num_blocks, 1),), **i32)
-        self.free_ids = torch.empty((max(num_blocks, 1),), **i32)
-        self.free_state = torch.empty((2,), **i32)
-        self.scratch = torch.empty((max(2 * num_blocks, 1),), **i32)
+        self.ref_counts = torch.empty((n1,), **i32)
+        self.free_ring = torch.empty((2 * n1,), **i32)
+        self.ring_pos = torch.empty((n1,), **i32)
+        self.free_state = torch.empty((3,), **i32)
+        self.scratch = torch.empty((3 * n1,), **i32)
+        self.table_size = 0
+        self.block_keys = self.key_table = self.cached = None
+        if prefix_cache:
+            self.table_size = 1 << max(1, (2 * n1 - 1).bit_length())
+            self.block_keys = torch.zeros((n1, 32), dtype=torch.uint8, device=device)
+            self.key_table = torch.empty((self.table_size,), **i32)
+            self.cached = torch.empty((n1,), **i32)
         self.reset()
 
     def _state(self) -> BlocksState:
+        ptr = lambda t: t.data_ptr() if t is not None else None
         return BlocksState(self.block_tables.data_ptr(), self.context_lens.data_ptr(), self.ref_counts.data_ptr(),
-                           self.free_ids.data_ptr(), self.free_state.data_ptr(), self.scratch.data_ptr(),
-                           self.num_blocks, self.max_seqs, self.max_blocks_per_seq)
+                           self.free_ring.data_ptr(), self.ring_pos.data_ptr(), self.free_state.data_ptr(),
+                           self.scratch.data_ptr(), ptr(self.block_keys), ptr(self.key_table), ptr(self.cached),
+                           self.num_blocks, self.max_seqs, self.max_blocks_per_seq, self.table_size)
+
+    def free_queue(self) -> list:
+        """The free block ids, least recently freed first (synchronises)."""
+        ring, pos = self.free_ring.cpu().tolist(), self.ring_pos.cpu().tolist()
+        head, entries, _ = self.free_state.cpu().tolist()
+        cap = 2 * self.num_blocks
+        out = []
+        for e in range(entries):
+            idx = (head + e) % cap
+            b = ring[idx]
+            if 0 <= b < self.num_blocks and pos[b] == idx:
+                out.append(b)
+        return out
+
+    def match(self, keys, num_keys, matched=None, stream=None):
+        """Prefix-cache hits for empty rows: returns matched [S] (int32 CUDA)."""
+        torch = _torch()
+        S = int(num_keys.shape[0])
+        matched = matched if matched is not None else torch.empty((max(S, 1),), dtype=torch.int32,
+                                                                  device=self.block_tables.device)
+        st = load().pkv_blocks_match(ctypes.byref(self._state()), _dev(keys, "keys", dtype=torch.uint8),
+                                     int(keys.shape[1]), _dev(num_keys, "num_keys", dtype=torch.int32), S,
+                                     _dev(matched, "matched", dtype=torch.int32), _stream_handle(stream))
+        _check(st, "pkv_blocks_match")
+        return matched
+
+    def register(self, keys, num_keys, stream=None) -> None:
+        """Give rows' full blocks their prefix-cache keys."""
+        torch = _torch()
+        st = load().pkv_blocks_register(ctypes.byref(self._state()), _dev(keys, "keys", dtype=torch.uint8),
+                                        int(keys.shape[1]), _dev(num_keys, "num_keys", dtype=torch.int32),
+                                        int(num_keys.shape[0]), _stream_handle(stream))
+        _check(st, "pkv_blocks_register")
 
     def reset(self, stream=None) -> None:
         """Every row empty, every block free (queued 0, 1, 2, ...)."""

@@ -188,12 +188,22 @@ namespace {
 
 pkv_status check_blocks(const pkv_blocks_t* b, pkv::BlocksArgs* a) {
     if (b == nullptr || b->block_tables == nullptr || b->context_lens == nullptr || b->ref_counts == nullptr ||
-        b->free_ids == nullptr || b->free_state == nullptr || b->scratch == nullptr)
+        b->free_ring == nullptr || b->ring_pos == nullptr || b->free_state == nullptr || b->scratch == nullptr)
         return PKV_ERR_NULL;
     if (b->num_blocks < 0 || b->max_seqs < 0 || b->max_blocks_per_seq < 1) return PKV_ERR_SHAPE;
-    if (static_cast<int64_t>(b->max_blocks_per_seq) * 16 > INT32_MAX) return PKV_ERR_SHAPE;
-    *a = pkv::BlocksArgs{b->block_tables, b->context_lens, b->ref_counts, b->free_ids, b->free_state,
-                         b->scratch,      b->num_blocks,   b->max_seqs,   b->max_blocks_per_seq};
+    if (static_cast<int64_t>(b->max_blocks_per_seq) * 16 > INT32_MAX || b->num_blocks > INT32_MAX / 3)
+        return PKV_ERR_SHAPE;
+    const int n_cache = (b->block_keys != nullptr) + (b->key_table != nullptr) + (b->cached != nullptr);
+    if (n_cache != 0 && n_cache != 3) return PKV_ERR_NULL;
+    if (n_cache == 3) {
+        const int64_t t = b->table_size;
+        if (t < 2 * static_cast<int64_t>(b->num_blocks) || t < 1 || (t & (t - 1)) != 0) return PKV_ERR_SHAPE;
+        if (!aligned16(b->block_keys)) return PKV_ERR_ALIGN;
+    }
+    *a = pkv::BlocksArgs{b->block_tables, b->context_lens, b->ref_counts, b->free_ring, b->ring_pos,
+                         b->free_state,   b->scratch,      b->block_keys, b->key_table, b->cached,
+                         b->num_blocks,   b->max_seqs,     b->max_blocks_per_seq,
+                         n_cache == 3 ? b->table_size : 0};
     return PKV_OK;
 }
 
@@ -238,6 +248,42 @@ PKV_API pkv_status pkv_blocks_fork(const pkv_blocks_t* blocks, const int32_t* pa
     DeviceState* dev = nullptr;
     if ((st = current_device(&dev)) != PKV_OK) return st;
     cudaError_t e = pkv::launch_blocks_fork(a, parents, children, n, dev->err, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e);
+}
+
+PKV_API pkv_status pkv_blocks_match(const pkv_blocks_t* blocks, const void* keys, int32_t key_stride,
+                                    const int32_t* num_keys, int32_t num_seqs, int32_t* matched, void* stream) {
+    pkv::BlocksArgs a;
+    pkv_status st = check_blocks(blocks, &a);
+    if (st != PKV_OK) return st;
+    if (a.key_table == nullptr) return PKV_ERR_NULL;
+    if (num_seqs < 0 || num_seqs > blocks->max_seqs || num_seqs > pkv::kBlocksMaxRows || key_stride < 0)
+        return PKV_ERR_SHAPE;
+    if (num_seqs == 0) return PKV_OK;
+    if (keys == nullptr || num_keys == nullptr || matched == nullptr) return PKV_ERR_NULL;
+    if (!aligned16(keys)) return PKV_ERR_ALIGN;
+    DeviceState* dev = nullptr;
+    if ((st = current_device(&dev)) != PKV_OK) return st;
+    cudaError_t e = pkv::launch_blocks_match(a, static_cast<const uint8_t*>(keys), key_stride, num_keys, num_seqs,
+                                             matched, dev->err, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e);
+}
+
+PKV_API pkv_status pkv_blocks_register(const pkv_blocks_t* blocks, const void* keys, int32_t key_stride,
+                                       const int32_t* num_keys, int32_t num_seqs, void* stream) {
+    pkv::BlocksArgs a;
+    pkv_status st = check_blocks(blocks, &a);
+    if (st != PKV_OK) return st;
+    if (a.key_table == nullptr) return PKV_ERR_NULL;
+    if (num_seqs < 0 || num_seqs > blocks->max_seqs || num_seqs > pkv::kBlocksMaxRows || key_stride < 0)
+        return PKV_ERR_SHAPE;
+    if (num_seqs == 0) return PKV_OK;
+    if (keys == nullptr || num_keys == nullptr) return PKV_ERR_NULL;
+    if (!aligned16(keys)) return PKV_ERR_ALIGN;
+    DeviceState* dev = nullptr;
+    if ((st = current_device(&dev)) != PKV_OK) return st;
+    cudaError_t e = pkv::launch_blocks_register(a, static_cast<const uint8_t*>(keys), key_stride, num_keys,
+                                                num_seqs, dev->err, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PKV_OK : cuda_fail(e);
 }
 

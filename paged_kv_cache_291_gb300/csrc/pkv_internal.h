@@ -81,10 +81,14 @@ struct BlocksArgs {
     int32_t* tables;      // [max_seqs][max_blocks]
     int32_t* lens;        // [max_seqs]
     int32_t* refs;        // [num_blocks]
-    int32_t* free_ids;    // [num_blocks] ring
-    int32_t* free_state;  // [2] {head, count}
-    int32_t* scratch;     // [2 * num_blocks], zero between calls
-    int32_t num_blocks, max_seqs, max_blocks;
+    int32_t* free_ring;   // [2 * num_blocks] ring of free block ids (LRU order; stale entries skipped)
+    int32_t* ring_pos;    // [num_blocks] ring index of a free block's live entry, -1 when held
+    int32_t* free_state;  // [3] {head, entries, free blocks}
+    int32_t* scratch;     // [3 * num_blocks]; the first 2 * num_blocks zero between calls
+    uint8_t* block_keys;  // [num_blocks][32] prefix-cache keys, or null (no prefix cache)
+    int32_t* key_table;   // [table_size] block ids by key (linear probing, -1 empty), or null
+    int32_t* cached;      // [num_blocks] 1 if the block's key is in the table, or null
+    int32_t num_blocks, max_seqs, max_blocks, table_size;
 };
 
 // Rows per fork or release call (the kernels keep per-row offsets on chip).
@@ -99,6 +103,12 @@ cudaError_t launch_blocks_fork(const BlocksArgs& st, const int32_t* parents, con
 cudaError_t launch_prefix_keys(const int32_t* token_ids, const int32_t* token_start_loc, const int64_t* extra,
                                const uint8_t* parent_keys, int32_t num_seqs, int32_t max_blocks, uint8_t* keys,
                                unsigned long long* err, cudaStream_t stream);
+cudaError_t launch_blocks_match(const BlocksArgs& st, const uint8_t* keys, int32_t key_stride,
+                                const int32_t* num_keys, int32_t num_seqs, int32_t* matched,
+                                unsigned long long* err, cudaStream_t stream);
+cudaError_t launch_blocks_register(const BlocksArgs& st, const uint8_t* keys, int32_t key_stride,
+                                   const int32_t* num_keys, int32_t num_seqs, unsigned long long* err,
+                                   cudaStream_t stream);
 cudaError_t launch_blocks_release(const BlocksArgs& st, const int32_t* rows, int32_t n, unsigned long long* err,
                                   cudaStream_t stream);
 

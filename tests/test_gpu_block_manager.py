@@ -8,6 +8,7 @@ import torch
 
 import oracle
 from oracle import block_manager as bm
+from oracle import prefix_keys as pk
 import pkv_workloads as W
 from gpu_helpers import assert_close, dev_tensor, host_bits
 
@@ -27,14 +28,26 @@ def i32(x):
     return torch.tensor(np.asarray(x, dtype=np.int32), device="cuda")
 
 
+def u8(x):
+    return torch.tensor(np.ascontiguousarray(x, dtype=np.uint8), device="cuda")
+
+
 def assert_same_state(blocks, st, what):
     assert np.array_equal(blocks.block_tables.cpu().numpy(), st.tables), f"{what}: tables"
     assert np.array_equal(blocks.context_lens.cpu().numpy(), st.context_lens), f"{what}: lengths"
     n = st.num_blocks
     assert np.array_equal(blocks.ref_counts.cpu().numpy()[:n], st.ref_counts), f"{what}: counts"
-    assert np.array_equal(blocks.free_ids.cpu().numpy()[:n], st.free_ids), f"{what}: free ring"
-    assert blocks.free_state.cpu().tolist() == [st.free_head, st.free_count], f"{what}: ring head/count"
-    assert not blocks.scratch.cpu().numpy().any(), f"{what}: scratch not left zero"
+    assert blocks.free_queue() == st.free_queue(), f"{what}: free queue"
+    assert blocks.free_state.cpu().tolist()[2] == st.free_count, f"{what}: free count"
+    assert not blocks.scratch.cpu().numpy()[:2 * n].any(), f"{what}: scratch not left zero"
+    if blocks.cached is not None:
+        cached = blocks.cached.cpu().numpy()[:n]
+        keys = blocks.block_keys.cpu().numpy()
+        assert set(np.flatnonzero(cached).tolist()) == set(st.block_key), f"{what}: cached blocks"
+        for b, k in st.block_key.items():
+            assert bytes(keys[b]) == k, f"{what}: key of block {b}"
+        table = blocks.key_table.cpu().numpy()
+        assert sorted(table[table >= 0].tolist()) == sorted(st.block_key), f"{what}: table contents"
 
 
 def run_append(pkv, blocks, st, qsl, what):
@@ -170,3 +183,132 @@ def test_step_through_the_state_matches_the_oracle(pkv):
     assert pkv.get_error() == (0, 0)
     ref = oracle.decode_attention(k_pool, v_pool, q, st.context_lens, st.tables, 1.0 / np.sqrt(d), threads=8)
     assert_close(out.cpu().numpy(), ref, "blocks step")
+
+
+def _keys(tokens, n, stride):
+    out = np.zeros((stride, 32), dtype=np.uint8)
+    for i, k in enumerate(pk.sequence_keys(np.asarray(tokens, dtype=np.int64))[:n]):
+        out[i] = np.frombuffer(k, dtype=np.uint8)
+    return out
+
+
+@pytest.mark.parametrize("seed,rows,num_blocks", [(0, 8, 40), (1, 8, 24), (2, 24, 120)])
+def test_prefix_cache_lifecycles_match_oracle(pkv, seed, rows, num_blocks):
+    """Requests with prompts from a few shared prefixes come and go (match,
+    append of the rest, register, decode steps, release), with the pool small
+    enough that cached blocks get evicted: after every call the device state
+    (tables, counts, free queue in LRU order, cached keys) equals the
+    oracle's."""
+    rng = np.random.default_rng(200 + seed)
+    MB = 12
+    blocks = pkv.Blocks(num_blocks, rows, MB, prefix_cache=True)
+    st = bm.BlockState(num_blocks, rows, MB)
+    assert_same_state(blocks, st, "reset")
+    hist = {r: [] for r in range(rows)}
+    prefixes = [rng.integers(0, 1000, size=int(rng.integers(16, 70))) for _ in range(3)]
+    hits = evictions_seen = 0
+    for step in range(60):
+        what = f"seed {seed} step {step}"
+        op = rng.integers(0, 10)
+        empty = [r for r in range(rows) if st.context_lens[r] == 0]
+        live = [r for r in range(rows) if st.context_lens[r] > 0]
+        if op < 4 and empty:
+            r = int(rng.choice(empty))
+            prompt = np.concatenate([prefixes[rng.integers(0, 3)], rng.integers(0, 1000, size=rng.integers(0, 20))])
+            nf = len(prompt) // B
+            keys = np.zeros((rows, MB, 32), dtype=np.uint8)
+            keys[r] = _keys(prompt, nf, MB)
+            nk = np.zeros(rows, dtype=np.int32)
+            nk[r] = nf
+            m = blocks.match(u8(keys), i32(nk))
+            status, om = bm.match(st, keys, nk)
+            assert pkv.get_error() == (0, 0) and status == bm.OK
+            assert np.array_equal(m.cpu().numpy()[:rows], om), f"{what}: matched"
+            hits += int(om[r])
+            assert_same_state(blocks, st, what + " match")
+            q = np.zeros(rows, dtype=np.int64)
+            q[r] = len(prompt) - om[r] * B
+            status = run_append(pkv, blocks, st, np.concatenate([[0], np.cumsum(q)]), what + " prompt")
+            if status != bm.OK:
+                blocks.release(i32([r]))
+                assert pkv.get_error() == (0, 0) and bm.release(st, [r]) == bm.OK
+                hist[r] = []
+                continue
+            hist[r] = list(prompt)
+        elif op < 8 and live:
+            q = np.zeros(rows, dtype=np.int64)
+            q[live] = 1
+            status = run_append(pkv, blocks, st, np.concatenate([[0], np.cumsum(q)]), what + " decode")
+            if status == bm.OK:
+                for r in live:
+                    hist[r].append(int(rng.integers(0, 1000)))
+        elif live:
+            r = int(rng.choice(live))
+            blocks.release(i32([r]))
+            assert pkv.get_error() == (0, 0) and bm.release(st, [r]) == bm.OK
+            hist[r] = []
+            assert_same_state(blocks, st, what + " release")
+        cached_before = len(st.block_key)
+        keys = np.zeros((rows, MB, 32), dtype=np.uint8)
+        nk = np.zeros(rows, dtype=np.int32)
+        for r in range(rows):
+            nk[r] = int(st.context_lens[r]) // B
+            keys[r] = _keys(hist[r], int(nk[r]), MB)
+        blocks.register(u8(keys), i32(nk))
+        assert pkv.get_error() == (0, 0) and bm.register(st, keys, nk) == bm.OK
+        assert_same_state(blocks, st, what + " register")
+        evictions_seen += max(0, cached_before - len(st.block_key))
+    assert hits > 0
+
+
+def test_stale_entries_are_compacted_away(pkv):
+    """A prompt's blocks are released (content kept) and matched back again
+    and again: every match leaves stale ring entries, so the ring of
+    2 * num_blocks entries must be compacted on release; the free queue stays
+    the oracle's throughout."""
+    NB, MB = 6, 4
+    blocks = pkv.Blocks(NB, 2, MB, prefix_cache=True)
+    st = bm.BlockState(NB, 2, MB)
+    prompt = np.arange(48)                                     # 3 full blocks
+    run_append(pkv, blocks, st, [0, 48], "prompt")
+    keys = np.zeros((2, MB, 32), dtype=np.uint8)
+    keys[0] = _keys(prompt, 3, MB)
+    blocks.register(u8(keys), i32([3, 0]))
+    assert bm.register(st, keys, [3, 0]) == bm.OK
+    most = 0
+    for cycle in range(12):
+        blocks.release(i32([0]))
+        assert pkv.get_error() == (0, 0) and bm.release(st, [0]) == bm.OK
+        assert_same_state(blocks, st, f"cycle {cycle} release")
+        most = max(most, blocks.free_state.cpu().tolist()[1])
+        m = blocks.match(u8(keys), i32([3, 0]))
+        status, om = bm.match(st, keys, [3, 0])
+        assert pkv.get_error() == (0, 0) and status == bm.OK and om.tolist() == [3, 0]
+        assert m.cpu().tolist()[:2] == [3, 0]
+        assert_same_state(blocks, st, f"cycle {cycle} match")
+    assert most == 2 * NB, "the ring never filled, so compaction was not exercised"
+
+
+def test_equal_prompts_registered_together_keep_the_first_rows_blocks(pkv):
+    """Rows 0 and 2 computed the same 40-token prompt separately and row 1 is
+    a fork of row 0: one register call gives each key to row 0's block (row
+    1's entries are the same blocks, row 2's equal keys lose and are removed
+    from the table again)."""
+    NB, MB, R = 16, 4, 3
+    blocks = pkv.Blocks(NB, R, MB, prefix_cache=True)
+    st = bm.BlockState(NB, R, MB)
+    prompt = np.arange(500, 540)
+    run_append(pkv, blocks, st, [0, 40], "row 0")
+    blocks.fork(i32([0]), i32([1]))
+    assert pkv.get_error() == (0, 0) and bm.fork(st, [0], [1]) == bm.OK
+    run_append(pkv, blocks, st, [0, 0, 0, 40], "row 2")
+    keys = np.stack([_keys(prompt, 2, MB)] * R)
+    for trial in range(3):                                      # the race between equal keys varies
+        blocks.register(u8(keys), i32([2, 2, 2]))
+        assert pkv.get_error() == (0, 0)
+        if trial == 0:
+            assert bm.register(st, keys, [2, 2, 2]) == bm.OK
+        assert_same_state(blocks, st, f"register, trial {trial}")
+    assert sorted(st.block_key) == sorted(st.tables[0, :2].tolist())
+    m = blocks.match(u8(np.stack([np.zeros((MB, 32), np.uint8)] * R)), i32([0, 0, 0]))
+    assert pkv.get_error() == (0, 0)

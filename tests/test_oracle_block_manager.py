@@ -15,6 +15,7 @@ import numpy as np
 import pytest
 
 from oracle import block_manager as bm
+from oracle import prefix_keys as pk
 
 B = bm.BLOCK_SIZE
 
@@ -131,9 +132,9 @@ def test_errors_leave_the_state_unchanged():
     assert bm.fork(st, [0], [1]) == bm.ERR_RANGE                 # child is not empty
     assert bm.release(st, [1, 1]) == bm.ERR_ALIAS
     assert bm.release(st, [5]) == bm.ERR_RANGE
-    for a in ("tables", "context_lens", "ref_counts", "free_ids"):
+    for a in ("tables", "context_lens", "ref_counts"):
         assert np.array_equal(getattr(st, a), getattr(snap, a))
-    assert (st.free_head, st.free_count) == (snap.free_head, snap.free_count)
+    assert st.free_queue() == snap.free_queue()
 
 
 @pytest.mark.parametrize("seed", range(6))
@@ -176,3 +177,130 @@ def test_random_lifecycles_replay_and_invariants(seed):
         check_invariants(st)
         rp.check(st)
     assert copies > 0, "the random walk never exercised copy-on-write"
+
+
+def keys_of(tokens, n):
+    ks = pk.sequence_keys(tokens)[:n]
+    return [np.frombuffer(k, dtype=np.uint8) for k in ks]
+
+
+def test_a_reused_prompt_takes_its_cached_blocks_and_allocation_follows_lru():
+    st = bm.BlockState(8, 3, 4)
+    prompt = np.arange(100, 140)                                 # 40 tokens: 2 full blocks + 8
+    assert bm.append(st, [0, 40])[0] == bm.OK                    # blocks 0, 1, 2
+    assert bm.register(st, [keys_of(prompt, 2)], [2]) == bm.OK
+    assert bm.release(st, [0]) == bm.OK
+    assert st.free_queue() == [3, 4, 5, 6, 7, 2, 1, 0]           # content kept, last block first
+    status, m = bm.match(st, [keys_of(prompt, 2), []], [2, 0])
+    assert status == bm.OK and m.tolist() == [2, 0]
+    assert st.tables[0, :2].tolist() == [0, 1] and st.context_lens[0] == 32
+    assert st.free_queue() == [3, 4, 5, 6, 7, 2]
+    status, slots, _, _ = bm.append(st, [0, 8])                 # the 8 tokens left: block 3
+    assert slots.tolist() == list(range(3 * B, 3 * B + 8))
+
+
+def test_reusing_a_freed_block_drops_its_key():
+    st = bm.BlockState(3, 3, 4)
+    prompt = np.arange(32)
+    bm.append(st, [0, 32])                                       # blocks 0, 1
+    bm.register(st, [keys_of(prompt, 2)], [2])
+    bm.release(st, [0])                                          # queue: 2, 1, 0
+    bm.append(st, [0, 0, 20])                                    # row 1 takes 2 and 1 (1 loses its key)
+    assert st.tables[1, :2].tolist() == [2, 1]
+    status, m = bm.match(st, [[], [], keys_of(prompt, 2)], [0, 0, 2])
+    assert status == bm.OK and m.tolist() == [0, 0, 1]           # block 0 still cached; block 1's key is gone
+    assert st.tables[2, 0] == 0 and st.context_lens[1] == 20 and st.free_queue() == []
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_random_requests_with_shared_prefixes_replay(seed):
+    """Requests with prompts from a few shared prefixes come and go: cached
+    blocks are reused, evicted under pressure, and every row still reads its
+    own tokens; every cached key's block holds the tokens it was given."""
+    rng = np.random.default_rng(100 + seed)
+    R, NB, MB = 8, 40, 12
+    st = bm.BlockState(NB, R, MB)
+    rp = Replay(st)
+    hist = {r: [] for r in range(R)}                               # token ids per row
+    prefixes = [rng.integers(0, 1000, size=int(rng.integers(16, 70))) for _ in range(3)]
+    key_tokens = {}
+    hits = 0
+    for _ in range(80):
+        op = rng.integers(0, 10)
+        empty = [r for r in range(R) if st.context_lens[r] == 0]
+        live = [r for r in range(R) if st.context_lens[r] > 0]
+        if op < 4 and empty:                                       # a new request
+            r = int(rng.choice(empty))
+            prompt = np.concatenate([prefixes[rng.integers(0, 3)], rng.integers(0, 1000, size=rng.integers(0, 20))])
+            nf = len(prompt) // B
+            ks = [[] for _ in range(R)]
+            nk = [0] * R
+            ks[r], nk[r] = keys_of(prompt, nf), nf
+            status, m = bm.match(st, ks, nk)
+            assert status == bm.OK
+            hits += int(m[r])
+            hist[r] = list(prompt[:m[r] * B])
+            rp.hist[r] = list(prompt[:m[r] * B])
+            q = np.zeros(R, dtype=np.int64)
+            q[r] = len(prompt) - m[r] * B
+            qsl = np.concatenate([[0], np.cumsum(q)])
+            status, slots, cs, cd = bm.append(st, qsl)
+            if status != bm.OK:                                    # pool exhausted: drop the request
+                assert status == bm.ERR_NO_BLOCKS
+                assert bm.release(st, [r]) == bm.OK
+                hist[r], rp.hist[r] = [], []
+                continue
+            for s_, d_ in zip(cs, cd):
+                rp.pool[d_ * B:(d_ + 1) * B] = rp.pool[s_ * B:(s_ + 1) * B]
+            tail = prompt[m[r] * B:]
+            for i, sl in enumerate(slots):
+                rp.pool[sl] = tail[i]
+            hist[r] = list(prompt)
+            rp.hist[r] = list(prompt)
+        elif op < 8 and live:                                      # a decode step for every live row
+            q = np.zeros(R, dtype=np.int64)
+            q[live] = 1
+            qsl = np.concatenate([[0], np.cumsum(q)])
+            snap = st.clone()
+            status, slots, cs, cd = bm.append(st, qsl)
+            if status != bm.OK:
+                assert status == bm.ERR_NO_BLOCKS and st.free_queue() == snap.free_queue()
+                continue
+            for s_, d_ in zip(cs, cd):
+                rp.pool[d_ * B:(d_ + 1) * B] = rp.pool[s_ * B:(s_ + 1) * B]
+            for i, r in enumerate(live):
+                t = int(rng.integers(0, 1000))
+                rp.pool[slots[i]] = t
+                hist[r].append(t)
+                rp.hist[r].append(t)
+        elif live:                                                 # a request ends
+            r = int(rng.choice(live))
+            assert bm.release(st, [r]) == bm.OK
+            hist[r], rp.hist[r] = [], []
+        # every row registers its full blocks
+        ks, nk = [], []
+        for r in range(R):
+            nf = int(st.context_lens[r]) // B
+            ks.append(keys_of(np.array(hist[r], dtype=np.int64), nf))
+            nk.append(nf)
+            for i in range(nf):
+                key_tokens.setdefault(bytes(ks[r][i]), list(hist[r][i * B:(i + 1) * B]))
+        assert bm.register(st, ks, nk) == bm.OK
+        check_invariants(st)
+        rp.check(st)
+        for k, b in st.cache.items():
+            assert st.block_key[b] == k
+            assert rp.pool[b * B:(b + 1) * B].tolist() == key_tokens[k], "a cached key's block was overwritten"
+    assert hits > 0, "no prefix was ever reused"
+
+
+def test_equal_keys_in_one_register_call_go_to_the_first_row():
+    st = bm.BlockState(16, 3, 4)
+    prompt = np.arange(500, 540)
+    bm.append(st, [0, 40])                                       # row 0: blocks 0, 1, 2
+    bm.fork(st, [0], [1])
+    bm.append(st, [0, 0, 0, 40])                                 # row 2: blocks 3, 4, 5
+    ks = [keys_of(prompt, 2)] * 3
+    assert bm.register(st, ks, [2, 2, 2]) == bm.OK
+    assert sorted(st.block_key) == [0, 1]
+    assert all(st.cache[bytes(k)] == b for k, b in zip(keys_of(prompt, 2), [0, 1]))
