@@ -503,6 +503,45 @@ def prefix_cache_timing(w, pkv, torch, dev, stream):
             "bound": "latency (one CTA; register inserts from one thread, in order)"}
 
 
+def swap_timing(w, pkv, torch, dev, stream, reps):
+    """Device time of swapping every block the workload's rows hold out to
+    page-locked host memory and back in (pkv_swap_blocks), next to one
+    contiguous copy of the same bytes by the copy engines (cudaMemcpyAsync
+    through torch), in each direction."""
+    import numpy as np
+    blocks_np = np.unique(np.concatenate([w.block_tables[s, :-(-int(w.context_lens[s]) // 16)]
+                                          for s in range(w.num_seqs)]))
+    n = int(min(len(blocks_np), 65535))
+    blocks_np = blocks_np[:n].astype(np.int32)
+    r = reps[0]
+    slab = 2 * w.num_kv_heads * 16 * w.head_dim * 2
+    host = torch.empty((n * slab // 2,), dtype=torch.int16).pin_memory()
+    dbuf = torch.empty_like(host, device=dev)
+    blocks = torch.tensor(blocks_np, device=dev)
+    slots = torch.arange(n, dtype=torch.int32, device=dev)
+    out = {}
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    legs = [("out_gbs", lambda: pkv.swap_out(r["k"], r["v"], blocks, slots, host, stream=stream)),
+            ("in_gbs", lambda: pkv.swap_in(r["k"], r["v"], blocks, slots, host, stream=stream)),
+            ("memcpy_d2h_gbs", lambda: host.copy_(dbuf, non_blocking=True)),
+            ("memcpy_h2d_gbs", lambda: dbuf.copy_(host, non_blocking=True))]
+    with torch.cuda.stream(stream):
+        for key, fn in legs:
+            fn()
+            e0.record(stream)
+            for _ in range(3):
+                fn()
+            e1.record(stream)
+            stream.synchronize()
+            out[key] = 3 * n * slab / (e0.elapsed_time(e1) * 1e-3) / 1e9
+    status = pkv.get_error(stream)
+    if status[0] != 0:
+        raise RuntimeError(f"device error in the swap timing: {status}")
+    return {"call": "pkv_swap_blocks", "workload": f"{n} blocks of {slab // 1024} KB ({n * slab / 1e6:.0f} MB) "
+            "to and from page-locked host memory", **out, "launches_per_call": 1,
+            "bound": "the host link (compared with the copy engines' contiguous copy)"}
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -788,6 +827,7 @@ def run_ours(args):
     line["block_manager"] = block_manager_timing(w, pkv, torch, dev, stream)
     line["prefix_keys"] = prefix_keys_timing(w, pkv, torch, dev, stream)
     line["prefix_cache"] = prefix_cache_timing(w, pkv, torch, dev, stream)
+    line["swap"] = swap_timing(w, pkv, torch, dev, stream, reps)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_budget)
     print(json.dumps(line), flush=True)

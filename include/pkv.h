@@ -67,7 +67,8 @@ typedef enum pkv_status {
     PKV_ERR_CUDA = 11,       /* a CUDA runtime call failed (see pkv_last_cuda_error)        */
     PKV_ERR_UNSUPPORTED = 12, /* the current device is not compute capability 10.3          */
     PKV_ERR_SCRATCH_LIMIT = 13, /* the problem needs more than the built-in scratch buffer  */
-    PKV_ERR_NO_BLOCKS = 14   /* (device) the free queue cannot supply the blocks an append needs */
+    PKV_ERR_NO_BLOCKS = 14,  /* (device) the free queue cannot supply the blocks an append needs */
+    PKV_ERR_HOST_MEMORY = 15 /* a host buffer is not page-locked memory mapped for the device    */
 } pkv_status;
 
 typedef struct pkv_cache {
@@ -115,6 +116,30 @@ pkv_status pkv_cache_write(const pkv_cache_t* cache, const void* k_new, const vo
  */
 pkv_status pkv_copy_blocks(const pkv_cache_t* cache, const int32_t* src, const int32_t* dst, int32_t num_pairs,
                            const int32_t* src_host, const int32_t* dst_host, void* stream);
+
+/*
+ * pkv_swap_blocks -- move whole blocks between the pool and host memory (KV
+ * offloading).  [ENG] "traffic characteristics and system control": a
+ * request idle for seconds or minutes (an agent waiting on a tool) has its KV
+ * cache swapped out to cheaper, larger CPU memory and swapped back in when
+ * the next turn starts, instead of holding GPU memory; [KV2] section 5: a
+ * request that loses its KV is otherwise prefilled again from the start.
+ *
+ *   direction      0 = out (pool -> host), 1 = in (host -> pool)
+ *   blocks, slots  int32 [n], device: pair i moves pool block blocks[i] and
+ *                  host slab slots[i]; a negative block id skips the pair
+ *   host           page-locked host memory mapped for the device
+ *                  (cudaHostAlloc, or cudaHostRegister with the mapped flag),
+ *                  16-byte aligned, holding num_host_slots slabs of
+ *                  [2][num_kv_heads][16][head_dim] bf16 (the K block, then the
+ *                  V block); the kernel reads and writes it directly, over the
+ *                  host link, bit-exact
+ *   Returns PKV_ERR_HOST_MEMORY, launching nothing, when `host` is not such
+ *   memory.  Block ids or slots out of range found on the device are skipped
+ *   and raise PKV_ERR_RANGE.  n <= 65535 pairs per call.
+ */
+pkv_status pkv_swap_blocks(const pkv_cache_t* cache, int32_t direction, const int32_t* blocks, const int32_t* slots,
+                           int32_t n, void* host, int64_t num_host_slots, void* stream);
 
 /*
  * pkv_decode_workspace_size -- bytes of workspace pkv_decode_attention needs

@@ -111,6 +111,21 @@ def copy_blocks(k_pool, v_pool, src, dst):
         raise OracleError(f"oracle_copy_blocks -> {rc}")
 
 
+def swap_blocks(direction, k_pool, v_pool, blocks, slots, host):
+    """In place, for every pair with blocks[i] >= 0: host[slots[i]] = (K, V) of
+    pool block blocks[i] (direction 0), or the reverse (direction 1).  ``host``
+    is uint16 [num_slots][2][Hkv][16][d]."""
+    for b, h in zip(np.asarray(blocks).tolist(), np.asarray(slots).tolist()):
+        if b < 0:
+            continue
+        if direction == 0:
+            host[h, 0] = k_pool[b]
+            host[h, 1] = v_pool[b]
+        else:
+            k_pool[b] = host[h, 0]
+            v_pool[b] = host[h, 1]
+
+
 def paged_attention(k_pool, v_pool, q, query_start_loc, context_lens, block_tables, scale, threads=1):
     """Causal attention of ``q`` ([Tq][Hq][d] bf16 bits) over the paged cache.
 

@@ -21,7 +21,7 @@ from typing import Optional, Tuple
 __all__ = [
     "PKVError", "lib_path", "load", "version", "status_string", "cache_write", "copy_blocks",
     "decode_workspace_size", "decode_attention", "prefill_workspace_size", "chunked_prefill_attention",
-    "get_error", "Cache", "Blocks", "prefix_keys",
+    "get_error", "Cache", "Blocks", "prefix_keys", "swap_out", "swap_in",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -33,7 +33,7 @@ STATUS_NAMES = {
     0: "PKV_OK", 1: "PKV_ERR_NULL", 2: "PKV_ERR_SHAPE", 3: "PKV_ERR_HEADS", 4: "PKV_ERR_HEADDIM",
     5: "PKV_ERR_BLOCKSIZE", 6: "PKV_ERR_ALIAS", 7: "PKV_ERR_WORKSPACE", 8: "PKV_ERR_ALIGN", 9: "PKV_ERR_RANGE",
     10: "PKV_ERR_TIMEOUT", 11: "PKV_ERR_CUDA", 12: "PKV_ERR_UNSUPPORTED", 13: "PKV_ERR_SCRATCH_LIMIT",
-    14: "PKV_ERR_NO_BLOCKS",
+    14: "PKV_ERR_NO_BLOCKS", 15: "PKV_ERR_HOST_MEMORY",
 }
 
 
@@ -91,6 +91,7 @@ def load():
         "pkv_blocks_match": ([ctypes.POINTER(BlocksState), P, i32, P, i32, P, P], ctypes.c_int),
         "pkv_blocks_register": ([ctypes.POINTER(BlocksState), P, i32, P, i32, P], ctypes.c_int),
         "pkv_prefix_keys": ([P, P, P, P, i32, i32, P, P], ctypes.c_int),
+        "pkv_swap_blocks": ([CP, i32, P, P, i32, P, ctypes.c_int64, P], ctypes.c_int),
         "pkv_get_error": ([P, ctypes.POINTER(i32)], ctypes.c_int),
         "pkv_status_string": ([ctypes.c_int], ctypes.c_char_p),
         "pkv_last_cuda_error": ([], ctypes.c_char_p),
@@ -282,6 +283,36 @@ def chunked_prefill_attention(k_pool, v_pool, q, query_start_loc, context_lens, 
         workspace.numel() * workspace.element_size(), _stream_handle(stream))
     _check(st, "pkv_chunked_prefill_attention")
     return out
+
+
+def _swap(direction, k_pool, v_pool, blocks, slots, host, stream):
+    torch = _torch()
+    lib = load()
+    c = _cache(k_pool, v_pool)
+    n = int(blocks.shape[0])
+    if slots.shape[0] != n:
+        raise ValueError("blocks and slots must have the same length")
+    if not isinstance(host, torch.Tensor) or host.is_cuda or not host.is_contiguous():
+        raise ValueError("host must be a contiguous CPU tensor in page-locked memory")
+    slab = 2 * c.num_kv_heads * 16 * c.head_dim * 2
+    if host.numel() * host.element_size() % slab:
+        raise ValueError("host must hold whole slabs of [2][num_kv_heads][16][head_dim] bf16")
+    num_slots = host.numel() * host.element_size() // slab
+    st = lib.pkv_swap_blocks(ctypes.byref(c), int(direction), _dev(blocks, "blocks", dtype=torch.int32),
+                             _dev(slots, "slots", dtype=torch.int32), n, ctypes.c_void_p(host.data_ptr()),
+                             num_slots, _stream_handle(stream))
+    _check(st, "pkv_swap_blocks")
+
+
+def swap_out(k_pool, v_pool, blocks, slots, host, stream=None) -> None:
+    """host slab slots[i] <- pool block blocks[i] (K then V); ``host`` is a
+    pinned CPU tensor of whole [2][Hkv][16][d] bf16 slabs."""
+    _swap(0, k_pool, v_pool, blocks, slots, host, stream)
+
+
+def swap_in(k_pool, v_pool, blocks, slots, host, stream=None) -> None:
+    """pool block blocks[i] <- host slab slots[i]."""
+    _swap(1, k_pool, v_pool, blocks, slots, host, stream)
 
 
 def prefix_keys(token_ids, token_start_loc, max_blocks: int, extra=None, parent_keys=None, keys=None,

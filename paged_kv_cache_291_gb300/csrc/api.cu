@@ -129,6 +129,7 @@ PKV_API const char* pkv_status_string(pkv_status s) {
         case PKV_ERR_SCRATCH_LIMIT:
             return "PKV_ERR_SCRATCH_LIMIT: the batch needs more workspace than the built-in 4 MiB scratch buffer";
         case PKV_ERR_NO_BLOCKS: return "PKV_ERR_NO_BLOCKS: the free queue holds fewer blocks than the append needs";
+        case PKV_ERR_HOST_MEMORY: return "PKV_ERR_HOST_MEMORY: the host buffer is not page-locked memory mapped for the device";
     }
     return "unknown pkv_status";
 }
@@ -313,6 +314,31 @@ PKV_API pkv_status pkv_prefix_keys(const int32_t* token_ids, const int32_t* toke
     cudaError_t e = pkv::launch_prefix_keys(token_ids, token_start_loc, extra,
                                             static_cast<const uint8_t*>(parent_keys), num_seqs, max_blocks,
                                             static_cast<uint8_t*>(keys), dev->err, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e);
+}
+
+PKV_API pkv_status pkv_swap_blocks(const pkv_cache_t* cache, int32_t direction, const int32_t* blocks,
+                                   const int32_t* slots, int32_t n, void* host, int64_t num_host_slots, void* stream) {
+    pkv_status st = check_cache(cache);
+    if (st != PKV_OK) return st;
+    if (direction != 0 && direction != 1) return PKV_ERR_SHAPE;
+    if (n < 0 || n > 65535 || num_host_slots < 0) return PKV_ERR_SHAPE;
+    if (n == 0) return PKV_OK;
+    if (blocks == nullptr || slots == nullptr || host == nullptr) return PKV_ERR_NULL;
+    if (!aligned16(host)) return PKV_ERR_ALIGN;
+    DeviceState* dev = nullptr;
+    if ((st = current_device(&dev)) != PKV_OK) return st;
+    // Only page-locked host memory mapped for this device is handed to the
+    // kernel, through the device pointer the runtime reports for it.
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, host) != cudaSuccess) {
+        cudaGetLastError();
+        return PKV_ERR_HOST_MEMORY;
+    }
+    if (attr.type != cudaMemoryTypeHost || attr.devicePointer == nullptr) return PKV_ERR_HOST_MEMORY;
+    cudaError_t e = pkv::launch_swap_blocks(direction, blocks, slots, n, attr.devicePointer, num_host_slots,
+                                            cache->k_pool, cache->v_pool, cache->num_blocks, cache->num_kv_heads,
+                                            cache->head_dim, dev->err, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PKV_OK : cuda_fail(e);
 }
 

@@ -84,7 +84,50 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(const int32_t* __restr
     }
 }
 
+// Grid: x = chunk groups, y = pair.  Pair i moves block blocks[i] of the
+// pool and slab slots[i] of the host buffer ([slots][2][Hkv][16][d] bf16:
+// the K block, then the V block) in the given direction.
+__global__ void __launch_bounds__(256) swap_blocks_kernel(int32_t direction, const int32_t* __restrict__ blocks,
+                                                          const int32_t* __restrict__ slots, int64_t block_chunks,
+                                                          int32_t num_blocks, int64_t num_slots,
+                                                          uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
+                                                          uint4* __restrict__ host, unsigned long long* err) {
+    griddep_launch_dependents();
+    griddep_wait();
+    const int32_t pair = blockIdx.y;
+    const int32_t b = __ldg(blocks + pair);
+    const int32_t h = __ldg(slots + pair);
+    if (b < 0) return;  // unused pair entry
+    if (b >= num_blocks || h < 0 || h >= num_slots) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) record_error(err, kErrRange, static_cast<uint32_t>(pair));
+        return;
+    }
+    uint4* kb = k_pool + static_cast<int64_t>(b) * block_chunks;
+    uint4* vb = v_pool + static_cast<int64_t>(b) * block_chunks;
+    uint4* slab = host + static_cast<int64_t>(h) * 2 * block_chunks;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < 2 * block_chunks;
+         i += stride) {
+        uint4* dev = i < block_chunks ? kb + i : vb + (i - block_chunks);
+        if (direction == 0) slab[i] = *dev;
+        else *dev = slab[i];
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_swap_blocks(int32_t direction, const int32_t* blocks, const int32_t* slots, int32_t n,
+                               void* host, int64_t num_slots, void* k_pool, void* v_pool, int32_t num_blocks,
+                               int32_t num_kv_heads, int32_t head_dim, unsigned long long* err, cudaStream_t stream) {
+    const int64_t block_chunks = static_cast<int64_t>(num_kv_heads) * kBlockSize * head_dim * 2 / 16;
+    const int threads = 256;
+    int64_t gx = (2 * block_chunks + threads - 1) / threads;
+    if (gx > 64) gx = 64;
+    dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(n));
+    return launch_overlapped(swap_blocks_kernel, grid, dim3(threads), 0, stream, direction, blocks, slots,
+                             block_chunks, num_blocks, num_slots, static_cast<uint4*>(k_pool),
+                             static_cast<uint4*>(v_pool), static_cast<uint4*>(host), err);
+}
 
 cudaError_t launch_cache_write(const void* k_new, const void* v_new, const int32_t* slot_mapping,
                                int32_t num_tokens, void* k_pool, void* v_pool, int32_t num_blocks,
