@@ -418,6 +418,9 @@ def block_manager_timing(w, pkv, torch, dev, stream, iters=200, warm=10):
     status = pkv.get_error(stream)
     if status[0] != 0:
         raise RuntimeError(f"device error in the block-manager timing: {status}")
+    expect = int(np.sum(prefix + ql * (warm + iters)))
+    if int(blocks.context_lens.sum().item()) != expect:
+        raise RuntimeError("the timed appends did not all take effect")
     us = e0.elapsed_time(e1) * 1e3 / iters
     return {"call": "pkv_blocks_append", "workload": f"{S} rows, {T} new tokens per call, "
             f"{int(prefix.sum())} tokens held at the start", "us_per_call": us, "rows_per_s": S / (us * 1e-6),
@@ -500,7 +503,7 @@ def prefix_cache_timing(w, pkv, torch, dev, stream):
     return {"calls": "pkv_blocks_register, pkv_blocks_match",
             "workload": f"{S} rows, {int(np.sum(lens // 16))} full blocks, all new (register) / all hits (match)",
             **times, "launches_per_call": 1,
-            "bound": "latency (one CTA; register inserts from one thread, in order)"}
+            "bound": "latency (one CTA per call)"}
 
 
 def swap_timing(w, pkv, torch, dev, stream, reps):
