@@ -13,7 +13,8 @@
 // free queue tail block first.
 //
 // The state is caller-owned device memory (pkv_blocks_t): tables, lengths,
-// reference counts and a FIFO ring of free block ids.  Keeping it on the
+// reference counts and a ring of free block ids, least recently freed
+// first (with the prefix cache: keys and a key table).  Keeping it on the
 // device lets one decode step (append -> copy-on-write copies -> cache write
 // -> attention) run without a host round trip, and be captured in a graph.
 //
@@ -24,7 +25,13 @@
 //    allocation takes blocks from the ring's head in sequence order, the
 //    copy-on-write block first, then new blocks in logical order;
 //  * release, in the given row order, each row's blocks last first: a block
-//    joins the ring's tail when its count reaches 0.
+//    joins the ring's tail when its count reaches 0, keeping its content and
+//    (if registered) its key;
+//  * match (prefix cache, section 4): an empty row takes the cached blocks of
+//    its leading keys up to the first key not cached, taking a free one back
+//    out of the queue; an append that takes a cached block drops its key;
+//  * register, in (row, block) order: a block keeps a key it has, and a key
+//    already cached (or given earlier in the call) keeps its first block.
 // The kernels reach the same result in parallel: per-block counters in a
 // scratch array (atomicAdd of holders, atomicMax of the last holder's
 // position) decide who copies or frees, and CTA-wide exclusive scans turn the
