@@ -172,9 +172,13 @@ size_t pkv_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t 
  *   max_context_len host-side upper bound of context_lens (sizes the split)
  *   out            fp32 [num_seqs][num_q_heads][head_dim]
  *   workspace      device buffer of >= pkv_decode_workspace_size() bytes,
- *                  256-byte aligned, ZERO-FILLED BEFORE ITS FIRST USE; every
- *                  call leaves it zeroed again.  Calls that run concurrently
- *                  need separate workspaces.
+ *                  256-byte aligned, ZERO-FILLED BEFORE ITS FIRST USE.  Its
+ *                  first part (a 256-byte header and one arrival counter per
+ *                  (sequence, kv head)) must be zero when a call starts, and
+ *                  every call leaves it zero again, so the same workspace
+ *                  serves the next call as is; the rest holds split-KV
+ *                  partial results and is scratch.  Calls that run
+ *                  concurrently need separate workspaces.
  *   partition_blocks 0 = automatic; > 0 forces the size of a work range in
  *                  units (the workspace must be sized with the same value).
  *   Work is the sequence of units (sequence, kv head, 16-token block) cut
@@ -214,7 +218,9 @@ size_t pkv_prefill_workspace_size(int32_t num_seqs, int32_t num_tokens, int32_t 
  *   context_lens          int32 [num_seqs], device, including this step's rows
  *   out                   fp32 [num_tokens][num_q_heads][head_dim]
  *   workspace             >= pkv_prefill_workspace_size() bytes, 256-byte
- *                         aligned, zero-filled before first use (left zeroed)
+ *                         aligned, zero-filled before first use; used as the
+ *                         decode workspace for the decode rows (its counters
+ *                         are left zero, so it is reused as is)
  *   Query rows are computed on tcgen05 tensor cores: Q.K^T in bf16, P.V in
  *   fp16 (P rounded to fp16, V converted from bf16 exactly for
  *   2^-14 <= |v| <= 65504); decode rows take the decode kernel.  A V entry
