@@ -37,9 +37,10 @@
  * KV is cut into fixed blocks of 16 tokens that may sit anywhere in the pool;
  * each sequence's block table maps its logical block i to a physical block.
  * K and V are separate pools, each
- *     bf16 [num_blocks][num_kv_heads][16][head_dim]
- * so the 16 rows of one (block, kv head) are one contiguous run of
- * 16*head_dim*2 bytes.  Token p of a sequence is row p % 16 of physical block
+ *     elem [num_blocks][num_kv_heads][16][head_dim]
+ * with elem bf16 (2 bytes) or an 8-bit e4m3 code (pkv_cache_t.kv_dtype), so
+ * the 16 rows of one (block, kv head) are one contiguous run of
+ * 16*head_dim*sizeof(elem) bytes.  Token p of a sequence is row p % 16 of physical block
  * block_table[p / 16].  A slot id is block * 16 + row.
  */
 #ifndef PKV_H
@@ -68,16 +69,33 @@ typedef enum pkv_status {
     PKV_ERR_UNSUPPORTED = 12, /* the current device is not compute capability 10.3          */
     PKV_ERR_SCRATCH_LIMIT = 13, /* the problem needs more than the built-in scratch buffer  */
     PKV_ERR_NO_BLOCKS = 14,  /* (device) the free queue cannot supply the blocks an append needs */
-    PKV_ERR_HOST_MEMORY = 15 /* a host buffer is not page-locked memory mapped for the device    */
+    PKV_ERR_HOST_MEMORY = 15, /* a host buffer is not page-locked memory mapped for the device   */
+    PKV_ERR_DTYPE = 16       /* kv_dtype unknown, e4m3 scales not finite and > 0, or the call
+                                does not take an e4m3 pool                                     */
 } pkv_status;
 
+/*
+ * Element type of the pools.  PKV_KV_E4M3 halves the bytes decode reads:
+ * each element is an 8-bit code of the OCP e4m3 format (sign, 4 exponent
+ * bits with bias 7, 3 mantissa bits; subnormals; largest finite 448; S.1111.111
+ * is NaN, no infinities), and stands for value(code) * scale, one scale per
+ * pool.  The pages have no fp8 pool: it is the bandwidth-halving variant of
+ * the write and the gather, chosen because decode reads the whole cache every
+ * step ([ENG] "Prefill/Decode").
+ */
+enum { PKV_KV_BF16 = 0, PKV_KV_E4M3 = 1 };
+
 typedef struct pkv_cache {
-    void* k_pool;         /* bf16 [num_blocks][num_kv_heads][16][head_dim], device        */
+    void* k_pool;         /* elem [num_blocks][num_kv_heads][16][head_dim], device        */
     void* v_pool;         /* same layout                                                  */
     int32_t num_blocks;   /* physical blocks in each pool, >= 0                           */
     int32_t num_kv_heads; /* >= 1                                                         */
     int32_t head_dim;     /* 64 or 128                                                    */
     int32_t block_size;   /* tokens per block; must be 16 ([KV2] section 2 default)       */
+    int32_t kv_dtype;     /* PKV_KV_BF16 (0, also what zero-initialisation gives) or
+                             PKV_KV_E4M3                                                   */
+    float k_scale;        /* e4m3 pools: K element = value(code) * k_scale; finite, > 0    */
+    float v_scale;        /* e4m3 pools: V element = value(code) * v_scale; ignored for bf16 */
 } pkv_cache_t;
 
 /*
@@ -92,6 +110,10 @@ typedef struct pkv_cache {
  *                 slot skips the row.  Slots within one call must be distinct.
  *   A slot >= num_blocks*16 is not written and raises PKV_ERR_RANGE on the
  *   device.  The copy is bit-exact.  num_tokens == 0 is a no-op.
+ *   e4m3 pools: each element x is stored as the code nearest to
+ *   x * (1/scale), where 1/scale is the fp32 reciprocal of the pool's scale
+ *   and the product is rounded to fp32 first; ties go to the even code and
+ *   values beyond 448 saturate to +-448 (a NaN gives a NaN code).
  */
 pkv_status pkv_cache_write(const pkv_cache_t* cache, const void* k_new, const void* v_new,
                            const int32_t* slot_mapping, int32_t num_tokens, void* stream);
@@ -131,7 +153,7 @@ pkv_status pkv_copy_blocks(const pkv_cache_t* cache, const int32_t* src, const i
  *   host           page-locked host memory mapped for the device
  *                  (cudaHostAlloc, or cudaHostRegister with the mapped flag),
  *                  16-byte aligned, holding num_host_slots slabs of
- *                  [2][num_kv_heads][16][head_dim] bf16 (the K block, then the
+ *                  [2][num_kv_heads][16][head_dim] pool elements (the K block, then the
  *                  V block); the kernel reads and writes it directly, over the
  *                  host link, bit-exact
  *   Returns PKV_ERR_HOST_MEMORY, launching nothing, when `host` is not such
@@ -186,6 +208,9 @@ size_t pkv_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t 
  *   blocks straddle ranges is computed as split-KV partitions whose partial
  *   results are merged with the log-sum-exp rule inside the same launch, in
  *   a fixed order (results are bitwise reproducible).
+ *   e4m3 pools: K_j and V_j are value(code) * k_scale and value(code) *
+ *   v_scale, exactly as pkv_cache_write defines them; the NaN codes, which
+ *   that call never stores for finite input, read as +-480.
  */
 pkv_status pkv_decode_attention(const pkv_cache_t* cache, const void* q, int32_t num_q_heads,
                                 const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* context_lens,
@@ -226,7 +251,7 @@ size_t pkv_prefill_workspace_size(int32_t num_seqs, int32_t num_tokens, int32_t 
  *   2^-14 <= |v| <= 65504); decode rows take the decode kernel.  A V entry
  *   of a visible key that fp16 cannot hold (|v| > 65504, inf or NaN) raises
  *   PKV_ERR_RANGE (detail: the sequence); the output of that call is then
- *   unspecified.
+ *   unspecified.  Takes bf16 pools only (an e4m3 pool: PKV_ERR_DTYPE).
  */
 pkv_status pkv_chunked_prefill_attention(const pkv_cache_t* cache, const void* q, int32_t num_q_heads,
                                          int32_t num_tokens, const int32_t* query_start_loc,

@@ -33,8 +33,9 @@ STATUS_NAMES = {
     0: "PKV_OK", 1: "PKV_ERR_NULL", 2: "PKV_ERR_SHAPE", 3: "PKV_ERR_HEADS", 4: "PKV_ERR_HEADDIM",
     5: "PKV_ERR_BLOCKSIZE", 6: "PKV_ERR_ALIAS", 7: "PKV_ERR_WORKSPACE", 8: "PKV_ERR_ALIGN", 9: "PKV_ERR_RANGE",
     10: "PKV_ERR_TIMEOUT", 11: "PKV_ERR_CUDA", 12: "PKV_ERR_UNSUPPORTED", 13: "PKV_ERR_SCRATCH_LIMIT",
-    14: "PKV_ERR_NO_BLOCKS", 15: "PKV_ERR_HOST_MEMORY",
+    14: "PKV_ERR_NO_BLOCKS", 15: "PKV_ERR_HOST_MEMORY", 16: "PKV_ERR_DTYPE",
 }
+PKV_KV_BF16, PKV_KV_E4M3 = 0, 1
 
 
 class PKVError(RuntimeError):
@@ -49,7 +50,8 @@ class PKVError(RuntimeError):
 class Cache(ctypes.Structure):
     """Mirror of ``pkv_cache_t``."""
     _fields_ = [("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p), ("num_blocks", ctypes.c_int32),
-                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32)]
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("kv_dtype", ctypes.c_int32), ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float)]
 
 
 class BlocksState(ctypes.Structure):
@@ -142,11 +144,20 @@ def _dev(t, name, elem_size=None, dtype=None):
     return ctypes.c_void_p(t.data_ptr())
 
 
-def _cache(k_pool, v_pool) -> Cache:
+def _cache(k_pool, v_pool, k_scale=None, v_scale=None, need_scales=False) -> Cache:
+    """Descriptor of a pool pair: 2-byte elements are bf16, 1-byte elements
+    (uint8 or float8_e4m3fn) e4m3 codes with one scale per pool."""
     if k_pool.shape != v_pool.shape or k_pool.dim() != 4:
         raise ValueError("k_pool and v_pool must both be [num_blocks][num_kv_heads][16][head_dim]")
     nb, hkv, bs, d = k_pool.shape
-    return Cache(_dev(k_pool, "k_pool", 2).value, _dev(v_pool, "v_pool", 2).value, nb, hkv, d, bs)
+    es = k_pool.element_size()
+    if es not in (1, 2):
+        raise TypeError("pools must have 2-byte (bf16) or 1-byte (e4m3) elements")
+    if es == 1 and need_scales and (k_scale is None or v_scale is None):
+        raise ValueError("an e4m3 pool needs k_scale and v_scale")
+    return Cache(_dev(k_pool, "k_pool", es).value, _dev(v_pool, "v_pool", es).value, nb, hkv, d, bs,
+                 PKV_KV_E4M3 if es == 1 else PKV_KV_BF16,
+                 1.0 if k_scale is None else float(k_scale), 1.0 if v_scale is None else float(v_scale))
 
 
 def _check(status, what):
@@ -162,11 +173,12 @@ def _host_i32(x):
 
 # ---------------------------------------------------------------- calls
 
-def cache_write(k_pool, v_pool, k_new, v_new, slot_mapping, stream=None) -> None:
-    """Store rows k_new/v_new [T][Hkv][d] at ``slot_mapping`` [T] (negative = skip)."""
+def cache_write(k_pool, v_pool, k_new, v_new, slot_mapping, stream=None, k_scale=None, v_scale=None) -> None:
+    """Store rows k_new/v_new [T][Hkv][d] at ``slot_mapping`` [T] (negative = skip).
+    e4m3 pools (1-byte elements) store code(x * (1/scale)) and need the scales."""
     torch = _torch()
     lib = load()
-    c = _cache(k_pool, v_pool)
+    c = _cache(k_pool, v_pool, k_scale, v_scale, need_scales=True)
     T = int(slot_mapping.shape[0])
     if k_new.shape != (T, c.num_kv_heads, c.head_dim) or v_new.shape != k_new.shape:
         raise ValueError("k_new/v_new must be [num_tokens][num_kv_heads][head_dim]")
@@ -221,11 +233,13 @@ def new_workspace(nbytes: int, device=None):
 
 
 def decode_attention(k_pool, v_pool, q, block_tables, context_lens, max_context_len: int, scale: float,
-                     out=None, workspace=None, partition_blocks: int = 0, stream=None):
-    """Paged decode attention; returns ``out`` float32 [B][Hq][d]."""
+                     out=None, workspace=None, partition_blocks: int = 0, stream=None, k_scale=None,
+                     v_scale=None):
+    """Paged decode attention; returns ``out`` float32 [B][Hq][d].  e4m3 pools
+    (1-byte elements) need the scales they were written with."""
     torch = _torch()
     lib = load()
-    c = _cache(k_pool, v_pool)
+    c = _cache(k_pool, v_pool, k_scale, v_scale, need_scales=True)
     B, hq, d = q.shape
     if d != c.head_dim:
         raise ValueError("q head_dim does not match the pools")
@@ -294,9 +308,9 @@ def _swap(direction, k_pool, v_pool, blocks, slots, host, stream):
         raise ValueError("blocks and slots must have the same length")
     if not isinstance(host, torch.Tensor) or host.is_cuda or not host.is_contiguous():
         raise ValueError("host must be a contiguous CPU tensor in page-locked memory")
-    slab = 2 * c.num_kv_heads * 16 * c.head_dim * 2
+    slab = 2 * c.num_kv_heads * 16 * c.head_dim * k_pool.element_size()
     if host.numel() * host.element_size() % slab:
-        raise ValueError("host must hold whole slabs of [2][num_kv_heads][16][head_dim] bf16")
+        raise ValueError("host must hold whole slabs of [2][num_kv_heads][16][head_dim] pool elements")
     num_slots = host.numel() * host.element_size() // slab
     st = lib.pkv_swap_blocks(ctypes.byref(c), int(direction), _dev(blocks, "blocks", dtype=torch.int32),
                              _dev(slots, "slots", dtype=torch.int32), n, ctypes.c_void_p(host.data_ptr()),
@@ -306,7 +320,7 @@ def _swap(direction, k_pool, v_pool, blocks, slots, host, stream):
 
 def swap_out(k_pool, v_pool, blocks, slots, host, stream=None) -> None:
     """host slab slots[i] <- pool block blocks[i] (K then V); ``host`` is a
-    pinned CPU tensor of whole [2][Hkv][16][d] bf16 slabs."""
+    pinned CPU tensor of whole [2][Hkv][16][d] slabs of the pools' elements."""
     _swap(0, k_pool, v_pool, blocks, slots, host, stream)
 
 

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
@@ -86,8 +87,16 @@ pkv_status check_cache(const pkv_cache_t* c) {
     if (c->num_blocks < 0 || c->num_kv_heads < 1) return PKV_ERR_SHAPE;
     if (c->head_dim != 64 && c->head_dim != 128) return PKV_ERR_HEADDIM;
     if (!aligned16(c->k_pool) || !aligned16(c->v_pool)) return PKV_ERR_ALIGN;
+    if (c->kv_dtype != PKV_KV_BF16 && c->kv_dtype != PKV_KV_E4M3) return PKV_ERR_DTYPE;
+    if (c->kv_dtype == PKV_KV_E4M3) {
+        // 1/scale must be a finite fp32 too.
+        for (float x : {c->k_scale, c->v_scale})
+            if (!(std::isfinite(x) && x > 0.f && std::isfinite(1.f / x))) return PKV_ERR_DTYPE;
+    }
     return PKV_OK;
 }
+
+int32_t elem_bytes(const pkv_cache_t* c) { return c->kv_dtype == PKV_KV_E4M3 ? 1 : 2; }
 
 pkv_status check_heads(int32_t hq, int32_t hkv) {
     if (hq < 1 || hkv < 1 || hq % hkv != 0) return PKV_ERR_HEADS;
@@ -130,6 +139,8 @@ PKV_API const char* pkv_status_string(pkv_status s) {
             return "PKV_ERR_SCRATCH_LIMIT: the batch needs more workspace than the built-in 4 MiB scratch buffer";
         case PKV_ERR_NO_BLOCKS: return "PKV_ERR_NO_BLOCKS: the free queue holds fewer blocks than the append needs";
         case PKV_ERR_HOST_MEMORY: return "PKV_ERR_HOST_MEMORY: the host buffer is not page-locked memory mapped for the device";
+        case PKV_ERR_DTYPE:
+            return "PKV_ERR_DTYPE: unknown kv_dtype, e4m3 scales not finite and positive, or a call without e4m3 support";
     }
     return "unknown pkv_status";
 }
@@ -144,9 +155,15 @@ PKV_API pkv_status pkv_cache_write(const pkv_cache_t* cache, const void* k_new, 
     if (!aligned16(k_new) || !aligned16(v_new)) return PKV_ERR_ALIGN;
     DeviceState* dev = nullptr;
     if ((st = current_device(&dev)) != PKV_OK) return st;
-    cudaError_t e = pkv::launch_cache_write(k_new, v_new, slot_mapping, num_tokens, cache->k_pool, cache->v_pool,
-                                            cache->num_blocks, cache->num_kv_heads, cache->head_dim, dev->err,
-                                            static_cast<cudaStream_t>(stream));
+    cudaError_t e =
+        cache->kv_dtype == PKV_KV_E4M3
+            ? pkv::launch_cache_write_e4m3(k_new, v_new, slot_mapping, num_tokens, cache->k_pool, cache->v_pool,
+                                           cache->num_blocks, cache->num_kv_heads, cache->head_dim,
+                                           1.f / cache->k_scale, 1.f / cache->v_scale, dev->err,
+                                           static_cast<cudaStream_t>(stream))
+            : pkv::launch_cache_write(k_new, v_new, slot_mapping, num_tokens, cache->k_pool, cache->v_pool,
+                                      cache->num_blocks, cache->num_kv_heads, cache->head_dim, dev->err,
+                                      static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PKV_OK : cuda_fail(e);
 }
 
@@ -178,8 +195,8 @@ PKV_API pkv_status pkv_copy_blocks(const pkv_cache_t* cache, const int32_t* src,
     for (int32_t base = 0; base < num_pairs; base += 65535) {
         const int32_t n = std::min<int32_t>(65535, num_pairs - base);
         cudaError_t e = pkv::launch_copy_blocks(src + base, dst + base, n, cache->k_pool, cache->v_pool,
-                                                cache->num_blocks, cache->num_kv_heads, cache->head_dim, dev->err,
-                                                static_cast<cudaStream_t>(stream));
+                                                cache->num_blocks, cache->num_kv_heads, cache->head_dim,
+                                                elem_bytes(cache), dev->err, static_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) return cuda_fail(e);
     }
     return PKV_OK;
@@ -338,7 +355,8 @@ PKV_API pkv_status pkv_swap_blocks(const pkv_cache_t* cache, int32_t direction, 
     if (attr.type != cudaMemoryTypeHost || attr.devicePointer == nullptr) return PKV_ERR_HOST_MEMORY;
     cudaError_t e = pkv::launch_swap_blocks(direction, blocks, slots, n, attr.devicePointer, num_host_slots,
                                             cache->k_pool, cache->v_pool, cache->num_blocks, cache->num_kv_heads,
-                                            cache->head_dim, dev->err, static_cast<cudaStream_t>(stream));
+                                            cache->head_dim, elem_bytes(cache), dev->err,
+                                            static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PKV_OK : cuda_fail(e);
 }
 
@@ -399,6 +417,9 @@ pkv_status decode_common(const pkv_cache_t* cache, const void* q, int32_t num_q_
     a.max_context_len = max_context_len;
     a.plan = plan;
     a.scale = scale;
+    a.kv_e4m3 = cache->kv_dtype == PKV_KV_E4M3;
+    a.k_scale = cache->k_scale;
+    a.v_scale = cache->v_scale;
     cudaError_t e = pkv::launch_decode(a, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PKV_OK : cuda_fail(e);
 }
@@ -429,6 +450,7 @@ PKV_API pkv_status pkv_chunked_prefill_attention(const pkv_cache_t* cache, const
                                                  void* stream) {
     pkv_status st = check_cache(cache);
     if (st != PKV_OK) return st;
+    if (cache->kv_dtype != PKV_KV_BF16) return PKV_ERR_DTYPE;  // the tcgen05 tiles read bf16 K/V
     if ((st = check_heads(num_q_heads, cache->num_kv_heads)) != PKV_OK) return st;
     if (num_seqs < 0 || num_tokens < 0 || max_blocks_per_seq < 0 || max_context_len < 0) return PKV_ERR_SHAPE;
     if (num_seqs == 0 || num_tokens == 0) return PKV_OK;

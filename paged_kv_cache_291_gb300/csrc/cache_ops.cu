@@ -11,6 +11,12 @@
 // Both are pure byte movement: 16-byte vector loads and stores, coalesced
 // along head_dim, bit-exact.  Both wait for the previous kernel on the
 // stream before their first access (overlapped launch, pkv_device.cuh).
+//
+//  cache_write_e4m3: the write into a pool of 8-bit e4m3 codes (the OCP
+//  format: 4 exponent bits with bias 7, 3 mantissa bits, largest finite
+//  448).  Each bf16 element is multiplied by the pool's fp32 inverse scale
+//  (one rounding) and converted to the nearest code, ties to even, values
+//  beyond 448 saturating to +-448 (cvt.rn.satfinite).
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -53,8 +59,54 @@ __global__ void __launch_bounds__(256) cache_write_kernel(const uint4* __restric
     v_pool[dst] = vv;
 }
 
+// Two fp32 -> two e4m3 codes, lo in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Eight bf16 (one uint4) times inv -> eight codes (one uint2).
+__device__ __forceinline__ uint2 quantise8(uint4 x, float inv) {
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t c[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float lo = __fmul_rn(__uint_as_float(w[i] << 16), inv);
+        const float hi = __fmul_rn(__uint_as_float(w[i] & 0xffff0000u), inv);
+        c[i] = e4m3x2(lo, hi);
+    }
+    return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+}
+
+// One thread per 8 elements of one (token, kv head) row, K and V.
+__global__ void __launch_bounds__(256) cache_write_e4m3_kernel(
+    const uint4* __restrict__ k_new, const uint4* __restrict__ v_new, const int32_t* __restrict__ slot_mapping,
+    int64_t total, int32_t chunks_per_row, int32_t num_kv_heads, int64_t num_slots, float k_inv, float v_inv,
+    uint2* __restrict__ k_pool, uint2* __restrict__ v_pool, unsigned long long* err) {
+    griddep_launch_dependents();
+    griddep_wait();
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= total) return;
+    const int64_t row = i / chunks_per_row;
+    const int32_t c = static_cast<int32_t>(i - row * chunks_per_row);
+    const int64_t t = row / num_kv_heads;
+    const int32_t h = static_cast<int32_t>(row - t * num_kv_heads);
+    const int64_t slot = __ldg(slot_mapping + t);
+    if (slot < 0) return;
+    if (slot >= num_slots) {
+        if (h == 0 && c == 0) record_error(err, kErrRange, static_cast<uint32_t>(t));
+        return;
+    }
+    const int64_t block = slot / kBlockSize;
+    const int64_t off = slot - block * kBlockSize;
+    const int64_t dst = ((block * num_kv_heads + h) * kBlockSize + off) * chunks_per_row + c;
+    k_pool[dst] = quantise8(__ldg(k_new + i), k_inv);
+    v_pool[dst] = quantise8(__ldg(v_new + i), v_inv);
+}
+
 // Grid: x = chunk groups, y = pair.  Each pair copies the K slab then the V
-// slab of one block ([Hkv][16][d] bf16 each).
+// slab of one block ([Hkv][16][d] elements each).
 __global__ void __launch_bounds__(256) copy_blocks_kernel(const int32_t* __restrict__ src,
                                                           const int32_t* __restrict__ dst, int64_t block_chunks,
                                                           int32_t num_blocks, uint4* __restrict__ k_pool,
@@ -85,8 +137,8 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(const int32_t* __restr
 }
 
 // Grid: x = chunk groups, y = pair.  Pair i moves block blocks[i] of the
-// pool and slab slots[i] of the host buffer ([slots][2][Hkv][16][d] bf16:
-// the K block, then the V block) in the given direction.
+// pool and slab slots[i] of the host buffer ([slots][2][Hkv][16][d] pool
+// elements: the K block, then the V block) in the given direction.
 __global__ void __launch_bounds__(256) swap_blocks_kernel(int32_t direction, const int32_t* __restrict__ blocks,
                                                           const int32_t* __restrict__ slots, int64_t block_chunks,
                                                           int32_t num_blocks, int64_t num_slots,
@@ -118,8 +170,9 @@ __global__ void __launch_bounds__(256) swap_blocks_kernel(int32_t direction, con
 
 cudaError_t launch_swap_blocks(int32_t direction, const int32_t* blocks, const int32_t* slots, int32_t n,
                                void* host, int64_t num_slots, void* k_pool, void* v_pool, int32_t num_blocks,
-                               int32_t num_kv_heads, int32_t head_dim, unsigned long long* err, cudaStream_t stream) {
-    const int64_t block_chunks = static_cast<int64_t>(num_kv_heads) * kBlockSize * head_dim * 2 / 16;
+                               int32_t num_kv_heads, int32_t head_dim, int32_t elem_bytes, unsigned long long* err,
+                               cudaStream_t stream) {
+    const int64_t block_chunks = static_cast<int64_t>(num_kv_heads) * kBlockSize * head_dim * elem_bytes / 16;
     const int threads = 256;
     int64_t gx = (2 * block_chunks + threads - 1) / threads;
     if (gx > 64) gx = 64;
@@ -144,11 +197,26 @@ cudaError_t launch_cache_write(const void* k_new, const void* v_new, const int32
                              static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), err);
 }
 
+cudaError_t launch_cache_write_e4m3(const void* k_new, const void* v_new, const int32_t* slot_mapping,
+                                    int32_t num_tokens, void* k_pool, void* v_pool, int32_t num_blocks,
+                                    int32_t num_kv_heads, int32_t head_dim, float k_inv_scale, float v_inv_scale,
+                                    unsigned long long* err, cudaStream_t stream) {
+    if (num_tokens == 0) return cudaSuccess;
+    const int32_t chunks = head_dim / 8;
+    const int64_t total = static_cast<int64_t>(num_tokens) * num_kv_heads * chunks;
+    const int threads = 256;
+    const int64_t blocks = (total + threads - 1) / threads;
+    return launch_overlapped(cache_write_e4m3_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, stream,
+                             static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slot_mapping, total,
+                             chunks, num_kv_heads, static_cast<int64_t>(num_blocks) * kBlockSize, k_inv_scale,
+                             v_inv_scale, static_cast<uint2*>(k_pool), static_cast<uint2*>(v_pool), err);
+}
+
 cudaError_t launch_copy_blocks(const int32_t* src, const int32_t* dst, int32_t num_pairs, void* k_pool,
                                void* v_pool, int32_t num_blocks, int32_t num_kv_heads, int32_t head_dim,
-                               unsigned long long* err, cudaStream_t stream) {
+                               int32_t elem_bytes, unsigned long long* err, cudaStream_t stream) {
     if (num_pairs == 0) return cudaSuccess;
-    const int64_t block_chunks = static_cast<int64_t>(num_kv_heads) * kBlockSize * head_dim * 2 / 16;
+    const int64_t block_chunks = static_cast<int64_t>(num_kv_heads) * kBlockSize * head_dim * elem_bytes / 16;
     const int threads = 256;
     int64_t gx = (2 * block_chunks + threads - 1) / threads;
     if (gx > 64) gx = 64;

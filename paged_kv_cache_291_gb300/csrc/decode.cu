@@ -40,6 +40,13 @@
 //    Until that kernel has finished, the CTA only prefetches context_lens,
 //    the block tables and q into L2, so its first reads after the wait hit
 //    L2.
+//  * e4m3 pools (one byte per element, the same layout and the same
+//    kernel with half the bytes per slab): a lane loads its 8 dims with one
+//    8-byte shared load and turns each code into an fp32 with integer ops
+//    only -- sign to bit 31, the 7 magnitude bits to bits 20..26 -- which is
+//    the code's value times 2^-120 exactly, subnormal codes included.  The
+//    2^-120 and the K scale fold into q and the row sum; for V they fold
+//    into the final 1/l, so no per-element multiply is added.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -97,12 +104,13 @@ struct DecodeParams {
     int32_t num_blocks, hkv, hq, num_seqs, max_blocks, ctx_cap;
     int32_t range_units;  // units per range, 0 = automatic
     int32_t max_ranges;   // ranges the workspace holds
-    float scale_log2;
+    float scale_log2;     // softmax scale * log2(e); e4m3 pools: also * k_scale * 2^64
+    float v_scale;        // e4m3 pools: the V pool's scale
 };
 
 constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
-template <int D, int G>
+template <int D, int G, int EB>
 struct Cfg {
     static constexpr int W = consumer_warps<G>();     // consumer warps
     static_assert(W >= 1 && W <= 16, "consumer warps");
@@ -116,7 +124,7 @@ struct Cfg {
     static constexpr int LPR = D / 8;                  // lanes per K/V row, 8 dims (16 B) each
     static constexpr int RPP = 32 / LPR;               // rows per warp pass
     static constexpr int NV = kBlockSize / RPP;        // rows per lane per block
-    static constexpr int SLAB = kBlockSize * D * 2;    // bytes of one (block, kv head)
+    static constexpr int SLAB = kBlockSize * D * EB;   // bytes of one (block, kv head); EB = 2 (bf16) or 1 (e4m3)
     static constexpr int STAGE_BYTES = 2 * SLAB;       // K slab then V slab
     static constexpr int QBYTES = G * D * 2;
     static constexpr int HG = G < 4 ? G : 4;           // heads per pass over K
@@ -133,7 +141,8 @@ struct Cfg {
     // order (an mbarrier parity wait is only exact when the waiter is at
     // most one phase ahead of the barrier).
     static constexpr int SW_FIT = STAGES_FIT / W;
-    static constexpr int SW = SW_FIT < 6 ? SW_FIT : 6;
+    static constexpr int SW_CAP = EB == 2 ? 6 : 12;    // the same bytes in flight for either element
+    static constexpr int SW = SW_FIT < SW_CAP ? SW_FIT : SW_CAP;
     static constexpr int STAGES = SW * W;
     static constexpr int NBAR = 2 * STAGES + 2 * kItemRing + 2 * MERGE_BUFS;
     static constexpr int OFF_REST = STAGES * STAGE_BYTES;
@@ -215,15 +224,47 @@ __device__ __forceinline__ uint4 lds128(const void* p) {
 
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t u) { return make_float2(bf16lo(u), bf16hi(u)); }
 
+__device__ __forceinline__ uint2 lds64(const void* p) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(smem_addr(p)));
+    return v;
+}
+
+// Four e4m3 codes (bytes of w, lowest first) -> their values times 2^-120:
+// a code's sign and 7 magnitude bits placed at fp32 bits 31 and 20..26 make
+// the exponent field the e4m3 exponent, so the fp32 value is the e4m3 value
+// scaled by 2^(7-127); e4m3 subnormals land on fp32 subnormals, so the map
+// is exact (the NaN codes read as 480 * 2^-120).
+__device__ __forceinline__ void e4m3x4_scaled(uint32_t w, float2& a, float2& b) {
+    a = make_float2(__uint_as_float(((w << 24) & 0x80000000u) | ((w << 20) & 0x07f00000u)),
+                    __uint_as_float(((w << 16) & 0x80000000u) | ((w << 12) & 0x07f00000u)));
+    b = make_float2(__uint_as_float(((w << 8) & 0x80000000u) | ((w << 4) & 0x07f00000u)),
+                    __uint_as_float((w & 0x80000000u) | ((w >> 4) & 0x07f00000u)));
+}
+
+// o / l of one output chunk.  An e4m3 pool's o is in units of 2^-120 V
+// codes; o / l is a weighted mean of those (at most 480 * 2^-120), so
+// scaling it by 2^120 / l first and then by v_scale cannot overflow unless
+// the output itself does.  (l >= 1: the reference m never exceeds a score.)
+template <int EB>
+__device__ __forceinline__ float4 normalise(float4 a, float l, float v_scale) {
+    if constexpr (EB == 2) {
+        return make_float4(a.x / l, a.y / l, a.z / l, a.w / l);
+    } else {
+        const float f = 0x1p120f / l;
+        return make_float4(a.x * f * v_scale, a.y * f * v_scale, a.z * f * v_scale, a.w * f * v_scale);
+    }
+}
+
 // One 16-row block for one warp.  Lane (sub, cl) owns dims 8cl..8cl+7 of
 // rows i*RPP + sub.  q.K partial dots use packed fp32x2 FMAs; the row sums
 // come from a transpose-reduce over the LPR lanes of a row; P.V accumulates
 // with packed fp32x2 FMAs.  Rows >= valid are never loaded.
-template <int D, int G>
+template <int D, int G, int EB>
 __device__ __forceinline__ void compute_block(const uint8_t* kst, const uint8_t* vst, int valid,
                                               const float2 (&q2)[G][4], float (&m)[G], float (&lsum)[G],
                                               float2 (&o2)[G][4], float2* psm, int lane) {
-    using C = Cfg<D, G>;
+    using C = Cfg<D, G, EB>;
     const int sub = lane / C::LPR;
     const int cl = lane % C::LPR;
     const int myrow = ((lane >> 1) & (C::NV - 1)) * C::RPP + sub;
@@ -233,10 +274,18 @@ __device__ __forceinline__ void compute_block(const uint8_t* kst, const uint8_t*
 #pragma unroll
         for (int i = 0; i < C::NV; ++i) {
             const int row = i * C::RPP + sub;
-            uint4 u = make_uint4(0u, 0u, 0u, 0u);
-            if (row < valid) u = lds128(kst + row * D * 2 + cl * 16);
-            const float2 k0 = bf16x2_to_float2(u.x), k1 = bf16x2_to_float2(u.y);
-            const float2 k2 = bf16x2_to_float2(u.z), k3 = bf16x2_to_float2(u.w);
+            float2 k0, k1, k2, k3;
+            if constexpr (EB == 2) {
+                uint4 u = make_uint4(0u, 0u, 0u, 0u);
+                if (row < valid) u = lds128(kst + row * D * 2 + cl * 16);
+                k0 = bf16x2_to_float2(u.x), k1 = bf16x2_to_float2(u.y);
+                k2 = bf16x2_to_float2(u.z), k3 = bf16x2_to_float2(u.w);
+            } else {  // e4m3 values * 2^-120; q carries k_scale * 2^64, the row sum gets 2^56
+                uint2 u = make_uint2(0u, 0u);
+                if (row < valid) u = lds64(kst + row * D + cl * 8);
+                e4m3x4_scaled(u.x, k0, k1);
+                e4m3x4_scaled(u.y, k2, k3);
+            }
 #pragma unroll
             for (int g = 0; g < C::HG; ++g) {
                 float2 a = __fmul2_rn(q2[g0 + g][0], k0);
@@ -249,6 +298,7 @@ __device__ __forceinline__ void compute_block(const uint8_t* kst, const uint8_t*
 #pragma unroll
         for (int g = 0; g < C::HG; ++g) {
             float sc = transpose_reduce<C::NV, C::LPR>(acc[g], lane);
+            if constexpr (EB == 1) sc *= 0x1p56f;
             sc = (myrow < valid) ? sc : -INFINITY;
             const float mb = warp_max_redux(sc);
             // The reference m moves only when a block's maximum exceeds it by
@@ -273,9 +323,16 @@ __device__ __forceinline__ void compute_block(const uint8_t* kst, const uint8_t*
     for (int i = 0; i < C::NV; ++i) {
         const int row = i * C::RPP + sub;
         if (row < valid) {
-            const uint4 u = lds128(vst + row * D * 2 + cl * 16);
-            const float2 v0 = bf16x2_to_float2(u.x), v1 = bf16x2_to_float2(u.y);
-            const float2 v2 = bf16x2_to_float2(u.z), v3 = bf16x2_to_float2(u.w);
+            float2 v0, v1, v2, v3;
+            if constexpr (EB == 2) {
+                const uint4 u = lds128(vst + row * D * 2 + cl * 16);
+                v0 = bf16x2_to_float2(u.x), v1 = bf16x2_to_float2(u.y);
+                v2 = bf16x2_to_float2(u.z), v3 = bf16x2_to_float2(u.w);
+            } else {  // e4m3 values * 2^-120: 2^120 * v_scale is applied with 1/l at the end
+                const uint2 u = lds64(vst + row * D + cl * 8);
+                e4m3x4_scaled(u.x, v0, v1);
+                e4m3x4_scaled(u.y, v2, v3);
+            }
             // p of this row for every head: psm is [row][head] (p, p) pairs,
             // read two heads per 16-byte load.
             float2 pr[G];
@@ -302,10 +359,10 @@ __device__ __forceinline__ void compute_block(const uint8_t* kst, const uint8_t*
     __syncwarp();
 }
 
-template <int D, int G>
+template <int D, int G, int EB>
 __device__ void run_producer(const DecodeParams& P, uint8_t* smem, const Bars& B, volatile int* abort_flag,
                              int lane) {
-    using C = Cfg<D, G>;
+    using C = Cfg<D, G, EB>;
     ItemDesc* descs = reinterpret_cast<ItemDesc*>(smem + C::OFF_DESC);
     const unsigned FULL = 0xffffffffu;
     // Work is the sequence of units (s, kv head, block), sequences in order,
@@ -562,10 +619,10 @@ __device__ void run_producer(const DecodeParams& P, uint8_t* smem, const Bars& B
     }
 }
 
-template <int D, int G>
+template <int D, int G, int EB>
 __device__ void run_consumer(const DecodeParams& P, uint8_t* smem, const Bars& B, volatile int* abort_flag,
                              int warp, int lane) {
-    using C = Cfg<D, G>;
+    using C = Cfg<D, G, EB>;
     const ItemDesc* descs = reinterpret_cast<const ItemDesc*>(smem + C::OFF_DESC);
     float2* psm = reinterpret_cast<float2*>(smem + C::OFF_P) + warp * G * kBlockSize;
     float* mo = reinterpret_cast<float*>(smem + C::OFF_MO);
@@ -619,7 +676,7 @@ __device__ void run_consumer(const DecodeParams& P, uint8_t* smem, const Bars& B
             const int blk = d.b0 + b;
             const int valid = min(kBlockSize, d.n - blk * kBlockSize);
             const uint8_t* kst = smem + st * C::STAGE_BYTES;
-            compute_block<D, G>(kst, kst + C::SLAB, valid, q2, m, lsum, o2, psm, lane);
+            compute_block<D, G, EB>(kst, kst + C::SLAB, valid, q2, m, lsum, o2, psm, lane);
             if (lane == 0) mbar_arrive(&B.empty[st]);
             ++taken;
         }
@@ -659,9 +716,9 @@ __device__ void run_consumer(const DecodeParams& P, uint8_t* smem, const Bars& B
     }
 }
 
-template <int D, int G>
+template <int D, int G, int EB>
 __device__ void run_merger(const DecodeParams& P, uint8_t* smem, const Bars& B, volatile int* abort_flag, int lane) {
-    using C = Cfg<D, G>;
+    using C = Cfg<D, G, EB>;
     const ItemDesc* descs = reinterpret_cast<const ItemDesc*>(smem + C::OFF_DESC);
     const float* mo = reinterpret_cast<const float*>(smem + C::OFF_MO);
     const float2* ml = reinterpret_cast<const float2*>(smem + C::OFF_ML);
@@ -737,7 +794,7 @@ __device__ void run_merger(const DecodeParams& P, uint8_t* smem, const Bars& B, 
                 }
                 if (d.nparts == 1) {
                     const float L = msm[g].y;
-                    a = (L > 0.f) ? make_float4(a.x / L, a.y / L, a.z / L, a.w / L) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    a = (L > 0.f) ? normalise<EB>(a, L, P.v_scale) : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
                 dst[k] = a;
             }
@@ -826,8 +883,7 @@ __device__ void run_merger(const DecodeParams& P, uint8_t* smem, const Bars& B, 
                     const int c = lane + 32 * j;
                     if (c < CH) {
                         const float Lg = pick(L, c / (D / 4));
-                        out4[c] = (Lg > 0.f) ? make_float4(acc[j].x / Lg, acc[j].y / Lg, acc[j].z / Lg, acc[j].w / Lg)
-                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+                        out4[c] = (Lg > 0.f) ? normalise<EB>(acc[j], Lg, P.v_scale) : make_float4(0.f, 0.f, 0.f, 0.f);
                     }
                 }
                 if (lane == 0) atomicExch(ctr, 0u);
@@ -887,9 +943,9 @@ __device__ void prefetch_inputs(const DecodeParams& P, int t, int nthr) {
 // the guess.
 constexpr int kSpecWindows = 8;
 
-template <int D, int G>
+template <int D, int G, int EB>
 __device__ void prefetch_first_blocks(const DecodeParams& P, int lane, int max_units) {
-    using C = Cfg<D, G>;
+    using C = Cfg<D, G, EB>;
     const unsigned FULL = 0xffffffffu;
     if (P.num_seqs > kSpecWindows * 32) return;
     int u[kSpecWindows], incl[kSpecWindows];
@@ -947,9 +1003,9 @@ __device__ void prefetch_first_blocks(const DecodeParams& P, int lane, int max_u
     }
 }
 
-template <int D, int G>
-__global__ void __launch_bounds__(Cfg<D, G>::THREADS, 1) decode_kernel(const DecodeParams P) {
-    using C = Cfg<D, G>;
+template <int D, int G, int EB>
+__global__ void __launch_bounds__(Cfg<D, G, EB>::THREADS, 1) decode_kernel(const DecodeParams P) {
+    using C = Cfg<D, G, EB>;
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     Bars B;
@@ -984,39 +1040,39 @@ __global__ void __launch_bounds__(Cfg<D, G>::THREADS, 1) decode_kernel(const Dec
     // Consumer warps read shared memory only and need no wait.
     if (warp == C::PRODUCER_WARP) {
         griddep_wait();
-        run_producer<D, G>(P, smem, B, abort_flag, lane);
+        run_producer<D, G, EB>(P, smem, B, abort_flag, lane);
     } else if (warp == C::MERGER_WARP) {
-        prefetch_first_blocks<D, G>(P, lane, C::STAGES);
+        prefetch_first_blocks<D, G, EB>(P, lane, C::STAGES);
         griddep_wait();
-        run_merger<D, G>(P, smem, B, abort_flag, lane);
+        run_merger<D, G, EB>(P, smem, B, abort_flag, lane);
     } else {
         prefetch_inputs<D>(P, threadIdx.x, C::W * 32);
-        run_consumer<D, G>(P, smem, B, abort_flag, warp, lane);
+        run_consumer<D, G, EB>(P, smem, B, abort_flag, warp, lane);
     }
 }
 
-template <int D, int G>
+template <int D, int G, int EB>
 cudaError_t launch_one(const DecodeParams& P, int grid, cudaStream_t stream) {
-    using C = Cfg<D, G>;
+    using C = Cfg<D, G, EB>;
     static bool configured[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, G, EB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::SMEM);
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    return launch_overlapped(decode_kernel<D, G>, dim3(grid), dim3(C::THREADS), C::SMEM, stream, P);
+    return launch_overlapped(decode_kernel<D, G, EB>, dim3(grid), dim3(C::THREADS), C::SMEM, stream, P);
 }
 
-template <int D>
+template <int D, int EB>
 cudaError_t dispatch_g(const DecodeParams& P, int G, int grid, cudaStream_t stream) {
     switch (G) {
-        case 1: return launch_one<D, 1>(P, grid, stream);
-        case 2: return launch_one<D, 2>(P, grid, stream);
-        case 4: return launch_one<D, 4>(P, grid, stream);
-        case 8: return launch_one<D, 8>(P, grid, stream);
+        case 1: return launch_one<D, 1, EB>(P, grid, stream);
+        case 2: return launch_one<D, 2, EB>(P, grid, stream);
+        case 4: return launch_one<D, 4, EB>(P, grid, stream);
+        case 8: return launch_one<D, 8, EB>(P, grid, stream);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -1085,9 +1141,18 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     P.range_units = a.plan.range_units;
     P.max_ranges = a.plan.max_ranges;
     P.scale_log2 = a.scale * kLog2e;
+    P.v_scale = 1.f;
     const int G = a.num_q_heads / a.num_kv_heads;
-    if (a.head_dim == 128) return dispatch_g<128>(P, G, a.plan.grid, stream);
-    if (a.head_dim == 64) return dispatch_g<64>(P, G, a.plan.grid, stream);
+    if (a.kv_e4m3) {
+        // q' = q * scale*log2(e) * k_scale * 2^64 against K codes * 2^-120.
+        P.scale_log2 = a.scale * kLog2e * a.k_scale * 0x1p64f;
+        P.v_scale = a.v_scale;
+        if (a.head_dim == 128) return dispatch_g<128, 1>(P, G, a.plan.grid, stream);
+        if (a.head_dim == 64) return dispatch_g<64, 1>(P, G, a.plan.grid, stream);
+        return cudaErrorInvalidValue;
+    }
+    if (a.head_dim == 128) return dispatch_g<128, 2>(P, G, a.plan.grid, stream);
+    if (a.head_dim == 64) return dispatch_g<64, 2>(P, G, a.plan.grid, stream);
     return cudaErrorInvalidValue;
 }
 

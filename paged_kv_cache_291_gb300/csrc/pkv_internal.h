@@ -35,6 +35,8 @@ struct DecodeArgs {
     int32_t num_seqs, max_blocks_per_seq, max_context_len;
     DecodePlan plan;
     float scale;
+    bool kv_e4m3;                  // pools hold e4m3 codes (else bf16)
+    float k_scale, v_scale;        // e4m3 pools: element = code value * scale
 };
 
 struct DecodeWsLayout {
@@ -54,13 +56,22 @@ cudaError_t launch_cache_write(const void* k_new, const void* v_new, const int32
                                void* k_pool, void* v_pool, int32_t num_blocks, int32_t num_kv_heads,
                                int32_t head_dim, unsigned long long* err, cudaStream_t stream);
 
+// e4m3 pools: code(bf16 value * inv_scale), the product in fp32, nearest
+// even, saturating to +-448.
+cudaError_t launch_cache_write_e4m3(const void* k_new, const void* v_new, const int32_t* slot_mapping,
+                                    int32_t num_tokens, void* k_pool, void* v_pool, int32_t num_blocks,
+                                    int32_t num_kv_heads, int32_t head_dim, float k_inv_scale, float v_inv_scale,
+                                    unsigned long long* err, cudaStream_t stream);
+
+// elem_bytes: 2 for bf16 pools, 1 for e4m3 pools.
 cudaError_t launch_copy_blocks(const int32_t* src, const int32_t* dst, int32_t num_pairs, void* k_pool,
                                void* v_pool, int32_t num_blocks, int32_t num_kv_heads, int32_t head_dim,
-                               unsigned long long* err, cudaStream_t stream);
+                               int32_t elem_bytes, unsigned long long* err, cudaStream_t stream);
 
 cudaError_t launch_swap_blocks(int32_t direction, const int32_t* blocks, const int32_t* slots, int32_t n,
                                void* host, int64_t num_slots, void* k_pool, void* v_pool, int32_t num_blocks,
-                               int32_t num_kv_heads, int32_t head_dim, unsigned long long* err, cudaStream_t stream);
+                               int32_t num_kv_heads, int32_t head_dim, int32_t elem_bytes, unsigned long long* err,
+                               cudaStream_t stream);
 
 // Chunked prefill (tcgen05) launch description.
 struct PrefillArgs {

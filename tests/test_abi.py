@@ -90,3 +90,47 @@ def test_sources_use_no_closed_copy_calls():
         for f in files:
             if f.endswith((".py", ".cu", ".cuh", ".h", ".c", ".cpp")):
                 assert not pat.search(open(os.path.join(dirpath, f), errors="ignore").read()), f
+
+
+def test_descriptor_structs_match_the_header(tmp_path):
+    """The binding's ctypes mirrors have the header's field offsets and sizes
+    (a C program compiled against include/pkv.h prints them)."""
+    import paged_kv_cache_291_gb300 as pkv
+    structs = {"pkv_cache_t": pkv.Cache, "pkv_blocks_t": pkv.BlocksState}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "pkv.h"', 'int main(void) {']
+    for cname, py in structs.items():
+        lines.append(f'printf("{cname} size %zu\\n", sizeof({cname}));')
+        for f, _ in py._fields_:
+            lines.append(f'printf("{cname} {f} %zu\\n", offsetof({cname}, {f}));')
+    lines.append('return 0; }')
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
+    got = {tuple(ln.split()[:2]): int(ln.split()[2]) for ln in out if ln}
+    for cname, py in structs.items():
+        assert got[(cname, "size")] == ctypes.sizeof(py), cname
+        for f, _ in py._fields_:
+            assert got[(cname, f)] == getattr(py, f).offset, (cname, f)
+
+
+def test_e4m3_descriptor_checks_without_gpu(lib):
+    """The pool descriptor is checked on the host before anything touches a
+    device: an unknown kv_dtype or e4m3 scales that are not finite and
+    positive give PKV_ERR_DTYPE (16); a valid e4m3 descriptor with no rows
+    is a no-op."""
+    import paged_kv_cache_291_gb300 as pkv
+    fake = 1 << 20                      # aligned, never dereferenced
+    lib.pkv_cache_write.restype = ctypes.c_int
+
+    def write(dtype, ks, vs):
+        c = pkv.Cache(fake, fake, 4, 8, 128, 16, dtype, ks, vs)
+        return lib.pkv_cache_write(ctypes.byref(c), ctypes.c_void_p(fake), ctypes.c_void_p(fake),
+                                   ctypes.c_void_p(fake), 0, None)
+    assert write(pkv.PKV_KV_E4M3, 0.01, 0.02) == 0
+    assert write(pkv.PKV_KV_BF16, 0.0, 0.0) == 0          # scales are ignored for bf16
+    assert write(7, 1.0, 1.0) == 16
+    for bad in (0.0, -0.5, float("inf"), float("nan"), 1e-45):
+        assert write(pkv.PKV_KV_E4M3, bad, 1.0) == 16
+        assert write(pkv.PKV_KV_E4M3, 1.0, bad) == 16
