@@ -209,8 +209,8 @@ size_t pkv_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t 
  *   results are merged with the log-sum-exp rule inside the same launch, in
  *   a fixed order (results are bitwise reproducible).
  *   e4m3 pools: K_j and V_j are value(code) * k_scale and value(code) *
- *   v_scale, exactly as pkv_cache_write defines them; the NaN codes, which
- *   that call never stores for finite input, read as +-480.
+ *   v_scale, exactly as pkv_cache_write defines them (a NaN code, which that
+ *   call never stores for finite input, reads as NaN).
  */
 pkv_status pkv_decode_attention(const pkv_cache_t* cache, const void* q, int32_t num_q_heads,
                                 const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* context_lens,

@@ -42,11 +42,12 @@
 //    L2.
 //  * e4m3 pools (one byte per element, the same layout and the same
 //    kernel with half the bytes per slab): a lane loads its 8 dims with one
-//    8-byte shared load and turns each code into an fp32 with integer ops
-//    only -- sign to bit 31, the 7 magnitude bits to bits 20..26 -- which is
-//    the code's value times 2^-120 exactly, subnormal codes included.  The
-//    2^-120 and the K scale fold into q and the row sum; for V they fold
-//    into the final 1/l, so no per-element multiply is added.
+//    8-byte shared load and widens them with cvt.rn.f16x2.e4m3x2 (two codes
+//    per instruction, exact: every e4m3 value is an fp16 value) and
+//    cvt.f32.f16.  The K scale folds into q and the V scale into the final
+//    1/l, so no per-element multiply is added.  The extra conversion work
+//    per block makes the consumers the limit, so e4m3 pools with head
+//    groups of 1 and 2 run 16 consumer warps.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -63,14 +64,17 @@ namespace {
 // Consumer warps per CTA: 12 for head groups of 1 or 2 (their per-lane state
 // is small, and a fourth warp per scheduler hides more of the latency of the
 // dependent shuffle and FMA chains), 8 for groups of 4 and 8 (which need
-// more than the 128 registers a thread that 14 warps leave).  A build can
-// force one count for every group with PKV_DECODE_CONSUMER_WARPS.
-template <int G>
+// more than the 128 registers a thread that 14 warps leave).  e4m3 pools
+// (EB = 1) with groups of 1 or 2 take 16: their blocks cost more issue
+// (the widening) and half the ring bytes, so the same ring still gives each
+// warp 3 stages.  A build can force one count for every group with
+// PKV_DECODE_CONSUMER_WARPS.
+template <int G, int EB>
 constexpr int consumer_warps() {
 #ifdef PKV_DECODE_CONSUMER_WARPS
     return PKV_DECODE_CONSUMER_WARPS;
 #else
-    return G <= 2 ? 12 : 8;
+    return G <= 2 ? (EB == 1 ? 16 : 12) : 8;
 #endif
 }
 constexpr int kItemRing = 8;
@@ -104,7 +108,7 @@ struct DecodeParams {
     int32_t num_blocks, hkv, hq, num_seqs, max_blocks, ctx_cap;
     int32_t range_units;  // units per range, 0 = automatic
     int32_t max_ranges;   // ranges the workspace holds
-    float scale_log2;     // softmax scale * log2(e); e4m3 pools: also * k_scale * 2^64
+    float scale_log2;     // softmax scale * log2(e); e4m3 pools: also * k_scale
     float v_scale;        // e4m3 pools: the V pool's scale
 };
 
@@ -112,7 +116,7 @@ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
 template <int D, int G, int EB>
 struct Cfg {
-    static constexpr int W = consumer_warps<G>();     // consumer warps
+    static constexpr int W = consumer_warps<G, EB>();  // consumer warps
     static_assert(W >= 1 && W <= 16, "consumer warps");
     // Lanes per q head in the merger's weight reduction: W rounded up to a
     // power of two (the extra lanes carry empty states).
@@ -230,29 +234,37 @@ __device__ __forceinline__ uint2 lds64(const void* p) {
     return v;
 }
 
-// Four e4m3 codes (bytes of w, lowest first) -> their values times 2^-120:
-// a code's sign and 7 magnitude bits placed at fp32 bits 31 and 20..26 make
-// the exponent field the e4m3 exponent, so the fp32 value is the e4m3 value
-// scaled by 2^(7-127); e4m3 subnormals land on fp32 subnormals, so the map
-// is exact (the NaN codes read as 480 * 2^-120).
-__device__ __forceinline__ void e4m3x4_scaled(uint32_t w, float2& a, float2& b) {
-    a = make_float2(__uint_as_float(((w << 24) & 0x80000000u) | ((w << 20) & 0x07f00000u)),
-                    __uint_as_float(((w << 16) & 0x80000000u) | ((w << 12) & 0x07f00000u)));
-    b = make_float2(__uint_as_float(((w << 8) & 0x80000000u) | ((w << 4) & 0x07f00000u)),
-                    __uint_as_float((w & 0x80000000u) | ((w >> 4) & 0x07f00000u)));
+__device__ __forceinline__ float2 f16x2_to_float2(uint32_t h) {
+    float2 r;
+    asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tcvt.f32.f16 %0, lo;\n\tcvt.f32.f16 %1, hi;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "r"(h));
+    return r;
 }
 
-// o / l of one output chunk.  An e4m3 pool's o is in units of 2^-120 V
-// codes; o / l is a weighted mean of those (at most 480 * 2^-120), so
-// scaling it by 2^120 / l first and then by v_scale cannot overflow unless
-// the output itself does.  (l >= 1: the reference m never exceeds a score.)
+// Four e4m3 codes (bytes of w, lowest first) -> their values as fp32, in
+// order: a = (code 0, code 1), b = (code 2, code 3).  e4m3 -> fp16 is exact
+// (every e4m3 value, subnormals included, is a normal fp16 or zero), and so
+// is fp16 -> fp32; a NaN code gives NaN.
+__device__ __forceinline__ void e4m3x4_to_float(uint32_t w, float2& a, float2& b) {
+    uint32_t h01, h23;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, lo;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+        : "=r"(h01), "=r"(h23)
+        : "r"(w));
+    a = f16x2_to_float2(h01);
+    b = f16x2_to_float2(h23);
+}
+
+// o / l of one output chunk; an e4m3 pool's o is in code units, so its V
+// scale is applied here (o / l is a weighted mean of codes, at most 448).
 template <int EB>
 __device__ __forceinline__ float4 normalise(float4 a, float l, float v_scale) {
     if constexpr (EB == 2) {
         return make_float4(a.x / l, a.y / l, a.z / l, a.w / l);
     } else {
-        const float f = 0x1p120f / l;
-        return make_float4(a.x * f * v_scale, a.y * f * v_scale, a.z * f * v_scale, a.w * f * v_scale);
+        const float f = v_scale / l;
+        return make_float4(a.x * f, a.y * f, a.z * f, a.w * f);
     }
 }
 
@@ -280,11 +292,11 @@ __device__ __forceinline__ void compute_block(const uint8_t* kst, const uint8_t*
                 if (row < valid) u = lds128(kst + row * D * 2 + cl * 16);
                 k0 = bf16x2_to_float2(u.x), k1 = bf16x2_to_float2(u.y);
                 k2 = bf16x2_to_float2(u.z), k3 = bf16x2_to_float2(u.w);
-            } else {  // e4m3 values * 2^-120; q carries k_scale * 2^64, the row sum gets 2^56
+            } else {  // e4m3 codes; q carries k_scale
                 uint2 u = make_uint2(0u, 0u);
                 if (row < valid) u = lds64(kst + row * D + cl * 8);
-                e4m3x4_scaled(u.x, k0, k1);
-                e4m3x4_scaled(u.y, k2, k3);
+                e4m3x4_to_float(u.x, k0, k1);
+                e4m3x4_to_float(u.y, k2, k3);
             }
 #pragma unroll
             for (int g = 0; g < C::HG; ++g) {
@@ -298,7 +310,6 @@ __device__ __forceinline__ void compute_block(const uint8_t* kst, const uint8_t*
 #pragma unroll
         for (int g = 0; g < C::HG; ++g) {
             float sc = transpose_reduce<C::NV, C::LPR>(acc[g], lane);
-            if constexpr (EB == 1) sc *= 0x1p56f;
             sc = (myrow < valid) ? sc : -INFINITY;
             const float mb = warp_max_redux(sc);
             // The reference m moves only when a block's maximum exceeds it by
@@ -328,10 +339,10 @@ __device__ __forceinline__ void compute_block(const uint8_t* kst, const uint8_t*
                 const uint4 u = lds128(vst + row * D * 2 + cl * 16);
                 v0 = bf16x2_to_float2(u.x), v1 = bf16x2_to_float2(u.y);
                 v2 = bf16x2_to_float2(u.z), v3 = bf16x2_to_float2(u.w);
-            } else {  // e4m3 values * 2^-120: 2^120 * v_scale is applied with 1/l at the end
+            } else {  // e4m3 codes: v_scale is applied with 1/l at the end
                 const uint2 u = lds64(vst + row * D + cl * 8);
-                e4m3x4_scaled(u.x, v0, v1);
-                e4m3x4_scaled(u.y, v2, v3);
+                e4m3x4_to_float(u.x, v0, v1);
+                e4m3x4_to_float(u.y, v2, v3);
             }
             // p of this row for every head: psm is [row][head] (p, p) pairs,
             // read two heads per 16-byte load.
@@ -1144,8 +1155,8 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     P.v_scale = 1.f;
     const int G = a.num_q_heads / a.num_kv_heads;
     if (a.kv_e4m3) {
-        // q' = q * scale*log2(e) * k_scale * 2^64 against K codes * 2^-120.
-        P.scale_log2 = a.scale * kLog2e * a.k_scale * 0x1p64f;
+        // q' = q * scale*log2(e) * k_scale against the K codes.
+        P.scale_log2 = a.scale * kLog2e * a.k_scale;
         P.v_scale = a.v_scale;
         if (a.head_dim == 128) return dispatch_g<128, 1>(P, G, a.plan.grid, stream);
         if (a.head_dim == 64) return dispatch_g<64, 1>(P, G, a.plan.grid, stream);

@@ -143,9 +143,9 @@ def test_fp8_split_kv_merge(pkv, pb):
 
 
 def test_fp8_small_and_large_scales(pkv):
-    """Scales far from 1 (q is pre-multiplied by k_scale * 2^64 inside the
-    kernel, V by 2^120 * v_scale at the end): the result must not overflow
-    or lose the small codes."""
+    """Scales far from 1 (q is pre-multiplied by k_scale inside the kernel,
+    the V scale is applied with 1/l at the end), with many subnormal codes
+    under the large scales."""
     w = W.make_paged("fp8 scales", 29, 16, 8, 128, [333, 64, 1], [1] * 3)
     run_fp8_step(pkv, w, ks=np.float32(3.1e-4), vs=np.float32(2.7e-5))
     run_fp8_step(pkv, w, ks=np.float32(5.3), vs=np.float32(9.1))
