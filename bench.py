@@ -43,6 +43,8 @@ CONFIG_ID = 2  # the Qwen3-1.7B decode step (34 sequences x 640 tokens)
 # sources it was taken on; reported only while the sources still match.
 NCU_TRAFFIC = {"bytes": 91992576, "sources_sha": "ce493bad71d6d71f",
                "capture": "profiles/decode_kernel_qwen3_1p7b_decode.md"}
+NCU_TRAFFIC_E4M3 = {"bytes": 44818432, "sources_sha": "ce493bad71d6d71f",
+                    "capture": "profiles/decode_kernel_e4m3_qwen3_1p7b_decode.md"}
 KERNEL_SOURCES = ["paged_kv_cache_291_gb300/csrc/decode.cu", "paged_kv_cache_291_gb300/csrc/pkv_device.cuh"]
 
 
@@ -545,7 +547,7 @@ def swap_timing(w, pkv, torch, dev, stream, reps):
             "bound": "the host link (compared with the copy engines' contiguous copy)"}
 
 
-def fp8_decode_timing(w, pkv, torch, dev, stream, reps, hbm, bf16_ms):
+def fp8_decode_timing(w, pkv, torch, dev, stream, reps, hbm, bf16_ms, traffic=None):
     """Decode of the same rows over e4m3 pools (one byte per element, one
     scale per pool): the pools are filled from the bf16 ones by the e4m3
     cache write, then the decode launches are replayed from a graph over
@@ -612,7 +614,7 @@ def fp8_decode_timing(w, pkv, torch, dev, stream, reps, hbm, bf16_ms):
            "workload": f"the decode rows of this step, {len(seqs)} sequences, pools written by the e4m3 cache write "
                        f"(k_scale = v_scale = 1/64), {R8} rotated replicas of {pool8 / 1e6:.0f} MB",
            "avg_launch_us": ms * 1e3, "algorithmic_bytes": nbytes, "achieved_gbs": achieved, "peak": hbm,
-           "frac": achieved / hbm, "launches_per_call": 1}
+           "frac": achieved / hbm, "traffic": traffic, "launches_per_call": 1}
     if bf16_ms:
         out["bf16_avg_launch_us"] = bf16_ms * 1e3
         out["speedup_vs_bf16"] = bf16_ms / ms
@@ -922,7 +924,10 @@ def run_ours(args):
     line["prefix_keys"] = prefix_keys_timing(w, pkv, torch, dev, stream)
     line["prefix_cache"] = prefix_cache_timing(w, pkv, torch, dev, stream)
     line["swap"] = swap_timing(w, pkv, torch, dev, stream, reps)
-    line["fp8_decode"] = fp8_decode_timing(w, pkv, torch, dev, stream, reps, hbm, dec_ms)
+    line["fp8_decode"] = fp8_decode_timing(
+        w, pkv, torch, dev, stream, reps, hbm, dec_ms,
+        traffic=(NCU_TRAFFIC_E4M3["bytes"] if NCU_TRAFFIC_E4M3["sources_sha"] == sources_sha()
+                 and args.config == CONFIG_ID else None))
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_budget)
     print(json.dumps(line), flush=True)

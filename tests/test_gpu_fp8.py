@@ -230,3 +230,53 @@ def test_fp8_pools_rejected_where_not_supported(pkv):
     with pytest.raises(ValueError):
         pkv.decode_attention(kd, vd, dev_tensor(w.q[:2]), dev_tensor(w.block_tables), dev_tensor(w.context_lens),
                              w.max_context_len, w.scale)
+
+
+def test_fp8_empty_context_and_output_bounds(pkv):
+    """An empty context gives a zero row; decode writes only its own output
+    rows (sentinel rows around them stay intact)."""
+    w = W.make_paged("fp8 empty", 41, 16, 8, 128, [5, 40, 1], [1] * 3)
+    ctx = w.context_lens.copy()
+    ctx[1] = 0
+    k8, v8 = codes_of(w.k_pool, K_SCALE), codes_of(w.v_pool, V_SCALE)
+    fp8.cache_write(k8, v8, w.k_new, w.v_new, w.slot_mapping, inv(K_SCALE), inv(V_SCALE))  # this step's rows
+    G = 8
+    full = torch.full((3 + 2 * G, 16, 128), float("nan"), dtype=torch.float32, device="cuda")
+    out = full[G:G + 3]
+    pkv.decode_attention(dev_tensor(k8), dev_tensor(v8), dev_tensor(w.q), dev_tensor(w.block_tables), dev_tensor(ctx),
+                         w.max_context_len, w.scale, out=out, k_scale=float(K_SCALE), v_scale=float(V_SCALE))
+    torch.cuda.synchronize()
+    assert pkv.get_error() == (0, 0)
+    f = full.cpu().numpy()
+    assert np.all(np.isnan(f[:G])) and np.all(np.isnan(f[G + 3:])), "decode wrote outside its rows"
+    got = f[G:G + 3]
+    assert not got[1].any(), "empty context must give a zero row"
+    ref = fp8.decode_attention(k8, v8, w.q, ctx, w.block_tables, w.scale, float(K_SCALE), float(V_SCALE))
+    assert_close(got, ref, "fp8 empty context")
+
+
+def test_fp8_allocation_free_entry_point(pkv):
+    """pkv_decode_attention_static takes the same e4m3 descriptor."""
+    import ctypes
+    lib = pkv.load()
+    P, i32, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float
+    lib.pkv_decode_attention_static.argtypes = [ctypes.POINTER(pkv.Cache), P, i32, P, i32, P, i32, i32, f32, P, P]
+    lib.pkv_decode_attention_static.restype = ctypes.c_int
+    w = W.make_paged("fp8 static", 43, 32, 8, 128, [700, 33, 260, 1], [1] * 4)
+    k8, v8 = codes_of(w.k_pool, K_SCALE), codes_of(w.v_pool, V_SCALE)
+    fp8.cache_write(k8, v8, w.k_new, w.v_new, w.slot_mapping, inv(K_SCALE), inv(V_SCALE))  # this step's rows
+    kd, vd = dev_tensor(k8), dev_tensor(v8)
+    q, t, c = dev_tensor(w.q), dev_tensor(w.block_tables), dev_tensor(w.context_lens)
+    cache = pkv._cache(kd, vd, float(K_SCALE), float(V_SCALE))
+    out = torch.full((4, 32, 128), float("nan"), dtype=torch.float32, device="cuda")
+    for _ in range(2):
+        st = lib.pkv_decode_attention_static(ctypes.byref(cache), ctypes.c_void_p(q.data_ptr()), 32,
+                                             ctypes.c_void_p(t.data_ptr()), int(t.shape[1]),
+                                             ctypes.c_void_p(c.data_ptr()), 4, w.max_context_len,
+                                             ctypes.c_float(w.scale), ctypes.c_void_p(out.data_ptr()), None)
+        assert st == 0, pkv.status_string(st)
+        torch.cuda.synchronize()
+        assert pkv.get_error() == (0, 0)
+        ref = fp8.decode_attention(k8, v8, w.q, w.context_lens, w.block_tables, w.scale, float(K_SCALE),
+                                   float(V_SCALE))
+        assert_close(out.cpu().numpy(), ref, "fp8 static entry point")
