@@ -1,18 +1,27 @@
 #!/usr/bin/env python3
-"""Benchmark of the paged-KV decode step on GB300.
+"""Benchmark of the paged-KV hot path on GB300.
 
-One step = the whole hot path for one decode iteration of the Qwen3-1.7B
-attention shape (one layer): cache_write of the 34 sequences' new K/V rows,
-then paged decode attention of 34 sequences x 640 tokens (16 q / 8 kv heads,
-head_dim 128, 16-token blocks, 22,048-token pool, shuffled block tables).
-Synthetic bf16 N(0,1) data from pkv_workloads (no weights, no dataset).
+Headline: one step = the whole hot path for one decode iteration of the
+Qwen3-1.7B attention shape (one layer): the store of the 34 sequences' new
+K/V rows and paged decode attention of 34 sequences x 640 tokens (16 q / 8 kv
+heads, head_dim 128, 16-token blocks, 22,048-token pool, shuffled block
+tables).  Synthetic bf16 N(0,1) data from pkv_workloads (no weights, no
+dataset).  `--config k` picks another workload for the headline.
 
-Timing: inputs resident in HBM; 8 replicas of the pool/tables/q (8 x 90 MB,
-larger than the 129 MB L2) are rotated step by step, so every step reads its
-K/V from HBM.  The steps are replayed from CUDA graphs (one graph per cycle
-through the replicas) and timed with CUDA events on the launching stream,
-synchronised on both sides.  The decode kernel's own average duration is
-timed the same way over decode-only replays.
+Beside the headline, the `configs` object reports every workload (1..5) the
+same way: the step rate, the decode kernel (and, for the mixed batch, the
+tensor-core prefill kernel) timed alone against its roofline, the e4m3 decode
+on the same rows, and the CPU oracle on the host cores (all of them and one
+thread) on a bounded sample.
+
+Timing: inputs resident in HBM; enough replicas of the pool, tables and q
+(more than 512 MB in all, larger than the 129 MB L2) are rotated step by
+step, so every step reads its K/V from HBM.  Steps are replayed from CUDA
+graphs (one graph per cycle through the replicas) and timed with CUDA events
+on the launching stream, synchronised on both sides.  Kernel-alone figures
+are graph replays of that kernel over the replicas: the mean over all
+launches, and the median and minimum of several trials; "warm" repeats one
+replica, so its inputs stay in L2 where they fit.
 
 Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle on
 the host cores instead, on a bounded sample of the same workload.
@@ -22,7 +31,6 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -37,14 +45,17 @@ if ROOT not in sys.path:
 METRIC = "paged decode attention: achieved HBM GB/s vs GB300 peak; sequences/s per layer"
 UNIT = "seqs/s"
 CONFIG_ID = 2  # the Qwen3-1.7B decode step (34 sequences x 640 tokens)
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal (the measured copy bandwidth is the roofline)
+L2_ROTATE_BYTES = 512 << 20
 
-# DRAM traffic of one decode launch on this workload from an ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum), and the hash of the kernel
+# DRAM traffic of one decode launch on a workload from an ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), with the hash of the kernel
 # sources it was taken on; reported only while the sources still match.
-NCU_TRAFFIC = {"bytes": 91992576, "sources_sha": "ce493bad71d6d71f",
-               "capture": "profiles/decode_kernel_qwen3_1p7b_decode.md"}
-NCU_TRAFFIC_E4M3 = {"bytes": 44818432, "sources_sha": "ce493bad71d6d71f",
-                    "capture": "profiles/decode_kernel_e4m3_qwen3_1p7b_decode.md"}
+# Keys: (config, pool element bytes).
+NCU_TRAFFIC = {
+    (2, 2): {"bytes": 91992576, "sources_sha": "ce493bad71d6d71f"},
+    (2, 1): {"bytes": 44818432, "sources_sha": "ce493bad71d6d71f"},
+}
 KERNEL_SOURCES = ["paged_kv_cache_291_gb300/csrc/decode.cu", "paged_kv_cache_291_gb300/csrc/pkv_device.cuh"]
 
 
@@ -54,6 +65,11 @@ def sources_sha() -> str:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
+
+
+def ncu_traffic(config, elem_bytes):
+    rec = NCU_TRAFFIC.get((config, elem_bytes))
+    return rec["bytes"] if rec is not None and rec["sources_sha"] == sources_sha() else None
 
 
 # ----------------------------------------------------------- multi-rank host logic
@@ -159,6 +175,7 @@ class NvmlClockSampler:
         import torch
         self.samples = []
         self._stop = threading.Event()
+        self._paused = threading.Event()
         self._thr = None
         self.fallback = None
         try:
@@ -184,6 +201,9 @@ class NvmlClockSampler:
         ct, lib, h = self.ct, self.lib, self.h
         clk, rs = ct.c_uint(), ct.c_ulonglong()
         while not self._stop.is_set():
+            if self._paused.is_set():
+                time.sleep(0.01)
+                continue
             ok = lib.nvmlDeviceGetClockInfo(h, 1, ct.byref(clk)) == 0 and self.reasons_fn(h, ct.byref(rs)) == 0
             if ok:
                 self.samples.append((time.time(), float(clk.value), int(rs.value)))
@@ -196,6 +216,13 @@ class NvmlClockSampler:
         self._thr = threading.Thread(target=self._poll, daemon=True)
         self._thr.start()
         time.sleep(0.01)
+
+    def pause(self, on: bool):
+        """Stop polling (on=True) while the host cores run something timed."""
+        if on:
+            self._paused.set()
+        else:
+            self._paused.clear()
 
     def stop(self):
         if self.lib is None:
@@ -215,7 +242,7 @@ class NvmlClockSampler:
                 "samples": len(rows)}
 
 
-# ----------------------------------------------------------- helpers
+# ----------------------------------------------------------- peaks, bytes, flops
 
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -247,18 +274,37 @@ def prefill_rows(w):
     return np.nonzero(w.query_lens > 1)[0]
 
 
-def decode_bytes(w, kv_elem_bytes=2) -> int:
+def decode_bytes(w, kv_elem_bytes=2, seqs=None) -> int:
     """Algorithmic bytes of one decode launch: Q + gathered K/V (once per kv
-    head) + block-table entries read + fp32 output, over the decode rows."""
+    head) + block-table entries read + fp32 output, over the decode rows (or
+    the sequences `seqs`)."""
     hq, hkv, d = w.num_q_heads, w.num_kv_heads, w.head_dim
     total = 0
-    for s in decode_rows(w).tolist():
-        n = int(w.context_lens[s])
+    for s in (decode_rows(w) if seqs is None else seqs):
+        n = int(w.context_lens[int(s)])
         total += hq * d * 2                     # q
         total += n * hkv * d * kv_elem_bytes * 2  # K and V rows
         total += -(-n // 16) * 4                # block-table entries
         total += hq * d * 4                     # fp32 output
     return total
+
+
+def decode_unique_bytes(w, kv_elem_bytes=2) -> int:
+    """The same launch with every distinct (physical block, kv head) slab
+    counted once: what HBM must deliver when blocks shared by several
+    sequences come from L2 after their first read (rows of the last,
+    partly filled block counted up to the longest context that uses it)."""
+    hq, hkv, d = w.num_q_heads, w.num_kv_heads, w.head_dim
+    rows = {}
+    for s in decode_rows(w).tolist():
+        n = int(w.context_lens[s])
+        nb = -(-n // 16)
+        for b in range(nb):
+            phys = int(w.block_tables[s, b])
+            rows[phys] = max(rows.get(phys, 0), min(16, n - 16 * b))
+    kv = sum(rows.values()) * hkv * d * kv_elem_bytes * 2
+    other = sum(hq * d * 2 + -(-int(w.context_lens[s]) // 16) * 4 + hq * d * 4 for s in decode_rows(w).tolist())
+    return int(kv + other)
 
 
 def prefill_flops(w) -> int:
@@ -271,9 +317,21 @@ def prefill_flops(w) -> int:
     return total * 4 * w.head_dim * w.num_q_heads
 
 
-def cache_write_bytes(w) -> int:
+def step_bytes(w) -> int:
+    """Algorithmic bytes of a whole step: copy-on-write copies (read and
+    write of whole blocks), the new rows' store (read and write), and the
+    attention's Q, gathered K/V, table entries and output (prefill rows:
+    their Q, the K/V of their keys once per kv head and their output)."""
+    hq, hkv, d = w.num_q_heads, w.num_kv_heads, w.head_dim
+    total = decode_bytes(w)
+    for s in prefill_rows(w).tolist():
+        n, ql = int(w.context_lens[s]), int(w.query_lens[s])
+        total += ql * hq * d * (2 + 4) + n * hkv * d * 2 * 2 + -(-n // 16) * 4
     T = w.slot_mapping.shape[0]
-    return T * (w.num_kv_heads * w.head_dim * 2 * 2 * 2 + 4)  # read + write of K and V rows, slot ids
+    total += T * (hkv * d * 2 * 2 * 2 + 4)
+    if w.copy_src is not None:
+        total += len(w.copy_src) * 2 * (2 * hkv * 16 * d * 2) + 8 * len(w.copy_src)
+    return total
 
 
 def subset(w, seqs):
@@ -291,16 +349,28 @@ def subset(w, seqs):
                 max_ctx=int(w.context_lens[seqs].max()) if len(seqs) else 0)
 
 
+# ----------------------------------------------------------- the oracle on the host cores
+
+def host_threads():
+    """(threads the process may run on, CPUs in the machine)."""
+    try:
+        aff = len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        aff = os.cpu_count() or 1
+    return max(1, aff), os.cpu_count() or 1
+
+
 _ORACLE_POOLS = {}
 
 
 def oracle_step_seconds(w, seqs, threads):
-    """Run the oracle's whole step (copy-on-write copies, cache_write of the
-    new rows, then attention) on the sequences `seqs`; returns seconds.  The
-    pools are copied once, outside the timing (the step is idempotent)."""
-    import numpy as np
+    """Run the oracle's whole step (copy-on-write copies, the store of the new
+    rows, then attention) with attention over the sequences `seqs`; returns
+    seconds.  The pools are copied once, outside the timing (the step is
+    idempotent)."""
     import oracle
     if id(w) not in _ORACLE_POOLS:
+        _ORACLE_POOLS.clear()
         _ORACLE_POOLS[id(w)] = (w.k_pool.copy(), w.v_pool.copy())
     k, v = _ORACLE_POOLS[id(w)]
     sub = subset(w, seqs)
@@ -312,33 +382,94 @@ def oracle_step_seconds(w, seqs, threads):
     return time.perf_counter() - t0
 
 
+def spread(B, n):
+    """n sequence indices spread evenly over 0..B-1 (first and last included)."""
+    import numpy as np
+    if n >= B:
+        return list(range(B))
+    return sorted(set(np.linspace(0, B - 1, n).round().astype(int).tolist()))
+
+
+def seq_cost(w, s):
+    """Relative oracle work of sequence s: the (query row, key) pairs of
+    every q head (a dot product and a V update each) plus the gather of the
+    context's K and V rows of every kv head."""
+    n, ql = int(w.context_lens[s]), int(w.query_lens[s])
+    pairs = ql * (n - ql) + ql * (ql + 1) // 2
+    return max(1, (pairs * w.num_q_heads + n * w.num_kv_heads) * 2 * w.head_dim)
+
+
+def predicted_cost(w, seqs, threads):
+    """The oracle deals the sequences of a call to its threads round-robin:
+    the step takes as long as the thread with the most work."""
+    per = [0] * max(1, threads)
+    for i, s in enumerate(seqs):
+        per[i % len(per)] += seq_cost(w, s)
+    return max(per)
+
+
 def oracle_sample(w, threads, budget_s):
-    """Sequences per oracle step so that one step takes about budget_s."""
+    """Sequences (spread over the batch) for an oracle step of about
+    budget_s on `threads` threads: the oracle's rate is measured on the
+    cheapest sequences, then the largest spread sample whose predicted time
+    fits the budget is taken."""
     B = w.num_seqs
-    n = 1
+    order = sorted(range(B), key=lambda s: seq_cost(w, s))
+    fixed = min(oracle_step_seconds(w, [], threads) for _ in range(3))  # the copies and the row store
+    k = 1
     while True:
-        t = oracle_step_seconds(w, list(range(n)), threads)
-        if t > 0.2 * budget_s or n >= B:
+        cal = sorted(order[:k])
+        t = oracle_step_seconds(w, cal, threads) - fixed
+        if t > 0.05 or k >= B:
             break
-        n = min(B, n * 4)
-    per_seq = t / n
-    return max(1, min(B, int(budget_s / max(per_seq, 1e-9))))
+        k = min(B, 2 * k)
+    rate = predicted_cost(w, cal, threads) / max(t, 1e-6)
+    best = [order[0]]
+    for n in range(1, B + 1):
+        seqs = spread(B, n)
+        if fixed + predicted_cost(w, seqs, threads) / rate <= budget_s:
+            best = seqs
+    return best
 
 
-def cpu_baseline(w, budget_s=12.0):
-    """The oracle on the host cores, repeated steps for about budget_s."""
-    threads = os.cpu_count() or 1
+def oracle_rate(w, seqs, threads, min_s=1.0, min_reps=3):
+    """Median and minimum seconds of repeated oracle steps over `seqs`."""
+    times = []
+    while len(times) < min_reps or sum(times) < min_s:
+        times.append(oracle_step_seconds(w, seqs, threads))
+        if len(times) >= 50:
+            break
+    return statistics.median(times), min(times), len(times)
+
+
+def oracle_leg(w, threads, budget_s, min_reps):
+    """The oracle's step over a sample of sequences sized for about budget_s
+    on `threads` threads: sequences, query rows and decode K/V bytes per
+    second from the median of repeated steps."""
+    seqs = oracle_sample(w, threads, budget_s)
+    med, mn, reps = oracle_rate(w, seqs, threads, min_s=budget_s, min_reps=min_reps)
+    rows = int(sum(int(w.query_lens[s]) for s in seqs))
+    dec = [s for s in seqs if int(w.query_lens[s]) == 1]
+    nbytes = decode_bytes(w, seqs=dec)
     B = w.num_seqs
-    n = oracle_sample(w, threads, budget_s / 4)
-    seqs = list(range(n))
-    reps, spent = 0, 0.0
-    while spent < budget_s and reps < 1000:
-        spent += oracle_step_seconds(w, seqs, threads)
-        reps += 1
-    what = "all" if n == B else f"the first {n} of"
-    return {"value": reps * n / spent, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"{reps} steps over {what} {B} sequences (copy-on-write, cache_write and attention), "
-                      f"{spent:.1f} s, {threads} threads"}
+    what = "all" if len(seqs) == B else f"{len(seqs)} (spread over the batch) of"
+    return {"value": len(seqs) / med, "unit": UNIT, "cores": threads, "median_s": med, "min_s": mn, "reps": reps,
+            "tokens_per_s": rows / med, "decode_gbs": nbytes / med / 1e9 if nbytes else None,
+            "sample": f"copy-on-write, the store of the new rows and attention over {what} {B} sequences "
+                      f"({rows} query rows) per step, {threads} thread{'s' if threads > 1 else ''}"}
+
+
+def cpu_baseline(w, budget_s=3.0, one_thread=True):
+    """The oracle as it stands (threaded over sequences), on all the host
+    cores the process may use and on one thread, each over a bounded sample
+    of sequences spread over the batch and sized for about budget_s, each
+    the median of repeated steps."""
+    threads, ncpu = host_threads()
+    out = {"kind": "oracle", "cpus": ncpu, "affinity_cpus": threads}
+    out.update(oracle_leg(w, threads, budget_s, 3))
+    if one_thread:
+        out["one_thread"] = oracle_leg(w, 1, budget_s, 1)
+    return out
 
 
 def build_workload(config, rank=0, threads=None):
@@ -355,18 +486,20 @@ def run_reference(args):
     if rank != 0:
         return 0
     w = build_workload(args.config)
-    threads = os.cpu_count() or 1
+    threads, _ = host_threads()
     B = w.num_seqs
     per_step_budget = 60.0 / max(1, args.steps + args.warmup)
-    n = oracle_sample(w, threads, per_step_budget)
-    seqs = list(range(n))
+    seqs = oracle_sample(w, threads, per_step_budget)
     for _ in range(args.warmup):
         oracle_step_seconds(w, seqs, threads)
     t = 0.0
     for _ in range(args.steps):
         t += oracle_step_seconds(w, seqs, threads)
+    n = len(seqs)
     value = args.steps * n / t
-    sample = f"first {n} of {B} sequences per step (copy-on-write, cache_write and attention), {threads} threads"
+    what = "all" if n == B else f"{n} (spread over the batch) of"
+    sample = (f"{what} {B} sequences per step (copy-on-write, the store of the new rows and attention), "
+              f"{threads} threads")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -377,7 +510,266 @@ def run_reference(args):
     return 0
 
 
-# ----------------------------------------------------------- our arm
+# ----------------------------------------------------------- one workload on the device
+
+class ConfigRun:
+    """One workload on the device: R rotated replicas of its inputs (more
+    than 512 MB in all), the step through the public calls (copy-on-write if
+    the workload has it, the store of the new rows, attention), and CUDA
+    graphs over the replicas."""
+
+    def __init__(self, config, w, pkv, torch, dev, stream, replicas=0, partition_blocks=0):
+        import numpy as np
+        self.config, self.w, self.pkv, self.torch, self.dev, self.stream = config, w, pkv, torch, dev, stream
+        self.pb = partition_blocks
+        pool_bytes = 2 * w.k_pool.nbytes
+        self.pool_bytes = pool_bytes
+        self.R = R = replicas or int(min(256, max(2, -(-L2_ROTATE_BYTES // pool_bytes))))
+        self.maxctx, self.scale, self.Tq = w.max_context_len, w.scale, w.num_tokens
+        # A step's inputs (everything but the pools) live in one staging
+        # buffer per replica, 256-byte aligned views, so that the end-to-end
+        # leg moves them from pinned host memory in a single copy.
+        step_inputs = [("q", w.q), ("kn", w.k_new), ("vn", w.v_new), ("slots", w.slot_mapping),
+                       ("tables", w.block_tables), ("ctx", w.context_lens), ("qsl", w.query_start_loc)]
+        if w.copy_src is not None:
+            step_inputs += [("src", w.copy_src), ("dst", w.copy_dst)]
+        layout, off = {}, 0
+        for key, a in step_inputs:
+            off = (off + 255) // 256 * 256
+            a = np.ascontiguousarray(a)
+            layout[key] = (off, a)
+            off += a.nbytes
+        stage_bytes = (off + 255) // 256 * 256
+        self.stage_np = stage_np = np.zeros(stage_bytes, dtype=np.uint8)
+        for key, (o, a) in layout.items():
+            stage_np[o:o + a.nbytes] = a.view(np.uint8).ravel()
+        tdt = {np.dtype(np.uint16): torch.int16, np.dtype(np.int32): torch.int32, np.dtype(np.int64): torch.int64}
+
+        def stage_views(stage):
+            views = {}
+            for key, (o, a) in layout.items():
+                t = stage[o:o + a.nbytes].view(tdt[a.dtype])
+                if a.dtype == np.uint16:
+                    t = t.view(torch.bfloat16)
+                views[key] = t.view(a.shape)
+            return views
+
+        k0, v0 = self.td(w.k_pool), self.td(w.v_pool)
+        self.reps = []
+        for i in range(R):
+            stage = torch.from_numpy(stage_np).to(dev)
+            r = dict(k=k0 if i == 0 else k0.clone(), v=v0 if i == 0 else v0.clone(), stage=stage,
+                     out=torch.empty((self.Tq, w.num_q_heads, w.head_dim), dtype=torch.float32, device=dev))
+            r.update(stage_views(stage))
+            self.reps.append(r)
+        if w.is_decode:
+            need = pkv.decode_workspace_size(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim, self.maxctx,
+                                             self.pb)
+        else:
+            need = pkv.prefill_workspace_size(w.num_seqs, self.Tq, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                              self.maxctx)
+        for r in self.reps:
+            r["ws"] = pkv.new_workspace(need, dev)
+        self.launches_per_step = (1 if w.copy_src is not None else 0) + 1 + (1 if w.is_decode else 0)
+        if not w.is_decode:
+            self.launches_per_step += (1 if len(decode_rows(w)) else 0) + (1 if len(prefill_rows(w)) else 0)
+        with torch.cuda.stream(stream):
+            for r in self.reps:  # eager once (also loads kernels)
+                self.step(r)
+        stream.synchronize()
+        self.check("eager step")
+        self.g_step = self.capture(self.step, self.reps)
+        self.g_single = [self.capture(self.step, [r]) for r in self.reps]
+
+    def td(self, a):
+        import numpy as np
+        torch = self.torch
+        x = torch.from_numpy(np.ascontiguousarray(a))
+        if a.dtype == np.uint16:
+            x = x.view(torch.int16).view(torch.bfloat16)
+        return x.to(self.dev)
+
+    def check(self, what):
+        st = self.pkv.get_error(self.stream)
+        if st[0] != 0:
+            raise RuntimeError(f"device error during {what} ({self.w.name}): {st}")
+
+    def attention(self, r):
+        w, pkv, s = self.w, self.pkv, self.stream
+        if w.is_decode:
+            pkv.decode_attention(r["k"], r["v"], r["q"], r["tables"], r["ctx"], self.maxctx, self.scale,
+                                 out=r["out"], workspace=r["ws"], partition_blocks=self.pb, stream=s)
+        else:
+            pkv.chunked_prefill_attention(r["k"], r["v"], r["q"], r["qsl"], r["ctx"], r["tables"], self.maxctx,
+                                          self.scale, out=r["out"], workspace=r["ws"],
+                                          query_start_loc_host=w.query_start_loc, stream=s)
+
+    def step(self, r):
+        w, pkv, s = self.w, self.pkv, self.stream
+        if w.copy_src is not None:
+            pkv.copy_blocks(r["k"], r["v"], r["src"], r["dst"], src_host=w.copy_src, dst_host=w.copy_dst, stream=s)
+        pkv.cache_write(r["k"], r["v"], r["kn"], r["vn"], r["slots"], stream=s)
+        self.attention(r)
+
+    def capture(self, fn, items):
+        g = self.torch.cuda.CUDAGraph()
+        with self.torch.cuda.graph(g, stream=self.stream):
+            for it in items:
+                fn(it)
+        return g
+
+    def run_steps(self, n):
+        cycles, rem = divmod(n, self.R)
+        for _ in range(cycles):
+            self.g_step.replay()
+        for i in range(rem):
+            self.g_single[i].replay()
+
+    def timed(self, fn, sync):
+        """Device milliseconds of fn() between events on the stream."""
+        torch = self.torch
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        sync()
+        with torch.cuda.stream(self.stream):
+            e0.record(self.stream)
+            fn()
+            e1.record(self.stream)
+        sync()
+        return e0.elapsed_time(e1)
+
+    def sync(self):
+        self.torch.cuda.synchronize(self.dev)
+
+    def step_trials(self, min_steps=200, min_ms=20.0, trials=5):
+        """Steps timed in `trials` trials of equal length (whole cycles)."""
+        with self.torch.cuda.stream(self.stream):
+            self.run_steps(2 * self.R)
+        self.sync()
+        per = self.timed(lambda: self.run_steps(self.R), self.sync) / self.R
+        n = max(min_steps, int(min_ms / max(per, 1e-6)))
+        cyc = max(1, -(-n // (self.R * trials)))
+        ms = [self.timed(lambda: self.run_steps(cyc * self.R), self.sync) / (cyc * self.R) for _ in range(trials)]
+        self.check("timed steps")
+        total = cyc * self.R * trials
+        return {"mean_ms": statistics.fmean(ms), "median_ms": statistics.median(ms), "min_ms": min(ms),
+                "steps": total, "trials": trials}
+
+    def kernel_alone(self, seqs, kv_e4m3=False, min_launches=200, min_ms=20.0, trials=5, warm_launches=50):
+        """One attention launch over the sequences `seqs` (decode rows or
+        prefill rows), replayed from graphs over the replicas (bf16 pools) or
+        over e4m3 copies of them (kv_e4m3, pools written by the e4m3 store);
+        mean over all launches, median and minimum of the trials, and a warm
+        figure repeating one replica."""
+        import numpy as np
+        torch, pkv, w, dev = self.torch, self.pkv, self.w, self.dev
+        sub = subset(w, seqs)
+        nb, hkv, _, d = w.k_pool.shape
+        ks = vs = None
+        if kv_e4m3:
+            ks = vs = 1.0 / 64  # N(0, 1) values: +-7 reaches the e4m3 maximum of 448
+            pool8 = 2 * w.k_pool.size
+            R = int(min(256, max(2, -(-L2_ROTATE_BYTES // pool8))))
+            slots = torch.arange(nb * 16, dtype=torch.int32, device=dev)
+        else:
+            R = self.R
+        items = []
+        with torch.cuda.stream(self.stream):
+            for i in range(R):
+                r = self.reps[i % self.R]
+                if kv_e4m3:
+                    k = torch.empty(tuple(w.k_pool.shape), dtype=torch.uint8, device=dev)
+                    v = torch.empty_like(k)
+                    rk = r["k"].permute(0, 2, 1, 3).reshape(nb * 16, hkv, d).contiguous()
+                    rv = r["v"].permute(0, 2, 1, 3).reshape(nb * 16, hkv, d).contiguous()
+                    pkv.cache_write(k, v, rk, rv, slots, stream=self.stream, k_scale=ks, v_scale=vs)
+                    del rk, rv
+                else:
+                    k, v = r["k"], r["v"]
+                it = dict(k=k, v=v, q=self.td(sub["q"]), tables=self.td(sub["tables"]), ctx=self.td(sub["ctx"]),
+                          qsl=self.td(sub["qsl"]), out=torch.empty((sub["q"].shape[0], w.num_q_heads, d),
+                                                                   dtype=torch.float32, device=dev))
+                if sub["decode"]:
+                    n = pkv.decode_workspace_size(len(seqs), w.num_q_heads, hkv, d, sub["max_ctx"], self.pb)
+                else:
+                    n = pkv.prefill_workspace_size(len(seqs), sub["q"].shape[0], w.num_q_heads, hkv, d,
+                                                   sub["max_ctx"])
+                it["ws"] = pkv.new_workspace(n, dev)
+                items.append(it)
+        self.stream.synchronize()
+
+        def f(it):
+            if sub["decode"]:
+                pkv.decode_attention(it["k"], it["v"], it["q"], it["tables"], it["ctx"], sub["max_ctx"], self.scale,
+                                     out=it["out"], workspace=it["ws"], partition_blocks=self.pb, stream=self.stream,
+                                     k_scale=ks, v_scale=vs)
+            else:
+                pkv.chunked_prefill_attention(it["k"], it["v"], it["q"], it["qsl"], it["ctx"], it["tables"],
+                                              sub["max_ctx"], self.scale, out=it["out"], workspace=it["ws"],
+                                              query_start_loc_host=sub["qsl"], stream=self.stream)
+        with torch.cuda.stream(self.stream):
+            for it in items:
+                f(it)
+        self.stream.synchronize()
+        g = self.capture(f, items)
+        g_warm = self.capture(f, [items[0]] * warm_launches)
+        with torch.cuda.stream(self.stream):
+            g.replay()
+        per = self.timed(g.replay, self.sync) / R
+        n = max(min_launches, int(min_ms / max(per, 1e-6)))
+        cyc = max(1, -(-n // (R * trials)))
+
+        def run():
+            for _ in range(cyc):
+                g.replay()
+        ms = [self.timed(run, self.sync) / (cyc * R) for _ in range(trials)]
+        with torch.cuda.stream(self.stream):
+            g_warm.replay()
+        warm = self.timed(g_warm.replay, self.sync) / warm_launches
+        self.check("kernel-alone timing")
+        del items, g, g_warm
+        return {"mean_us": 1e3 * statistics.fmean(ms), "median_us": 1e3 * statistics.median(ms),
+                "min_us": 1e3 * min(ms), "warm_us": 1e3 * warm, "launches": cyc * R * trials, "trials": trials,
+                "replicas": R}
+
+    def free(self):
+        self.reps = []
+        self.g_step = None
+        self.g_single = []
+        self.torch.cuda.synchronize(self.dev)
+        self.torch.cuda.empty_cache()
+
+
+def decode_entry(w, t, hbm, hbm_kind, kv_elem_bytes=2, traffic=None):
+    """Roofline record of the decode kernel from a kernel_alone timing."""
+    nbytes = decode_bytes(w, kv_elem_bytes=kv_elem_bytes)
+    achieved = nbytes / (t["mean_us"] * 1e-6) / 1e9
+    rec = {"bound": "hbm", "kernel": "decode_kernel" + (" (e4m3 pools)" if kv_elem_bytes == 1 else ""),
+           "achieved": achieved, "peak": hbm,
+           "peak_kind": f"{hbm_kind} (MEASURED_PEAKS.json hbm_gbs, copy)" if hbm_kind == "measured" else "fallback",
+           "unit": "GB/s", "frac": achieved / hbm, "frac_nominal": achieved / NOMINAL_HBM_GBS,
+           "nominal_peak": NOMINAL_HBM_GBS, "traffic": traffic, "algorithmic_bytes": nbytes,
+           "avg_launch_us": t["mean_us"], "median_us": t["median_us"], "min_us": t["min_us"],
+           "warm_us": t["warm_us"], "launches": t["launches"], "replicas": t["replicas"],
+           "seqs_per_s": len(decode_rows(w)) / (t["mean_us"] * 1e-6)}
+    ub = decode_unique_bytes(w, kv_elem_bytes)
+    if ub != nbytes:  # blocks shared between sequences
+        rec["unique_bytes"] = ub
+        rec["achieved_unique_gbs"] = ub / (t["mean_us"] * 1e-6) / 1e9
+        rec["frac_unique"] = rec["achieved_unique_gbs"] / hbm
+    return rec
+
+
+def prefill_entry(w, t, peak, kind):
+    fl = prefill_flops(w)
+    achieved = fl / (t["mean_us"] * 1e-6) / 1e12
+    return {"bound": "tensor", "kernel": "prefill_kernel", "achieved": achieved, "peak": peak, "peak_kind": kind,
+            "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None, "algorithmic_flops": fl,
+            "avg_launch_us": t["mean_us"], "median_us": t["median_us"], "min_us": t["min_us"],
+            "warm_us": t["warm_us"], "launches": t["launches"], "replicas": t["replicas"],
+            "tokens_per_s": int(sum(int(w.query_lens[s]) for s in prefill_rows(w))) / (t["mean_us"] * 1e-6)}
+
+
+# ----------------------------------------------------------- other calls of the library
 
 def block_manager_timing(w, pkv, torch, dev, stream, iters=200, warm=10):
     """Device time of one pkv_blocks_append for this batch's rows: every row
@@ -547,82 +939,45 @@ def swap_timing(w, pkv, torch, dev, stream, reps):
             "bound": "the host link (compared with the copy engines' contiguous copy)"}
 
 
-def fp8_decode_timing(w, pkv, torch, dev, stream, reps, hbm, bf16_ms, traffic=None):
-    """Decode of the same rows over e4m3 pools (one byte per element, one
-    scale per pool): the pools are filled from the bf16 ones by the e4m3
-    cache write, then the decode launches are replayed from a graph over
-    enough pool replicas to exceed L2, like the bf16 timing."""
-    import numpy as np
-    seqs = decode_rows(w)
-    if not len(seqs):
-        return None
-    sub = subset(w, seqs)
-    nb, hkv, _, d = w.k_pool.shape
-    pool8 = 2 * w.k_pool.size
-    R8 = int(min(256, max(2, -(-512 * 2 ** 20 // pool8))))
-    k_scale = v_scale = 1.0 / 64          # N(0, 1) values: +-7 reaches the e4m3 maximum of 448
-    slots = torch.arange(nb * 16, dtype=torch.int32, device=dev)
-
-    def td(a):
-        x = torch.from_numpy(np.ascontiguousarray(a))
-        if a.dtype == np.uint16:
-            x = x.view(torch.int16).view(torch.bfloat16)
-        return x.to(dev)
-
-    items = []
-    with torch.cuda.stream(stream):
-        for i in range(R8):
-            r = reps[i % len(reps)]
-            k8 = torch.empty(tuple(w.k_pool.shape), dtype=torch.uint8, device=dev)
-            v8 = torch.empty_like(k8)
-            rows_k = r["k"].permute(0, 2, 1, 3).reshape(nb * 16, hkv, d).contiguous()
-            rows_v = r["v"].permute(0, 2, 1, 3).reshape(nb * 16, hkv, d).contiguous()
-            pkv.cache_write(k8, v8, rows_k, rows_v, slots, stream=stream, k_scale=k_scale, v_scale=v_scale)
-            n = pkv.decode_workspace_size(len(seqs), w.num_q_heads, hkv, d, sub["max_ctx"])
-            items.append(dict(k=k8, v=v8, q=td(sub["q"]), tables=td(sub["tables"]), ctx=td(sub["ctx"]),
-                              out=torch.empty((len(seqs), w.num_q_heads, d), dtype=torch.float32, device=dev),
-                              ws=pkv.new_workspace(n, dev)))
-    stream.synchronize()
-
-    def f(it):
-        pkv.decode_attention(it["k"], it["v"], it["q"], it["tables"], it["ctx"], sub["max_ctx"], w.scale,
-                             out=it["out"], workspace=it["ws"], stream=stream, k_scale=k_scale, v_scale=v_scale)
-    with torch.cuda.stream(stream):
-        for it in items:
-            f(it)
-    stream.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        for it in items:
-            f(it)
-    cycles = max(3, 4096 // R8)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        g.replay()
-        e0.record(stream)
-        for _ in range(cycles):
-            g.replay()
-        e1.record(stream)
-    stream.synchronize()
-    st = pkv.get_error(stream)
-    if st[0] != 0:
-        raise RuntimeError(f"device error in the e4m3 decode timing: {st}")
-    ms = e0.elapsed_time(e1) / (cycles * R8)
-    nbytes = decode_bytes(w, kv_elem_bytes=1)
-    achieved = nbytes / (ms * 1e-3) / 1e9
-    out = {"call": "pkv_decode_attention on e4m3 pools", "kernel": "decode_kernel (e4m3)",
-           "workload": f"the decode rows of this step, {len(seqs)} sequences, pools written by the e4m3 cache write "
-                       f"(k_scale = v_scale = 1/64), {R8} rotated replicas of {pool8 / 1e6:.0f} MB",
-           "avg_launch_us": ms * 1e3, "algorithmic_bytes": nbytes, "achieved_gbs": achieved, "peak": hbm,
-           "frac": achieved / hbm, "traffic": traffic, "launches_per_call": 1}
-    if bf16_ms:
-        out["bf16_avg_launch_us"] = bf16_ms * 1e3
-        out["speedup_vs_bf16"] = bf16_ms / ms
-    return out
+def config_entry(run, hbm, hbm_kind, tpeak, tkind, clocks=None, cpu=True, cpu_budget=3.0, step=None):
+    """Everything reported for one workload: step rate, kernel-alone
+    rooflines (decode, prefill), the e4m3 decode and the oracle's rates."""
+    w = run.w
+    t0 = time.time()
+    st = step or run.step_trials()
+    sb = step_bytes(w)
+    entry = {"workload": w.name, "config": run.config, "seqs": w.num_seqs, "query_rows": w.num_tokens,
+             "step": {**st, "seqs_per_s": w.num_seqs / (st["mean_ms"] * 1e-3),
+                      "tokens_per_s": w.num_tokens / (st["mean_ms"] * 1e-3),
+                      "launches_per_step": run.launches_per_step, "algorithmic_bytes": sb,
+                      "achieved_gbs": sb / (st["mean_ms"] * 1e-3) / 1e9,
+                      "frac": sb / (st["mean_ms"] * 1e-3) / 1e9 / hbm},
+             "l2": f"{run.R} rotated input replicas of {run.pool_bytes / 1e6:.0f} MB pools"}
+    dec, pre = decode_rows(w), prefill_rows(w)
+    dec_t = None
+    if len(dec):
+        dec_t = run.kernel_alone(dec)
+        entry["decode"] = decode_entry(w, dec_t, hbm, hbm_kind, traffic=ncu_traffic(run.config, 2))
+    if len(pre):
+        entry["prefill"] = prefill_entry(w, run.kernel_alone(pre), tpeak, tkind)
+    if len(dec):
+        t8 = run.kernel_alone(dec, kv_e4m3=True)
+        e8 = decode_entry(w, t8, hbm, hbm_kind, kv_elem_bytes=1, traffic=ncu_traffic(run.config, 1))
+        e8["speedup_vs_bf16"] = dec_t["mean_us"] / t8["mean_us"]
+        e8["scales"] = "k_scale = v_scale = 1/64, pools written by the e4m3 store"
+        entry["fp8_decode"] = e8
+    if clocks is not None:
+        entry["clocks"] = clocks.summary(t0, time.time())
+    if cpu:
+        if clocks is not None:
+            clocks.pause(True)
+        entry["cpu_baseline"] = cpu_baseline(w, cpu_budget)
+        if clocks is not None:
+            clocks.pause(False)
+    return entry
 
 
 def run_ours(args):
-    import numpy as np
     import torch
 
     import paged_kv_cache_291_gb300 as pkv
@@ -639,110 +994,15 @@ def run_ours(args):
         torch.cuda.set_device(0)
     dev = torch.device("cuda", torch.cuda.current_device())
     pkv.load()
+    stream = torch.cuda.Stream(device=dev)
+    hbm, hbm_kind = measured_peaks()
+    tpeak, tkind = measured_tensor_peak()
 
     # Each rank builds its own batch (weak scaling: sequences are independent
     # units, every rank owns its own pool, tables and sequences).
     w = build_workload(args.config, rank)
-    pool_bytes = 2 * w.k_pool.nbytes
-    R = args.replicas or int(min(256, max(2, -(-512 * 2 ** 20 // pool_bytes))))
-
-    def td(a):
-        x = torch.from_numpy(np.ascontiguousarray(a))
-        if a.dtype == np.uint16:
-            x = x.view(torch.int16).view(torch.bfloat16)
-        return x.to(dev)
-
-    maxctx, scale = w.max_context_len, w.scale
-    Tq = w.num_tokens
-    # A step's inputs (everything but the pools) live in one staging buffer
-    # per replica, 256-byte aligned views, so that the end-to-end leg moves
-    # them from pinned host memory in a single copy.
-    step_inputs = [("q", w.q), ("kn", w.k_new), ("vn", w.v_new), ("slots", w.slot_mapping),
-                   ("tables", w.block_tables), ("ctx", w.context_lens), ("qsl", w.query_start_loc)]
-    if w.copy_src is not None:
-        step_inputs += [("src", w.copy_src), ("dst", w.copy_dst)]
-    layout, off = {}, 0
-    for key, a in step_inputs:
-        off = (off + 255) // 256 * 256
-        a = np.ascontiguousarray(a)
-        layout[key] = (off, a)
-        off += a.nbytes
-    stage_bytes = (off + 255) // 256 * 256
-    stage_np = np.zeros(stage_bytes, dtype=np.uint8)
-    for key, (o, a) in layout.items():
-        stage_np[o:o + a.nbytes] = a.view(np.uint8).ravel()
-    torch_dtype = {np.dtype(np.uint16): torch.int16, np.dtype(np.int32): torch.int32, np.dtype(np.int64): torch.int64}
-
-    def stage_views(stage):
-        views = {}
-        for key, (o, a) in layout.items():
-            t = stage[o:o + a.nbytes].view(torch_dtype[a.dtype])
-            if a.dtype == np.uint16:
-                t = t.view(torch.bfloat16)
-            views[key] = t.view(a.shape)
-        return views
-
-    reps = []
-    for _ in range(R):
-        stage = torch.from_numpy(stage_np).to(dev)
-        r = dict(k=td(w.k_pool), v=td(w.v_pool), stage=stage,
-                 out=torch.empty((Tq, w.num_q_heads, w.head_dim), dtype=torch.float32, device=dev))
-        r.update(stage_views(stage))
-        reps.append(r)
-    pb = args.partition_blocks
-    if w.is_decode:
-        need = pkv.decode_workspace_size(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim, maxctx, pb)
-    else:
-        need = pkv.prefill_workspace_size(w.num_seqs, Tq, w.num_q_heads, w.num_kv_heads, w.head_dim, maxctx)
-    for r in reps:
-        r["ws"] = pkv.new_workspace(need, dev)
-    stream = torch.cuda.Stream(device=dev)
-    qsl_host = w.query_start_loc
-
-    def attention(r):
-        if w.is_decode:
-            pkv.decode_attention(r["k"], r["v"], r["q"], r["tables"], r["ctx"], maxctx, scale, out=r["out"],
-                                 workspace=r["ws"], partition_blocks=pb, stream=stream)
-        else:
-            pkv.chunked_prefill_attention(r["k"], r["v"], r["q"], r["qsl"], r["ctx"], r["tables"], maxctx, scale,
-                                          out=r["out"], workspace=r["ws"], query_start_loc_host=qsl_host,
-                                          stream=stream)
-
-    def step(r):
-        if w.copy_src is not None:
-            pkv.copy_blocks(r["k"], r["v"], r["src"], r["dst"], src_host=w.copy_src, dst_host=w.copy_dst,
-                            stream=stream)
-        pkv.cache_write(r["k"], r["v"], r["kn"], r["vn"], r["slots"], stream=stream)
-        attention(r)
-
-    launches_per_step = (1 if w.copy_src is not None else 0) + 1 + (1 if w.is_decode else 0)
-    if not w.is_decode:
-        launches_per_step += (1 if len(decode_rows(w)) else 0) + (1 if len(prefill_rows(w)) else 0)
-
-    with torch.cuda.stream(stream):
-        for r in reps:  # eager once (also loads kernels)
-            step(r)
-    stream.synchronize()
-    status = pkv.get_error(stream)
-    if status[0] != 0:
-        raise RuntimeError(f"device error during eager step: {status}")
-
-    def capture(fn, items):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for it in items:
-                fn(it)
-        return g
-
-    g_step = capture(step, reps)
-    g_single = [capture(step, [r]) for r in reps]
-
-    def run_steps(n):
-        cycles, rem = divmod(n, R)
-        for _ in range(cycles):
-            g_step.replay()
-        for i in range(rem):
-            g_single[i].replay()
+    run = ConfigRun(args.config, w, pkv, torch, dev, stream, args.replicas, args.partition_blocks)
+    R, Tq, B = run.R, run.Tq, w.num_seqs
 
     def barrier():
         if dist is not None:
@@ -750,7 +1010,7 @@ def run_ours(args):
         torch.cuda.synchronize()
 
     with torch.cuda.stream(stream):
-        run_steps(max(args.warmup, 3))
+        run.run_steps(max(args.warmup, 3))
     barrier()
 
     clocks = NvmlClockSampler(torch.cuda.current_device()) if rank == 0 else None
@@ -761,87 +1021,39 @@ def run_ours(args):
     t_wall0 = time.time()
     with torch.cuda.stream(stream):
         e0.record(stream)
-        run_steps(args.steps)
+        run.run_steps(args.steps)
         e1.record(stream)
     barrier()
     t_wall1 = time.time()
     step_ms = e0.elapsed_time(e1) / args.steps
     step_ms_max = reduce_max(step_ms, dist)
-
-    # Kernel-alone timings: decode rows and prefill rows as separate batches
-    # over the same pools, replayed back to back from graphs.
-    def kernel_time(seqs):
-        sub = subset(w, seqs)
-        items = []
-        for r in reps:
-            it = dict(k=r["k"], v=r["v"], q=td(sub["q"]), tables=td(sub["tables"]), ctx=td(sub["ctx"]),
-                      qsl=td(sub["qsl"]), out=torch.empty((sub["q"].shape[0], w.num_q_heads, w.head_dim),
-                                                           dtype=torch.float32, device=dev))
-            if sub["decode"]:
-                n = pkv.decode_workspace_size(len(seqs), w.num_q_heads, w.num_kv_heads, w.head_dim, sub["max_ctx"], pb)
-            else:
-                n = pkv.prefill_workspace_size(len(seqs), sub["q"].shape[0], w.num_q_heads, w.num_kv_heads,
-                                               w.head_dim, sub["max_ctx"])
-            it["ws"] = pkv.new_workspace(n, dev)
-            items.append(it)
-
-        def f(it):
-            if sub["decode"]:
-                pkv.decode_attention(it["k"], it["v"], it["q"], it["tables"], it["ctx"], sub["max_ctx"], scale,
-                                     out=it["out"], workspace=it["ws"], partition_blocks=pb, stream=stream)
-            else:
-                pkv.chunked_prefill_attention(it["k"], it["v"], it["q"], it["qsl"], it["ctx"], it["tables"],
-                                              sub["max_ctx"], scale, out=it["out"], workspace=it["ws"],
-                                              query_start_loc_host=sub["qsl"], stream=stream)
-        with torch.cuda.stream(stream):
-            for it in items:
-                f(it)
-        stream.synchronize()
-        g = capture(f, items)
-        cycles = max(1, min(args.steps // R, 2000))
-        d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            g.replay()
-            d0.record(stream)
-            for _ in range(cycles):
-                g.replay()
-            d1.record(stream)
-        barrier()
-        return d0.elapsed_time(d1) / (cycles * R)
-
-    dec_ms = kernel_time(decode_rows(w)) if len(decode_rows(w)) else None
-    pre_ms = kernel_time(prefill_rows(w)) if len(prefill_rows(w)) else None
-    if clocks:
-        clocks.stop()
-    st = pkv.get_error(stream)
-    if st[0] != 0:
-        raise RuntimeError(f"device error during timing: {st}")
+    run.check("timed steps")
+    ck = clocks.summary(t_wall0, t_wall1) if clocks else {}
 
     # End to end through the public API with pinned host buffers: every step
     # copies all its inputs (one staging buffer, one copy) to the device,
-    # runs the calls and reads the output back.
+    # runs the calls and reads the output back.  As a serving loop does, the
+    # step (its input copy from pinned memory, the calls, the output copy
+    # back) is captured through the same public calls in CUDA graphs and
+    # replayed: one graph per cycle over the replicas, and one per replica
+    # for the remainder.
     e2e_steps = min(args.steps, args.e2e_steps)
-    host_stage = torch.from_numpy(stage_np).pin_memory()
+    host_stage = torch.from_numpy(run.stage_np).pin_memory()
     host_out = torch.empty((Tq, w.num_q_heads, w.head_dim), dtype=torch.float32).pin_memory()
     h2d = host_stage.numel()
     d2h = host_out.numel() * host_out.element_size()
 
     def e2e_step(r):
         r["stage"].copy_(host_stage, non_blocking=True)
-        step(r)
+        run.step(r)
         host_out.copy_(r["out"], non_blocking=True)
 
     with torch.cuda.stream(stream):
         for i in range(3):
-            e2e_step(reps[i % R])
+            e2e_step(run.reps[i % R])
     stream.synchronize()
-    # As a serving loop does, the step (its input copy from pinned memory,
-    # the calls, the output copy back) is captured through the same public
-    # calls in CUDA graphs and replayed: one graph per cycle over the
-    # replicas, as for the device-timed steps, and one per replica for the
-    # remainder.
-    g_e2e_cycle = capture(e2e_step, reps)
-    g_e2e = [capture(e2e_step, [r]) for r in reps]
+    g_e2e_cycle = run.capture(e2e_step, run.reps)
+    g_e2e = [run.capture(e2e_step, [r]) for r in run.reps]
 
     def run_e2e(n):
         cycles, rem = divmod(n, R)
@@ -860,16 +1072,14 @@ def run_ours(args):
         x1.record(stream)
     barrier()
     e2e_ms = reduce_max(x0.elapsed_time(x1) / e2e_steps, dist)
+    run.check("end-to-end steps")
+    del g_e2e_cycle, g_e2e
 
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
         return 0
 
-    B = w.num_seqs
-    hbm, hbm_kind = measured_peaks()
-    tflops_peak, tf_kind = measured_tensor_peak()
-    dbytes = decode_bytes(w)
     line = {
         "metric": METRIC,
         "value": world * B / (step_ms_max * 1e-3),
@@ -885,51 +1095,64 @@ def run_ours(args):
         "data": "synthetic",
         "config": {"workload": w.name, "global_batch": world * B, "seq_len": int(w.context_lens.max()),
                    "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
-                   "l2": f"{R} rotated input replicas of {pool_bytes / 1e6:.0f} MB pools (> 129 MB L2 in total)",
+                   "l2": f"{R} rotated input replicas of {run.pool_bytes / 1e6:.0f} MB pools (> 129 MB L2 in total)",
                    "graph": "CUDA graph per cycle of replicas"},
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": run.launches_per_step * args.steps,
         # query rows (decode rows and prefill tokens) per second over the whole step
         "tokens_per_s": world * Tq / (step_ms_max * 1e-3),
         "e2e": {"value": world * B / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps, "ms_per_step": e2e_ms},
+        "clocks": {"sm_mhz": ck.get("sm_mhz"), "sm_max_mhz": ck.get("sm_max_mhz"),
+                   "reasons": ck.get("reasons", []), "samples": ck.get("samples", 0)},
     }
-    decode_roof = None
-    if dec_ms is not None:
-        achieved = dbytes / (dec_ms * 1e-3) / 1e9
-        traffic = (NCU_TRAFFIC["bytes"] if NCU_TRAFFIC["sources_sha"] == sources_sha() and args.config == CONFIG_ID
-                   else None)
-        decode_roof = {"bound": "hbm", "kernel": "decode_kernel", "achieved": achieved, "peak": hbm,
-                       "peak_kind": f"{hbm_kind} (MEASURED_PEAKS.json hbm_gbs, copy)" if hbm_kind == "measured"
-                       else "fallback", "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
-                       "algorithmic_bytes": dbytes, "avg_launch_us": dec_ms * 1e3}
-    prefill_roof = None
-    if pre_ms is not None:
-        fl = prefill_flops(w)
-        achieved = fl / (pre_ms * 1e-3) / 1e12
-        prefill_roof = {"bound": "tensor", "kernel": "prefill_kernel", "achieved": achieved, "peak": tflops_peak,
-                        "peak_kind": tf_kind, "unit": "TFLOP/s", "frac": achieved / tflops_peak, "traffic": None,
-                        "algorithmic_flops": fl, "avg_launch_us": pre_ms * 1e3}
-    if prefill_roof is not None and (decode_roof is None or pre_ms > dec_ms):
-        line["roofline"] = prefill_roof
-        if decode_roof is not None:
-            line["decode_roofline"] = decode_roof
+
+    # The headline workload's own entry: kernel-alone rooflines, e4m3 decode.
+    head = config_entry(run, hbm, hbm_kind, tpeak, tkind, clocks, cpu=False)
+    dec, pre = head.get("decode"), head.get("prefill")
+    if pre is not None and (dec is None or pre["avg_launch_us"] > dec["avg_launch_us"]):
+        line["roofline"] = pre
+        if dec is not None:
+            line["decode_roofline"] = dec
     else:
-        line["roofline"] = decode_roof
-        if prefill_roof is not None:
-            line["prefill_roofline"] = prefill_roof
-    ck = clocks.summary(t_wall0, t_wall1) if clocks else {}
-    line["clocks"] = {"sm_mhz": ck.get("sm_mhz"), "sm_max_mhz": ck.get("sm_max_mhz"),
-                      "reasons": ck.get("reasons", []), "samples": ck.get("samples", 0)}
+        line["roofline"] = dec
+        if pre is not None:
+            line["prefill_roofline"] = pre
+    line["fp8_decode"] = head.get("fp8_decode")
     line["block_manager"] = block_manager_timing(w, pkv, torch, dev, stream)
     line["prefix_keys"] = prefix_keys_timing(w, pkv, torch, dev, stream)
     line["prefix_cache"] = prefix_cache_timing(w, pkv, torch, dev, stream)
-    line["swap"] = swap_timing(w, pkv, torch, dev, stream, reps)
-    line["fp8_decode"] = fp8_decode_timing(
-        w, pkv, torch, dev, stream, reps, hbm, dec_ms,
-        traffic=(NCU_TRAFFIC_E4M3["bytes"] if NCU_TRAFFIC_E4M3["sources_sha"] == sources_sha()
-                 and args.config == CONFIG_ID else None))
-    if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, args.cpu_budget)
+    line["swap"] = swap_timing(w, pkv, torch, dev, stream, run.reps)
+    run.free()
+    del run
+
+    # Every workload (the headline's entry is the one above).
+    configs = {}
+    sweep = [] if args.sweep == "none" else [int(x) for x in args.sweep.split(",") if x]
+    cpu_on = world == 1 and not args.no_cpu_baseline
+    for k in sweep:
+        if k == args.config:
+            configs[str(k)] = head
+            if cpu_on:
+                clocks.pause(True)
+                head["cpu_baseline"] = cpu_baseline(w, args.cpu_budget)
+                clocks.pause(False)
+            continue
+        wk = build_workload(k)
+        rk = ConfigRun(k, wk, pkv, torch, dev, stream, 0, args.partition_blocks)
+        with torch.cuda.stream(stream):
+            rk.run_steps(max(3, rk.R))
+        stream.synchronize()
+        configs[str(k)] = config_entry(rk, hbm, hbm_kind, tpeak, tkind, clocks, cpu=cpu_on,
+                                       cpu_budget=args.cpu_budget)
+        rk.free()
+        del rk, wk
+    if clocks:
+        clocks.stop()
+    if configs:
+        line["configs"] = configs
+    if cpu_on:
+        own = configs.get(str(args.config))
+        line["cpu_baseline"] = own["cpu_baseline"] if own else cpu_baseline(w, args.cpu_budget)
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
@@ -944,9 +1167,12 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--replicas", type=int, default=0, help="0 = enough pool replicas to exceed 512 MB")
     ap.add_argument("--config", type=int, default=CONFIG_ID, choices=[1, 2, 3, 4, 5],
-                    help="workload (default: the Qwen3-1.7B decode step the metric is quoted on)")
+                    help="headline workload (default: the Qwen3-1.7B decode step the metric is quoted on)")
+    ap.add_argument("--sweep", default="1,2,3,4,5",
+                    help="workloads reported in the `configs` object (comma list, or 'none')")
     ap.add_argument("--e2e-steps", type=int, default=4000)
-    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--cpu-budget", type=float, default=3.0,
+                    help="seconds of one-thread oracle work per sampled step of each workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--partition-blocks", type=int, default=0, help="0 = automatic split-KV partitioning")
     args = ap.parse_args(argv)

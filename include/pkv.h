@@ -197,10 +197,13 @@ size_t pkv_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t 
  *                  256-byte aligned, ZERO-FILLED BEFORE ITS FIRST USE.  Its
  *                  first part (a 256-byte header and one arrival counter per
  *                  (sequence, kv head)) must be zero when a call starts, and
- *                  every call leaves it zero again, so the same workspace
- *                  serves the next call as is; the rest holds split-KV
- *                  partial results and is scratch.  Calls that run
- *                  concurrently need separate workspaces.
+ *                  every call that completes without PKV_ERR_TIMEOUT leaves
+ *                  it zero again, so the same workspace serves the next call
+ *                  as is; the rest holds split-KV partial results and is
+ *                  scratch.  After a call that reported PKV_ERR_TIMEOUT,
+ *                  zero-fill the workspace again before reusing it (a part
+ *                  that gave up may leave its pair's counter raised).  Calls
+ *                  that run concurrently need separate workspaces.
  *   partition_blocks 0 = automatic; > 0 forces the size of a work range in
  *                  units (the workspace must be sized with the same value).
  *   Work is the sequence of units (sequence, kv head, 16-token block) cut
@@ -454,6 +457,19 @@ pkv_status pkv_blocks_release(const pkv_blocks_t* blocks, const int32_t* rows, i
  */
 pkv_status pkv_prefix_keys(const int32_t* token_ids, const int32_t* token_start_loc, const int64_t* extra,
                            const void* parent_keys, int32_t num_seqs, int32_t max_blocks, void* keys, void* stream);
+
+/*
+ * pkv_test_arm_decode_stall -- test hook for the bounded waits; no page
+ * describes it.  The next `launches` decode launches of this process (those
+ * of pkv_decode_attention, pkv_decode_attention_static and the decode rows of
+ * pkv_chunked_prefill_attention, on any device) run with a producer warp that
+ * issues no work: their other warps wait for work descriptors that never
+ * arrive, give up after the bounded wait (2 s), and the launch records
+ * PKV_ERR_TIMEOUT (detail: the wait site).  Nothing is copied or in flight
+ * when they leave; the output is not written and the workspace is left as it
+ * was.  0 disarms.  Returns PKV_ERR_SHAPE for a negative count.
+ */
+pkv_status pkv_test_arm_decode_stall(int32_t launches);
 
 /*
  * pkv_get_error -- synchronise `stream`, then return (and clear) the first

@@ -18,8 +18,7 @@ A plain sequential model of the bookkeeping around the cache:
 - Section 4 ("Prefix cache") of the same blog: blocks of a finished request
   go back to the free queue tail block first.
 
-Readings where the pages leave a step open (each is listed in the design
-notes):
+Readings where the pages leave a step open:
 
 - Sequences of one call are processed in index order.  A holder of a
   shared, partly filled last block copies it when the block's count is above

@@ -6,7 +6,7 @@ leg may import this module.  It shares no code with the CUDA library.
 The pages do not have an fp8 pool; it is the bandwidth-halving variant of
 the cache write and the decode gather that follows from decode being bound
 by reading the whole cache every step ("Prefill/Decode" of the
-inference-engine talk write-up).  Readings (listed in the design notes):
+inference-engine talk write-up).  Readings taken where the pages are silent:
 
 - e4m3 is the OCP 8-bit format with 4 exponent bits (bias 7) and 3 mantissa
   bits, subnormals, no infinities, one NaN pattern per sign (S.1111.111);

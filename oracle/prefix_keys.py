@@ -10,7 +10,7 @@ Because the previous key is part of it, one key stands for the whole prefix
 up to its block: the same 16 tokens after a different prefix get a different
 key.  Only full blocks are keyed.  The default hash is SHA-256.
 
-Readings (listed in the design notes):
+Readings taken where the pages give the parts of a key but not its bytes:
 - the hashed message is parent key (32 bytes) || the block's 16 token ids as
   little-endian int32 (64 bytes) || the sequence's extra value as a
   little-endian int64 (8 bytes), 104 bytes;

@@ -21,7 +21,7 @@ from typing import Optional, Tuple
 __all__ = [
     "PKVError", "lib_path", "load", "version", "status_string", "cache_write", "copy_blocks",
     "decode_workspace_size", "decode_attention", "prefill_workspace_size", "chunked_prefill_attention",
-    "get_error", "Cache", "Blocks", "prefix_keys", "swap_out", "swap_in",
+    "get_error", "Cache", "Blocks", "prefix_keys", "swap_out", "swap_in", "test_arm_decode_stall",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -95,6 +95,7 @@ def load():
         "pkv_prefix_keys": ([P, P, P, P, i32, i32, P, P], ctypes.c_int),
         "pkv_swap_blocks": ([CP, i32, P, P, i32, P, ctypes.c_int64, P], ctypes.c_int),
         "pkv_get_error": ([P, ctypes.POINTER(i32)], ctypes.c_int),
+        "pkv_test_arm_decode_stall": ([i32], ctypes.c_int),
         "pkv_status_string": ([ctypes.c_int], ctypes.c_char_p),
         "pkv_last_cuda_error": ([], ctypes.c_char_p),
         "pkv_version": ([], ctypes.c_char_p),
@@ -461,6 +462,13 @@ class Blocks:
         st = load().pkv_blocks_release(ctypes.byref(self._state()), _dev(rows, "rows", dtype=torch.int32),
                                        int(rows.shape[0]), _stream_handle(stream))
         _check(st, "pkv_blocks_release")
+
+
+def test_arm_decode_stall(launches: int) -> None:
+    """Test hook: the next ``launches`` decode launches time out on purpose
+    (their producer warp issues nothing; the bounded waits of the other warps
+    expire after 2 s and record PKV_ERR_TIMEOUT).  0 disarms."""
+    _check(load().pkv_test_arm_decode_stall(int(launches)), "pkv_test_arm_decode_stall")
 
 
 def get_error(stream=None) -> Tuple[int, int]:

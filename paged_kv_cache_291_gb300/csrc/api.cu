@@ -500,6 +500,12 @@ PKV_API pkv_status pkv_chunked_prefill_attention(const pkv_cache_t* cache, const
     return PKV_OK;
 }
 
+PKV_API pkv_status pkv_test_arm_decode_stall(int32_t launches) {
+    if (launches < 0) return PKV_ERR_SHAPE;
+    pkv::arm_decode_stall(launches);
+    return PKV_OK;
+}
+
 PKV_API pkv_status pkv_get_error(void* stream, int32_t* detail) {
     DeviceState* dev = nullptr;
     pkv_status st = current_device(&dev);

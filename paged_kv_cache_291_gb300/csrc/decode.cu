@@ -51,6 +51,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 
@@ -110,6 +111,7 @@ struct DecodeParams {
     int32_t max_ranges;   // ranges the workspace holds
     float scale_log2;     // softmax scale * log2(e); e4m3 pools: also * k_scale
     float v_scale;        // e4m3 pools: the V pool's scale
+    int32_t stall;        // test hook: the producer issues nothing (see arm_decode_stall)
 };
 
 constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
@@ -1051,7 +1053,9 @@ __global__ void __launch_bounds__(Cfg<D, G, EB>::THREADS, 1) decode_kernel(const
     // Consumer warps read shared memory only and need no wait.
     if (warp == C::PRODUCER_WARP) {
         griddep_wait();
-        run_producer<D, G, EB>(P, smem, B, abort_flag, lane);
+        // Test hook: no descriptor is ever published, so the other warps
+        // leave through their bounded waits; nothing is in flight.
+        if (!P.stall) run_producer<D, G, EB>(P, smem, B, abort_flag, lane);
     } else if (warp == C::MERGER_WARP) {
         prefetch_first_blocks<D, G, EB>(P, lane, C::STAGES);
         griddep_wait();
@@ -1088,7 +1092,20 @@ cudaError_t dispatch_g(const DecodeParams& P, int G, int grid, cudaStream_t stre
     }
 }
 
+// Decode launches still to be made with a stalled producer (test hook).
+std::atomic<int> g_stall_launches{0};
+
+// Takes one armed stall, if any.
+bool take_stall() {
+    int n = g_stall_launches.load();
+    while (n > 0 && !g_stall_launches.compare_exchange_weak(n, n - 1)) {
+    }
+    return n > 0;
+}
+
 }  // namespace
+
+void arm_decode_stall(int32_t launches) { g_stall_launches.store(launches > 0 ? launches : 0); }
 
 static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
@@ -1153,6 +1170,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     P.max_ranges = a.plan.max_ranges;
     P.scale_log2 = a.scale * kLog2e;
     P.v_scale = 1.f;
+    P.stall = take_stall() ? 1 : 0;
     const int G = a.num_q_heads / a.num_kv_heads;
     if (a.kv_e4m3) {
         // q' = q * scale*log2(e) * k_scale against the K codes.

@@ -34,8 +34,8 @@ void* g_scratch_addr[kMaxDevices] = {};
 std::mutex g_scratch_mutex;
 
 // Device address of the scratch array on the current device, looked up once
-// per device with that device current.
-pkv_status scratch_address(void** out) {
+// per device with that device current; also returns the device index.
+pkv_status scratch_address(void** out, int* dev_out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return PKV_ERR_UNSUPPORTED;
@@ -46,6 +46,7 @@ pkv_status scratch_address(void** out) {
         g_scratch_addr[dev] = p;
     }
     *out = g_scratch_addr[dev];
+    *dev_out = dev;
     return PKV_OK;
 }
 
@@ -58,7 +59,13 @@ PKV_API pkv_status pkv_decode_attention_static(const pkv_cache_t* cache, const v
                                                const int32_t* context_lens, int32_t num_seqs,
                                                int32_t max_context_len, float scale, float* out, void* stream) {
     if (cache == nullptr) return PKV_ERR_NULL;
-    if (num_seqs == 0) return PKV_OK;
+    if (num_seqs == 0) {
+        // Nothing to launch, but the arguments are checked exactly as the
+        // regular call checks them (it returns PKV_OK for an empty batch
+        // before it looks at the workspace).
+        return pkv_decode_attention(cache, q, num_q_heads, block_tables, max_blocks_per_seq, context_lens, 0,
+                                    max_context_len, scale, out, nullptr, 0, 0, stream);
+    }
     const size_t need = pkv_decode_workspace_size(num_seqs, num_q_heads, cache->num_kv_heads, cache->head_dim,
                                                   max_context_len, 0);
     if (need == 0) {
@@ -68,13 +75,12 @@ PKV_API pkv_status pkv_decode_attention_static(const pkv_cache_t* cache, const v
     }
     if (need > kScratchBytes) return PKV_ERR_SCRATCH_LIMIT;
     void* scratch = nullptr;
-    pkv_status st = scratch_address(&scratch);
+    int dev = 0;
+    pkv_status st = scratch_address(&scratch, &dev);
     if (st != PKV_OK) return st;
     // Every call shares the array and finds the previous call's contents:
     // clear the counters that must start at zero (the partial results are
     // always written before they are read).
-    int dev = 0;
-    cudaGetDevice(&dev);
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return PKV_ERR_CUDA;
     const pkv::DecodePlan plan = pkv::plan_decode_ranges(num_seqs, cache->num_kv_heads, max_context_len, sms, 0);

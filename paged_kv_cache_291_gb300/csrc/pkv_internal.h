@@ -52,6 +52,10 @@ DecodeWsLayout decode_ws_layout(int32_t num_seqs, int32_t num_q_heads, int32_t n
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 
+// Test hook: the next `launches` decode launches run with a producer warp
+// that issues nothing, so their other warps time out (PKV_ERR_TIMEOUT).
+void arm_decode_stall(int32_t launches);
+
 cudaError_t launch_cache_write(const void* k_new, const void* v_new, const int32_t* slot_mapping, int32_t num_tokens,
                                void* k_pool, void* v_pool, int32_t num_blocks, int32_t num_kv_heads,
                                int32_t head_dim, unsigned long long* err, cudaStream_t stream);

@@ -74,6 +74,10 @@ constexpr int OFF_TMEM = OFF_INFO + 16 * 4;
 constexpr int SMEM_USED = OFF_TMEM + 16;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;         // slack to align the base to 1024 B
 static_assert(SMEM_BYTES <= 232448, "shared memory budget (227 KB)");
+// One CTA per SM: the CTA allocates all 512 TMEM columns, and tcgen05.alloc
+// would wait for a second resident CTA to free them.  A footprint above half
+// of the SM's 228 KB of shared memory rules a second CTA out.
+static_assert(2 * SMEM_BYTES > 228 * 1024, "the 512-column TMEM allocation needs one CTA per SM");
 
 constexpr int kSoftmaxWarps = 4;                     // per unit
 constexpr int kLoadWarp = 8;
