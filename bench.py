@@ -570,9 +570,15 @@ class ConfigRun:
                                               self.maxctx)
         for r in self.reps:
             r["ws"] = pkv.new_workspace(need, dev)
-        self.launches_per_step = (1 if w.copy_src is not None else 0) + 1 + (1 if w.is_decode else 0)
-        if not w.is_decode:
-            self.launches_per_step += (1 if len(decode_rows(w)) else 0) + (1 if len(prefill_rows(w)) else 0)
+        # One new row per sequence at its last position (a plain decode step):
+        # the store and the attention run as one launch (pkv_decode_step).
+        self.fused = bool(w.is_decode and w.copy_src is None and w.slot_mapping.shape[0] == w.num_seqs)
+        if self.fused:
+            self.launches_per_step = 1
+        else:
+            self.launches_per_step = (1 if w.copy_src is not None else 0) + 1 + (1 if w.is_decode else 0)
+            if not w.is_decode:
+                self.launches_per_step += (1 if len(decode_rows(w)) else 0) + (1 if len(prefill_rows(w)) else 0)
         with torch.cuda.stream(stream):
             for r in self.reps:  # eager once (also loads kernels)
                 self.step(r)
@@ -606,6 +612,10 @@ class ConfigRun:
 
     def step(self, r):
         w, pkv, s = self.w, self.pkv, self.stream
+        if self.fused:
+            pkv.decode_step(r["k"], r["v"], r["kn"], r["vn"], r["slots"], r["q"], r["tables"], r["ctx"], self.maxctx,
+                            self.scale, out=r["out"], workspace=r["ws"], partition_blocks=self.pb, stream=s)
+            return
         if w.copy_src is not None:
             pkv.copy_blocks(r["k"], r["v"], r["src"], r["dst"], src_host=w.copy_src, dst_host=w.copy_dst, stream=s)
         pkv.cache_write(r["k"], r["v"], r["kn"], r["vn"], r["slots"], stream=s)
@@ -654,9 +664,11 @@ class ConfigRun:
         return {"mean_ms": statistics.fmean(ms), "median_ms": statistics.median(ms), "min_ms": min(ms),
                 "steps": total, "trials": trials}
 
-    def kernel_alone(self, seqs, kv_e4m3=False, min_launches=200, min_ms=20.0, trials=5, warm_launches=50):
+    def kernel_alone(self, seqs, kv_e4m3=False, fused=False, min_launches=200, min_ms=20.0, trials=5,
+                     warm_launches=50):
         """One attention launch over the sequences `seqs` (decode rows or
-        prefill rows), replayed from graphs over the replicas (bf16 pools) or
+        prefill rows; fused: the whole decode step, the new rows' store
+        included), replayed from graphs over the replicas (bf16 pools) or
         over e4m3 copies of them (kv_e4m3, pools written by the e4m3 store);
         mean over all launches, median and minimum of the trials, and a warm
         figure repeating one replica."""
@@ -688,6 +700,8 @@ class ConfigRun:
                 it = dict(k=k, v=v, q=self.td(sub["q"]), tables=self.td(sub["tables"]), ctx=self.td(sub["ctx"]),
                           qsl=self.td(sub["qsl"]), out=torch.empty((sub["q"].shape[0], w.num_q_heads, d),
                                                                    dtype=torch.float32, device=dev))
+                if fused:
+                    it.update(kn=r["kn"], vn=r["vn"], slots=r["slots"])
                 if sub["decode"]:
                     n = pkv.decode_workspace_size(len(seqs), w.num_q_heads, hkv, d, sub["max_ctx"], self.pb)
                 else:
@@ -698,7 +712,11 @@ class ConfigRun:
         self.stream.synchronize()
 
         def f(it):
-            if sub["decode"]:
+            if fused:
+                pkv.decode_step(it["k"], it["v"], it["kn"], it["vn"], it["slots"], it["q"], it["tables"], it["ctx"],
+                                sub["max_ctx"], self.scale, out=it["out"], workspace=it["ws"],
+                                partition_blocks=self.pb, stream=self.stream, k_scale=ks, v_scale=vs)
+            elif sub["decode"]:
                 pkv.decode_attention(it["k"], it["v"], it["q"], it["tables"], it["ctx"], sub["max_ctx"], self.scale,
                                      out=it["out"], workspace=it["ws"], partition_blocks=self.pb, stream=self.stream,
                                      k_scale=ks, v_scale=vs)
@@ -739,11 +757,20 @@ class ConfigRun:
         self.torch.cuda.empty_cache()
 
 
-def decode_entry(w, t, hbm, hbm_kind, kv_elem_bytes=2, traffic=None):
-    """Roofline record of the decode kernel from a kernel_alone timing."""
-    nbytes = decode_bytes(w, kv_elem_bytes=kv_elem_bytes)
+def new_row_bytes(w, kv_elem_bytes=2) -> int:
+    """Bytes of a step's new-row store: rows read (bf16), rows written
+    (pool elements) and slot ids."""
+    T = w.slot_mapping.shape[0]
+    return T * (w.num_kv_heads * w.head_dim * 2 * (2 + kv_elem_bytes) + 4)
+
+
+def decode_entry(w, t, hbm, hbm_kind, kv_elem_bytes=2, traffic=None, fused=False):
+    """Roofline record of the decode kernel from a kernel_alone timing
+    (fused: the decode step's kernel, the new rows' store included)."""
+    nbytes = decode_bytes(w, kv_elem_bytes=kv_elem_bytes) + (new_row_bytes(w, kv_elem_bytes) if fused else 0)
     achieved = nbytes / (t["mean_us"] * 1e-6) / 1e9
-    rec = {"bound": "hbm", "kernel": "decode_kernel" + (" (e4m3 pools)" if kv_elem_bytes == 1 else ""),
+    name = "decode_kernel" + (" (fused step: new rows' store + attention)" if fused else "")
+    rec = {"bound": "hbm", "kernel": name + (" (e4m3 pools)" if kv_elem_bytes == 1 else ""),
            "achieved": achieved, "peak": hbm,
            "peak_kind": f"{hbm_kind} (MEASURED_PEAKS.json hbm_gbs, copy)" if hbm_kind == "measured" else "fallback",
            "unit": "GB/s", "frac": achieved / hbm, "frac_nominal": achieved / NOMINAL_HBM_GBS,
@@ -751,7 +778,7 @@ def decode_entry(w, t, hbm, hbm_kind, kv_elem_bytes=2, traffic=None):
            "avg_launch_us": t["mean_us"], "median_us": t["median_us"], "min_us": t["min_us"],
            "warm_us": t["warm_us"], "launches": t["launches"], "replicas": t["replicas"],
            "seqs_per_s": len(decode_rows(w)) / (t["mean_us"] * 1e-6)}
-    ub = decode_unique_bytes(w, kv_elem_bytes)
+    ub = decode_unique_bytes(w, kv_elem_bytes) + (new_row_bytes(w, kv_elem_bytes) if fused else 0)
     if ub != nbytes:  # blocks shared between sequences
         rec["unique_bytes"] = ub
         rec["achieved_unique_gbs"] = ub / (t["mean_us"] * 1e-6) / 1e9
@@ -955,9 +982,12 @@ def config_entry(run, hbm, hbm_kind, tpeak, tkind, clocks=None, cpu=True, cpu_bu
              "l2": f"{run.R} rotated input replicas of {run.pool_bytes / 1e6:.0f} MB pools"}
     dec, pre = decode_rows(w), prefill_rows(w)
     dec_t = None
+    if run.fused:
+        entry["decode_step"] = decode_entry(w, run.kernel_alone(dec, fused=True), hbm, hbm_kind,
+                                            traffic=ncu_traffic(run.config, 2), fused=True)
     if len(dec):
         dec_t = run.kernel_alone(dec)
-        entry["decode"] = decode_entry(w, dec_t, hbm, hbm_kind, traffic=ncu_traffic(run.config, 2))
+        entry["decode"] = decode_entry(w, dec_t, hbm, hbm_kind)
     if len(pre):
         entry["prefill"] = prefill_entry(w, run.kernel_alone(pre), tpeak, tkind)
     if len(dec):
@@ -1108,7 +1138,7 @@ def run_ours(args):
 
     # The headline workload's own entry: kernel-alone rooflines, e4m3 decode.
     head = config_entry(run, hbm, hbm_kind, tpeak, tkind, clocks, cpu=False)
-    dec, pre = head.get("decode"), head.get("prefill")
+    dec, pre = head.get("decode_step") or head.get("decode"), head.get("prefill")
     if pre is not None and (dec is None or pre["avg_launch_us"] > dec["avg_launch_us"]):
         line["roofline"] = pre
         if dec is not None:
@@ -1159,6 +1189,33 @@ def run_ours(args):
     return 0
 
 
+def run_ncu_case(args):
+    """A short run for a profiler: the workload's step once, then
+    `--ncu-launches` launches of one kernel (decode, decode_step, prefill or
+    fp8_decode) over one copy of the inputs, no timing loops."""
+    import torch
+
+    import paged_kv_cache_291_gb300 as pkv
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    pkv.load()
+    stream = torch.cuda.Stream(device=dev)
+    w = build_workload(args.config)
+    run = ConfigRun(args.config, w, pkv, torch, dev, stream, 1, args.partition_blocks)
+    dec, pre = decode_rows(w), prefill_rows(w)
+    which = args.ncu_case
+    if which == "decode_step" and not run.fused:
+        raise SystemExit(f"{w.name}: its step is not a plain decode step")
+    seqs = pre if which == "prefill" else dec
+    if not len(seqs):
+        raise SystemExit(f"{w.name} has no rows for {which}")
+    t = run.kernel_alone(seqs, kv_e4m3=which == "fp8_decode", fused=which == "decode_step",
+                         min_launches=args.ncu_launches, min_ms=0.0, trials=1, warm_launches=1)
+    print(json.dumps({"ncu_case": which, "workload": w.name, "launches": t["launches"] + 3,
+                      "mean_us": t["mean_us"]}), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -1175,9 +1232,14 @@ def main(argv=None):
                     help="seconds of one-thread oracle work per sampled step of each workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--partition-blocks", type=int, default=0, help="0 = automatic split-KV partitioning")
+    ap.add_argument("--ncu-case", choices=["decode", "decode_step", "prefill", "fp8_decode"], default=None,
+                    help="a short run of one kernel for a profiler (no timing, no JSON bench line)")
+    ap.add_argument("--ncu-launches", type=int, default=3)
     args = ap.parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.ncu_case:
+        return run_ncu_case(args)
     return run_ours(args)
 
 

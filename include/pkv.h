@@ -221,6 +221,37 @@ pkv_status pkv_decode_attention(const pkv_cache_t* cache, const void* q, int32_t
                                 size_t workspace_bytes, int32_t partition_blocks, void* stream);
 
 /*
+ * pkv_decode_step -- one decode step in one launch: the store of each
+ * sequence's new K/V row (pkv_cache_write) and decode attention over the
+ * context that includes it (pkv_decode_attention).  [ENG] "KV Cache": a
+ * step computes only the new token's column, keeps it, and attends over all
+ * the columns; [KV2] section 2: the new token lands in its sequence's
+ * current (last) block.
+ *
+ *   k_new, v_new   bf16 [num_seqs][num_kv_heads][head_dim]: row s is the new
+ *                  token of sequence s, at position context_lens[s] - 1
+ *   slot_mapping   int32 [num_seqs]: the slot of that position, i.e.
+ *                  block_tables[s][(n-1)/16] * 16 + (n-1) % 16 with
+ *                  n = context_lens[s]; a negative slot skips the store (the
+ *                  pool's row at that position is then used as it is)
+ *   All other arguments, the workspace rules and the result are those of
+ *   pkv_decode_attention; the pools end as pkv_cache_write leaves them.
+ *   The result equals pkv_cache_write(cache, k_new, v_new, slot_mapping,
+ *   num_seqs) followed by pkv_decode_attention(...).  A non-negative slot
+ *   that is not the slot of position n - 1 is not written and raises
+ *   PKV_ERR_RANGE (detail: the sequence); that sequence then attends over
+ *   the pool's row as it is.  The new rows' blocks must not be read by other
+ *   sequences of the batch (they are the sequences' own last blocks, as
+ *   copy-on-write guarantees).  e4m3 pools store code(x * (1/scale)) as
+ *   pkv_cache_write does and attend over those codes.
+ */
+pkv_status pkv_decode_step(const pkv_cache_t* cache, const void* k_new, const void* v_new,
+                           const int32_t* slot_mapping, const void* q, int32_t num_q_heads,
+                           const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* context_lens,
+                           int32_t num_seqs, int32_t max_context_len, float scale, float* out, void* workspace,
+                           size_t workspace_bytes, int32_t partition_blocks, void* stream);
+
+/*
  * pkv_prefill_workspace_size -- bytes of workspace
  * pkv_chunked_prefill_attention needs.  Returns 0 for invalid arguments.
  */

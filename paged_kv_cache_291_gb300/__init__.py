@@ -20,7 +20,8 @@ from typing import Optional, Tuple
 
 __all__ = [
     "PKVError", "lib_path", "load", "version", "status_string", "cache_write", "copy_blocks",
-    "decode_workspace_size", "decode_attention", "prefill_workspace_size", "chunked_prefill_attention",
+    "decode_workspace_size", "decode_attention", "decode_step", "prefill_workspace_size",
+    "chunked_prefill_attention",
     "get_error", "Cache", "Blocks", "prefix_keys", "swap_out", "swap_in", "test_arm_decode_stall",
 ]
 
@@ -83,6 +84,7 @@ def load():
         "pkv_copy_blocks": ([CP, P, P, i32, P, P, P], ctypes.c_int),
         "pkv_decode_workspace_size": ([i32, i32, i32, i32, i32, i32], sz),
         "pkv_decode_attention": ([CP, P, i32, P, i32, P, i32, i32, f32, P, P, sz, i32, P], ctypes.c_int),
+        "pkv_decode_step": ([CP, P, P, P, P, i32, P, i32, P, i32, i32, f32, P, P, sz, i32, P], ctypes.c_int),
         "pkv_prefill_workspace_size": ([i32, i32, i32, i32, i32, i32], sz),
         "pkv_chunked_prefill_attention": ([CP, P, i32, i32, P, P, P, i32, P, i32, i32, f32, P, P, sz, P],
                                           ctypes.c_int),
@@ -259,6 +261,38 @@ def decode_attention(k_pool, v_pool, q, block_tables, context_lens, max_context_
                                   _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
                                   int(partition_blocks), _stream_handle(stream))
     _check(st, "pkv_decode_attention")
+    return out
+
+
+def decode_step(k_pool, v_pool, k_new, v_new, slot_mapping, q, block_tables, context_lens, max_context_len: int,
+                scale: float, out=None, workspace=None, partition_blocks: int = 0, stream=None, k_scale=None,
+                v_scale=None):
+    """One decode step in one launch: store row s of k_new/v_new [B][Hkv][d]
+    at slot_mapping[s] (the slot of position context_lens[s] - 1; negative =
+    skip) and attend over the context; returns ``out`` float32 [B][Hq][d]."""
+    torch = _torch()
+    lib = load()
+    c = _cache(k_pool, v_pool, k_scale, v_scale, need_scales=True)
+    B, hq, d = q.shape
+    if d != c.head_dim:
+        raise ValueError("q head_dim does not match the pools")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.shape[0] != B:
+        raise ValueError("block_tables must be [B][max_blocks] and context_lens [B]")
+    if k_new.shape != (B, c.num_kv_heads, d) or v_new.shape != k_new.shape or slot_mapping.shape[0] != B:
+        raise ValueError("k_new/v_new must be [B][num_kv_heads][head_dim] and slot_mapping [B]")
+    if out is None:
+        out = torch.empty((B, hq, d), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        need = lib.pkv_decode_workspace_size(B, hq, c.num_kv_heads, d, int(max_context_len), int(partition_blocks))
+        workspace = new_workspace(need, q.device)
+    st = lib.pkv_decode_step(ctypes.byref(c), _dev(k_new, "k_new", 2), _dev(v_new, "v_new", 2),
+                             _dev(slot_mapping, "slot_mapping", dtype=torch.int32), _dev(q, "q", 2), hq,
+                             _dev(block_tables, "block_tables", dtype=torch.int32), int(block_tables.shape[1]),
+                             _dev(context_lens, "context_lens", dtype=torch.int32), B, int(max_context_len),
+                             float(scale), _dev(out, "out", dtype=torch.float32), _dev(workspace, "workspace"),
+                             workspace.numel() * workspace.element_size(), int(partition_blocks),
+                             _stream_handle(stream))
+    _check(st, "pkv_decode_step")
     return out
 
 

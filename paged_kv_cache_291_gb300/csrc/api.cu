@@ -380,7 +380,8 @@ pkv_status decode_common(const pkv_cache_t* cache, const void* q, int32_t num_q_
                          const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* context_lens,
                          const int32_t* query_start_loc, int32_t num_seqs, int32_t max_context_len, float scale,
                          float* out, void* workspace, size_t workspace_bytes, int32_t partition_blocks,
-                         void* stream) {
+                         void* stream, const void* k_new = nullptr, const void* v_new = nullptr,
+                         const int32_t* slot_mapping = nullptr) {
     pkv_status st = check_cache(cache);
     if (st != PKV_OK) return st;
     if ((st = check_heads(num_q_heads, cache->num_kv_heads)) != PKV_OK) return st;
@@ -420,6 +421,9 @@ pkv_status decode_common(const pkv_cache_t* cache, const void* q, int32_t num_q_
     a.kv_e4m3 = cache->kv_dtype == PKV_KV_E4M3;
     a.k_scale = cache->k_scale;
     a.v_scale = cache->v_scale;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.slot_mapping = slot_mapping;
     cudaError_t e = pkv::launch_decode(a, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PKV_OK : cuda_fail(e);
 }
@@ -433,6 +437,23 @@ PKV_API pkv_status pkv_decode_attention(const pkv_cache_t* cache, const void* q,
                                         int32_t partition_blocks, void* stream) {
     return decode_common(cache, q, num_q_heads, block_tables, max_blocks_per_seq, context_lens, nullptr, num_seqs,
                          max_context_len, scale, out, workspace, workspace_bytes, partition_blocks, stream);
+}
+
+PKV_API pkv_status pkv_decode_step(const pkv_cache_t* cache, const void* k_new, const void* v_new,
+                                   const int32_t* slot_mapping, const void* q, int32_t num_q_heads,
+                                   const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                   const int32_t* context_lens, int32_t num_seqs, int32_t max_context_len,
+                                   float scale, float* out, void* workspace, size_t workspace_bytes,
+                                   int32_t partition_blocks, void* stream) {
+    pkv_status st = check_cache(cache);
+    if (st != PKV_OK) return st;
+    if (num_seqs > 0) {
+        if (k_new == nullptr || v_new == nullptr || slot_mapping == nullptr) return PKV_ERR_NULL;
+        if (!aligned16(k_new) || !aligned16(v_new)) return PKV_ERR_ALIGN;
+    }
+    return decode_common(cache, q, num_q_heads, block_tables, max_blocks_per_seq, context_lens, nullptr, num_seqs,
+                         max_context_len, scale, out, workspace, workspace_bytes, partition_blocks, stream, k_new,
+                         v_new, slot_mapping);
 }
 
 PKV_API size_t pkv_prefill_workspace_size(int32_t num_seqs, int32_t num_tokens, int32_t num_q_heads,

@@ -59,26 +59,6 @@ __global__ void __launch_bounds__(256) cache_write_kernel(const uint4* __restric
     v_pool[dst] = vv;
 }
 
-// Two fp32 -> two e4m3 codes, lo in the low byte.
-__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
-    uint16_t r;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
-// Eight bf16 (one uint4) times inv -> eight codes (one uint2).
-__device__ __forceinline__ uint2 quantise8(uint4 x, float inv) {
-    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-    uint32_t c[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float lo = __fmul_rn(__uint_as_float(w[i] << 16), inv);
-        const float hi = __fmul_rn(__uint_as_float(w[i] & 0xffff0000u), inv);
-        c[i] = e4m3x2(lo, hi);
-    }
-    return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
-}
-
 // One thread per 8 elements of one (token, kv head) row, K and V.
 __global__ void __launch_bounds__(256) cache_write_e4m3_kernel(
     const uint4* __restrict__ k_new, const uint4* __restrict__ v_new, const int32_t* __restrict__ slot_mapping,

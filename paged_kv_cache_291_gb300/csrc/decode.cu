@@ -95,8 +95,8 @@ struct __align__(16) ItemDesc {
 };
 
 struct DecodeParams {
-    const uint8_t* k_pool;
-    const uint8_t* v_pool;
+    uint8_t* k_pool;  // written only by a fused step (its new rows)
+    uint8_t* v_pool;
     const uint8_t* q;
     const int32_t* block_tables;
     const int32_t* context_lens;
@@ -112,6 +112,13 @@ struct DecodeParams {
     float scale_log2;     // softmax scale * log2(e); e4m3 pools: also * k_scale
     float v_scale;        // e4m3 pools: the V pool's scale
     int32_t stall;        // test hook: the producer issues nothing (see arm_decode_stall)
+    // Fused step (pkv_decode_step): this step's new rows, stored into the
+    // pool by the warp that takes the pair's last block and used from
+    // registers in that block.  k_new == nullptr: plain decode.
+    const uint8_t* k_new;         // bf16 [S][Hkv][D]
+    const uint8_t* v_new;
+    const int32_t* slot_mapping;  // [S]
+    float k_inv, v_inv;           // e4m3 pools: 1 / scale (fp32)
 };
 
 constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
@@ -160,7 +167,8 @@ struct Cfg {
     static constexpr int OFF_WT = OFF_REST + R_WT;
     static constexpr int OFF_BAR = OFF_REST + R_BAR;
     static constexpr int OFF_FLAG = OFF_BAR + NBAR * 8;
-    static constexpr int SMEM = OFF_FLAG + 16;
+    static constexpr int OFF_NEW = OFF_FLAG + 16;  // [STAGES] fused step: slot of a stage's new row, or -1
+    static constexpr int SMEM = OFF_NEW + STAGES * 4;
     static_assert(SW >= 1, "ring too shallow");
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
     static_assert(NV * RPP == kBlockSize, "rows");
@@ -199,6 +207,30 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[NV], int lane) {
 #pragma unroll
     for (; off >= 1; off >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
     return v[0];
+}
+
+// A fused step stores a sequence's new row only at the slot of its last
+// position n - 1: row srow = (n - 1) % 16 of the pair's last block, whose id
+// must lie inside the pool.
+__device__ __forceinline__ bool new_row_fits(int slot, int phys, int srow, int num_blocks) {
+    return slot >= 0 && phys >= 0 && phys < num_blocks && slot == phys * kBlockSize + srow;
+}
+
+// e4m3 pools, fused step: quantise this lane's 8 elements of the new K and V
+// rows (bytes `off` of k_new/v_new), store the codes to the pool (byte `at`)
+// and over the stage's row (kr, V at kr + slab).  Out of line: it runs once
+// per pair and keeps its registers out of the consumers' block loop.
+__device__ __noinline__ void store_new_row_e4m3(const DecodeParams& P, size_t off, size_t at, uint8_t* kr,
+                                                int slab) {
+    const uint2 kc = quantise8(__ldg(reinterpret_cast<const uint4*>(P.k_new + off)), P.k_inv);
+    const uint2 vc = quantise8(__ldg(reinterpret_cast<const uint4*>(P.v_new + off)), P.v_inv);
+    *reinterpret_cast<uint2*>(P.k_pool + at) = kc;
+    *reinterpret_cast<uint2*>(P.v_pool + at) = vc;
+    *reinterpret_cast<uint2*>(kr) = kc;
+    *reinterpret_cast<uint2*>(kr + slab) = vc;
+    // The stage is refilled by bulk copies (async proxy) once the warp
+    // releases it.
+    fence_proxy_async_shared();
 }
 
 // Units of work of one kv head of sequence s: one per 16-token block of its
@@ -377,6 +409,7 @@ __device__ void run_producer(const DecodeParams& P, uint8_t* smem, const Bars& B
                              int lane) {
     using C = Cfg<D, G, EB>;
     ItemDesc* descs = reinterpret_cast<ItemDesc*>(smem + C::OFF_DESC);
+    int* stage_new = reinterpret_cast<int*>(smem + C::OFF_NEW);
     const unsigned FULL = 0xffffffffu;
     // Work is the sequence of units (s, kv head, block), sequences in order,
     // kv heads in order within a sequence, blocks in order within a head.
@@ -476,6 +509,13 @@ __device__ void run_producer(const DecodeParams& P, uint8_t* smem, const Bars& B
         // First batch of table entries, requested before the descriptor work.
         int e = 0;
         if (lane < b1 - b0) e = __ldg(trow + b0 + lane);
+        // Fused step (bf16 pools): the item holds the pair's last block, whose
+        // row srow is the new token; its slot is read now, used when that
+        // block is issued.
+        const bool has_new = P.k_new != nullptr && n > 0 && b1 == nblk && b1 > b0;
+        const int srow = (n - 1) % kBlockSize;
+        int new_slot = -1;
+        if (has_new && lane == 0) new_slot = __ldg(P.slot_mapping + s);
         const uint32_t slot = item_seq % kItemRing;
         if (!mbar_wait_warp(&B.iempty[slot], ((item_seq / kItemRing) & 1) ^ 1)) {
             aborted = true;
@@ -518,6 +558,10 @@ __device__ void run_producer(const DecodeParams& P, uint8_t* smem, const Bars& B
             const uint32_t jw = static_cast<uint32_t>(__shfl_sync(FULL, static_cast<int>(given), w)) +
                                 static_cast<uint32_t>((bl - first_w) / C::W);
             const uint32_t st = static_cast<uint32_t>(w * C::SW) + jw % C::SW;
+            // The lane of this batch (if any) that issues the pair's last block.
+            const int last_lane = has_new ? b1 - 1 - base : -1;
+            int ns = -1;
+            if (last_lane >= 0 && last_lane < cnt) ns = __shfl_sync(FULL, new_slot, 0);
             int bad = 0;
             if (lane < cnt) {
                 int phys = e;
@@ -530,9 +574,32 @@ __device__ void run_producer(const DecodeParams& P, uint8_t* smem, const Bars& B
                 } else {
                     const size_t slab = (static_cast<size_t>(phys) * P.hkv + g) * C::SLAB;
                     uint8_t* dst = smem + st * C::STAGE_BYTES;
-                    mbar_arrive_expect_tx(&B.full[st], 2 * C::SLAB);
-                    bulk_g2s_hint(dst, P.k_pool + slab, C::SLAB, &B.full[st], policy);
-                    bulk_g2s_hint(dst + C::SLAB, P.v_pool + slab, C::SLAB, &B.full[st], policy);
+                    // Tell the consumer whether this stage carries a new row
+                    // (visible to it through the arrive below).
+                    const bool fresh = lane == last_lane && new_row_fits(ns, e, srow, P.num_blocks);
+                    if (P.k_new != nullptr) stage_new[st] = fresh ? ns : -1;
+                    if (lane == last_lane && ns >= 0 && !fresh) {
+                        // A slot other than position n - 1's: reported, not
+                        // written (the pool's row is used as it is).
+                        record_error(P.err, kErrRange, static_cast<uint32_t>(s));
+                    }
+                    if (EB == 2 && fresh) {
+                        // Rows before the new token from the pool, the new
+                        // row from k_new/v_new (rows past it are never read).
+                        constexpr uint32_t kRow = D * EB;
+                        const size_t nr = (static_cast<size_t>(s) * P.hkv + g) * kRow;
+                        mbar_arrive_expect_tx(&B.full[st], 2 * (srow + 1) * kRow);
+                        if (srow > 0) {
+                            bulk_g2s_hint(dst, P.k_pool + slab, srow * kRow, &B.full[st], policy);
+                            bulk_g2s_hint(dst + C::SLAB, P.v_pool + slab, srow * kRow, &B.full[st], policy);
+                        }
+                        bulk_g2s(dst + srow * kRow, P.k_new + nr, kRow, &B.full[st]);
+                        bulk_g2s(dst + C::SLAB + srow * kRow, P.v_new + nr, kRow, &B.full[st]);
+                    } else {
+                        mbar_arrive_expect_tx(&B.full[st], 2 * C::SLAB);
+                        bulk_g2s_hint(dst, P.k_pool + slab, C::SLAB, &B.full[st], policy);
+                        bulk_g2s_hint(dst + C::SLAB, P.v_pool + slab, C::SLAB, &B.full[st], policy);
+                    }
                 }
             }
             if (__any_sync(FULL, bad)) {
@@ -637,6 +704,7 @@ __device__ void run_consumer(const DecodeParams& P, uint8_t* smem, const Bars& B
                              int warp, int lane) {
     using C = Cfg<D, G, EB>;
     const ItemDesc* descs = reinterpret_cast<const ItemDesc*>(smem + C::OFF_DESC);
+    const volatile int* stage_new = reinterpret_cast<const volatile int*>(smem + C::OFF_NEW);
     float2* psm = reinterpret_cast<float2*>(smem + C::OFF_P) + warp * G * kBlockSize;
     float* mo = reinterpret_cast<float*>(smem + C::OFF_MO);
     float2* ml = reinterpret_cast<float2*>(smem + C::OFF_ML);
@@ -680,6 +748,9 @@ __device__ void run_consumer(const DecodeParams& P, uint8_t* smem, const Bars& B
         // item is summed in an order that does not depend on which CTA took
         // it (results are bitwise reproducible).
         const int first = (warp - d.rot + C::W) % C::W;
+        // Fused step: the pair's last block may carry the new token's row
+        // (the producer checked its slot and noted it for the stage).
+        const bool may_have_new = P.k_new != nullptr && d.b1 == (d.n + kBlockSize - 1) / kBlockSize;
         for (int b = first; b < nb; b += C::W) {
             const uint32_t st = static_cast<uint32_t>(warp * C::SW) + taken % C::SW;
             if (*abort_flag || !mbar_wait_warp(&B.full[st], (taken / C::SW) & 1)) {
@@ -688,7 +759,30 @@ __device__ void run_consumer(const DecodeParams& P, uint8_t* smem, const Bars& B
             }
             const int blk = d.b0 + b;
             const int valid = min(kBlockSize, d.n - blk * kBlockSize);
-            const uint8_t* kst = smem + st * C::STAGE_BYTES;
+            uint8_t* kst = smem + st * C::STAGE_BYTES;
+            if (may_have_new && b == nb - 1) {
+                const int ns = stage_new[st];
+                if (ns >= 0) {
+                    // Row srow of this block is the new token: store it to
+                    // the pool.  bf16 pools: the producer placed it in the
+                    // stage.  e4m3 pools: quantise it here and write the
+                    // codes over the stage's row too.
+                    const int srow = ns % kBlockSize;
+                    if (sub == srow % C::RPP) {
+                        const size_t at = (static_cast<size_t>(ns / kBlockSize) * P.hkv + d.g) * C::SLAB +
+                                          static_cast<size_t>(srow) * D * EB + cl * 8 * EB;
+                        uint8_t* kr = kst + srow * D * EB + cl * 8 * EB;
+                        if constexpr (EB == 2) {
+                            *reinterpret_cast<uint4*>(P.k_pool + at) = lds128(kr);
+                            *reinterpret_cast<uint4*>(P.v_pool + at) = lds128(kr + C::SLAB);
+                        } else {
+                            const size_t off = (static_cast<size_t>(d.s) * P.hkv + d.g) * D * 2 + cl * 16;
+                            store_new_row_e4m3(P, off, at, kr, C::SLAB);
+                        }
+                    }
+                    __syncwarp();
+                }
+            }
             compute_block<D, G, EB>(kst, kst + C::SLAB, valid, q2, m, lsum, o2, psm, lane);
             if (lane == 0) mbar_arrive(&B.empty[st]);
             ++taken;
@@ -928,7 +1022,12 @@ __device__ void prefetch_inputs(const DecodeParams& P, int t, int nthr) {
     const long long n_tab = (S * nb * 4 <= kPrefetchCap) ? S * lpr : 0;
     const long long q_bytes = S * P.hq * D * 2;
     const long long n_q = (P.qsl == nullptr && q_bytes <= kPrefetchCap) ? range_lines(q_bytes) : 0;
-    const long long total = n_ctx + n_qsl + n_tab + n_q;
+    // Fused step: the new rows and their slots.
+    const long long kn_bytes = S * P.hkv * D * 2;
+    const long long n_kn = (P.k_new != nullptr && kn_bytes <= kPrefetchCap) ? range_lines(kn_bytes) : 0;
+    const long long n_sl = P.k_new != nullptr ? range_lines(S * 4) : 0;
+    const long long base_new = n_ctx + n_qsl + n_tab + n_q;
+    const long long total = base_new + 2 * n_kn + n_sl;
     const long long step = static_cast<long long>(gridDim.x) * nthr;
     for (long long k = static_cast<long long>(blockIdx.x) * nthr + t; k < total; k += step) {
         const void* a;
@@ -939,8 +1038,14 @@ __device__ void prefetch_inputs(const DecodeParams& P, int t, int nthr) {
         } else if (k < n_ctx + n_qsl + n_tab) {
             const long long j = k - n_ctx - n_qsl;
             a = range_line(P.block_tables + (j / lpr) * P.max_blocks, nb * 4, j % lpr);
-        } else {
+        } else if (k < base_new) {
             a = range_line(P.q, q_bytes, k - n_ctx - n_qsl - n_tab);
+        } else if (k < base_new + n_kn) {
+            a = range_line(P.k_new, kn_bytes, k - base_new);
+        } else if (k < base_new + 2 * n_kn) {
+            a = range_line(P.v_new, kn_bytes, k - base_new - n_kn);
+        } else {
+            a = range_line(P.slot_mapping, S * 4, k - base_new - 2 * n_kn);
         }
         if (a != nullptr) prefetch_l2(a);
     }
@@ -1148,8 +1253,8 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
         decode_ws_layout(a.num_seqs, a.num_q_heads, a.num_kv_heads, a.head_dim, a.plan.max_ranges);
     uint8_t* ws = static_cast<uint8_t*>(a.workspace);
     DecodeParams P;
-    P.k_pool = static_cast<const uint8_t*>(a.k_pool);
-    P.v_pool = static_cast<const uint8_t*>(a.v_pool);
+    P.k_pool = static_cast<uint8_t*>(a.k_pool);
+    P.v_pool = static_cast<uint8_t*>(a.v_pool);
     P.q = static_cast<const uint8_t*>(a.q);
     P.block_tables = a.block_tables;
     P.context_lens = a.context_lens;
@@ -1171,6 +1276,11 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     P.scale_log2 = a.scale * kLog2e;
     P.v_scale = 1.f;
     P.stall = take_stall() ? 1 : 0;
+    P.k_new = static_cast<const uint8_t*>(a.k_new);
+    P.v_new = static_cast<const uint8_t*>(a.v_new);
+    P.slot_mapping = a.slot_mapping;
+    P.k_inv = a.kv_e4m3 ? 1.f / a.k_scale : 1.f;
+    P.v_inv = a.kv_e4m3 ? 1.f / a.v_scale : 1.f;
     const int G = a.num_q_heads / a.num_kv_heads;
     if (a.kv_e4m3) {
         // q' = q * scale*log2(e) * k_scale against the K codes.

@@ -121,6 +121,12 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity) {
     return __all_sync(0xffffffffu, ok);
 }
 
+// Generic-proxy shared-memory writes ordered before later async-proxy
+// (bulk copy) accesses of the same bytes.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ------------------------------------------------------ bulk (TMA) copies
 // 1-D bulk copy global -> shared, completion signalled on `bar` as tx bytes.
 // Both addresses 16-byte aligned, bytes a multiple of 16.
@@ -156,6 +162,29 @@ __device__ __forceinline__ uint2 lds64(const void* p) {
     uint2 v;
     asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(smem_addr(p)));
     return v;
+}
+
+// ---------------------------------------------------------------- e4m3
+// Two fp32 -> two e4m3 codes (nearest, ties to even, saturating to +-448),
+// lo in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Eight bf16 (one uint4) times inv (one fp32 rounding each) -> eight codes
+// (one uint2), element 0 in the lowest byte.
+__device__ __forceinline__ uint2 quantise8(uint4 x, float inv) {
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t c[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float lo = __fmul_rn(__uint_as_float(w[i] << 16), inv);
+        const float hi = __fmul_rn(__uint_as_float(w[i] & 0xffff0000u), inv);
+        c[i] = e4m3x2(lo, hi);
+    }
+    return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
 }
 
 __device__ __forceinline__ float warp_max(float v) {

@@ -22,8 +22,8 @@ DecodePlan plan_decode_ranges(int32_t num_seqs, int32_t num_kv_heads, int32_t ma
 
 // Split-KV decode launch description (everything already validated).
 struct DecodeArgs {
-    const void* k_pool;
-    const void* v_pool;
+    void* k_pool;                  // written only by a fused step (its new rows)
+    void* v_pool;
     const void* q;                 // bf16 rows of [rows][Hq][d]
     const int32_t* block_tables;   // [S][max_blocks]
     const int32_t* context_lens;   // [S]
@@ -37,6 +37,11 @@ struct DecodeArgs {
     float scale;
     bool kv_e4m3;                  // pools hold e4m3 codes (else bf16)
     float k_scale, v_scale;        // e4m3 pools: element = code value * scale
+    // Fused step: each sequence's new row (bf16 [S][Hkv][d]) and its slot,
+    // stored and used in the same launch; all null for plain decode.
+    const void* k_new = nullptr;
+    const void* v_new = nullptr;
+    const int32_t* slot_mapping = nullptr;
 };
 
 struct DecodeWsLayout {
