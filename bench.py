@@ -369,10 +369,10 @@ def oracle_step_seconds(w, seqs, threads):
     seconds.  The pools are copied once, outside the timing (the step is
     idempotent)."""
     import oracle
-    if id(w) not in _ORACLE_POOLS:
+    if _ORACLE_POOLS.get("w") is not w:  # the workload itself is kept, so a new one never matches
         _ORACLE_POOLS.clear()
-        _ORACLE_POOLS[id(w)] = (w.k_pool.copy(), w.v_pool.copy())
-    k, v = _ORACLE_POOLS[id(w)]
+        _ORACLE_POOLS.update(w=w, kv=(w.k_pool.copy(), w.v_pool.copy()))
+    k, v = _ORACLE_POOLS["kv"]
     sub = subset(w, seqs)
     t0 = time.perf_counter()
     if w.copy_src is not None:

@@ -281,11 +281,14 @@ size_t pkv_prefill_workspace_size(int32_t num_seqs, int32_t num_tokens, int32_t 
  *                         decode workspace for the decode rows (its counters
  *                         are left zero, so it is reused as is)
  *   Query rows are computed on tcgen05 tensor cores: Q.K^T in bf16, P.V in
- *   fp16 (P rounded to fp16, V converted from bf16 exactly for
- *   2^-14 <= |v| <= 65504); decode rows take the decode kernel.  A V entry
- *   of a visible key that fp16 cannot hold (|v| > 65504, inf or NaN) raises
- *   PKV_ERR_RANGE (detail: the sequence); the output of that call is then
- *   unspecified.  Takes bf16 pools only (an e4m3 pool: PKV_ERR_DTYPE).
+ *   fp16 (P rounded to fp16, V converted from bf16, exact for 2^-14 <= |v|
+ *   <= 65504); decode rows take the decode kernel.  A tile of 128 query rows
+ *   (of one or two q heads) whose visible V values leave that range (some
+ *   |v| > 65504, or every |v| < 2^-12) is recomputed in the same launch in
+ *   fp32 on CUDA cores, so every finite bf16 V is accepted (|v| up to about
+ *   1e36, where fp32 sums of weighted rows overflow), at a lower speed for
+ *   such tiles.  head_dim 64 or 128.  Takes bf16 pools only (an e4m3 pool:
+ *   PKV_ERR_DTYPE).
  */
 pkv_status pkv_chunked_prefill_attention(const pkv_cache_t* cache, const void* q, int32_t num_q_heads,
                                          int32_t num_tokens, const int32_t* query_start_loc,

@@ -28,8 +28,11 @@
 //    carry all the weight.  The MMA needs V in the same type, so warps 0-7
 //    rewrite each V tile in shared memory from bf16 to fp16 in place, an
 //    eighth each, between their softmax passes (exact for 2^-14 <= |v| <=
-//    65504, absolute error at most 2^-25 below; a larger |v| becomes inf
-//    and is reported as PKV_ERR_RANGE).  l sums P in fp32.
+//    65504, absolute error at most 2^-25 below).  l sums P in fp32.
+//  * A CTA whose visible V values leave that range (some |v| above 65504,
+//    which became inf, or every |v| below 2^-12, mostly fp16 subnormals)
+//    recomputes its rows after the tensor-core pass, in fp32 on CUDA cores.
+//  * head_dim 64 or 128: a tile is one or two 64-dim swizzled panels.
 //  * Online softmax in the log2 domain; the running maximum is only moved
 //    (and O rescaled in TMEM) when it grows by more than 2^8; the final
 //    O / l uses the same reference, so the result is unchanged.
@@ -56,7 +59,7 @@ namespace {
 
 constexpr int kTileM = 128;                          // query rows per unit
 constexpr int kTileN = 128;                          // keys per key tile
-constexpr int kHeadDim = 128;                        // head_dim of the tensor-core path
+constexpr int kMaxHeadDim = 128;                     // head_dim 64 uses the first panel of each tile
 constexpr int kUnits = 2;                            // q heads per CTA (max)
 constexpr int kBlocksPerTile = kTileN / kBlockSize;  // 8
 constexpr int kPanelBytes = 128 * 128;               // 128 rows x 128 B (64 bf16)
@@ -94,6 +97,9 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct PrefillParams {
+    const uint8_t* q;       // bf16 [num_tokens][hq][D] (for the exact fallback)
+    const uint8_t* k_pool;  // bf16 [num_blocks][hkv][16][D] (for the exact fallback)
+    const uint8_t* v_pool;
     const int32_t* block_tables;
     const int32_t* context_lens;
     const int32_t* qsl;
@@ -117,7 +123,7 @@ enum {
 };
 
 // Tile info slots (written by warp 0 before the CTA-wide sync).
-enum { I_S = 0, I_ROW0, I_ROWS, I_PMIN, I_PMAX, I_NT, I_KLAST, I_BAD, I_CTX };
+enum { I_S = 0, I_ROW0, I_ROWS, I_PMIN, I_PMAX, I_NT, I_KLAST, I_BAD, I_CTX, I_VMAX };
 
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
@@ -141,13 +147,75 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x, float& vmax) {
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) { return mbar_wait_warp(bar, parity); }
 
+// Exact fallback of a CTA's rows on CUDA cores (fp32 scores, online softmax
+// in the log2 domain, fp32 P.V), for V values the fp16 tensor-core P.V
+// cannot carry.  Warp w takes the (row, unit) items w, w + 10, ...; lane l
+// owns D/32 consecutive dims of q, K, V and the output; keys go in order,
+// read through the block table.
+template <int D>
+__device__ __noinline__ void redo_rows_exact(const PrefillParams& P, int s, int row0, int rows, int pmin, int h0,
+                                             int units, int g, int warp, int lane) {
+    constexpr int DPL = D / 32;
+    const int32_t* trow = P.block_tables + static_cast<size_t>(s) * P.max_blocks;
+    auto load = [](const uint8_t* p, float (&x)[DPL]) {
+        if constexpr (DPL == 4) {
+            const uint2 u = *reinterpret_cast<const uint2*>(p);
+            x[0] = bf16lo(u.x), x[1] = bf16hi(u.x), x[2] = bf16lo(u.y), x[3] = bf16hi(u.y);
+        } else {
+            const uint32_t u = *reinterpret_cast<const uint32_t*>(p);
+            x[0] = bf16lo(u), x[1] = bf16hi(u);
+        }
+    };
+    for (int item = warp; item < rows * units; item += kThreads / 32) {
+        const int m = item / units, h = h0 + item % units, pos = pmin + m;
+        float q[DPL], o[DPL];
+        load(P.q + ((static_cast<size_t>(row0 + m) * P.hq + h) * D + lane * DPL) * 2, q);
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) {
+            q[i] *= P.scale_log2;
+            o[i] = 0.f;
+        }
+        float mx = -INFINITY, l = 0.f;
+        for (int j = 0; j <= pos; ++j) {
+            int phys = __ldg(trow + j / kBlockSize);
+            if (phys < 0 || phys >= P.num_blocks) phys = 0;  // reported by the tensor-core pass already
+            const size_t at = (((static_cast<size_t>(phys) * P.hkv + g) * kBlockSize + j % kBlockSize) * D +
+                               lane * DPL) * 2;
+            float k[DPL], v[DPL];
+            load(P.k_pool + at, k);
+            load(P.v_pool + at, v);
+            float part = 0.f;
+#pragma unroll
+            for (int i = 0; i < DPL; ++i) part = fmaf(q[i], k[i], part);
+            const float x = warp_sum(part);
+            if (x > mx) {
+                const float alpha = fast_exp2(mx - x);
+                l *= alpha;
+#pragma unroll
+                for (int i = 0; i < DPL; ++i) o[i] *= alpha;
+                mx = x;
+            }
+            const float p = fast_exp2(x - mx);
+            l += p;
+#pragma unroll
+            for (int i = 0; i < DPL; ++i) o[i] = fmaf(p, v[i], o[i]);
+        }
+        float* orow = P.out + (static_cast<size_t>(row0 + m) * P.hq + h) * D + lane * DPL;
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) orow[i] = o[i] / l;
+    }
+}
+
 __device__ __forceinline__ uint32_t tmem_lane_addr(uint32_t base, int warp, uint32_t col) {
     return base + (static_cast<uint32_t>((warp & 3) * 32) << 16) + col;
 }
 
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams P) {
+    static_assert(D == 64 || D == 128, "head_dim");
+    constexpr int kPanels = D / 64;  // 64-dim swizzled panels of a tile
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
@@ -221,6 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             info[I_KLAST] = klast;
             info[I_BAD] = bad;
             info[I_CTX] = ctx;
+            info[I_VMAX] = 0;  // largest |v| the converters see (fp32 bits; non-negative floats order as ints)
         }
     }
     if (threadIdx.x == 32 * kMmaWarp) {
@@ -257,11 +326,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kLoadWarp && nt > 0) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
-            mbar_arrive_expect_tx(&bar[B_QFULL], static_cast<uint32_t>(units) * kTileBytes);
+            mbar_arrive_expect_tx(&bar[B_QFULL], static_cast<uint32_t>(units) * kPanels * kPanelBytes);
             for (int u = 0; u < units; ++u) {
                 uint8_t* dq = smem + OFF_Q + u * kTileBytes;
-                tc::tma_load_3d(dq, &tm_q, 0, h0 + u, row0, &bar[B_QFULL]);
-                tc::tma_load_3d(dq + kPanelBytes, &tm_q, 64, h0 + u, row0, &bar[B_QFULL]);
+#pragma unroll
+                for (int pn = 0; pn < kPanels; ++pn)
+                    tc::tma_load_3d(dq + pn * kPanelBytes, &tm_q, 64 * pn, h0 + u, row0, &bar[B_QFULL]);
             }
         }
         const int32_t* trow = P.block_tables + static_cast<size_t>(s) * P.max_blocks;
@@ -280,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int rowsel[kBlocksPerTile];
 #pragma unroll
             for (int b = 0; b < kBlocksPerTile; ++b) rowsel[b] = (__shfl_sync(FULL, e, b) * P.hkv + g) * kBlockSize;
-            const uint32_t bytes = static_cast<uint32_t>(nvb) * 2 * kBoxBytes;
+            const uint32_t bytes = static_cast<uint32_t>(nvb) * kPanels * kBoxBytes;
             if (!warp_wait(&bar[B_KEMPTY + st], ph ^ 1)) { ok = false; break; }
             if (lane == 0) {
                 mbar_arrive_expect_tx(&bar[B_KFULL + st], bytes);
@@ -288,8 +358,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int b = 0; b < kBlocksPerTile; ++b) {
                     if (b < nvb) {
-                        tc::tma_load_2d(dst + b * kBoxBytes, &tm_k, 0, rowsel[b], &bar[B_KFULL + st]);
-                        tc::tma_load_2d(dst + kPanelBytes + b * kBoxBytes, &tm_k, 64, rowsel[b], &bar[B_KFULL + st]);
+#pragma unroll
+                        for (int pn = 0; pn < kPanels; ++pn)
+                            tc::tma_load_2d(dst + pn * kPanelBytes + b * kBoxBytes, &tm_k, 64 * pn, rowsel[b],
+                                            &bar[B_KFULL + st]);
                     }
                 }
             }
@@ -301,8 +373,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int b = 0; b < kBlocksPerTile; ++b) {
                     if (b < nvb) {
-                        tc::tma_load_2d(dst + b * kBoxBytes, &tm_v, 0, rowsel[b], &bar[B_VFULL + sv]);
-                        tc::tma_load_2d(dst + kPanelBytes + b * kBoxBytes, &tm_v, 64, rowsel[b], &bar[B_VFULL + sv]);
+#pragma unroll
+                        for (int pn = 0; pn < kPanels; ++pn)
+                            tc::tma_load_2d(dst + pn * kPanelBytes + b * kBoxBytes, &tm_v, 64 * pn, rowsel[b],
+                                            &bar[B_VFULL + sv]);
                     }
                 }
             }
@@ -311,13 +385,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kMmaWarp && nt > 0) {
         // ------------------------------------------------------ MMA issuer
         constexpr uint32_t kIdescQK = tc::idesc_bf16_f32(kTileM, kTileN, 0, 0);
-        constexpr uint32_t kIdescPV = tc::idesc_f16_f32(kTileM, kHeadDim, 0, 1);
+        constexpr uint32_t kIdescPV = tc::idesc_f16_f32(kTileM, D, 0, 1);
         // S_u = Q_u K^T for K tile j into the unit's S/P columns.
         auto qk = [&](int u, int j) {
             const uint32_t sq = smem_addr(smem + OFF_Q + u * kTileBytes);
             const uint32_t sk = smem_addr(smem + OFF_K + (j & 1) * kTileBytes);
 #pragma unroll
-            for (int k = 0; k < kHeadDim / 16; ++k) {
+            for (int k = 0; k < D / 16; ++k) {
                 const uint32_t off = (k >> 2) * kPanelBytes + (k & 3) * 32;
                 tc::mma_bf16_ss(tmem + col_s(u), tc::smem_desc_sw128(sq + off, 16, 1024),
                                 tc::smem_desc_sw128(sk + off, 16, 1024), kIdescQK, k > 0 ? 1u : 0u);
@@ -388,11 +462,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto convert_v = [&](int j) -> bool {
             const int sv = j % kVStages;
             if (!warp_wait(&bar[B_VFULL + sv], (j / kVStages) & 1)) return false;
-            const uint32_t base = smem_addr(smem + OFF_V + sv * kTileBytes) + static_cast<uint32_t>(warp) * 4096u;
+            constexpr int kChunksPerWarp = kPanels * kPanelBytes / 16 / kConvWarps;  // 16-byte chunks
+            const uint32_t base = smem_addr(smem + OFF_V + sv * kTileBytes) +
+                                  static_cast<uint32_t>(warp) * (kChunksPerWarp * 16u);
             const int nrows = (j == nt - 1) ? klast : kTileN;
 #pragma unroll
-            for (int n = 0; n < 8; ++n) {
-                const int i = warp * 256 + n * 32 + lane;  // chunk of the tile
+            for (int n = 0; n < kChunksPerWarp / 32; ++n) {
+                const int i = warp * kChunksPerWarp + n * 32 + lane;  // chunk of the tile
                 const uint32_t a = base + static_cast<uint32_t>(n * 32 + lane) * 16u;
                 if (((i >> 3) & (kTileN - 1)) < nrows) {
                     uint32_t x[4];
@@ -500,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (rescale) {
 #pragma unroll
-                for (int c = 0; c < kHeadDim / 32; ++c) {
+                for (int c = 0; c < D / 32; ++c) {
                     uint32_t r[32];
                     const uint32_t ta = tmem_lane_addr(tmem, warp, col_o(u) + 32 * c);
                     tc::tmem_ld32(ta, r);
@@ -522,9 +598,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::fence_after_sync();
                 const float inv = 1.f / (((l2[0].x + l2[0].y) + (l2[1].x + l2[1].y)) +
                                          ((l2[2].x + l2[2].y) + (l2[3].x + l2[3].y)));
-                float* orow = P.out + (static_cast<size_t>(row0 + m) * P.hq + h) * kHeadDim;
+                float* orow = P.out + (static_cast<size_t>(row0 + m) * P.hq + h) * D;
 #pragma unroll
-                for (int c = 0; c < kHeadDim / 32; ++c) {
+                for (int c = 0; c < D / 32; ++c) {
                     uint32_t r[32];
                     tc::tmem_ld32(tmem_lane_addr(tmem, warp, col_o(u) + 32 * c), r);
                     tc::tmem_wait_ld();
@@ -538,12 +614,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         } else if (bad && s >= 0 && m < rows) {
-            float* orow = P.out + (static_cast<size_t>(row0 + m) * P.hq + h) * kHeadDim;
-            for (int c = 0; c < kHeadDim; c += 4) *reinterpret_cast<float4*>(orow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+            float* orow = P.out + (static_cast<size_t>(row0 + m) * P.hq + h) * D;
+            for (int c = 0; c < D; c += 4) *reinterpret_cast<float4*>(orow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
         }
-        // A V entry beyond the fp16 range (inf included) became inf.
-        if (vmax > 65504.f) record_error(P.err, kErrRange, static_cast<uint32_t>(s));
+        // The CTA's largest visible |v|, for the range check after the loop.
+        const float wmax = warp_max(vmax);
+        if (lane == 0) atomicMax(reinterpret_cast<unsigned int*>(&info[I_VMAX]), __float_as_uint(wmax));
     }
     if (!ok) record_error(P.err, kErrTimeout, 0x100u + static_cast<uint32_t>(warp));
     // ---------------------------------------------------------- teardown
@@ -551,6 +628,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc::fence_after_sync();
     if (warp == kLoadWarp) tc::tmem_dealloc(tmem, kTmemCols);
+    // V values outside the range where the fp16 P.V holds the tolerance (a
+    // visible |v| above 65504 became inf; if every |v| is below 2^-12 most
+    // of them are fp16 subnormals): recompute this CTA's rows exactly.
+    const float cta_vmax = __uint_as_float(static_cast<unsigned int>(info[I_VMAX]));
+    if (nt > 0 && !bad && (cta_vmax > 65504.f || cta_vmax < 0x1p-12f)) {
+        const bool all_ok = __syncthreads_and(ok);
+        if (all_ok) redo_rows_exact<D>(P, s, row0, rows, pmin, h0, units, g, warp, lane);
+    }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -581,7 +666,7 @@ bool make_map(CUtensorMap* map, const void* base, cuuint32_t rank, const cuuint6
 }  // namespace
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
-    if (a.head_dim != kHeadDim) return cudaErrorNotSupported;
+    if (a.head_dim != 64 && a.head_dim != kMaxHeadDim) return cudaErrorNotSupported;
     if (a.num_tiles == 0) return cudaSuccess;
     CUtensorMap tq, tk, tv;
     {
@@ -601,6 +686,9 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
         if (!make_map(&tv, a.v_pool, 2, dims, strides, box)) return cudaErrorInvalidValue;
     }
     PrefillParams P;
+    P.q = static_cast<const uint8_t*>(a.q);
+    P.k_pool = static_cast<const uint8_t*>(a.k_pool);
+    P.v_pool = static_cast<const uint8_t*>(a.v_pool);
     P.block_tables = a.block_tables;
     P.context_lens = a.context_lens;
     P.qsl = a.query_start_loc;
@@ -617,16 +705,18 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
     // Two q heads per CTA when a GQA group holds an even number of them.
     P.units = ((a.num_q_heads / a.num_kv_heads) % 2 == 0) ? 2 : 1;
     P.scale_log2 = a.scale * kLog2e;
-    static bool configured[64] = {};
+    auto kernel = a.head_dim == 64 ? prefill_kernel<64> : prefill_kernel<kMaxHeadDim>;
+    static bool configured[2][64] = {};
+    const int which = a.head_dim == 64 ? 0 : 1;
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (dev >= 0 && dev < 64 && !configured[which][dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        configured[dev] = true;
+        configured[which][dev] = true;
     }
     dim3 grid(static_cast<unsigned>(a.num_tiles), static_cast<unsigned>(a.num_q_heads / P.units));
-    return launch_overlapped(prefill_kernel, grid, dim3(kThreads), SMEM_BYTES, stream, tq, tk, tv, P);
+    return launch_overlapped(kernel, grid, dim3(kThreads), SMEM_BYTES, stream, tq, tk, tv, P);
 }
 
 }  // namespace pkv

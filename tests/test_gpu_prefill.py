@@ -85,12 +85,19 @@ def test_chunked_equals_one_shot_on_gpu(pkv):
     assert_close(chunked.cpu().numpy(), ref, "chunked")
 
 
-def test_prefill_head_dim_64_is_rejected_cleanly(pkv):
-    w = W.make_paged("d64", 5, 8, 2, 64, [40], [20])
-    ds = DeviceStep(w)
-    with pytest.raises(pkv.PKVError) as e:
-        ds.run(pkv)
-    assert e.value.status == 12
+def test_prefill_head_dim_64_mixed_batch(pkv):
+    """The Llama-3.2-1B attention shape (32 q / 8 kv heads, head_dim 64) in a
+    mixed batch: chunks on the tensor cores (one 64-dim panel per tile),
+    decode rows beside them."""
+    w = W.make_paged("llama1b mixed", 64, 32, 8, 64, [300, 40, 700, 1, 513, 17], [150, 1, 300, 1, 129, 1])
+    run_and_check(pkv, w)
+
+
+@pytest.mark.parametrize("hq,hkv,qlen,prefix", [(8, 8, 128, 0), (16, 4, 129, 15), (8, 1, 200, 17),
+                                                (16, 8, 2, 1024)])
+def test_prefill_head_dim_64_edges(pkv, hq, hkv, qlen, prefix):
+    w = W.make_paged("d64 edge", 640 + hq + hkv + qlen, hq, hkv, 64, [prefix + qlen, 33], [qlen, 1])
+    run_and_check(pkv, w)
 
 
 def _bf16(x):
@@ -131,14 +138,33 @@ def test_prefill_dominant_keys_and_tiny_weights(pkv):
     run_and_check(pkv, w)
 
 
-def test_prefill_v_beyond_fp16_range_reports_range_error(pkv):
-    """A V entry of a visible key that fp16 cannot hold (|v| > 65504) is
-    reported as PKV_ERR_RANGE (detail: the sequence), without a fault."""
+def test_prefill_v_beyond_fp16_range_is_exact(pkv):
+    """A V entry of a visible key that fp16 cannot hold (|v| > 65504): the
+    CTA recomputes its rows exactly, with no error."""
     w = W.make_paged("v-range", 32, 16, 8, 128, [300], [200])
     blk, row = _pool_index(w, 0, 5)
     w.v_pool[blk, 3, row, 7] = _bf16(70000.0)
+    run_and_check(pkv, w)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("log2_scale", [17, -20])
+def test_prefill_v_magnitudes(pkv, d, log2_scale):
+    """Every V value multiplied by 2^17 (|v| up to ~5e5, beyond fp16) or by
+    2^-20 (|v| ~1e-6, fp16 subnormals): scaling V by a power of two scales the
+    exact result by the same power, so the output divided by it is held to
+    the usual tolerance against the oracle's, with no error reported."""
+    w = W.make_paged("v-scale", 90 + d + log2_scale, 16, 8, d, [700, 40, 300], [300, 1, 129])
+    f = np.float32(2.0 ** log2_scale)
+
+    def scaled(bits):  # exact for every finite bf16 value here; the NaN poison stays NaN
+        return W._f32_to_bf16_bits((bits.astype(np.uint32) << 16).view(np.float32) * f)
+
+    w.v_pool[:] = scaled(w.v_pool)
+    w.v_new[:] = scaled(w.v_new)
     ds = DeviceStep(w)
-    ds.run(pkv)
+    out = ds.run(pkv)
     torch.cuda.synchronize()
-    assert pkv.get_error() == (9, 0)
     assert pkv.get_error() == (0, 0)
+    _, _, ref = oracle.run_step(w, threads=16)
+    assert_close(out.cpu().numpy() / float(f), ref / float(f), f"V x 2^{log2_scale}")
