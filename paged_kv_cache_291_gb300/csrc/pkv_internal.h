@@ -56,6 +56,8 @@ DecodeWsLayout decode_ws_layout(int32_t num_seqs, int32_t num_q_heads, int32_t n
                                 int32_t max_ranges);
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+// The fused step's variant (a.k_new set), called by launch_decode.
+cudaError_t launch_decode_fused(const DecodeArgs& a, bool stall, cudaStream_t stream);
 
 // Test hook: the next `launches` decode launches run with a producer warp
 // that issues nothing, so their other warps time out (PKV_ERR_TIMEOUT).

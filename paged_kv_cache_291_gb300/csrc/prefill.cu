@@ -147,11 +147,21 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x, float& vmax) {
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) { return mbar_wait_warp(bar, parity); }
 
+// Compensated fp32 sum (Neumaier): s + c carries the sum of the added
+// terms to about one rounding of the largest of them, so small terms added
+// to a large accumulator are not lost.
+__device__ __forceinline__ void sum2(float& s, float& c, float y) {
+    const float t = __fadd_rn(s, y);
+    c = __fadd_rn(c, fabsf(s) >= fabsf(y) ? __fadd_rn(__fsub_rn(s, t), y) : __fadd_rn(__fsub_rn(y, t), s));
+    s = t;
+}
+
 // Exact fallback of a CTA's rows on CUDA cores (fp32 scores, online softmax
-// in the log2 domain, fp32 P.V), for V values the fp16 tensor-core P.V
-// cannot carry.  Warp w takes the (row, unit) items w, w + 10, ...; lane l
-// owns D/32 consecutive dims of q, K, V and the output; keys go in order,
-// read through the block table.
+// in the log2 domain whose reference moves only when the maximum grows by
+// more than 2^8, compensated fp32 sums for P.V and the row sum), for V values
+// the fp16 tensor-core P.V cannot carry.  Warp w takes the (row, unit) items
+// w, w + 10, ...; lane l owns D/32 consecutive dims of q, K, V and the
+// output; keys go in order, read through the block table.
 template <int D>
 __device__ __noinline__ void redo_rows_exact(const PrefillParams& P, int s, int row0, int rows, int pmin, int h0,
                                              int units, int g, int warp, int lane) {
@@ -168,14 +178,15 @@ __device__ __noinline__ void redo_rows_exact(const PrefillParams& P, int s, int 
     };
     for (int item = warp; item < rows * units; item += kThreads / 32) {
         const int m = item / units, h = h0 + item % units, pos = pmin + m;
-        float q[DPL], o[DPL];
+        float q[DPL], o[DPL], oc[DPL];
         load(P.q + ((static_cast<size_t>(row0 + m) * P.hq + h) * D + lane * DPL) * 2, q);
 #pragma unroll
         for (int i = 0; i < DPL; ++i) {
             q[i] *= P.scale_log2;
             o[i] = 0.f;
+            oc[i] = 0.f;
         }
-        float mx = -INFINITY, l = 0.f;
+        float mx = -INFINITY, l = 0.f, lc = 0.f;
         for (int j = 0; j <= pos; ++j) {
             int phys = __ldg(trow + j / kBlockSize);
             if (phys < 0 || phys >= P.num_blocks) phys = 0;  // reported by the tensor-core pass already
@@ -188,21 +199,26 @@ __device__ __noinline__ void redo_rows_exact(const PrefillParams& P, int s, int 
 #pragma unroll
             for (int i = 0; i < DPL; ++i) part = fmaf(q[i], k[i], part);
             const float x = warp_sum(part);
-            if (x > mx) {
+            if (x > mx + kRescaleThreshold) {
                 const float alpha = fast_exp2(mx - x);
                 l *= alpha;
+                lc *= alpha;
 #pragma unroll
-                for (int i = 0; i < DPL; ++i) o[i] *= alpha;
+                for (int i = 0; i < DPL; ++i) {
+                    o[i] *= alpha;
+                    oc[i] *= alpha;
+                }
                 mx = x;
             }
             const float p = fast_exp2(x - mx);
-            l += p;
+            sum2(l, lc, p);
 #pragma unroll
-            for (int i = 0; i < DPL; ++i) o[i] = fmaf(p, v[i], o[i]);
+            for (int i = 0; i < DPL; ++i) sum2(o[i], oc[i], __fmul_rn(p, v[i]));
         }
+        const float lt = l + lc;
         float* orow = P.out + (static_cast<size_t>(row0 + m) * P.hq + h) * D + lane * DPL;
 #pragma unroll
-        for (int i = 0; i < DPL; ++i) orow[i] = o[i] / l;
+        for (int i = 0; i < DPL; ++i) orow[i] = (o[i] + oc[i]) / lt;
     }
 }
 
