@@ -48,15 +48,16 @@ CONFIG_ID = 2  # the Qwen3-1.7B decode step (34 sequences x 640 tokens)
 NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal (the measured copy bandwidth is the roofline)
 L2_ROTATE_BYTES = 512 << 20
 
-# DRAM traffic of one decode launch on a workload from an ncu capture
+# DRAM traffic of one launch of a kernel on a workload from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), with the hash of the kernel
 # sources it was taken on; reported only while the sources still match.
-# Keys: (config, pool element bytes).
+# Keys: (kernel entry, config).
 NCU_TRAFFIC = {
-    (2, 2): {"bytes": 91992576, "sources_sha": "ce493bad71d6d71f"},
-    (2, 1): {"bytes": 44818432, "sources_sha": "ce493bad71d6d71f"},
+    ("decode_step", 2): {"bytes": 91886080, "sources_sha": "d71b593ebff90b04"},
+    ("decode", 4): {"bytes": 18808320, "sources_sha": "d71b593ebff90b04"},
 }
-KERNEL_SOURCES = ["paged_kv_cache_291_gb300/csrc/decode.cu", "paged_kv_cache_291_gb300/csrc/pkv_device.cuh"]
+KERNEL_SOURCES = ["paged_kv_cache_291_gb300/csrc/decode_kernel.cuh", "paged_kv_cache_291_gb300/csrc/decode.cu",
+                  "paged_kv_cache_291_gb300/csrc/decode_fused.cu", "paged_kv_cache_291_gb300/csrc/pkv_device.cuh"]
 
 
 def sources_sha() -> str:
@@ -67,8 +68,8 @@ def sources_sha() -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(config, elem_bytes):
-    rec = NCU_TRAFFIC.get((config, elem_bytes))
+def ncu_traffic(kernel, config):
+    rec = NCU_TRAFFIC.get((kernel, config))
     return rec["bytes"] if rec is not None and rec["sources_sha"] == sources_sha() else None
 
 
@@ -159,90 +160,110 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(rows)}
 
 
+def _nvml_poll(bus, conn, dense, paused, stop):
+    """Child process: poll the SM clock and the clock-event reasons of the
+    GPU at PCI bus id `bus` through read-only NVML queries, every half
+    millisecond (back to back while `dense` is set), until `stop`; then send
+    the (time, MHz, reasons) samples back.  A process of its own, so that
+    polling never competes with the benchmark's launches for the GIL."""
+    import ctypes
+    out = []
+    try:
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByPciBusId_v2(bus, ctypes.byref(h)) != 0:
+            raise OSError("no NVML handle")
+        fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        mx = ctypes.c_uint()
+        lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))  # 1 = NVML_CLOCK_SM
+        conn.send(("max", float(mx.value)))
+        while not stop.is_set():
+            if paused.is_set():
+                time.sleep(0.01)
+                continue
+            if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and fn(h, ctypes.byref(rs)) == 0:
+                out.append((time.time(), float(clk.value), int(rs.value)))
+            if not dense.is_set():
+                time.sleep(0.0005)
+    except (OSError, AttributeError) as e:
+        conn.send(("error", str(e)))
+    conn.send(("samples", out))
+    conn.close()
+
+
 class NvmlClockSampler:
     """SM clock and clock-event reasons polled through NVML (read-only
     queries: nvmlDeviceGetClockInfo, nvmlDeviceGetMaxClockInfo,
-    nvmlDeviceGetCurrentClocksEventReasons) every half millisecond while the
-    timed region runs, so that even a region of a few milliseconds has
-    samples.  The device is matched by PCI bus id.  Falls back to
-    nvidia-smi sampling when NVML cannot be loaded."""
+    nvmlDeviceGetCurrentClocksEventReasons) in a child process, every half
+    millisecond, back to back during the headline's timed region, so that
+    even a region of a few hundred microseconds has samples.  The device is
+    matched by PCI bus id.  Falls back to nvidia-smi sampling when NVML
+    cannot be used."""
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
                0x80: "hw_power_brake_slowdown"}
 
     def __init__(self, device: int):
-        import ctypes
+        import multiprocessing as mp
 
         import torch
         self.samples = []
-        self._stop = threading.Event()
-        self._paused = threading.Event()
-        self._dense = threading.Event()
-        self._thr = None
+        self.max_mhz = None
         self.fallback = None
-        try:
-            lib = ctypes.CDLL("libnvidia-ml.so.1")
-            if lib.nvmlInit_v2() != 0:
-                raise OSError("nvmlInit failed")
-            pr = torch.cuda.get_device_properties(device)
-            bus = f"{pr.pci_domain_id:08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0".encode()
-            h = ctypes.c_void_p()
-            if lib.nvmlDeviceGetHandleByPciBusId_v2(bus, ctypes.byref(h)) != 0:
-                raise OSError("no NVML handle for " + bus.decode())
-            self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
-                lib.nvmlDeviceGetCurrentClocksThrottleReasons
-            self.lib, self.h, self.ct = lib, h, ctypes
-            mx = ctypes.c_uint()
-            lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))  # 1 = NVML_CLOCK_SM
-            self.max_mhz = float(mx.value)
-        except (OSError, AttributeError, RuntimeError):
-            self.lib = None
-            self.fallback = ClockSampler(device)
-
-    def _poll(self):
-        ct, lib, h = self.ct, self.lib, self.h
-        clk, rs = ct.c_uint(), ct.c_ulonglong()
-        while not self._stop.is_set():
-            if self._paused.is_set():
-                time.sleep(0.01)
-                continue
-            ok = lib.nvmlDeviceGetClockInfo(h, 1, ct.byref(clk)) == 0 and self.reasons_fn(h, ct.byref(rs)) == 0
-            if ok:
-                self.samples.append((time.time(), float(clk.value), int(rs.value)))
-            if not self._dense.is_set():
-                time.sleep(0.0005)
+        pr = torch.cuda.get_device_properties(device)
+        bus = f"{pr.pci_domain_id:08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0".encode()
+        ctx = mp.get_context("spawn")  # CUDA is initialised in this process: never fork it
+        self._dense, self._paused, self._stop = ctx.Event(), ctx.Event(), ctx.Event()
+        self._conn, child = ctx.Pipe(duplex=False)
+        self._proc = ctx.Process(target=_nvml_poll, args=(bus, child, self._dense, self._paused, self._stop),
+                                 daemon=True)
+        self.gpu_index = device
 
     def start(self):
-        if self.lib is None:
-            self.fallback.start()
-            return
-        self._thr = threading.Thread(target=self._poll, daemon=True)
-        self._thr.start()
-        time.sleep(0.01)
+        try:
+            self._proc.start()
+            if self._conn.poll(30):
+                kind, val = self._conn.recv()
+                if kind == "max":
+                    self.max_mhz = val
+                    return
+        except (EOFError, OSError):
+            pass
+        self._stop.set()
+        self._proc.join(timeout=5)
+        self.fallback = ClockSampler(self.gpu_index)
+        self.fallback.start()
 
     def dense(self, on: bool):
         """Poll back to back (on=True), for a timed region of a few hundred
         microseconds."""
-        if on:
-            self._dense.set()
-        else:
-            self._dense.clear()
+        (self._dense.set if on else self._dense.clear)()
+        time.sleep(0.002)
 
     def pause(self, on: bool):
         """Stop polling (on=True) while the host cores run something timed."""
-        if on:
-            self._paused.set()
-        else:
-            self._paused.clear()
+        (self._paused.set if on else self._paused.clear)()
 
     def stop(self):
-        if self.lib is None:
+        if self.fallback is not None:
             self.fallback.stop()
             return
         self._stop.set()
-        self._thr.join(timeout=2)
+        try:
+            while self._conn.poll(30):
+                kind, val = self._conn.recv()
+                if kind == "samples":
+                    self.samples = val
+                    break
+        except (EOFError, OSError):
+            pass
+        self._proc.join(timeout=10)
 
     def summary(self, t0: float, t1: float):
-        if self.lib is None:
+        if self.fallback is not None:
             return self.fallback.summary(t0, t1)
         rows = [(mhz, rs) for ts, mhz, rs in self.samples if t0 <= ts <= t1]
         if not rows:
@@ -994,20 +1015,20 @@ def config_entry(run, hbm, hbm_kind, tpeak, tkind, clocks=None, cpu=True, cpu_bu
     dec_t = None
     if run.fused:
         entry["decode_step"] = decode_entry(w, run.kernel_alone(dec, fused=True), hbm, hbm_kind,
-                                            traffic=ncu_traffic(run.config, 2), fused=True)
+                                            traffic=ncu_traffic("decode_step", run.config), fused=True)
     if len(dec):
         dec_t = run.kernel_alone(dec)
-        entry["decode"] = decode_entry(w, dec_t, hbm, hbm_kind)
+        entry["decode"] = decode_entry(w, dec_t, hbm, hbm_kind, traffic=ncu_traffic("decode", run.config))
     if len(pre):
         entry["prefill"] = prefill_entry(w, run.kernel_alone(pre), tpeak, tkind)
     if len(dec):
         t8 = run.kernel_alone(dec, kv_e4m3=True)
-        e8 = decode_entry(w, t8, hbm, hbm_kind, kv_elem_bytes=1, traffic=ncu_traffic(run.config, 1))
+        e8 = decode_entry(w, t8, hbm, hbm_kind, kv_elem_bytes=1, traffic=ncu_traffic("fp8_decode", run.config))
         e8["speedup_vs_bf16"] = dec_t["mean_us"] / t8["mean_us"]
         e8["scales"] = "k_scale = v_scale = 1/64, pools written by the e4m3 store"
         entry["fp8_decode"] = e8
     if clocks is not None:
-        entry["clocks"] = clocks.summary(t0, time.time())
+        entry["clocks"] = (t0, time.time())  # summarised once the sampler has stopped
     if cpu:
         if clocks is not None:
             clocks.pause(True)
@@ -1072,7 +1093,6 @@ def run_ours(args):
     step_ms = e0.elapsed_time(e1) / args.steps
     step_ms_max = reduce_max(step_ms, dist)
     run.check("timed steps")
-    ck = clocks.summary(t_wall0, t_wall1) if clocks else {}
 
     # End to end through the public API with pinned host buffers: every step
     # copies all its inputs (one staging buffer, one copy) to the device,
@@ -1146,8 +1166,6 @@ def run_ours(args):
         "tokens_per_s": world * Tq / (step_ms_max * 1e-3),
         "e2e": {"value": world * B / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps, "ms_per_step": e2e_ms},
-        "clocks": {"sm_mhz": ck.get("sm_mhz"), "sm_max_mhz": ck.get("sm_max_mhz"),
-                   "reasons": ck.get("reasons", []), "samples": ck.get("samples", 0)},
     }
 
     # The headline workload's own entry: kernel-alone rooflines, e4m3 decode.
@@ -1192,6 +1210,12 @@ def run_ours(args):
         del rk, wk
     if clocks:
         clocks.stop()
+        ck = clocks.summary(t_wall0, t_wall1)
+        line["clocks"] = {"sm_mhz": ck.get("sm_mhz"), "sm_max_mhz": ck.get("sm_max_mhz"),
+                          "reasons": ck.get("reasons", []), "samples": ck.get("samples", 0)}
+        for entry in configs.values():
+            if isinstance(entry.get("clocks"), tuple):
+                entry["clocks"] = clocks.summary(*entry["clocks"])
     if configs:
         line["configs"] = configs
     if cpu_on:
