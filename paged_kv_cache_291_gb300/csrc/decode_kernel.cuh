@@ -755,8 +755,8 @@ __device__ __forceinline__ void store_stage_new_row(const DecodeParams& P, const
 // S lands as keys {g, g+8} x heads {2t, 2t+1}, the heads of the lane's O
 // columns as well, so the online softmax needs no data movement; P goes to
 // the B layout (head g, keys 2t, 2t+1, 2t+8, 2t+9) by shuffles.  P is split
-// into a hi and a lo part (P.V runs twice), which keeps it to about 2^-17
-// relative.  bf16 pools use bf16 MMAs on the raw bf16 K, V and q; e4m3 pools
+// into a hi and a lo part (P.V runs twice), which keeps it to 2^-18
+// relative (bf16) or 2^-22 (f16).  bf16 pools use bf16 MMAs on the raw bf16 K, V and q; e4m3 pools
 // widen codes to f16 (exact) and use f16 MMAs, with q scaled by a power of
 // two per head (exact) into [1, 2) for f16.  Rows past the context are
 // masked in S and zeroed in V (0 x NaN would poison the sum).
@@ -797,8 +797,8 @@ __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
     return r;
 }
 
-// (lo, hi) of a pair of probabilities as 16-bit MMA operands: hi carries
-// the leading bits, lo the rounded rest, so hi + lo = p to ~2^-17.
+// A pair of probabilities as two 16-bit MMA operands: hi is p rounded, lo
+// the rounded rest, so hi + lo = p to 2^-18 relative (bf16) or 2^-22 (f16).
 template <bool F16>
 __device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi, uint32_t& lo) {
     if constexpr (F16) {
@@ -806,10 +806,8 @@ __device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi, uint3
         const float2 h = f16x2_to_float2(hi);
         lo = f16x2_rn(a - h.x, b - h.y);
     } else {
-        // bf16: hi is the truncated top half (exact), lo the rounded rest.
-        const uint32_t ua = __float_as_uint(a) & 0xFFFF0000u, ub = __float_as_uint(b) & 0xFFFF0000u;
-        hi = (ua >> 16) | ub;
-        lo = bf16x2_rn(a - __uint_as_float(ua), b - __uint_as_float(ub));
+        hi = bf16x2_rn(a, b);
+        lo = bf16x2_rn(a - bf16lo(hi), b - bf16hi(hi));
     }
 }
 
