@@ -66,13 +66,16 @@ namespace pkv {
 
 namespace {
 
-// Block math of the consumer warps: warp-level MMAs (run_consumer_mma), or
-// packed fp32 FMAs on the CUDA cores (run_consumer) in a build with
-// PKV_DECODE_CUDA_CORES defined.
-#ifdef PKV_DECODE_CUDA_CORES
-constexpr bool kConsumerMma = false;
-#else
+// Block math of the consumer warps: packed fp32 FMAs on the CUDA cores
+// (run_consumer), or warp-level MMAs (run_consumer_mma) in a build with
+// PKV_DECODE_MMA defined.  The MMA variant issues about 2.5x fewer
+// instructions per block, but its fragment layouts read the same bank group
+// of several 256-byte key rows at once (the slabs are unswizzled 1-D copies),
+// and it measured slower on every bandwidth-bound workload.
+#ifdef PKV_DECODE_MMA
 constexpr bool kConsumerMma = true;
+#else
+constexpr bool kConsumerMma = false;
 #endif
 
 // Consumer warps per CTA.  MMA block math: 8 (a block costs a warp few
