@@ -66,33 +66,20 @@ namespace pkv {
 
 namespace {
 
-// Block math of the consumer warps: packed fp32 FMAs on the CUDA cores
-// (run_consumer), or warp-level MMAs (run_consumer_mma) in a build with
-// PKV_DECODE_MMA defined.  The MMA variant issues about 2.5x fewer
-// instructions per block, but its fragment layouts read the same bank group
-// of several 256-byte key rows at once (the slabs are unswizzled 1-D copies),
-// and it measured slower on every bandwidth-bound workload.
-#ifdef PKV_DECODE_MMA
-constexpr bool kConsumerMma = true;
-#else
-constexpr bool kConsumerMma = false;
-#endif
-
-// Consumer warps per CTA.  MMA block math: 8 (a block costs a warp few
-// instructions, and 8 warps leave each thread the registers its fragments
-// need).  CUDA-core block math: 12 for head groups of 1 or 2 (their per-lane
-// state is small, and a fourth warp per scheduler hides more of the latency
-// of the dependent shuffle and FMA chains), 8 for groups of 4 and 8 (which
-// need more than the 128 registers a thread that 14 warps leave); e4m3
-// pools (EB = 1) with groups of 1 or 2 take 16: their blocks cost more issue
+// Consumer warps per CTA: 12 for head groups of 1 or 2 (their per-lane state
+// is small, and a fourth warp per scheduler hides more of the latency of the
+// dependent shuffle and FMA chains), 8 for groups of 4 and 8 (which need
+// more than the 128 registers a thread that 14 warps leave).  e4m3 pools
+// (EB = 1) with groups of 1 or 2 take 16: their blocks cost more issue
 // (the widening) and half the ring bytes, so the same ring still gives each
-// warp 3 stages.  A build can force one count with PKV_DECODE_CONSUMER_WARPS.
+// warp 3 stages.  A build can force one count for every group with
+// PKV_DECODE_CONSUMER_WARPS.
 template <int G, int EB>
 constexpr int consumer_warps() {
 #ifdef PKV_DECODE_CONSUMER_WARPS
     return PKV_DECODE_CONSUMER_WARPS;
 #else
-    return kConsumerMma ? 8 : (G <= 2 ? (EB == 1 ? 16 : 12) : 8);
+    return G <= 2 ? (EB == 1 ? 16 : 12) : 8;
 #endif
 }
 constexpr int kItemRing = 8;
@@ -714,6 +701,34 @@ __device__ void run_producer(const DecodeParams& P, uint8_t* smem, const Bars& B
                 if (sl < item_seq) mbar_wait(&B.ifull[sl], ((item_seq - 1 - sl) / kItemRing) & 1);
         }
     }
+}
+
+// Fused step: if the producer noted a new row (slot ns >= 0) for this stage,
+// row srow = ns % 16 of the block is the new token: store it to the pool.
+// bf16 pools: the producer placed it in the stage.  e4m3 pools: quantise it
+// here and write the codes over the stage's row too.  Lane (sub, cl) moves
+// 8 elements (the lane layout of a K/V row in compute_block).
+template <int D, int G, int EB>
+__device__ __forceinline__ void store_stage_new_row(const DecodeParams& P, const ItemDesc& d, uint8_t* kst, int ns,
+                                                    int lane) {
+    using C = Cfg<D, G, EB>;
+    if (ns < 0) return;
+    const int sub = lane / C::LPR;
+    const int cl = lane % C::LPR;
+    const int srow = ns % kBlockSize;
+    if (sub == srow % C::RPP) {
+        const size_t at = (static_cast<size_t>(ns / kBlockSize) * P.hkv + d.g) * C::SLAB +
+                          static_cast<size_t>(srow) * D * EB + cl * 8 * EB;
+        uint8_t* kr = kst + srow * D * EB + cl * 8 * EB;
+        if constexpr (EB == 2) {
+            *reinterpret_cast<uint4*>(P.k_pool + at) = lds128(kr);
+            *reinterpret_cast<uint4*>(P.v_pool + at) = lds128(kr + C::SLAB);
+        } else {
+            const size_t off = (static_cast<size_t>(d.s) * P.hkv + d.g) * D * 2 + cl * 16;
+            store_new_row_e4m3(P, off, at, kr, C::SLAB);
+        }
+    }
+    __syncwarp();
 }
 
 // Fused step: if the producer noted a new row (slot ns >= 0) for this stage,
@@ -1511,10 +1526,7 @@ __global__ void __launch_bounds__(Cfg<D, G, EB>::THREADS, 1) decode_kernel(const
         run_merger<D, G, EB>(P, smem, B, abort_flag, lane);
     } else {
         prefetch_inputs<D, FUSED>(P, threadIdx.x, C::W * 32);
-        if constexpr (kConsumerMma)
-            run_consumer_mma<D, G, EB, FUSED>(P, smem, B, abort_flag, warp, lane);
-        else
-            run_consumer<D, G, EB, FUSED>(P, smem, B, abort_flag, warp, lane);
+        run_consumer<D, G, EB, FUSED>(P, smem, B, abort_flag, warp, lane);
     }
 }
 
