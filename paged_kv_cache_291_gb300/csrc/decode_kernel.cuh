@@ -731,355 +731,6 @@ __device__ __forceinline__ void store_stage_new_row(const DecodeParams& P, const
     __syncwarp();
 }
 
-// Fused step: if the producer noted a new row (slot ns >= 0) for this stage,
-// row srow = ns % 16 of the block is the new token: store it to the pool.
-// bf16 pools: the producer placed it in the stage.  e4m3 pools: quantise it
-// here and write the codes over the stage's row too.  Lane (sub, cl) moves
-// 8 elements (the lane layout of a K/V row in compute_block).
-template <int D, int G, int EB>
-__device__ __forceinline__ void store_stage_new_row(const DecodeParams& P, const ItemDesc& d, uint8_t* kst, int ns,
-                                                    int lane) {
-    using C = Cfg<D, G, EB>;
-    if (ns < 0) return;
-    const int sub = lane / C::LPR;
-    const int cl = lane % C::LPR;
-    const int srow = ns % kBlockSize;
-    if (sub == srow % C::RPP) {
-        const size_t at = (static_cast<size_t>(ns / kBlockSize) * P.hkv + d.g) * C::SLAB +
-                          static_cast<size_t>(srow) * D * EB + cl * 8 * EB;
-        uint8_t* kr = kst + srow * D * EB + cl * 8 * EB;
-        if constexpr (EB == 2) {
-            *reinterpret_cast<uint4*>(P.k_pool + at) = lds128(kr);
-            *reinterpret_cast<uint4*>(P.v_pool + at) = lds128(kr + C::SLAB);
-        } else {
-            const size_t off = (static_cast<size_t>(d.s) * P.hkv + d.g) * D * 2 + cl * 16;
-            store_new_row_e4m3(P, off, at, kr, C::SLAB);
-        }
-    }
-    __syncwarp();
-}
-
-// ---------------------------------------------------------------- MMA consumers
-// The consumers' per-block math on warp-level tensor-core MMAs (mma.sync
-// m16n8k16, fp32 accumulators): per 16-row block, S = K q^T (16 keys x 8 head
-// columns, the group's G heads and zero columns) and O^T += V^T P^T (16 dims
-// x 8 heads per MMA).  Lane (g, t) = (lane / 4, lane % 4) holds the MMA
-// fragments.  The contractions are sums, so their order may be permuted:
-//  * q.K^T: k-slot pair (2t, 2t+1) of k-step kk is dims t*D/4 + 4kk + {0, 1}
-//    and pair (2t+8, 2t+9) is dims t*D/4 + 4kk + {2, 3}, so a lane reads one
-//    contiguous D/4-dim span of key rows g and g+8;
-//  * P.V: MMA mm's rows g and g+8 are dims g*D/8 + 2mm and + 1, so a lane
-//    reads one contiguous D/8-dim span of key rows 2t, 2t+1, 2t+8, 2t+9.
-// S lands as keys {g, g+8} x heads {2t, 2t+1}, the heads of the lane's O
-// columns as well, so the online softmax needs no data movement; P goes to
-// the B layout (head g, keys 2t, 2t+1, 2t+8, 2t+9) by shuffles.  P is split
-// into a hi and a lo part (P.V runs twice), which keeps it to 2^-18
-// relative (bf16) or 2^-22 (f16).  bf16 pools use bf16 MMAs on the raw bf16 K, V and q; e4m3 pools
-// widen codes to f16 (exact) and use f16 MMAs, with q scaled by a power of
-// two per head (exact) into [1, 2) for f16.  Rows past the context are
-// masked in S and zeroed in V (0 x NaN would poison the sum).
-template <bool F16>
-__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-    if constexpr (F16) {
-        asm volatile(
-            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-            "{%0, %1, %2, %3};"
-            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-    } else {
-        asm volatile(
-            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-            "{%0, %1, %2, %3};"
-            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-    }
-}
-
-// Two e4m3 codes (low 16 bits of w) -> f16x2, exact.
-__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t w) {
-    uint32_t h;
-    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, lo;\n\t}" : "=r"(h) : "r"(w));
-    return h;
-}
-
-// Two floats -> f16x2 / bf16x2 (round to nearest even), lo in the low half.
-__device__ __forceinline__ uint32_t f16x2_rn(float lo, float hi) {
-    uint32_t r;
-    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
-    uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
-// A pair of probabilities as two 16-bit MMA operands: hi is p rounded, lo
-// the rounded rest, so hi + lo = p to 2^-18 relative (bf16) or 2^-22 (f16).
-template <bool F16>
-__device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi, uint32_t& lo) {
-    if constexpr (F16) {
-        hi = f16x2_rn(a, b);
-        const float2 h = f16x2_to_float2(hi);
-        lo = f16x2_rn(a - h.x, b - h.y);
-    } else {
-        hi = bf16x2_rn(a, b);
-        lo = bf16x2_rn(a - bf16lo(hi), b - bf16hi(hi));
-    }
-}
-
-template <int D, int G, int EB>
-__device__ __forceinline__ void compute_block_mma(const uint8_t* kst, const uint8_t* vst, int valid,
-                                                  const uint32_t (&qb)[D / 8], float f0, float f1, float& m0,
-                                                  float& m1, float& l0, float& l1, float (&o)[D / 16][4],
-                                                  int lane) {
-    constexpr bool F16 = EB == 1;
-    const unsigned FULL = 0xffffffffu;
-    const int g = lane >> 2, t = lane & 3;
-    // ---- S = K q^T
-    float s[4] = {0.f, 0.f, 0.f, 0.f};
-    {
-        const uint8_t* k0 = kst + g * D * EB + t * (D / 4) * EB;
-        const uint8_t* k8 = k0 + 8 * D * EB;
-        if constexpr (EB == 2) {
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {  // 8 dims (two k-steps) per 16-byte chunk
-                const uint4 r0 = lds128(k0 + 16 * c), r8 = lds128(k8 + 16 * c);
-                mma16816<false>(s, r0.x, r8.x, r0.y, r8.y, qb[4 * c], qb[4 * c + 1]);
-                mma16816<false>(s, r0.z, r8.z, r0.w, r8.w, qb[4 * c + 2], qb[4 * c + 3]);
-            }
-        } else {
-#pragma unroll
-            for (int c = 0; c < D / 64; ++c) {  // 16 codes (four k-steps) per 16-byte chunk
-                const uint4 r0 = lds128(k0 + 16 * c), r8 = lds128(k8 + 16 * c);
-                const uint32_t w0[4] = {r0.x, r0.y, r0.z, r0.w}, w8[4] = {r8.x, r8.y, r8.z, r8.w};
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const int kk = 4 * c + w;
-                    mma16816<true>(s, e4m3x2_f16x2(w0[w]), e4m3x2_f16x2(w8[w]), e4m3x2_f16x2(w0[w] >> 16),
-                                   e4m3x2_f16x2(w8[w] >> 16), qb[2 * kk], qb[2 * kk + 1]);
-                }
-            }
-        }
-    }
-    // ---- online softmax (log2 domain) on keys {g, g+8} x heads {2t, 2t+1}
-    const bool vg = g < valid, vg8 = g + 8 < valid;
-    const float x00 = vg ? s[0] * f0 : -INFINITY, x01 = vg ? s[1] * f1 : -INFINITY;
-    const float x10 = vg8 ? s[2] * f0 : -INFINITY, x11 = vg8 ? s[3] * f1 : -INFINITY;
-    float mb0 = fmaxf(x00, x10), mb1 = fmaxf(x01, x11);
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-        mb0 = fmaxf(mb0, __shfl_xor_sync(FULL, mb0, off));
-        mb1 = fmaxf(mb1, __shfl_xor_sync(FULL, mb1, off));
-    }
-    // The reference moves only when the block's maximum exceeds it by more
-    // than 2^8, so P stays below 256 and O is rescaled on few blocks.
-    if (mb0 > m0 + kRescaleThreshold) {
-        const float a = fast_exp2(m0 - mb0);
-        l0 *= a;
-#pragma unroll
-        for (int mm = 0; mm < D / 16; ++mm) o[mm][0] *= a, o[mm][2] *= a;
-        m0 = mb0;
-    }
-    if (mb1 > m1 + kRescaleThreshold) {
-        const float a = fast_exp2(m1 - mb1);
-        l1 *= a;
-#pragma unroll
-        for (int mm = 0; mm < D / 16; ++mm) o[mm][1] *= a, o[mm][3] *= a;
-        m1 = mb1;
-    }
-    const float p00 = fast_exp2(x00 - m0), p01 = fast_exp2(x01 - m1);
-    const float p10 = fast_exp2(x10 - m0), p11 = fast_exp2(x11 - m1);
-    l0 += p00 + p10;
-    l1 += p01 + p11;
-    // ---- P^T in the B layout: head g, keys (2t, 2t+1) and (2t+8, 2t+9).
-    // Key 2t of head g sits in lane 8t + g/2 (key 2t+1: + 4), as element
-    // g % 2 of its (key, key+8) pair.
-    uint32_t x0h, x0l, x1h, x1l;  // (key g, key g+8) of heads 2t and 2t+1
-    split_pair<F16>(p00, p10, x0h, x0l);
-    split_pair<F16>(p01, p11, x1h, x1l);
-    const int la = 8 * t + (g >> 1), lb = la + 4;
-    const bool odd = g & 1;
-    uint32_t ah = __shfl_sync(FULL, x0h, la), ah1 = __shfl_sync(FULL, x1h, la);
-    uint32_t bh = __shfl_sync(FULL, x0h, lb), bh1 = __shfl_sync(FULL, x1h, lb);
-    uint32_t al = __shfl_sync(FULL, x0l, la), al1 = __shfl_sync(FULL, x1l, la);
-    uint32_t bl = __shfl_sync(FULL, x0l, lb), bl1 = __shfl_sync(FULL, x1l, lb);
-    if (odd) ah = ah1, bh = bh1, al = al1, bl = bl1;
-    const uint32_t ph0 = __byte_perm(ah, bh, 0x5410), ph1 = __byte_perm(ah, bh, 0x7632);
-    const uint32_t pl0 = __byte_perm(al, bl, 0x5410), pl1 = __byte_perm(al, bl, 0x7632);
-    // ---- O^T += V^T P^T over this lane's dims g*D/8 .. + D/8
-    const int key0 = 2 * t, key2 = 2 * t + 8;
-    const uint8_t* vr = vst + (g * (D / 8)) * EB;
-    if constexpr (EB == 2) {
-        // Rows 2t, 2t+1, 2t+8, 2t+9; word j holds dims +2j, +2j+1 (MMA j).
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c) {  // 8 dims per 16-byte chunk
-            uint4 ra = lds128(vr + key0 * D * 2 + 16 * c), rb = lds128(vr + (key0 + 1) * D * 2 + 16 * c);
-            uint4 rc = lds128(vr + key2 * D * 2 + 16 * c), rd = lds128(vr + (key2 + 1) * D * 2 + 16 * c);
-            if (key0 >= valid) ra = make_uint4(0u, 0u, 0u, 0u);
-            if (key0 + 1 >= valid) rb = make_uint4(0u, 0u, 0u, 0u);
-            if (key2 >= valid) rc = make_uint4(0u, 0u, 0u, 0u);
-            if (key2 + 1 >= valid) rd = make_uint4(0u, 0u, 0u, 0u);
-            const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w}, wb[4] = {rb.x, rb.y, rb.z, rb.w};
-            const uint32_t wc[4] = {rc.x, rc.y, rc.z, rc.w}, wd[4] = {rd.x, rd.y, rd.z, rd.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int mm = 4 * c + j;
-                const uint32_t a0 = __byte_perm(wa[j], wb[j], 0x5410), a1 = __byte_perm(wa[j], wb[j], 0x7632);
-                const uint32_t a2 = __byte_perm(wc[j], wd[j], 0x5410), a3 = __byte_perm(wc[j], wd[j], 0x7632);
-                mma16816<false>(o[mm], a0, a1, a2, a3, ph0, ph1);
-                mma16816<false>(o[mm], a0, a1, a2, a3, pl0, pl1);
-            }
-        }
-    } else {
-        // Rows 2t, 2t+1, 2t+8, 2t+9; word i holds dims +4i .. +4i+3 (MMAs 2i, 2i+1).
-        constexpr int NW = D / 32;  // 32-bit words of D/8 codes
-        uint32_t wa[NW], wb[NW], wc[NW], wd[NW];
-        if constexpr (NW == 4) {
-            const uint4 ra = lds128(vr + key0 * D), rb = lds128(vr + (key0 + 1) * D);
-            const uint4 rc = lds128(vr + key2 * D), rd = lds128(vr + (key2 + 1) * D);
-            wa[0] = ra.x, wa[1] = ra.y, wa[2] = ra.z, wa[3] = ra.w;
-            wb[0] = rb.x, wb[1] = rb.y, wb[2] = rb.z, wb[3] = rb.w;
-            wc[0] = rc.x, wc[1] = rc.y, wc[2] = rc.z, wc[3] = rc.w;
-            wd[0] = rd.x, wd[1] = rd.y, wd[2] = rd.z, wd[3] = rd.w;
-        } else {
-            const uint2 ra = lds64(vr + key0 * D), rb = lds64(vr + (key0 + 1) * D);
-            const uint2 rc = lds64(vr + key2 * D), rd = lds64(vr + (key2 + 1) * D);
-            wa[0] = ra.x, wa[1] = ra.y, wb[0] = rb.x, wb[1] = rb.y;
-            wc[0] = rc.x, wc[1] = rc.y, wd[0] = rd.x, wd[1] = rd.y;
-        }
-#pragma unroll
-        for (int i = 0; i < NW; ++i) {
-            if (key0 >= valid) wa[i] = 0u;
-            if (key0 + 1 >= valid) wb[i] = 0u;
-            if (key2 >= valid) wc[i] = 0u;
-            if (key2 + 1 >= valid) wd[i] = 0u;
-            const uint32_t ab0 = __byte_perm(wa[i], wb[i], 0x5140), ab1 = __byte_perm(wa[i], wb[i], 0x7362);
-            const uint32_t cd0 = __byte_perm(wc[i], wd[i], 0x5140), cd1 = __byte_perm(wc[i], wd[i], 0x7362);
-            const uint32_t a0 = e4m3x2_f16x2(ab0), a1 = e4m3x2_f16x2(ab0 >> 16);
-            const uint32_t a2 = e4m3x2_f16x2(cd0), a3 = e4m3x2_f16x2(cd0 >> 16);
-            mma16816<true>(o[2 * i], a0, a1, a2, a3, ph0, ph1);
-            mma16816<true>(o[2 * i], a0, a1, a2, a3, pl0, pl1);
-            const uint32_t b0 = e4m3x2_f16x2(ab1), b1 = e4m3x2_f16x2(ab1 >> 16);
-            const uint32_t b2 = e4m3x2_f16x2(cd1), b3 = e4m3x2_f16x2(cd1 >> 16);
-            mma16816<true>(o[2 * i + 1], b0, b1, b2, b3, ph0, ph1);
-            mma16816<true>(o[2 * i + 1], b0, b1, b2, b3, pl0, pl1);
-        }
-    }
-}
-
-// Consumer warps with MMA block math: the item loop of run_consumer, with
-// the q fragments, softmax state and O held in the MMA layouts above.
-template <int D, int G, int EB, bool FUSED>
-__device__ void run_consumer_mma(const DecodeParams& P, uint8_t* smem, const Bars& B, volatile int* abort_flag,
-                                 int warp, int lane) {
-    using C = Cfg<D, G, EB>;
-    constexpr int QW = D / 8;  // q words (two elements each) of a lane: its D/4 dims
-    const unsigned FULL = 0xffffffffu;
-    const ItemDesc* descs = reinterpret_cast<const ItemDesc*>(smem + C::OFF_DESC);
-    const volatile int* stage_new = reinterpret_cast<const volatile int*>(smem + C::OFF_NEW);
-    float* mo = reinterpret_cast<float*>(smem + C::OFF_MO);
-    float2* ml = reinterpret_cast<float2*>(smem + C::OFF_ML);
-    const int g = lane >> 2, t = lane & 3;
-    uint32_t taken = 0, item_seq = 0;
-    bool ok = true;
-    while (ok) {
-        const uint32_t slot = item_seq % kItemRing;
-        if (*abort_flag || !mbar_wait_warp(&B.ifull[slot], (item_seq / kItemRing) & 1)) {
-            ok = false;
-            break;
-        }
-        const ItemDesc d = descs[slot];
-        if (d.s < 0) break;
-        // q of head g, dims t*D/4 .. + D/4, as B fragments (zero for g >= G).
-        uint32_t qb[QW];
-        float f0 = P.scale_log2, f1 = P.scale_log2;  // score factors of heads 2t, 2t+1
-        {
-            const uint8_t* qs = smem + C::OFF_ITEMQ + slot * C::QBYTES + (g * D + t * (D / 4)) * 2;
-#pragma unroll
-            for (int c = 0; c < QW / 4; ++c) {
-                uint4 u = make_uint4(0u, 0u, 0u, 0u);
-                if (g < G) u = lds128(qs + 16 * c);
-                qb[4 * c] = u.x, qb[4 * c + 1] = u.y, qb[4 * c + 2] = u.z, qb[4 * c + 3] = u.w;
-            }
-            if constexpr (EB == 1) {
-                // f16 MMAs: scale head g's q by 2^-e into [1, 2) (exact), and
-                // give the scores the factor 2^e back.
-                float mx = 0.f;
-#pragma unroll
-                for (int i = 0; i < QW; ++i) mx = fmaxf(mx, fmaxf(fabsf(bf16lo(qb[i])), fabsf(bf16hi(qb[i]))));
-                mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 1));
-                mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 2));
-                int e = (mx >= 0x1p-100f && mx < INFINITY) ? static_cast<int>((__float_as_uint(mx) >> 23) & 0xFF) - 127
-                                                             : 0;
-                e = min(e, 100);  // |q| up to 2^101 (f16 would overflow beyond)
-                const float down = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e
-                const float up = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);    // 2^e
-#pragma unroll
-                for (int i = 0; i < QW; ++i) qb[i] = f16x2_rn(bf16lo(qb[i]) * down, bf16hi(qb[i]) * down);
-                f0 = P.scale_log2 * __shfl_sync(FULL, up, (8 * t) & 31);
-                f1 = P.scale_log2 * __shfl_sync(FULL, up, (8 * t + 4) & 31);
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&B.iempty[slot]);
-        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-        float o[D / 16][4];
-#pragma unroll
-        for (int mm = 0; mm < D / 16; ++mm) o[mm][0] = o[mm][1] = o[mm][2] = o[mm][3] = 0.f;
-        const int nb = d.b1 - d.b0;
-        const int first = (warp - d.rot + C::W) % C::W;  // see run_consumer
-        const bool may_have_new = FUSED && d.b1 == (d.n + kBlockSize - 1) / kBlockSize;
-        for (int b = first; b < nb; b += C::W) {
-            const uint32_t st = static_cast<uint32_t>(warp * C::SW) + taken % C::SW;
-            if (*abort_flag || !mbar_wait_warp(&B.full[st], (taken / C::SW) & 1)) {
-                ok = false;
-                break;
-            }
-            const int blk = d.b0 + b;
-            const int valid = min(kBlockSize, d.n - blk * kBlockSize);
-            uint8_t* kst = smem + st * C::STAGE_BYTES;
-            if (may_have_new && b == nb - 1) store_stage_new_row<D, G, EB>(P, d, kst, stage_new[st], lane);
-            compute_block_mma<D, G, EB>(kst, kst + C::SLAB, valid, qb, f0, f1, m0, m1, l0, l1, o, lane);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&B.empty[st]);
-            ++taken;
-        }
-        if (!ok) break;
-        // Publish this warp's state for the merger: (m, l) and O of heads
-        // 2t and 2t+1 (those below G), each lane its dims g*D/8 .. + D/8.
-        const int buf = item_seq % C::MERGE_BUFS;
-        if (!mbar_wait_warp(&B.mempty[buf], ((item_seq / C::MERGE_BUFS) & 1) ^ 1)) {
-            ok = false;
-            break;
-        }
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            l0 += __shfl_xor_sync(FULL, l0, off);
-            l1 += __shfl_xor_sync(FULL, l1, off);
-        }
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int h = 2 * t + e;
-            if (h < G) {
-                const size_t base = static_cast<size_t>((buf * C::W + warp) * G + h);
-                if (g == 0) ml[base] = make_float2(e ? m1 : m0, e ? l1 : l0);
-                float2* dst = reinterpret_cast<float2*>(mo + base * D + g * (D / 8));
-#pragma unroll
-                for (int mm = 0; mm < D / 16; ++mm) dst[mm] = make_float2(o[mm][e], o[mm][2 + e]);
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&B.mfull[buf]);
-        ++item_seq;
-    }
-    if (!ok) {
-        *abort_flag = 1;
-        record_error(P.err, kErrTimeout, 2u);
-    }
-}
-
 template <int D, int G, int EB, bool FUSED>
 __device__ void run_consumer(const DecodeParams& P, uint8_t* smem, const Bars& B, volatile int* abort_flag,
                              int warp, int lane) {
