@@ -75,24 +75,11 @@ namespace {
 // warp 3 stages.  A build can force one count for every group with
 // PKV_DECODE_CONSUMER_WARPS.
 template <int G, int EB>
-constexpr int consumer_warps();
-
-// Block math of the consumer warps: packed fp32 FMAs on the CUDA cores
-// (run_consumer) on slabs copied whole, or, in a build with PKV_DECODE_MMA
-// defined, warp-level MMAs (run_consumer_mma) on slabs copied row by row
-// with a 16-byte pad after each row, with 8 consumer warps.
-#ifdef PKV_DECODE_MMA
-constexpr bool kConsumerMma = true;
-#else
-constexpr bool kConsumerMma = false;
-#endif
-
-template <int G, int EB>
 constexpr int consumer_warps() {
 #ifdef PKV_DECODE_CONSUMER_WARPS
     return PKV_DECODE_CONSUMER_WARPS;
 #else
-    return kConsumerMma ? 8 : (G <= 2 ? (EB == 1 ? 16 : 12) : 8);
+    return G <= 2 ? (EB == 1 ? 16 : 12) : 8;
 #endif
 }
 constexpr int kItemRing = 8;
@@ -155,11 +142,7 @@ struct Cfg {
     static constexpr int RPP = 32 / LPR;               // rows per warp pass
     static constexpr int NV = kBlockSize / RPP;        // rows per lane per block
     static constexpr int SLAB = kBlockSize * D * EB;   // bytes of one (block, kv head); EB = 2 (bf16) or 1 (e4m3)
-    // A slab in a stage: rows D * EB bytes apart, or 16 bytes more with MMA
-    // block math (rows copied one by one, the pad rotates their banks).
-    static constexpr int ROW_SMEM = D * EB + (kConsumerMma ? 16 : 0);
-    static constexpr int SLAB_SMEM = kBlockSize * ROW_SMEM;
-    static constexpr int STAGE_BYTES = 2 * SLAB_SMEM;  // K slab then V slab
+    static constexpr int STAGE_BYTES = 2 * SLAB;       // K slab then V slab
     static constexpr int QBYTES = G * D * 2;
     static constexpr int HG = G < 4 ? G : 4;           // heads per pass over K
     // Everything but the ring (offsets relative to the end of the ring).
@@ -168,8 +151,9 @@ struct Cfg {
     static constexpr int R_P = R_DESC + kItemRing * (int)sizeof(ItemDesc);
     static constexpr int R_MO = R_P + W * G * kBlockSize * 8;  // p stored as (p, p)
     static constexpr int R_ML = R_MO + MERGE_BUFS * W * G * D * 4;
-    static constexpr int R_WT = R_ML + MERGE_BUFS * W * G * 8;  // merger: [G][W] weights, [G] (M, L)
-    static constexpr int R_BAR = align_up(R_WT + G * W * 4 + G * 8, 8);
+    static constexpr int R_WT = R_ML + MERGE_BUFS * W * G * 8;  // merger: [G][W] weights
+    static constexpr int R_MSM = align_up(R_WT + G * W * 4, 8);  // merger: [G] (M, L), float2-aligned
+    static constexpr int R_BAR = align_up(R_MSM + G * 8, 8);
     static constexpr int STAGES_FIT = (220 * 1024 - R_BAR - 64 * 8 - 16) / STAGE_BYTES;
     // Each consumer warp owns SW consecutive stages that it consumes in
     // order (an mbarrier parity wait is only exact when the waiter is at
@@ -186,11 +170,16 @@ struct Cfg {
     static constexpr int OFF_MO = OFF_REST + R_MO;
     static constexpr int OFF_ML = OFF_REST + R_ML;
     static constexpr int OFF_WT = OFF_REST + R_WT;
+    static constexpr int OFF_MSM = OFF_REST + R_MSM;
     static constexpr int OFF_BAR = OFF_REST + R_BAR;
     static constexpr int OFF_FLAG = OFF_BAR + NBAR * 8;
     static constexpr int OFF_NEW = OFF_FLAG + 16;  // [STAGES] fused step: slot of a stage's new row, or -1
     static constexpr int SMEM = OFF_NEW + STAGES * 4;
     static_assert(SW >= 1, "ring too shallow");
+    static_assert(OFF_ITEMQ % 16 == 0 && OFF_DESC % 16 == 0 && OFF_P % 16 == 0 && OFF_MO % 16 == 0 &&
+                      OFF_ML % 8 == 0 && OFF_MSM % 8 == 0 && OFF_BAR % 8 == 0 && OFF_NEW % 4 == 0 &&
+                      STAGE_BYTES % 16 == 0,
+                  "shared-memory regions aligned for their widest access");
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
     static_assert(NV * RPP == kBlockSize, "rows");
 };
@@ -604,41 +593,22 @@ __device__ void run_producer(const DecodeParams& P, uint8_t* smem, const Bars& B
                         // written (the pool's row is used as it is).
                         record_error(P.err, kErrRange, static_cast<uint32_t>(s));
                     }
-                    constexpr uint32_t kRow = D * EB;
-                    if constexpr (kConsumerMma) {
-                        // Row by row into padded rows; the fused step's new
-                        // row (bf16) comes from k_new/v_new, rows past it are
-                        // never read.
-                        const bool from_new = FUSED && EB == 2 && fresh;
-                        const int nrows = from_new ? srow + 1 : kBlockSize;
-                        const size_t nr = (static_cast<size_t>(s) * P.hkv + g) * kRow;
-                        mbar_arrive_expect_tx(&B.full[st], 2 * nrows * kRow);
-                        for (int r = 0; r < nrows; ++r) {
-                            uint8_t* dk = dst + r * C::ROW_SMEM;
-                            if (from_new && r == srow) {
-                                bulk_g2s(dk, P.k_new + nr, kRow, &B.full[st]);
-                                bulk_g2s(dk + C::SLAB_SMEM, P.v_new + nr, kRow, &B.full[st]);
-                            } else {
-                                bulk_g2s_hint(dk, P.k_pool + slab + r * kRow, kRow, &B.full[st], policy);
-                                bulk_g2s_hint(dk + C::SLAB_SMEM, P.v_pool + slab + r * kRow, kRow, &B.full[st],
-                                              policy);
-                            }
-                        }
-                    } else if (FUSED && EB == 2 && fresh) {
+                    if (FUSED && EB == 2 && fresh) {
                         // Rows before the new token from the pool, the new
                         // row from k_new/v_new (rows past it are never read).
+                        constexpr uint32_t kRow = D * EB;
                         const size_t nr = (static_cast<size_t>(s) * P.hkv + g) * kRow;
                         mbar_arrive_expect_tx(&B.full[st], 2 * (srow + 1) * kRow);
                         if (srow > 0) {
                             bulk_g2s_hint(dst, P.k_pool + slab, srow * kRow, &B.full[st], policy);
-                            bulk_g2s_hint(dst + C::SLAB_SMEM, P.v_pool + slab, srow * kRow, &B.full[st], policy);
+                            bulk_g2s_hint(dst + C::SLAB, P.v_pool + slab, srow * kRow, &B.full[st], policy);
                         }
                         bulk_g2s(dst + srow * kRow, P.k_new + nr, kRow, &B.full[st]);
-                        bulk_g2s(dst + C::SLAB_SMEM + srow * kRow, P.v_new + nr, kRow, &B.full[st]);
+                        bulk_g2s(dst + C::SLAB + srow * kRow, P.v_new + nr, kRow, &B.full[st]);
                     } else {
                         mbar_arrive_expect_tx(&B.full[st], 2 * C::SLAB);
                         bulk_g2s_hint(dst, P.k_pool + slab, C::SLAB, &B.full[st], policy);
-                        bulk_g2s_hint(dst + C::SLAB_SMEM, P.v_pool + slab, C::SLAB, &B.full[st], policy);
+                        bulk_g2s_hint(dst + C::SLAB, P.v_pool + slab, C::SLAB, &B.full[st], policy);
                     }
                 }
             }
@@ -755,378 +725,16 @@ __device__ __forceinline__ void store_stage_new_row(const DecodeParams& P, const
     if (sub == srow % C::RPP) {
         const size_t at = (static_cast<size_t>(ns / kBlockSize) * P.hkv + d.g) * C::SLAB +
                           static_cast<size_t>(srow) * D * EB + cl * 8 * EB;
-        uint8_t* kr = kst + srow * C::ROW_SMEM + cl * 8 * EB;
+        uint8_t* kr = kst + srow * D * EB + cl * 8 * EB;
         if constexpr (EB == 2) {
             *reinterpret_cast<uint4*>(P.k_pool + at) = lds128(kr);
-            *reinterpret_cast<uint4*>(P.v_pool + at) = lds128(kr + C::SLAB_SMEM);
+            *reinterpret_cast<uint4*>(P.v_pool + at) = lds128(kr + C::SLAB);
         } else {
             const size_t off = (static_cast<size_t>(d.s) * P.hkv + d.g) * D * 2 + cl * 16;
-            store_new_row_e4m3(P, off, at, kr, C::SLAB_SMEM);
+            store_new_row_e4m3(P, off, at, kr, C::SLAB);
         }
     }
     __syncwarp();
-}
-
-// ---------------------------------------------------------------- MMA consumers
-// Block math on warp-level tensor-core MMAs (mma.sync m16n8k16, fp32
-// accumulators), for the decode variant whose slabs arrive row by row with a
-// 16-byte pad after each row (RS = row bytes + 16), so that rows fall on
-// rotating shared-memory bank groups.  Per 16-row block: S = K q^T (16 keys x
-// 8 head columns: the group's G heads, then zero columns) and O^T += V^T P^T
-// (16 dims x 8 heads per MMA).  Lane (g, t) = (lane / 4, lane % 4).  The
-// contractions are sums, so the order of their terms may be permuted, and it
-// is chosen so that the 8 lanes of every 16-byte load phase hit 8 different
-// bank groups:
-//  * q.K^T: lane t owns the 16-byte chunks c(t, i) of a key row (NC chunks a
-//    row: c = 2t + (i & 1) + 8 (i >> 1) for NC >= 8, c = t for NC = 4); in
-//    the k-step of a chunk's dims d .. d+3, slots (2t, 2t+1) are d, d+1 and
-//    slots (2t+8, 2t+9) are d+2, d+3.  q follows the same order.
-//  * P.V: lane g owns the dims of chunks g and g + 8 (bf16, head_dim 128),
-//    chunk g (8 chunks a row) or half of chunk g / 2 (4 chunks a row) of key
-//    rows 2t, 2t+1, 2t+8, 2t+9; MMA mm's rows g and g+8 are its dims 2mm and
-//    2mm + 1.
-// S lands as keys {g, g+8} x heads {2t, 2t+1}, the heads of the lane's O
-// columns too, so the online softmax needs no data movement; P goes to the B
-// layout (head g, keys 2t, 2t+1, 2t+8, 2t+9) by shuffles.  P is split into a
-// hi and a lo part (P.V runs twice), 2^-18 relative (bf16) or 2^-22 (f16).
-// bf16 pools use bf16 MMAs on the raw K, V and q; e4m3 pools widen codes to
-// f16 (exact) and use f16 MMAs, q scaled by a power of two per head (exact)
-// into [1, 2).  Rows past the context are masked in S and zeroed in V
-// (0 x NaN would poison the sum).
-template <bool F16>
-__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-    if constexpr (F16) {
-        asm volatile(
-            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-            "{%0, %1, %2, %3};"
-            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-    } else {
-        asm volatile(
-            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-            "{%0, %1, %2, %3};"
-            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-    }
-}
-
-// Two e4m3 codes (low 16 bits of w) -> f16x2, exact.
-__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t w) {
-    uint32_t h;
-    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, lo;\n\t}" : "=r"(h) : "r"(w));
-    return h;
-}
-
-// Two floats -> f16x2 / bf16x2 (round to nearest even), lo in the low half.
-__device__ __forceinline__ uint32_t f16x2_rn(float lo, float hi) {
-    uint32_t r;
-    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
-    uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
-// A pair of probabilities as two 16-bit MMA operands: hi is p rounded, lo
-// the rounded rest, so hi + lo = p to 2^-18 relative (bf16) or 2^-22 (f16).
-template <bool F16>
-__device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi, uint32_t& lo) {
-    if constexpr (F16) {
-        hi = f16x2_rn(a, b);
-        const float2 h = f16x2_to_float2(hi);
-        lo = f16x2_rn(a - h.x, b - h.y);
-    } else {
-        hi = bf16x2_rn(a, b);
-        lo = bf16x2_rn(a - bf16lo(hi), b - bf16hi(hi));
-    }
-}
-
-// Chunk layout of the MMA variant (see above).
-template <int D, int EB>
-struct MmaMap {
-    static constexpr int RS = D * EB + 16;   // padded row bytes in the stage
-    static constexpr int NC = D * EB / 16;   // 16-byte chunks of a row
-    static constexpr int KCH = NC / 4;       // q.K^T chunks of a lane
-    // 16-byte chunk i of lane t in q.K^T.
-    __device__ static __forceinline__ int kchunk(int t, int i) {
-        if constexpr (NC >= 8) return 2 * t + (i & 1) + 8 * (i >> 1);
-        else return t;
-    }
-    // P.V: dims of a lane (g): D / 8; byte offset in a row of its dim j.
-    static constexpr int VDIMS = D / 8;
-    static constexpr int VCH = (VDIMS * EB + 15) / 16;  // 16-byte chunks (1 or 2); 4-chunk rows use half a chunk
-    __device__ static __forceinline__ int vbyte(int g, int jj) {  // start of lane g's chunk jj
-        if constexpr (NC == 16) return (g + 8 * jj) * 16;
-        else if constexpr (NC == 8) return g * 16;
-        else return g * 8;  // half chunks
-    }
-    // First dim of the lane's chunk jj (for the output).
-    __device__ static __forceinline__ int vdim(int g, int jj) { return vbyte(g, jj) / EB; }
-};
-
-template <int D, int G, int EB>
-__device__ __forceinline__ void compute_block_mma(const uint8_t* kst, const uint8_t* vst, int valid,
-                                                  const uint32_t (&qb)[D / 8], float f0, float f1, float& m0,
-                                                  float& m1, float& l0, float& l1, float (&o)[D / 16][4],
-                                                  int lane) {
-    using M = MmaMap<D, EB>;
-    constexpr bool F16 = EB == 1;
-    const unsigned FULL = 0xffffffffu;
-    const int g = lane >> 2, t = lane & 3;
-    // ---- S = K q^T
-    float s[4] = {0.f, 0.f, 0.f, 0.f};
-    {
-        const uint8_t* k0 = kst + g * M::RS;
-        const uint8_t* k8 = kst + (g + 8) * M::RS;
-#pragma unroll
-        for (int i = 0; i < M::KCH; ++i) {
-            const int cb = M::kchunk(t, i) * 16;
-            const uint4 r0 = lds128(k0 + cb), r8 = lds128(k8 + cb);
-            if constexpr (EB == 2) {  // 8 dims: k-steps 2i (words x, y) and 2i+1 (z, w)
-                mma16816<false>(s, r0.x, r8.x, r0.y, r8.y, qb[4 * i], qb[4 * i + 1]);
-                mma16816<false>(s, r0.z, r8.z, r0.w, r8.w, qb[4 * i + 2], qb[4 * i + 3]);
-            } else {  // 16 codes: k-steps 4i + w, word w = dims 4w .. 4w + 3
-                const uint32_t w0[4] = {r0.x, r0.y, r0.z, r0.w}, w8[4] = {r8.x, r8.y, r8.z, r8.w};
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const int kk = 4 * i + w;
-                    mma16816<true>(s, e4m3x2_f16x2(w0[w]), e4m3x2_f16x2(w8[w]), e4m3x2_f16x2(w0[w] >> 16),
-                                   e4m3x2_f16x2(w8[w] >> 16), qb[2 * kk], qb[2 * kk + 1]);
-                }
-            }
-        }
-    }
-    // ---- online softmax (log2 domain) on keys {g, g+8} x heads {2t, 2t+1}
-    const bool vg = g < valid, vg8 = g + 8 < valid;
-    const float x00 = vg ? s[0] * f0 : -INFINITY, x01 = vg ? s[1] * f1 : -INFINITY;
-    const float x10 = vg8 ? s[2] * f0 : -INFINITY, x11 = vg8 ? s[3] * f1 : -INFINITY;
-    float mb0 = fmaxf(x00, x10), mb1 = fmaxf(x01, x11);
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-        mb0 = fmaxf(mb0, __shfl_xor_sync(FULL, mb0, off));
-        mb1 = fmaxf(mb1, __shfl_xor_sync(FULL, mb1, off));
-    }
-    // The reference moves only when the block's maximum exceeds it by more
-    // than 2^8, so P stays below 256 and O is rescaled on few blocks.
-    if (mb0 > m0 + kRescaleThreshold) {
-        const float a = fast_exp2(m0 - mb0);
-        l0 *= a;
-#pragma unroll
-        for (int mm = 0; mm < D / 16; ++mm) o[mm][0] *= a, o[mm][2] *= a;
-        m0 = mb0;
-    }
-    if (mb1 > m1 + kRescaleThreshold) {
-        const float a = fast_exp2(m1 - mb1);
-        l1 *= a;
-#pragma unroll
-        for (int mm = 0; mm < D / 16; ++mm) o[mm][1] *= a, o[mm][3] *= a;
-        m1 = mb1;
-    }
-    const float p00 = fast_exp2(x00 - m0), p01 = fast_exp2(x01 - m1);
-    const float p10 = fast_exp2(x10 - m0), p11 = fast_exp2(x11 - m1);
-    l0 += p00 + p10;
-    l1 += p01 + p11;
-    // ---- P^T in the B layout: head g, keys (2t, 2t+1) and (2t+8, 2t+9).
-    // Key 2t of head g sits in lane 8t + g/2 (key 2t+1: + 4), as element
-    // g % 2 of its (key, key+8) pair.
-    uint32_t x0h, x0l, x1h, x1l;  // (key g, key g+8) of heads 2t and 2t+1
-    split_pair<F16>(p00, p10, x0h, x0l);
-    split_pair<F16>(p01, p11, x1h, x1l);
-    const int la = 8 * t + (g >> 1), lb = la + 4;
-    const bool odd = g & 1;
-    uint32_t ah = __shfl_sync(FULL, x0h, la), ah1 = __shfl_sync(FULL, x1h, la);
-    uint32_t bh = __shfl_sync(FULL, x0h, lb), bh1 = __shfl_sync(FULL, x1h, lb);
-    uint32_t al = __shfl_sync(FULL, x0l, la), al1 = __shfl_sync(FULL, x1l, la);
-    uint32_t bl = __shfl_sync(FULL, x0l, lb), bl1 = __shfl_sync(FULL, x1l, lb);
-    if (odd) ah = ah1, bh = bh1, al = al1, bl = bl1;
-    const uint32_t ph0 = __byte_perm(ah, bh, 0x5410), ph1 = __byte_perm(ah, bh, 0x7632);
-    const uint32_t pl0 = __byte_perm(al, bl, 0x5410), pl1 = __byte_perm(al, bl, 0x7632);
-    // ---- O^T += V^T P^T over this lane's dims
-    const int key0 = 2 * t, key2 = 2 * t + 8;
-    const uint8_t* va = vst + key0 * M::RS;
-    const uint8_t* vb = vst + (key0 + 1) * M::RS;
-    const uint8_t* vc = vst + key2 * M::RS;
-    const uint8_t* vd = vst + (key2 + 1) * M::RS;
-    if constexpr (EB == 2) {
-        // Per chunk jj: 8 dims, word j holds dims +2j, +2j+1 (MMA 4jj + j).
-#pragma unroll
-        for (int jj = 0; jj < M::VCH; ++jj) {
-            const int cb = M::vbyte(g, jj);
-            uint4 ra = lds128(va + cb), rb = lds128(vb + cb), rc = lds128(vc + cb), rd = lds128(vd + cb);
-            if (key0 >= valid) ra = make_uint4(0u, 0u, 0u, 0u);
-            if (key0 + 1 >= valid) rb = make_uint4(0u, 0u, 0u, 0u);
-            if (key2 >= valid) rc = make_uint4(0u, 0u, 0u, 0u);
-            if (key2 + 1 >= valid) rd = make_uint4(0u, 0u, 0u, 0u);
-            const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w}, wb[4] = {rb.x, rb.y, rb.z, rb.w};
-            const uint32_t wc[4] = {rc.x, rc.y, rc.z, rc.w}, wd[4] = {rd.x, rd.y, rd.z, rd.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int mm = 4 * jj + j;
-                const uint32_t a0 = __byte_perm(wa[j], wb[j], 0x5410), a1 = __byte_perm(wa[j], wb[j], 0x7632);
-                const uint32_t a2 = __byte_perm(wc[j], wd[j], 0x5410), a3 = __byte_perm(wc[j], wd[j], 0x7632);
-                mma16816<false>(o[mm], a0, a1, a2, a3, ph0, ph1);
-                mma16816<false>(o[mm], a0, a1, a2, a3, pl0, pl1);
-            }
-        }
-    } else {
-        // D/8 codes: word i holds dims +4i .. +4i+3 (MMAs 2i, 2i+1).
-        constexpr int NW = D / 32;
-        uint32_t wa[NW], wb[NW], wc[NW], wd[NW];
-        const int cb = M::vbyte(g, 0);
-        if constexpr (NW == 4) {
-            const uint4 ra = lds128(va + cb), rb = lds128(vb + cb), rc = lds128(vc + cb), rd = lds128(vd + cb);
-            wa[0] = ra.x, wa[1] = ra.y, wa[2] = ra.z, wa[3] = ra.w;
-            wb[0] = rb.x, wb[1] = rb.y, wb[2] = rb.z, wb[3] = rb.w;
-            wc[0] = rc.x, wc[1] = rc.y, wc[2] = rc.z, wc[3] = rc.w;
-            wd[0] = rd.x, wd[1] = rd.y, wd[2] = rd.z, wd[3] = rd.w;
-        } else {
-            const uint2 ra = lds64(va + cb), rb = lds64(vb + cb), rc = lds64(vc + cb), rd = lds64(vd + cb);
-            wa[0] = ra.x, wa[1] = ra.y, wb[0] = rb.x, wb[1] = rb.y;
-            wc[0] = rc.x, wc[1] = rc.y, wd[0] = rd.x, wd[1] = rd.y;
-        }
-#pragma unroll
-        for (int i = 0; i < NW; ++i) {
-            if (key0 >= valid) wa[i] = 0u;
-            if (key0 + 1 >= valid) wb[i] = 0u;
-            if (key2 >= valid) wc[i] = 0u;
-            if (key2 + 1 >= valid) wd[i] = 0u;
-            const uint32_t ab0 = __byte_perm(wa[i], wb[i], 0x5140), ab1 = __byte_perm(wa[i], wb[i], 0x7362);
-            const uint32_t cd0 = __byte_perm(wc[i], wd[i], 0x5140), cd1 = __byte_perm(wc[i], wd[i], 0x7362);
-            const uint32_t a0 = e4m3x2_f16x2(ab0), a1 = e4m3x2_f16x2(ab0 >> 16);
-            const uint32_t a2 = e4m3x2_f16x2(cd0), a3 = e4m3x2_f16x2(cd0 >> 16);
-            mma16816<true>(o[2 * i], a0, a1, a2, a3, ph0, ph1);
-            mma16816<true>(o[2 * i], a0, a1, a2, a3, pl0, pl1);
-            const uint32_t b0 = e4m3x2_f16x2(ab1), b1 = e4m3x2_f16x2(ab1 >> 16);
-            const uint32_t b2 = e4m3x2_f16x2(cd1), b3 = e4m3x2_f16x2(cd1 >> 16);
-            mma16816<true>(o[2 * i + 1], b0, b1, b2, b3, ph0, ph1);
-            mma16816<true>(o[2 * i + 1], b0, b1, b2, b3, pl0, pl1);
-        }
-    }
-}
-
-// Consumer warps with MMA block math: the item loop of run_consumer, with
-// the q fragments, softmax state and O held in the MMA layouts above.
-template <int D, int G, int EB, bool FUSED>
-__device__ void run_consumer_mma(const DecodeParams& P, uint8_t* smem, const Bars& B, volatile int* abort_flag,
-                                 int warp, int lane) {
-    using C = Cfg<D, G, EB>;
-    using M = MmaMap<D, EB>;
-    constexpr int QW = D / 8;  // q words (two elements each) of a lane: its D/4 dims
-    const unsigned FULL = 0xffffffffu;
-    const ItemDesc* descs = reinterpret_cast<const ItemDesc*>(smem + C::OFF_DESC);
-    const volatile int* stage_new = reinterpret_cast<const volatile int*>(smem + C::OFF_NEW);
-    float* mo = reinterpret_cast<float*>(smem + C::OFF_MO);
-    float2* ml = reinterpret_cast<float2*>(smem + C::OFF_ML);
-    const int g = lane >> 2, t = lane & 3;
-    uint32_t taken = 0, item_seq = 0;
-    bool ok = true;
-    while (ok) {
-        const uint32_t slot = item_seq % kItemRing;
-        if (*abort_flag || !mbar_wait_warp(&B.ifull[slot], (item_seq / kItemRing) & 1)) {
-            ok = false;
-            break;
-        }
-        const ItemDesc d = descs[slot];
-        if (d.s < 0) break;
-        // q of head g in the q.K^T order of lane t, as B fragments (zero for
-        // g >= G): word 2kk, 2kk+1 of k-step kk.
-        uint32_t qb[QW];
-        float f0 = P.scale_log2, f1 = P.scale_log2;  // score factors of heads 2t, 2t+1
-        {
-            const uint8_t* qs = smem + C::OFF_ITEMQ + slot * C::QBYTES + g * D * 2;
-#pragma unroll
-            for (int i = 0; i < M::KCH; ++i) {
-                // the chunk's dims as bf16: 8 (bf16 pools) or 16 (e4m3 pools)
-                const int d0 = M::kchunk(t, i) * 16 / EB;
-#pragma unroll
-                for (int h = 0; h < 3 - EB; ++h) {
-                    uint4 u = make_uint4(0u, 0u, 0u, 0u);
-                    if (g < G) u = lds128(qs + (d0 + 8 * h) * 2);
-                    const int w0 = (i * (3 - EB) + h) * 4;
-                    qb[w0] = u.x, qb[w0 + 1] = u.y, qb[w0 + 2] = u.z, qb[w0 + 3] = u.w;
-                }
-            }
-            if constexpr (EB == 1) {
-                // f16 MMAs: scale head g's q by 2^-e into [1, 2) (exact), and
-                // give the scores the factor 2^e back.
-                float mx = 0.f;
-#pragma unroll
-                for (int i = 0; i < QW; ++i) mx = fmaxf(mx, fmaxf(fabsf(bf16lo(qb[i])), fabsf(bf16hi(qb[i]))));
-                mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 1));
-                mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 2));
-                int e = (mx >= 0x1p-100f && mx < INFINITY) ? static_cast<int>((__float_as_uint(mx) >> 23) & 0xFF) - 127
-                                                             : 0;
-                e = min(e, 100);  // |q| up to 2^101 (f16 would overflow beyond)
-                const float down = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e
-                const float up = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);    // 2^e
-#pragma unroll
-                for (int i = 0; i < QW; ++i) qb[i] = f16x2_rn(bf16lo(qb[i]) * down, bf16hi(qb[i]) * down);
-                f0 = P.scale_log2 * __shfl_sync(FULL, up, (8 * t) & 31);
-                f1 = P.scale_log2 * __shfl_sync(FULL, up, (8 * t + 4) & 31);
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&B.iempty[slot]);
-        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-        float o[D / 16][4];
-#pragma unroll
-        for (int mm = 0; mm < D / 16; ++mm) o[mm][0] = o[mm][1] = o[mm][2] = o[mm][3] = 0.f;
-        const int nb = d.b1 - d.b0;
-        const int first = (warp - d.rot + C::W) % C::W;  // see run_consumer
-        const bool may_have_new = FUSED && d.b1 == (d.n + kBlockSize - 1) / kBlockSize;
-        for (int b = first; b < nb; b += C::W) {
-            const uint32_t st = static_cast<uint32_t>(warp * C::SW) + taken % C::SW;
-            if (*abort_flag || !mbar_wait_warp(&B.full[st], (taken / C::SW) & 1)) {
-                ok = false;
-                break;
-            }
-            const int blk = d.b0 + b;
-            const int valid = min(kBlockSize, d.n - blk * kBlockSize);
-            uint8_t* kst = smem + st * C::STAGE_BYTES;
-            if (may_have_new && b == nb - 1) store_stage_new_row<D, G, EB>(P, d, kst, stage_new[st], lane);
-            compute_block_mma<D, G, EB>(kst, kst + C::SLAB_SMEM, valid, qb, f0, f1, m0, m1, l0, l1, o, lane);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&B.empty[st]);
-            ++taken;
-        }
-        if (!ok) break;
-        // Publish this warp's state for the merger: (m, l) and O of heads
-        // 2t and 2t+1 (those below G), each lane its dims.
-        const int buf = item_seq % C::MERGE_BUFS;
-        if (!mbar_wait_warp(&B.mempty[buf], ((item_seq / C::MERGE_BUFS) & 1) ^ 1)) {
-            ok = false;
-            break;
-        }
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            l0 += __shfl_xor_sync(FULL, l0, off);
-            l1 += __shfl_xor_sync(FULL, l1, off);
-        }
-        constexpr int MPC = (D / 16) / (M::VCH);  // MMAs of a lane chunk
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int h = 2 * t + e;
-            if (h < G) {
-                const size_t base = static_cast<size_t>((buf * C::W + warp) * G + h);
-                if (g == 0) ml[base] = make_float2(e ? m1 : m0, e ? l1 : l0);
-#pragma unroll
-                for (int mm = 0; mm < D / 16; ++mm) {
-                    const int dim = M::vdim(g, mm / MPC) + 2 * (mm % MPC);
-                    *reinterpret_cast<float2*>(mo + base * D + dim) = make_float2(o[mm][e], o[mm][2 + e]);
-                }
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&B.mfull[buf]);
-        ++item_seq;
-    }
-    if (!ok) {
-        *abort_flag = 1;
-        record_error(P.err, kErrTimeout, 2u);
-    }
 }
 
 template <int D, int G, int EB, bool FUSED>
@@ -1191,7 +799,7 @@ __device__ void run_consumer(const DecodeParams& P, uint8_t* smem, const Bars& B
             const int valid = min(kBlockSize, d.n - blk * kBlockSize);
             uint8_t* kst = smem + st * C::STAGE_BYTES;
             if (may_have_new && b == nb - 1) store_stage_new_row<D, G, EB>(P, d, kst, stage_new[st], lane);
-            compute_block<D, G, EB>(kst, kst + C::SLAB_SMEM, valid, q2, m, lsum, o2, psm, lane);
+            compute_block<D, G, EB>(kst, kst + C::SLAB, valid, q2, m, lsum, o2, psm, lane);
             if (lane == 0) mbar_arrive(&B.empty[st]);
             ++taken;
         }
@@ -1238,7 +846,7 @@ __device__ void run_merger(const DecodeParams& P, uint8_t* smem, const Bars& B, 
     const float* mo = reinterpret_cast<const float*>(smem + C::OFF_MO);
     const float2* ml = reinterpret_cast<const float2*>(smem + C::OFF_ML);
     float* wsm = reinterpret_cast<float*>(smem + C::OFF_WT);
-    float2* msm = reinterpret_cast<float2*>(smem + C::OFF_WT + G * C::W * 4);
+    float2* msm = reinterpret_cast<float2*>(smem + C::OFF_MSM);
     uint32_t item_seq = 0;
     bool ok = true;
     while (true) {
@@ -1575,10 +1183,7 @@ __global__ void __launch_bounds__(Cfg<D, G, EB>::THREADS, 1) decode_kernel(const
         run_merger<D, G, EB>(P, smem, B, abort_flag, lane);
     } else {
         prefetch_inputs<D, FUSED>(P, threadIdx.x, C::W * 32);
-        if constexpr (kConsumerMma)
-            run_consumer_mma<D, G, EB, FUSED>(P, smem, B, abort_flag, warp, lane);
-        else
-            run_consumer<D, G, EB, FUSED>(P, smem, B, abort_flag, warp, lane);
+        run_consumer<D, G, EB, FUSED>(P, smem, B, abort_flag, warp, lane);
     }
 }
 
