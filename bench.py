@@ -593,7 +593,15 @@ class ConfigRun:
                      out=torch.empty((self.Tq, w.num_q_heads, w.head_dim), dtype=torch.float32, device=dev))
             r.update(stage_views(stage))
             self.reps.append(r)
-        if w.is_decode:
+        # Sequences whose tables all start with the same full blocks (a shared
+        # prefix): decode reads those once per kv head for all of them.
+        self.shared_blocks = 0
+        if w.is_decode and w.num_seqs > 1 and self.pb == 0:
+            self.shared_blocks = pkv.common_prefix_blocks(w.block_tables, w.context_lens)
+        if self.shared_blocks > 0:
+            need = pkv.decode_shared_prefix_workspace_size(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                                           self.maxctx, self.shared_blocks)
+        elif w.is_decode:
             need = pkv.decode_workspace_size(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim, self.maxctx,
                                              self.pb)
         else:
@@ -607,7 +615,8 @@ class ConfigRun:
         if self.fused:
             self.launches_per_step = 1
         else:
-            self.launches_per_step = (1 if w.copy_src is not None else 0) + 1 + (1 if w.is_decode else 0)
+            self.launches_per_step = ((1 if w.copy_src is not None else 0) + 1 + (1 if w.is_decode else 0) +
+                                      (1 if self.shared_blocks > 0 else 0))
             if not w.is_decode:
                 self.launches_per_step += (1 if len(decode_rows(w)) else 0) + (1 if len(prefill_rows(w)) else 0)
         with torch.cuda.stream(stream):
@@ -633,7 +642,11 @@ class ConfigRun:
 
     def attention(self, r):
         w, pkv, s = self.w, self.pkv, self.stream
-        if w.is_decode:
+        if self.shared_blocks > 0:
+            pkv.decode_attention_shared_prefix(r["k"], r["v"], r["q"], r["tables"], r["ctx"], self.maxctx,
+                                               self.shared_blocks, self.scale, out=r["out"], workspace=r["ws"],
+                                               stream=s)
+        elif w.is_decode:
             pkv.decode_attention(r["k"], r["v"], r["q"], r["tables"], r["ctx"], self.maxctx, self.scale,
                                  out=r["out"], workspace=r["ws"], partition_blocks=self.pb, stream=s)
         else:
@@ -695,14 +708,15 @@ class ConfigRun:
         return {"mean_ms": statistics.fmean(ms), "median_ms": statistics.median(ms), "min_ms": min(ms),
                 "steps": total, "trials": trials}
 
-    def kernel_alone(self, seqs, kv_e4m3=False, fused=False, min_launches=200, min_ms=20.0, trials=5,
+    def kernel_alone(self, seqs, kv_e4m3=False, fused=False, shared=0, min_launches=200, min_ms=20.0, trials=5,
                      warm_launches=50):
         """One attention launch over the sequences `seqs` (decode rows or
         prefill rows; fused: the whole decode step, the new rows' store
-        included), replayed from graphs over the replicas (bf16 pools) or
-        over e4m3 copies of them (kv_e4m3, pools written by the e4m3 store);
-        mean over all launches, median and minimum of the trials, and a warm
-        figure repeating one replica."""
+        included; shared > 0: the shared-prefix decode over that many shared
+        blocks, its two launches), replayed from graphs over the replicas
+        (bf16 pools) or over e4m3 copies of them (kv_e4m3, pools written by
+        the e4m3 store); mean over all launches, median and minimum of the
+        trials, and a warm figure repeating one replica."""
         import numpy as np
         torch, pkv, w, dev = self.torch, self.pkv, self.w, self.dev
         sub = subset(w, seqs)
@@ -733,7 +747,10 @@ class ConfigRun:
                                                                    dtype=torch.float32, device=dev))
                 if fused:
                     it.update(kn=r["kn"], vn=r["vn"], slots=r["slots"])
-                if sub["decode"]:
+                if shared > 0:
+                    n = pkv.decode_shared_prefix_workspace_size(len(seqs), w.num_q_heads, hkv, d, sub["max_ctx"],
+                                                                shared)
+                elif sub["decode"]:
                     n = pkv.decode_workspace_size(len(seqs), w.num_q_heads, hkv, d, sub["max_ctx"], self.pb)
                 else:
                     n = pkv.prefill_workspace_size(len(seqs), sub["q"].shape[0], w.num_q_heads, hkv, d,
@@ -747,6 +764,10 @@ class ConfigRun:
                 pkv.decode_step(it["k"], it["v"], it["kn"], it["vn"], it["slots"], it["q"], it["tables"], it["ctx"],
                                 sub["max_ctx"], self.scale, out=it["out"], workspace=it["ws"],
                                 partition_blocks=self.pb, stream=self.stream, k_scale=ks, v_scale=vs)
+            elif shared > 0:
+                pkv.decode_attention_shared_prefix(it["k"], it["v"], it["q"], it["tables"], it["ctx"], sub["max_ctx"],
+                                                   shared, self.scale, out=it["out"], workspace=it["ws"],
+                                                   stream=self.stream)
             elif sub["decode"]:
                 pkv.decode_attention(it["k"], it["v"], it["q"], it["tables"], it["ctx"], sub["max_ctx"], self.scale,
                                      out=it["out"], workspace=it["ws"], partition_blocks=self.pb, stream=self.stream,
@@ -795,12 +816,15 @@ def new_row_bytes(w, kv_elem_bytes=2) -> int:
     return T * (w.num_kv_heads * w.head_dim * 2 * (2 + kv_elem_bytes) + 4)
 
 
-def decode_entry(w, t, hbm, hbm_kind, kv_elem_bytes=2, traffic=None, fused=False):
+def decode_entry(w, t, hbm, hbm_kind, kv_elem_bytes=2, traffic=None, fused=False, shared=0):
     """Roofline record of the decode kernel from a kernel_alone timing
-    (fused: the decode step's kernel, the new rows' store included)."""
+    (fused: the decode step's kernel, the new rows' store included; shared:
+    the shared-prefix kernel and the decode kernel, timed together)."""
     nbytes = decode_bytes(w, kv_elem_bytes=kv_elem_bytes) + (new_row_bytes(w, kv_elem_bytes) if fused else 0)
     achieved = nbytes / (t["mean_us"] * 1e-6) / 1e9
     name = "decode_kernel" + (" (fused step: new rows' store + attention)" if fused else "")
+    if shared:
+        name = f"shared_prefix_kernel + decode_kernel ({shared} shared blocks read once per kv head)"
     rec = {"bound": "hbm", "kernel": name + (" (e4m3 pools)" if kv_elem_bytes == 1 else ""),
            "achieved": achieved, "peak": hbm,
            "peak_kind": f"{hbm_kind} (MEASURED_PEAKS.json hbm_gbs, copy)" if hbm_kind == "measured" else "fallback",
@@ -1018,7 +1042,13 @@ def config_entry(run, hbm, hbm_kind, tpeak, tkind, clocks=None, cpu=True, cpu_bu
                                             traffic=ncu_traffic("decode_step", run.config), fused=True)
     if len(dec):
         dec_t = run.kernel_alone(dec)
-        entry["decode"] = decode_entry(w, dec_t, hbm, hbm_kind, traffic=ncu_traffic("decode", run.config))
+        if run.shared_blocks > 0:
+            entry["decode_per_sequence"] = decode_entry(w, dec_t, hbm, hbm_kind,
+                                                        traffic=ncu_traffic("decode", run.config))
+            entry["decode"] = decode_entry(w, run.kernel_alone(dec, shared=run.shared_blocks), hbm, hbm_kind,
+                                           shared=run.shared_blocks)
+        else:
+            entry["decode"] = decode_entry(w, dec_t, hbm, hbm_kind, traffic=ncu_traffic("decode", run.config))
     if len(pre):
         entry["prefill"] = prefill_entry(w, run.kernel_alone(pre), tpeak, tkind)
     if len(dec):
@@ -1229,8 +1259,9 @@ def run_ours(args):
 
 def run_ncu_case(args):
     """A short run for a profiler: the workload's step once, then
-    `--ncu-launches` launches of one kernel (decode, decode_step, prefill or
-    fp8_decode) over one copy of the inputs, no timing loops."""
+    `--ncu-launches` launches of one kernel (decode, decode_step, prefill,
+    fp8_decode or shared_prefix: the shared-prefix decode's two kernels) over
+    one copy of the inputs, no timing loops."""
     import torch
 
     import paged_kv_cache_291_gb300 as pkv
@@ -1244,10 +1275,13 @@ def run_ncu_case(args):
     which = args.ncu_case
     if which == "decode_step" and not run.fused:
         raise SystemExit(f"{w.name}: its step is not a plain decode step")
+    if which == "shared_prefix" and run.shared_blocks == 0:
+        raise SystemExit(f"{w.name}: its sequences share no prefix blocks")
     seqs = pre if which == "prefill" else dec
     if not len(seqs):
         raise SystemExit(f"{w.name} has no rows for {which}")
     t = run.kernel_alone(seqs, kv_e4m3=which == "fp8_decode", fused=which == "decode_step",
+                         shared=run.shared_blocks if which == "shared_prefix" else 0,
                          min_launches=args.ncu_launches, min_ms=0.0, trials=1, warm_launches=1)
     print(json.dumps({"ncu_case": which, "workload": w.name, "launches": t["launches"] + 3,
                       "mean_us": t["mean_us"]}), flush=True)
@@ -1270,7 +1304,8 @@ def main(argv=None):
                     help="seconds of one-thread oracle work per sampled step of each workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--partition-blocks", type=int, default=0, help="0 = automatic split-KV partitioning")
-    ap.add_argument("--ncu-case", choices=["decode", "decode_step", "prefill", "fp8_decode"], default=None,
+    ap.add_argument("--ncu-case", choices=["decode", "decode_step", "prefill", "fp8_decode", "shared_prefix"],
+                    default=None,
                     help="a short run of one kernel for a profiler (no timing, no JSON bench line)")
     ap.add_argument("--ncu-launches", type=int, default=3)
     args = ap.parse_args(argv)

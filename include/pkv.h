@@ -252,6 +252,54 @@ pkv_status pkv_decode_step(const pkv_cache_t* cache, const void* k_new, const vo
                            size_t workspace_bytes, int32_t partition_blocks, void* stream);
 
 /*
+ * pkv_decode_attention_shared_prefix -- pkv_decode_attention for a batch
+ * whose sequences all begin with the same blocks.  [KV2] section 2,
+ * "Sharing blocks": several requests may point at one physical block (a
+ * prompt shared by parallel samples or beams, a system prompt the prefix
+ * cache maps to the same blocks).  The first shared_blocks entries of every
+ * block table are read once per kv head and attended by the queries of all
+ * sequences together on tensor cores; each sequence's remaining blocks are
+ * attended by the decode kernel, which merges both parts (log-sum-exp).
+ *
+ *   shared_blocks  host int32: block_tables[s][j] is the same id for every
+ *                  s and every j < shared_blocks, and each context holds
+ *                  those blocks in full (context_lens[s] >= 16 *
+ *                  shared_blocks).  0 <= shared_blocks <= max_blocks_per_seq
+ *                  and 16 * shared_blocks <= max_context_len, else
+ *                  PKV_ERR_SHAPE.  pkv_common_prefix_blocks computes the
+ *                  largest such value from host copies of the tables.
+ *   workspace      device buffer of >= pkv_decode_shared_prefix_workspace_size()
+ *                  bytes, 256-byte aligned, under the rules of
+ *                  pkv_decode_attention (zero on first use; left zeroed).
+ *   All other arguments and the result are those of pkv_decode_attention
+ *   (automatic partitioning).  The result equals pkv_decode_attention's up
+ *   to fp32 rounding (the shared part's P is carried as a bf16 hi + lo pair,
+ *   2^-17 relative).
+ *   The promise is checked on the device: a sequence whose table differs in
+ *   the shared part, or whose context is shorter than it, raises
+ *   PKV_ERR_RANGE (detail: the sequence), and the call's results are then
+ *   not valid.  e4m3 pools (and pools of more than 2^31 rows of 16 tokens x
+ *   kv heads) attend the shared blocks per sequence, as
+ *   pkv_decode_attention does; the promise is then not checked.
+ */
+size_t pkv_decode_shared_prefix_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                               int32_t head_dim, int32_t max_context_len, int32_t shared_blocks);
+pkv_status pkv_decode_attention_shared_prefix(const pkv_cache_t* cache, const void* q, int32_t num_q_heads,
+                                              const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                              const int32_t* context_lens, int32_t num_seqs,
+                                              int32_t max_context_len, int32_t shared_blocks, float scale,
+                                              float* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * pkv_common_prefix_blocks -- host-only: the largest J such that the first J
+ * entries of every row of block_tables_host ([num_seqs][max_blocks_per_seq])
+ * equal row 0's and every context_lens_host[s] >= 16 J.  Reads host memory
+ * only; 0 when num_seqs <= 0, a pointer is NULL or max_blocks_per_seq <= 0.
+ */
+int32_t pkv_common_prefix_blocks(const int32_t* block_tables_host, int32_t max_blocks_per_seq,
+                                 const int32_t* context_lens_host, int32_t num_seqs);
+
+/*
  * pkv_prefill_workspace_size -- bytes of workspace
  * pkv_chunked_prefill_attention needs.  Returns 0 for invalid arguments.
  */

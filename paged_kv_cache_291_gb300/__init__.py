@@ -85,6 +85,10 @@ def load():
         "pkv_decode_workspace_size": ([i32, i32, i32, i32, i32, i32], sz),
         "pkv_decode_attention": ([CP, P, i32, P, i32, P, i32, i32, f32, P, P, sz, i32, P], ctypes.c_int),
         "pkv_decode_step": ([CP, P, P, P, P, i32, P, i32, P, i32, i32, f32, P, P, sz, i32, P], ctypes.c_int),
+        "pkv_decode_shared_prefix_workspace_size": ([i32, i32, i32, i32, i32, i32], sz),
+        "pkv_decode_attention_shared_prefix": ([CP, P, i32, P, i32, P, i32, i32, i32, f32, P, P, sz, P],
+                                               ctypes.c_int),
+        "pkv_common_prefix_blocks": ([P, i32, P, i32], i32),
         "pkv_prefill_workspace_size": ([i32, i32, i32, i32, i32, i32], sz),
         "pkv_chunked_prefill_attention": ([CP, P, i32, i32, P, P, P, i32, P, i32, i32, f32, P, P, sz, P],
                                           ctypes.c_int),
@@ -293,6 +297,58 @@ def decode_step(k_pool, v_pool, k_new, v_new, slot_mapping, q, block_tables, con
                              workspace.numel() * workspace.element_size(), int(partition_blocks),
                              _stream_handle(stream))
     _check(st, "pkv_decode_step")
+    return out
+
+
+def common_prefix_blocks(block_tables_host, context_lens_host) -> int:
+    """The largest J such that every row of the host block table
+    [B][max_blocks] starts with row 0's first J ids and every context holds
+    16 J tokens (pkv_common_prefix_blocks; host arrays only)."""
+    import numpy as np
+    t = np.ascontiguousarray(block_tables_host, dtype=np.int32)
+    n = np.ascontiguousarray(context_lens_host, dtype=np.int32)
+    if t.ndim != 2 or n.ndim != 1 or n.shape[0] != t.shape[0]:
+        raise ValueError("block_tables_host must be [B][max_blocks] and context_lens_host [B]")
+    return int(load().pkv_common_prefix_blocks(t.ctypes.data, t.shape[1], n.ctypes.data, t.shape[0]))
+
+
+def decode_shared_prefix_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len,
+                                        shared_blocks) -> int:
+    n = load().pkv_decode_shared_prefix_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                       max_context_len, shared_blocks)
+    if n == 0:
+        raise PKVError(2, "pkv_decode_shared_prefix_workspace_size")
+    return int(n)
+
+
+def decode_attention_shared_prefix(k_pool, v_pool, q, block_tables, context_lens, max_context_len: int,
+                                   shared_blocks: int, scale: float, out=None, workspace=None, stream=None,
+                                   k_scale=None, v_scale=None):
+    """Decode attention for a batch whose block tables all start with the
+    same ``shared_blocks`` full blocks: those are read once per kv head for
+    every sequence (tensor cores), the rest per sequence; returns ``out``
+    float32 [B][Hq][d].  e4m3 pools (with their scales) attend the shared
+    blocks per sequence."""
+    torch = _torch()
+    lib = load()
+    c = _cache(k_pool, v_pool, k_scale, v_scale, need_scales=True)
+    B, hq, d = q.shape
+    if d != c.head_dim:
+        raise ValueError("q head_dim does not match the pools")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.shape[0] != B:
+        raise ValueError("block_tables must be [B][max_blocks] and context_lens [B]")
+    if out is None:
+        out = torch.empty((B, hq, d), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        need = lib.pkv_decode_shared_prefix_workspace_size(B, hq, c.num_kv_heads, d, int(max_context_len),
+                                                           int(shared_blocks))
+        workspace = new_workspace(need, q.device)
+    st = lib.pkv_decode_attention_shared_prefix(
+        ctypes.byref(c), _dev(q, "q", 2), hq, _dev(block_tables, "block_tables", dtype=torch.int32),
+        int(block_tables.shape[1]), _dev(context_lens, "context_lens", dtype=torch.int32), B, int(max_context_len),
+        int(shared_blocks), float(scale), _dev(out, "out", dtype=torch.float32), _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _check(st, "pkv_decode_attention_shared_prefix")
     return out
 
 

@@ -106,11 +106,23 @@ pkv_status check_heads(int32_t hq, int32_t hkv) {
 }
 
 // Shared by the decode call and the decode rows of the mixed batch.
+// prefix: the workspace also holds the shared-prefix state of every
+// (sequence, q head).
 pkv_status plan_decode(int32_t num_seqs, int32_t hq, int32_t hkv, int32_t head_dim, int32_t max_context_len,
-                       int32_t req_range_units, int num_sms, pkv::DecodePlan* plan, size_t* ws_bytes) {
+                       int32_t req_range_units, int num_sms, pkv::DecodePlan* plan, size_t* ws_bytes,
+                       bool prefix = false) {
     if (num_seqs < 0 || max_context_len < 0 || req_range_units < 0) return PKV_ERR_SHAPE;
     *plan = pkv::plan_decode_ranges(num_seqs, hkv, max_context_len, num_sms, req_range_units);
-    *ws_bytes = pkv::decode_ws_layout(num_seqs, hq, hkv, head_dim, plan->max_ranges).total;
+    *ws_bytes = pkv::decode_ws_layout(num_seqs, hq, hkv, head_dim, plan->max_ranges, prefix).total;
+    return PKV_OK;
+}
+
+// Shared blocks are checked against max_context_len (every context holds
+// them in full) and the table width.
+pkv_status check_shared_blocks(int32_t shared_blocks, int32_t max_blocks_per_seq, int32_t max_context_len) {
+    if (shared_blocks < 0 || shared_blocks > max_blocks_per_seq ||
+        static_cast<int64_t>(shared_blocks) * 16 > max_context_len)
+        return PKV_ERR_SHAPE;
     return PKV_OK;
 }
 
@@ -381,7 +393,7 @@ pkv_status decode_common(const pkv_cache_t* cache, const void* q, int32_t num_q_
                          const int32_t* query_start_loc, int32_t num_seqs, int32_t max_context_len, float scale,
                          float* out, void* workspace, size_t workspace_bytes, int32_t partition_blocks,
                          void* stream, const void* k_new = nullptr, const void* v_new = nullptr,
-                         const int32_t* slot_mapping = nullptr) {
+                         const int32_t* slot_mapping = nullptr, int32_t shared_blocks = 0) {
     pkv_status st = check_cache(cache);
     if (st != PKV_OK) return st;
     if ((st = check_heads(num_q_heads, cache->num_kv_heads)) != PKV_OK) return st;
@@ -392,10 +404,16 @@ pkv_status decode_common(const pkv_cache_t* cache, const void* q, int32_t num_q_
     if (!aligned16(q) || !aligned16(out)) return PKV_ERR_ALIGN;
     DeviceState* dev = nullptr;
     if ((st = current_device(&dev)) != PKV_OK) return st;
+    // A shared prefix is read once for all sequences on bf16 pools whose rows
+    // a tensor map can address; otherwise every sequence reads it (the same
+    // result).  The workspace is sized for the shared-prefix states either way.
+    const int32_t chunks = pkv::shared_prefix_chunks(num_seqs, num_q_heads, cache->num_kv_heads, shared_blocks);
+    const bool share = chunks > 0 && cache->kv_dtype == PKV_KV_BF16 &&
+                       static_cast<int64_t>(cache->num_blocks) * cache->num_kv_heads * 16 <= INT32_MAX;
     pkv::DecodePlan plan;
     size_t need = 0;
     if ((st = plan_decode(num_seqs, num_q_heads, cache->num_kv_heads, cache->head_dim, max_context_len,
-                          partition_blocks, dev->num_sms, &plan, &need)) != PKV_OK)
+                          partition_blocks, dev->num_sms, &plan, &need, chunks > 0)) != PKV_OK)
         return st;
     if (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return PKV_ERR_WORKSPACE;
@@ -424,6 +442,12 @@ pkv_status decode_common(const pkv_cache_t* cache, const void* q, int32_t num_q_
     a.k_new = k_new;
     a.v_new = v_new;
     a.slot_mapping = slot_mapping;
+    if (share) {
+        a.skip_blocks = shared_blocks;
+        a.prefix_chunks = chunks;
+        cudaError_t e = pkv::launch_shared_prefix(a, static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
     cudaError_t e = pkv::launch_decode(a, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PKV_OK : cuda_fail(e);
 }
@@ -437,6 +461,54 @@ PKV_API pkv_status pkv_decode_attention(const pkv_cache_t* cache, const void* q,
                                         int32_t partition_blocks, void* stream) {
     return decode_common(cache, q, num_q_heads, block_tables, max_blocks_per_seq, context_lens, nullptr, num_seqs,
                          max_context_len, scale, out, workspace, workspace_bytes, partition_blocks, stream);
+}
+
+PKV_API size_t pkv_decode_shared_prefix_workspace_size(int32_t num_seqs, int32_t num_q_heads,
+                                                       int32_t num_kv_heads, int32_t head_dim,
+                                                       int32_t max_context_len, int32_t shared_blocks) {
+    if (check_heads(num_q_heads, num_kv_heads) != PKV_OK) return 0;
+    if (head_dim != 64 && head_dim != 128) return 0;
+    if (shared_blocks < 0 || static_cast<int64_t>(shared_blocks) * 16 > max_context_len) return 0;
+    DeviceState* dev = nullptr;
+    if (current_device(&dev) != PKV_OK) return 0;
+    pkv::DecodePlan plan;
+    size_t bytes = 0;
+    const bool prefix = pkv::shared_prefix_chunks(num_seqs, num_q_heads, num_kv_heads, shared_blocks) > 0;
+    if (plan_decode(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len, 0, dev->num_sms, &plan, &bytes,
+                    prefix) != PKV_OK)
+        return 0;
+    return bytes;
+}
+
+PKV_API pkv_status pkv_decode_attention_shared_prefix(const pkv_cache_t* cache, const void* q, int32_t num_q_heads,
+                                                      const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                                      const int32_t* context_lens, int32_t num_seqs,
+                                                      int32_t max_context_len, int32_t shared_blocks, float scale,
+                                                      float* out, void* workspace, size_t workspace_bytes,
+                                                      void* stream) {
+    pkv_status st = check_shared_blocks(shared_blocks, max_blocks_per_seq, max_context_len);
+    if (st != PKV_OK) return st;
+    return decode_common(cache, q, num_q_heads, block_tables, max_blocks_per_seq, context_lens, nullptr, num_seqs,
+                         max_context_len, scale, out, workspace, workspace_bytes, 0, stream, nullptr, nullptr,
+                         nullptr, shared_blocks);
+}
+
+PKV_API int32_t pkv_common_prefix_blocks(const int32_t* block_tables_host, int32_t max_blocks_per_seq,
+                                         const int32_t* context_lens_host, int32_t num_seqs) {
+    if (block_tables_host == nullptr || context_lens_host == nullptr || num_seqs <= 0 || max_blocks_per_seq <= 0)
+        return 0;
+    int32_t j = max_blocks_per_seq;
+    for (int32_t s = 0; s < num_seqs; ++s) {
+        const int32_t n = context_lens_host[s];
+        j = std::min(j, n > 0 ? n / 16 : 0);
+    }
+    for (int32_t s = 1; s < num_seqs && j > 0; ++s) {
+        const int32_t* row = block_tables_host + static_cast<size_t>(s) * max_blocks_per_seq;
+        int32_t k = 0;
+        while (k < j && row[k] == block_tables_host[k]) ++k;
+        j = k;
+    }
+    return j;
 }
 
 PKV_API pkv_status pkv_decode_step(const pkv_cache_t* cache, const void* k_new, const void* v_new,

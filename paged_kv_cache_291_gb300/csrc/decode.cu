@@ -33,7 +33,7 @@ void arm_decode_stall(int32_t launches) { g_stall_launches.store(launches > 0 ? 
 static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 DecodeWsLayout decode_ws_layout(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                                int32_t max_ranges) {
+                                int32_t max_ranges, bool prefix) {
     const size_t G = static_cast<size_t>(num_q_heads / num_kv_heads);
     DecodeWsLayout L;
     L.header = 0;
@@ -41,7 +41,10 @@ DecodeWsLayout decode_ws_layout(int32_t num_seqs, int32_t num_q_heads, int32_t n
     L.part_ml = L.counters + align256(static_cast<size_t>(num_seqs) * num_kv_heads * 4);
     const size_t slots = static_cast<size_t>(max_ranges) * 2 * G;
     L.part_o = L.part_ml + align256(slots * 8);
-    L.total = L.part_o + align256(slots * head_dim * 4);
+    L.pre_ml = L.part_o + align256(slots * head_dim * 4);
+    const size_t pre = prefix ? static_cast<size_t>(num_seqs) * num_q_heads : 0;
+    L.pre_o = L.pre_ml + align256(pre * 8);
+    L.total = L.pre_o + align256(pre * head_dim * 4);
     return L;
 }
 

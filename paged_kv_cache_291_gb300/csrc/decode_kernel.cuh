@@ -123,6 +123,14 @@ struct DecodeParams {
     const uint8_t* v_new;
     const int32_t* slot_mapping;  // [S]
     float k_inv, v_inv;           // e4m3 pools: 1 / scale (fp32)
+    // Shared prefix: the first skip_blocks blocks of every sequence were
+    // attended by the shared-prefix kernel, which left one state per
+    // (sequence, q head) in pre_ml ([S][Hq] (m, l), log2 domain) and pre_o
+    // ([S][Hq][D], unnormalised).  The item holding a pair's first block
+    // merges it into its own state.  null: no shared prefix.
+    int32_t skip_blocks;
+    const float2* pre_ml;
+    const float* pre_o;
 };
 
 constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
@@ -151,8 +159,8 @@ struct Cfg {
     static constexpr int R_P = R_DESC + kItemRing * (int)sizeof(ItemDesc);
     static constexpr int R_MO = R_P + W * G * kBlockSize * 8;  // p stored as (p, p)
     static constexpr int R_ML = R_MO + MERGE_BUFS * W * G * D * 4;
-    static constexpr int R_WT = R_ML + MERGE_BUFS * W * G * 8;  // merger: [G][W] weights
-    static constexpr int R_MSM = align_up(R_WT + G * W * 4, 8);  // merger: [G] (M, L), float2-aligned
+    static constexpr int R_WT = R_ML + MERGE_BUFS * W * G * 8;  // merger: [G][W] weights, then [G] prefix weights
+    static constexpr int R_MSM = align_up(R_WT + G * (W + 1) * 4, 8);  // merger: [G] (M, L), float2-aligned
     static constexpr int R_BAR = align_up(R_MSM + G * 8, 8);
     static constexpr int STAGES_FIT = (220 * 1024 - R_BAR - 64 * 8 - 16) / STAGE_BYTES;
     // Each consumer warp owns SW consecutive stages that it consumes in
@@ -244,9 +252,9 @@ __device__ __noinline__ void store_new_row_e4m3(const DecodeParams& P, size_t of
 }
 
 // Units of work of one kv head of sequence s: one per 16-token block of its
-// context (at least one, so that an empty context still yields its zero
-// output row), 0 for rows that are not decode rows.  The context length is
-// clamped to what the block table can address.
+// context past the shared prefix (at least one, so that an empty context
+// still yields its output row), 0 for rows that are not decode rows.  The
+// context length is clamped to what the block table can address.
 __device__ __forceinline__ int seq_units(const DecodeParams& P, int s, int& n_out, bool report) {
     const int qlen = P.qsl ? (__ldg(P.qsl + s + 1) - __ldg(P.qsl + s)) : 1;
     if (qlen != 1) {
@@ -259,7 +267,7 @@ __device__ __forceinline__ int seq_units(const DecodeParams& P, int s, int& n_ou
         n = n < 0 ? 0 : P.ctx_cap;
     }
     n_out = n;
-    return max(1, (n + kBlockSize - 1) / kBlockSize);
+    return max(1, (n + kBlockSize - 1) / kBlockSize - P.skip_blocks);
 }
 
 __device__ __forceinline__ uint4 lds128(const void* p) {
@@ -497,9 +505,11 @@ __device__ void run_producer(const DecodeParams& P, uint8_t* smem, const Bars& B
         const int g = static_cast<int>((pos - seq0) / u);
         const long long P0 = seq0 + static_cast<long long>(g) * u;  // the pair's units: [P0, P0 + u)
         const long long u1 = min(P0 + u, end);
+        // Block indices in the sequence's table: the pair's units start at
+        // its first block past the shared prefix.
         const int nblk = (n + kBlockSize - 1) / kBlockSize;
-        const int b0 = static_cast<int>(pos - P0);
-        const int b1 = min(static_cast<int>(u1 - P0), nblk);
+        const int b0 = P.skip_blocks + static_cast<int>(pos - P0);
+        const int b1 = min(P.skip_blocks + static_cast<int>(u1 - P0), nblk);
         const long long r0 = P0 / RU;
         // A pair is split by every boundary strictly inside it: for a pair
         // longer than a range these are the multiples of RU; a shorter pair
@@ -859,6 +869,30 @@ __device__ void run_merger(const DecodeParams& P, uint8_t* smem, const Bars& B, 
         if (d.s < 0) break;
         __syncwarp();
         if (lane == 0) mbar_arrive(&B.iempty[slot]);
+        const unsigned FULL = 0xffffffffu;
+        constexpr int W = C::W;
+        constexpr int CH = G * D / 4;
+        constexpr int WL = C::MERGE_LANES;
+        constexpr int NJ = (CH + 31) / 32;
+        const int h0 = d.g * G;
+        // Shared prefix: the item holding the pair's first block (the only
+        // part, or the first of a split pair) merges the prefix state of
+        // the pair's G heads into its own.  It is read now, while the
+        // consumers still work on the item: (m, l) of head `lane` and this
+        // lane's float4 chunks of the o rows.
+        const bool fold = P.pre_ml != nullptr && (d.nparts == 1 || d.slot == 1);
+        float2 pml = make_float2(-INFINITY, 0.f);
+        float4 po[NJ];
+        if (fold) {
+            const size_t hrow = static_cast<size_t>(d.s) * P.hq + h0;
+            if (lane < G) pml = __ldcg(P.pre_ml + hrow + lane);
+            const float4* src = reinterpret_cast<const float4*>(P.pre_o + hrow * D);
+#pragma unroll
+            for (int j = 0; j < NJ; ++j) {
+                const int k = lane + 32 * j;
+                po[j] = (k < CH) ? __ldcg(src + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
         const int buf = item_seq % C::MERGE_BUFS;
         if (!mbar_wait_warp(&B.mfull[buf], (item_seq / C::MERGE_BUFS) & 1)) {
             ok = false;
@@ -868,11 +902,9 @@ __device__ void run_merger(const DecodeParams& P, uint8_t* smem, const Bars& B, 
         // weights of all (q head g, warp w) pairs at once: lane g * W + w,
         // W lanes per head; then each lane combines whole float4 chunks of
         // the item's G output rows (contiguous in out and in part_o), with
-        // the W chunk loads issued together.
-        const unsigned FULL = 0xffffffffu;
-        constexpr int W = C::W;
-        constexpr int CH = G * D / 4;
-        constexpr int WL = C::MERGE_LANES;
+        // the W chunk loads issued together.  With a prefix state (m_p,
+        // l_p, o_p) the reference becomes max(M, m_p): the warps' weights
+        // take the factor 2^(M - max) and o_p the weight 2^(m_p - max).
 #pragma unroll
         for (int i0 = 0; i0 < G * WL; i0 += 32) {
             const int i = i0 + lane;
@@ -882,17 +914,27 @@ __device__ void run_merger(const DecodeParams& P, uint8_t* smem, const Bars& B, 
             float M = e.x;
 #pragma unroll
             for (int o = 1; o < WL; o <<= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, o));
-            const float wt = (e.x == -INFINITY) ? 0.f : fast_exp2(e.x - M);
+            float wt = (e.x == -INFINITY) ? 0.f : fast_exp2(e.x - M);
             float L = e.y * wt;
 #pragma unroll
             for (int o = 1; o < WL; o <<= 1) L += __shfl_xor_sync(FULL, L, o);
+            float wp = 0.f;  // weight of the prefix state
+            if (fold) {
+                const float2 pe = make_float2(__shfl_sync(FULL, pml.x, gi & 31), __shfl_sync(FULL, pml.y, gi & 31));
+                const float Mx = fmaxf(M, pe.x);
+                const float fl = (M == -INFINITY) ? 0.f : fast_exp2(M - Mx);
+                wp = (pe.x == -INFINITY) ? 0.f : fast_exp2(pe.x - Mx);
+                wt *= fl;
+                L = L * fl + pe.y * wp;
+                M = Mx;
+            }
             if (live) {
                 wsm[gi * W + w] = wt;
                 if (w == 0) msm[gi] = make_float2(M, L);
+                if (w == 0 && fold) wsm[G * W + gi] = wp;
             }
         }
         __syncwarp();
-        const int h0 = d.g * G;
         const size_t pi0 = (static_cast<size_t>(d.r) * 2 + d.slot) * G;  // this part's partial slots, one per head
         const float4* mo4 = reinterpret_cast<const float4*>(mo) + static_cast<size_t>(buf) * W * CH;
         float4* dst = (d.nparts == 1)
@@ -907,6 +949,10 @@ __device__ void run_merger(const DecodeParams& P, uint8_t* smem, const Bars& B, 
 #pragma unroll
                 for (int w = 0; w < W; ++w) v[w] = mo4[w * CH + k];
                 float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (fold) {
+                    const float wp = wsm[G * W + g];
+                    a = make_float4(po[j].x * wp, po[j].y * wp, po[j].z * wp, po[j].w * wp);
+                }
 #pragma unroll
                 for (int w = 0; w < W; ++w) {
                     const float wt = wsm[g * W + w];
@@ -963,7 +1009,6 @@ __device__ void run_merger(const DecodeParams& P, uint8_t* smem, const Bars& B, 
                 }
 #pragma unroll
                 for (int g = 0; g < G; ++g) M[g] = warp_max(M[g]);
-                constexpr int NJ = (CH + 31) / 32;
                 float4 acc[NJ];
 #pragma unroll
                 for (int j = 0; j < NJ; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1090,7 +1135,7 @@ __device__ void prefetch_first_blocks(const DecodeParams& P, int lane, int max_u
         if (s < P.num_seqs) {
             const bool dec = P.qsl == nullptr || ld_l2_only(P.qsl + s + 1) - ld_l2_only(P.qsl + s) == 1;
             const int n = min(max(ld_l2_only(P.context_lens + s), 0), P.ctx_cap);
-            u[w] = dec ? max(1, (n + kBlockSize - 1) / kBlockSize) : 0;
+            u[w] = dec ? max(1, (n + kBlockSize - 1) / kBlockSize - P.skip_blocks) : 0;
         }
     }
     long long per_head = 0;
@@ -1122,8 +1167,8 @@ __device__ void prefetch_first_blocks(const DecodeParams& P, int lane, int max_u
             const int g = static_cast<int>((x - seq0) / us);
             const int b0 = static_cast<int>(x - seq0 - static_cast<long long>(g) * us);
             const int cnt = static_cast<int>(min(static_cast<long long>(us - b0), hi - x));
-            const int32_t* trow = P.block_tables + static_cast<size_t>(w * 32 + j) * P.max_blocks;
-            for (int b = lane; b < cnt; b += 32) {
+            const int32_t* trow = P.block_tables + static_cast<size_t>(w * 32 + j) * P.max_blocks + P.skip_blocks;
+            for (int b = lane; b < cnt && P.skip_blocks + b0 + b < P.max_blocks; b += 32) {
                 const int phys = ld_l2_only(trow + b0 + b);
                 if (phys >= 0 && phys < P.num_blocks) {
                     const size_t slab = (static_cast<size_t>(phys) * P.hkv + g) * C::SLAB;
@@ -1218,7 +1263,8 @@ cudaError_t dispatch_g(const DecodeParams& P, int G, int grid, cudaStream_t stre
 template <bool FUSED>
 cudaError_t launch_decode_t(const DecodeArgs& a, bool stall, cudaStream_t stream) {
     const DecodeWsLayout L =
-        decode_ws_layout(a.num_seqs, a.num_q_heads, a.num_kv_heads, a.head_dim, a.plan.max_ranges);
+        decode_ws_layout(a.num_seqs, a.num_q_heads, a.num_kv_heads, a.head_dim, a.plan.max_ranges,
+                         a.prefix_chunks > 0);
     uint8_t* ws = static_cast<uint8_t*>(a.workspace);
     DecodeParams P;
     P.k_pool = static_cast<uint8_t*>(a.k_pool);
@@ -1249,6 +1295,9 @@ cudaError_t launch_decode_t(const DecodeArgs& a, bool stall, cudaStream_t stream
     P.slot_mapping = a.slot_mapping;
     P.k_inv = a.kv_e4m3 ? 1.f / a.k_scale : 1.f;
     P.v_inv = a.kv_e4m3 ? 1.f / a.v_scale : 1.f;
+    P.skip_blocks = a.skip_blocks;
+    P.pre_ml = a.prefix_chunks > 0 ? reinterpret_cast<const float2*>(ws + L.pre_ml) : nullptr;
+    P.pre_o = a.prefix_chunks > 0 ? reinterpret_cast<const float*>(ws + L.pre_o) : nullptr;
     const int G = a.num_q_heads / a.num_kv_heads;
     if (a.kv_e4m3) {
         // q' = q * scale*log2(e) * k_scale against the K codes.

@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace pkv {
@@ -42,6 +43,12 @@ struct DecodeArgs {
     const void* k_new = nullptr;
     const void* v_new = nullptr;
     const int32_t* slot_mapping = nullptr;
+    // Shared prefix: every sequence's first skip_blocks blocks are attended
+    // by launch_shared_prefix (prefix_chunks CTAs per kv head and query
+    // tile, one cluster), which leaves one state per (sequence, q head) in
+    // the workspace; decode attends the rest and merges.  0 for plain decode.
+    int32_t skip_blocks = 0;
+    int32_t prefix_chunks = 0;
 };
 
 struct DecodeWsLayout {
@@ -49,11 +56,26 @@ struct DecodeWsLayout {
     size_t counters;    // uint32 [S][Hkv] arrival tickets
     size_t part_ml;     // float2 [max_ranges][2][G]
     size_t part_o;      // float [max_ranges][2][G][d]
+    size_t pre_ml;      // shared prefix: float2 [S][Hq] (m, l) of the shared blocks
+    size_t pre_o;       //                float [S][Hq][d] their unnormalised o
     size_t total;
 };
 
 DecodeWsLayout decode_ws_layout(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                                int32_t max_ranges);
+                                int32_t max_ranges, bool prefix = false);
+
+// Shared-prefix decode: CTAs (one cluster) that split the shared blocks of
+// one kv head and query tile (0 when shared_blocks is 0).
+int32_t shared_prefix_chunks(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t shared_blocks);
+
+// The shared blocks' state per (sequence, q head) for a decode launch `a`
+// (a.skip_blocks shared blocks in a.prefix_chunks chunks, bf16 pools);
+// launch it right before launch_decode(a) on the same stream.
+cudaError_t launch_shared_prefix(const DecodeArgs& a, cudaStream_t stream);
+
+// A tiled tensor map of bf16 elements with the 128-byte swizzle.
+bool make_bf16_map(CUtensorMap* map, const void* base, cuuint32_t rank, const cuuint64_t* dims,
+                   const cuuint64_t* strides_bytes, const cuuint32_t* box);
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 // The fused step's variant (a.k_new set), called by launch_decode.

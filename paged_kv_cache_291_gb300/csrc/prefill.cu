@@ -654,7 +654,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+}  // namespace
+
+// The driver's tensor-map encoder, looked up once through the runtime.
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (fn == nullptr) {
         void* p = nullptr;
@@ -667,8 +670,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-bool make_map(CUtensorMap* map, const void* base, cuuint32_t rank, const cuuint64_t* dims,
-              const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+bool make_bf16_map(CUtensorMap* map, const void* base, cuuint32_t rank, const cuuint64_t* dims,
+                   const cuuint64_t* strides_bytes, const cuuint32_t* box) {
     auto fn = encode_fn();
     if (fn == nullptr) return false;
     const cuuint32_t elem_strides[3] = {1, 1, 1};
@@ -678,8 +681,6 @@ bool make_map(CUtensorMap* map, const void* base, cuuint32_t rank, const cuuint6
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
-
-}  // namespace
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
     if (a.head_dim != 64 && a.head_dim != kMaxHeadDim) return cudaErrorNotSupported;
@@ -691,15 +692,15 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
         const cuuint64_t strides[2] = {static_cast<cuuint64_t>(a.head_dim) * 2,
                                        static_cast<cuuint64_t>(a.num_q_heads) * a.head_dim * 2};
         const cuuint32_t box[3] = {64, 1, kTileM};
-        if (!make_map(&tq, a.q, 3, dims, strides, box)) return cudaErrorInvalidValue;
+        if (!make_bf16_map(&tq, a.q, 3, dims, strides, box)) return cudaErrorInvalidValue;
     }
     {
         const cuuint64_t rows = static_cast<cuuint64_t>(a.num_blocks) * a.num_kv_heads * kBlockSize;
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.head_dim), rows > 0 ? rows : 1};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.head_dim) * 2};
         const cuuint32_t box[2] = {64, kBlockSize};
-        if (!make_map(&tk, a.k_pool, 2, dims, strides, box)) return cudaErrorInvalidValue;
-        if (!make_map(&tv, a.v_pool, 2, dims, strides, box)) return cudaErrorInvalidValue;
+        if (!make_bf16_map(&tk, a.k_pool, 2, dims, strides, box)) return cudaErrorInvalidValue;
+        if (!make_bf16_map(&tv, a.v_pool, 2, dims, strides, box)) return cudaErrorInvalidValue;
     }
     PrefillParams P;
     P.q = static_cast<const uint8_t*>(a.q);
