@@ -50,14 +50,17 @@
 //    cvt.f32.f16.  The K scale folds into q and the V scale into the final
 //    1/l, so no per-element multiply is added.  The extra conversion work
 //    per block makes the consumers the limit, so e4m3 pools with head
-//    groups of 1 and 2 run 16 consumer warps.
+//    groups of 1 and 2 run 16 consumer warps; at d = 128 with G >= 2 the
+//    block math runs on tensor cores instead (run_consumer_mma).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
+#include <cstring>
 
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
@@ -66,20 +69,34 @@ namespace pkv {
 
 namespace {
 
+// e4m3 pools with d = 128 and head groups of 2 or more take the consumers'
+// block math on tensor cores (see run_consumer_mma); their slabs arrive as
+// swizzled TMA tiles.  With one q head per kv head, 7 of the MMA's 8
+// columns would be empty and the CUDA-core math is faster (LLaMA-13B MHA:
+// 389 against 418 us).  A build can turn it off with PKV_DECODE_NO_MMA.
+template <int D, int G, int EB>
+constexpr bool use_mma() {
+#ifdef PKV_DECODE_NO_MMA
+    return false;
+#else
+    return D == 128 && EB == 1 && G >= 2;
+#endif
+}
+
 // Consumer warps per CTA: 12 for head groups of 1 or 2 (their per-lane state
 // is small, and a fourth warp per scheduler hides more of the latency of the
 // dependent shuffle and FMA chains), 8 for groups of 4 and 8 (which need
 // more than the 128 registers a thread that 14 warps leave).  e4m3 pools
-// (EB = 1) with groups of 1 or 2 take 16: their blocks cost more issue
-// (the widening) and half the ring bytes, so the same ring still gives each
-// warp 3 stages.  A build can force one count for every group with
-// PKV_DECODE_CONSUMER_WARPS.
-template <int G, int EB>
+// (EB = 1) with groups of 1 or 2 on CUDA cores take 16: their blocks cost
+// more issue (the widening) and half the ring bytes, so the same ring still
+// gives each warp 3 stages.  A build can force one count for every group
+// with PKV_DECODE_CONSUMER_WARPS.
+template <int D, int G, int EB>
 constexpr int consumer_warps() {
 #ifdef PKV_DECODE_CONSUMER_WARPS
     return PKV_DECODE_CONSUMER_WARPS;
 #else
-    return G <= 2 ? (EB == 1 ? 16 : 12) : 8;
+    return use_mma<D, G, EB>() ? (G <= 2 ? 12 : 8) : (G <= 2 ? (EB == 1 ? 16 : 12) : 8);
 #endif
 }
 constexpr int kItemRing = 8;
@@ -137,7 +154,9 @@ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
 template <int D, int G, int EB>
 struct Cfg {
-    static constexpr int W = consumer_warps<G, EB>();  // consumer warps
+    static constexpr bool MMA = use_mma<D, G, EB>();
+    static constexpr int ALIGN_PAD = MMA ? 1024 : 0;  // swizzled tiles need a 1024-byte aligned ring
+    static constexpr int W = consumer_warps<D, G, EB>();  // consumer warps
     static_assert(W >= 1 && W <= 16, "consumer warps");
     // Lanes per q head in the merger's weight reduction: W rounded up to a
     // power of two (the extra lanes carry empty states).
@@ -162,7 +181,7 @@ struct Cfg {
     static constexpr int R_WT = R_ML + MERGE_BUFS * W * G * 8;  // merger: [G][W] weights, then [G] prefix weights
     static constexpr int R_MSM = align_up(R_WT + G * (W + 1) * 4, 8);  // merger: [G] (M, L), float2-aligned
     static constexpr int R_BAR = align_up(R_MSM + G * 8, 8);
-    static constexpr int STAGES_FIT = (220 * 1024 - R_BAR - 64 * 8 - 16) / STAGE_BYTES;
+    static constexpr int STAGES_FIT = (220 * 1024 - R_BAR - 64 * 8 - 16 - ALIGN_PAD) / STAGE_BYTES;
     // Each consumer warp owns SW consecutive stages that it consumes in
     // order (an mbarrier parity wait is only exact when the waiter is at
     // most one phase ahead of the barrier).
@@ -182,11 +201,11 @@ struct Cfg {
     static constexpr int OFF_BAR = OFF_REST + R_BAR;
     static constexpr int OFF_FLAG = OFF_BAR + NBAR * 8;
     static constexpr int OFF_NEW = OFF_FLAG + 16;  // [STAGES] fused step: slot of a stage's new row, or -1
-    static constexpr int SMEM = OFF_NEW + STAGES * 4;
+    static constexpr int SMEM = OFF_NEW + STAGES * 4 + ALIGN_PAD;
     static_assert(SW >= 1, "ring too shallow");
     static_assert(OFF_ITEMQ % 16 == 0 && OFF_DESC % 16 == 0 && OFF_P % 16 == 0 && OFF_MO % 16 == 0 &&
                       OFF_ML % 8 == 0 && OFF_MSM % 8 == 0 && OFF_BAR % 8 == 0 && OFF_NEW % 4 == 0 &&
-                      STAGE_BYTES % 16 == 0,
+                      STAGE_BYTES % 16 == 0 && (!MMA || STAGE_BYTES % 1024 == 0),
                   "shared-memory regions aligned for their widest access");
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
     static_assert(NV * RPP == kBlockSize, "rows");
@@ -280,11 +299,24 @@ __device__ __forceinline__ uint4 lds128(const void* p) {
 
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t u) { return make_float2(bf16lo(u), bf16hi(u)); }
 
-__device__ __forceinline__ uint2 lds64(const void* p) {
-    uint2 v;
-    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(smem_addr(p)));
-    return v;
+// Tiled 2-D TMA load of a box at (x, y) of `map` into shared memory,
+// completed on `bar` as tx bytes, with an L2 cache policy.
+__device__ __forceinline__ void tma_tile_g2s(void* smem_dst, const CUtensorMap* map, int32_t x, int32_t y,
+                                             uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], "
+        "[%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
 }
+
+// Byte offset of 16-byte chunk c of row r in a slab stored as 128-byte
+// swizzled panels of 16 rows (a tiled TMA copy with the 128-byte swizzle:
+// within a row's 128 bytes the chunk index is XORed with r mod 8).
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+    return static_cast<uint32_t>((c >> 3) * (kBlockSize * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
 
 __device__ __forceinline__ float2 f16x2_to_float2(uint32_t h) {
     float2 r;
@@ -423,8 +455,8 @@ __device__ __forceinline__ void compute_block(const uint8_t* kst, const uint8_t*
 }
 
 template <int D, int G, int EB, bool FUSED>
-__device__ void run_producer(const DecodeParams& P, uint8_t* smem, const Bars& B, volatile int* abort_flag,
-                             int lane) {
+__device__ void run_producer(const DecodeParams& P, const CUtensorMap* tmk, const CUtensorMap* tmv, uint8_t* smem,
+                             const Bars& B, volatile int* abort_flag, int lane) {
     using C = Cfg<D, G, EB>;
     ItemDesc* descs = reinterpret_cast<ItemDesc*>(smem + C::OFF_DESC);
     int* stage_new = reinterpret_cast<int*>(smem + C::OFF_NEW);
@@ -603,7 +635,7 @@ __device__ void run_producer(const DecodeParams& P, uint8_t* smem, const Bars& B
                         // written (the pool's row is used as it is).
                         record_error(P.err, kErrRange, static_cast<uint32_t>(s));
                     }
-                    if (FUSED && EB == 2 && fresh) {
+                    if (FUSED && EB == 2 && fresh && !C::MMA) {
                         // Rows before the new token from the pool, the new
                         // row from k_new/v_new (rows past it are never read).
                         constexpr uint32_t kRow = D * EB;
@@ -615,6 +647,14 @@ __device__ void run_producer(const DecodeParams& P, uint8_t* smem, const Bars& B
                         }
                         bulk_g2s(dst + srow * kRow, P.k_new + nr, kRow, &B.full[st]);
                         bulk_g2s(dst + C::SLAB + srow * kRow, P.v_new + nr, kRow, &B.full[st]);
+                    } else if constexpr (C::MMA) {
+                        // One swizzled 16-row tile per slab (rows of 128
+                        // bytes); its first row in the pool's row space.
+                        static_assert(D * EB == 128, "one 128-byte panel per row");
+                        const int y = (phys * P.hkv + g) * kBlockSize;
+                        mbar_arrive_expect_tx(&B.full[st], 2 * C::SLAB);
+                        tma_tile_g2s(dst, tmk, 0, y, &B.full[st], policy);
+                        tma_tile_g2s(dst + C::SLAB, tmv, 0, y, &B.full[st], policy);
                     } else {
                         mbar_arrive_expect_tx(&B.full[st], 2 * C::SLAB);
                         bulk_g2s_hint(dst, P.k_pool + slab, C::SLAB, &B.full[st], policy);
@@ -735,7 +775,10 @@ __device__ __forceinline__ void store_stage_new_row(const DecodeParams& P, const
     if (sub == srow % C::RPP) {
         const size_t at = (static_cast<size_t>(ns / kBlockSize) * P.hkv + d.g) * C::SLAB +
                           static_cast<size_t>(srow) * D * EB + cl * 8 * EB;
-        uint8_t* kr = kst + srow * D * EB + cl * 8 * EB;
+        // The stage holds the row at its place in the slab, or (MMA
+        // configurations) in the swizzled tile layout.
+        const int byte = cl * 8 * EB;
+        uint8_t* kr = kst + (C::MMA ? static_cast<int>(swz(srow, byte >> 4)) + (byte & 15) : srow * D * EB + byte);
         if constexpr (EB == 2) {
             *reinterpret_cast<uint4*>(P.k_pool + at) = lds128(kr);
             *reinterpret_cast<uint4*>(P.v_pool + at) = lds128(kr + C::SLAB);
@@ -745,6 +788,263 @@ __device__ __forceinline__ void store_stage_new_row(const DecodeParams& P, const
         }
     }
     __syncwarp();
+}
+
+// ---------------------------------------------------------------- MMA consumers
+// e4m3 pools with d = 128 and G >= 2 run the consumers' block math on
+// warp-level tensor cores (mma.sync m16n8k16, f16 operands, fp32
+// accumulators); their slabs arrive as tiled TMA copies with the 128-byte
+// swizzle (one 16-row box of 128 codes per slab), so no fragment load waits
+// on a bank conflict.  Per
+// 16-row block, S = K q^T (16 keys x 8 columns: the group's G heads, the
+// rest zero) and O^T += V^T P^T (16 dims x 8 heads per MMA).  Lane (g, t) =
+// (lane / 4, lane % 4) holds the MMA fragments; the contractions are sums,
+// so their order is permuted:
+//  * q.K^T: lane (g, t) reads 16-byte chunks 2t and 2t+1 of key rows g and
+//    g+8 (32 codes); q of head g over the same dims is its B fragment;
+//  * P.V: lane (g, t) reads chunk g (16 codes) of key rows 2t, 2t+1, 2t+8,
+//    2t+9; MMA 2i's rows g and g+8 are dims 16g + 4i and 16g + 4i + 1, MMA
+//    2i+1's dims 16g + 4i + 2 and + 3.
+// With the swizzle (chunk c of row r at 16 (c xor (r mod 8))), the 8 lanes
+// of every 16-byte load phase hit 8 different bank groups.  S lands as keys
+// {g, g+8} x heads {2t, 2t+1}, the heads of the lane's O columns, so the
+// online softmax moves no data; P goes to the B layout (head g, keys 2t,
+// 2t+1, 2t+8, 2t+9) by shuffles.  P is split into an f16 hi and lo part
+// (P.V runs twice), P to 2^-22 relative.  e4m3 codes widen to f16 exactly;
+// q is scaled per head by a power of two into [1, 2) (exact) for f16, the
+// factor given back to the scores.  Rows past the context are masked in S
+// and zeroed in V (0 x NaN would poison the sum).
+__device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two e4m3 codes (low 16 bits of w) -> f16x2, exact.
+__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t w) {
+    uint32_t h;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, lo;\n\t}" : "=r"(h) : "r"(w));
+    return h;
+}
+
+// Two floats -> f16x2 (nearest even), lo in the low half.
+__device__ __forceinline__ uint32_t f16x2_rn(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// A pair of probabilities (below 256) as two f16 MMA operands: hi is p
+// rounded, lo the rounded rest, so hi + lo = p to 2^-22 relative.
+__device__ __forceinline__ void split_pair_f16(float a, float b, uint32_t& hi, uint32_t& lo) {
+    hi = f16x2_rn(a, b);
+    const float2 h = f16x2_to_float2(hi);
+    lo = f16x2_rn(a - h.x, b - h.y);
+}
+
+template <int D, int G>
+__device__ __forceinline__ void compute_block_mma(const uint8_t* kst, const uint8_t* vst, int valid,
+                                                  const uint32_t (&qb)[D / 8], float f0, float f1, float& m0,
+                                                  float& m1, float& l0, float& l1, float (&o)[D / 16][4],
+                                                  int lane) {
+    const unsigned FULL = 0xffffffffu;
+    const int g = lane >> 2, t = lane & 3;
+    // ---- S = K q^T: chunk 2t + c of key rows g and g + 8, 16 codes =
+    // k-steps 4c .. 4c + 3.
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int c = 0; c < D / 64; ++c) {
+        const uint4 r0 = lds128(kst + swz(g, 2 * t + c)), r8 = lds128(kst + swz(g + 8, 2 * t + c));
+        const uint32_t w0[4] = {r0.x, r0.y, r0.z, r0.w}, w8[4] = {r8.x, r8.y, r8.z, r8.w};
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const int kk = 4 * c + w;
+            mma_f16(s, e4m3x2_f16x2(w0[w]), e4m3x2_f16x2(w8[w]), e4m3x2_f16x2(w0[w] >> 16),
+                    e4m3x2_f16x2(w8[w] >> 16), qb[2 * kk], qb[2 * kk + 1]);
+        }
+    }
+    // ---- online softmax (log2 domain) on keys {g, g+8} x heads {2t, 2t+1}
+    const bool vg = g < valid, vg8 = g + 8 < valid;
+    const float x00 = vg ? s[0] * f0 : -INFINITY, x01 = vg ? s[1] * f1 : -INFINITY;
+    const float x10 = vg8 ? s[2] * f0 : -INFINITY, x11 = vg8 ? s[3] * f1 : -INFINITY;
+    float mb0 = fmaxf(x00, x10), mb1 = fmaxf(x01, x11);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        mb0 = fmaxf(mb0, __shfl_xor_sync(FULL, mb0, off));
+        mb1 = fmaxf(mb1, __shfl_xor_sync(FULL, mb1, off));
+    }
+    // The reference moves only when the block's maximum exceeds it by more
+    // than 2^8, so P stays below 256 and O is rescaled on few blocks.
+    if (mb0 > m0 + kRescaleThreshold) {
+        const float a = fast_exp2(m0 - mb0);
+        l0 *= a;
+#pragma unroll
+        for (int mm = 0; mm < D / 16; ++mm) o[mm][0] *= a, o[mm][2] *= a;
+        m0 = mb0;
+    }
+    if (mb1 > m1 + kRescaleThreshold) {
+        const float a = fast_exp2(m1 - mb1);
+        l1 *= a;
+#pragma unroll
+        for (int mm = 0; mm < D / 16; ++mm) o[mm][1] *= a, o[mm][3] *= a;
+        m1 = mb1;
+    }
+    const float p00 = fast_exp2(x00 - m0), p01 = fast_exp2(x01 - m1);
+    const float p10 = fast_exp2(x10 - m0), p11 = fast_exp2(x11 - m1);
+    l0 += p00 + p10;
+    l1 += p01 + p11;
+    // ---- P^T in the B layout: head g, keys (2t, 2t+1) and (2t+8, 2t+9).
+    // Key 2t of head g sits in lane 8t + g/2 (key 2t+1: + 4), as element
+    // g % 2 of its (key, key+8) pair.
+    uint32_t x0h, x0l, x1h, x1l;  // (key g, key g+8) of heads 2t and 2t+1
+    split_pair_f16(p00, p10, x0h, x0l);
+    split_pair_f16(p01, p11, x1h, x1l);
+    const int la = 8 * t + (g >> 1), lb = la + 4;
+    const bool odd = g & 1;
+    uint32_t ah = __shfl_sync(FULL, x0h, la), ah1 = __shfl_sync(FULL, x1h, la);
+    uint32_t bh = __shfl_sync(FULL, x0h, lb), bh1 = __shfl_sync(FULL, x1h, lb);
+    uint32_t al = __shfl_sync(FULL, x0l, la), al1 = __shfl_sync(FULL, x1l, la);
+    uint32_t bl = __shfl_sync(FULL, x0l, lb), bl1 = __shfl_sync(FULL, x1l, lb);
+    if (odd) ah = ah1, bh = bh1, al = al1, bl = bl1;
+    const uint32_t ph0 = __byte_perm(ah, bh, 0x5410), ph1 = __byte_perm(ah, bh, 0x7632);
+    const uint32_t pl0 = __byte_perm(al, bl, 0x5410), pl1 = __byte_perm(al, bl, 0x7632);
+    // ---- O^T += V^T P^T over this lane's dims 16g .. 16g + 15: chunk g of
+    // rows 2t, 2t+1, 2t+8, 2t+9; word i holds dims 16g + 4i .. + 3 (MMAs
+    // 2i, 2i+1).  Rows past the context are zero.
+    const int key0 = 2 * t, key2 = 2 * t + 8;
+    uint4 ra = lds128(vst + swz(key0, g)), rb = lds128(vst + swz(key0 + 1, g));
+    uint4 rc = lds128(vst + swz(key2, g)), rd = lds128(vst + swz(key2 + 1, g));
+    if (key0 >= valid) ra = make_uint4(0u, 0u, 0u, 0u);
+    if (key0 + 1 >= valid) rb = make_uint4(0u, 0u, 0u, 0u);
+    if (key2 >= valid) rc = make_uint4(0u, 0u, 0u, 0u);
+    if (key2 + 1 >= valid) rd = make_uint4(0u, 0u, 0u, 0u);
+    const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w}, wb[4] = {rb.x, rb.y, rb.z, rb.w};
+    const uint32_t wc[4] = {rc.x, rc.y, rc.z, rc.w}, wd[4] = {rd.x, rd.y, rd.z, rd.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t ab0 = __byte_perm(wa[i], wb[i], 0x5140), ab1 = __byte_perm(wa[i], wb[i], 0x7362);
+        const uint32_t cd0 = __byte_perm(wc[i], wd[i], 0x5140), cd1 = __byte_perm(wc[i], wd[i], 0x7362);
+        const uint32_t a0 = e4m3x2_f16x2(ab0), a1 = e4m3x2_f16x2(ab0 >> 16);
+        const uint32_t a2 = e4m3x2_f16x2(cd0), a3 = e4m3x2_f16x2(cd0 >> 16);
+        mma_f16(o[2 * i], a0, a1, a2, a3, ph0, ph1);
+        mma_f16(o[2 * i], a0, a1, a2, a3, pl0, pl1);
+        const uint32_t b0 = e4m3x2_f16x2(ab1), b1 = e4m3x2_f16x2(ab1 >> 16);
+        const uint32_t b2 = e4m3x2_f16x2(cd1), b3 = e4m3x2_f16x2(cd1 >> 16);
+        mma_f16(o[2 * i + 1], b0, b1, b2, b3, ph0, ph1);
+        mma_f16(o[2 * i + 1], b0, b1, b2, b3, pl0, pl1);
+    }
+}
+
+// Consumer warps with MMA block math (e4m3 pools, d = 128): the item loop
+// of run_consumer, with q, the softmax state and O in the MMA layouts.
+template <int D, int G, int EB, bool FUSED>
+__device__ void run_consumer_mma(const DecodeParams& P, uint8_t* smem, const Bars& B, volatile int* abort_flag,
+                                 int warp, int lane) {
+    using C = Cfg<D, G, EB>;
+    constexpr int QW = D / 8;  // q words (two elements each) of a lane: its D/4 dims
+    const unsigned FULL = 0xffffffffu;
+    const ItemDesc* descs = reinterpret_cast<const ItemDesc*>(smem + C::OFF_DESC);
+    const volatile int* stage_new = reinterpret_cast<const volatile int*>(smem + C::OFF_NEW);
+    float* mo = reinterpret_cast<float*>(smem + C::OFF_MO);
+    float2* ml = reinterpret_cast<float2*>(smem + C::OFF_ML);
+    const int g = lane >> 2, t = lane & 3;
+    uint32_t taken = 0, item_seq = 0;
+    bool ok = true;
+    while (ok) {
+        const uint32_t slot = item_seq % kItemRing;
+        if (*abort_flag || !mbar_wait_warp(&B.ifull[slot], (item_seq / kItemRing) & 1)) {
+            ok = false;
+            break;
+        }
+        const ItemDesc d = descs[slot];
+        if (d.s < 0) break;
+        // q of head g, dims 32t .. 32t + 31, as B fragments (zero for
+        // g >= G), scaled by 2^-e into [1, 2) for f16 (exact); the scores
+        // of heads 2t and 2t + 1 get the factor 2^e back.
+        uint32_t qb[QW];
+        float f0, f1;
+        {
+            const uint8_t* qs = smem + C::OFF_ITEMQ + slot * C::QBYTES + (g * D + t * (D / 4)) * 2;
+#pragma unroll
+            for (int c = 0; c < QW / 4; ++c) {
+                uint4 u = make_uint4(0u, 0u, 0u, 0u);
+                if (g < G) u = lds128(qs + 16 * c);
+                qb[4 * c] = u.x, qb[4 * c + 1] = u.y, qb[4 * c + 2] = u.z, qb[4 * c + 3] = u.w;
+            }
+            float mx = 0.f;
+#pragma unroll
+            for (int i = 0; i < QW; ++i) mx = fmaxf(mx, fmaxf(fabsf(bf16lo(qb[i])), fabsf(bf16hi(qb[i]))));
+            mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 2));
+            int e = (mx >= 0x1p-100f && mx < INFINITY) ? static_cast<int>((__float_as_uint(mx) >> 23) & 0xFF) - 127
+                                                         : 0;
+            e = min(e, 100);  // |q| up to 2^101 (f16 would overflow beyond)
+            const float down = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e
+            const float up = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);    // 2^e
+#pragma unroll
+            for (int i = 0; i < QW; ++i) qb[i] = f16x2_rn(bf16lo(qb[i]) * down, bf16hi(qb[i]) * down);
+            f0 = P.scale_log2 * __shfl_sync(FULL, up, (8 * t) & 31);
+            f1 = P.scale_log2 * __shfl_sync(FULL, up, (8 * t + 4) & 31);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&B.iempty[slot]);
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+        float o[D / 16][4];
+#pragma unroll
+        for (int mm = 0; mm < D / 16; ++mm) o[mm][0] = o[mm][1] = o[mm][2] = o[mm][3] = 0.f;
+        const int nb = d.b1 - d.b0;
+        const int first = (warp - d.rot + C::W) % C::W;  // see run_consumer
+        const bool may_have_new = FUSED && d.b1 == (d.n + kBlockSize - 1) / kBlockSize;
+        for (int b = first; b < nb; b += C::W) {
+            const uint32_t st = static_cast<uint32_t>(warp * C::SW) + taken % C::SW;
+            if (*abort_flag || !mbar_wait_warp(&B.full[st], (taken / C::SW) & 1)) {
+                ok = false;
+                break;
+            }
+            const int blk = d.b0 + b;
+            const int valid = min(kBlockSize, d.n - blk * kBlockSize);
+            uint8_t* kst = smem + st * C::STAGE_BYTES;
+            if (may_have_new && b == nb - 1) store_stage_new_row<D, G, EB>(P, d, kst, stage_new[st], lane);
+            compute_block_mma<D, G>(kst, kst + C::SLAB, valid, qb, f0, f1, m0, m1, l0, l1, o, lane);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&B.empty[st]);
+            ++taken;
+        }
+        if (!ok) break;
+        // Publish this warp's state for the merger: (m, l) and O of heads
+        // 2t and 2t+1 (those below G), each lane its dims 16g .. 16g + 15.
+        const int buf = item_seq % C::MERGE_BUFS;
+        if (!mbar_wait_warp(&B.mempty[buf], ((item_seq / C::MERGE_BUFS) & 1) ^ 1)) {
+            ok = false;
+            break;
+        }
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            l0 += __shfl_xor_sync(FULL, l0, off);
+            l1 += __shfl_xor_sync(FULL, l1, off);
+        }
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int h = 2 * t + e;
+            if (h < G) {
+                const size_t base = static_cast<size_t>((buf * C::W + warp) * G + h);
+                if (g == 0) ml[base] = make_float2(e ? m1 : m0, e ? l1 : l0);
+                float2* dst = reinterpret_cast<float2*>(mo + base * D + g * (D / 8));
+#pragma unroll
+                for (int mm = 0; mm < D / 16; ++mm) dst[mm] = make_float2(o[mm][e], o[mm][2 + e]);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&B.mfull[buf]);
+        ++item_seq;
+    }
+    if (!ok) {
+        *abort_flag = 1;
+        record_error(P.err, kErrTimeout, 2u);
+    }
 }
 
 template <int D, int G, int EB, bool FUSED>
@@ -1183,9 +1483,14 @@ __device__ void prefetch_first_blocks(const DecodeParams& P, int lane, int max_u
 }
 
 template <int D, int G, int EB, bool FUSED>
-__global__ void __launch_bounds__(Cfg<D, G, EB>::THREADS, 1) decode_kernel(const DecodeParams P) {
+__global__ void __launch_bounds__(Cfg<D, G, EB>::THREADS, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const DecodeParams P) {
     using C = Cfg<D, G, EB>;
-    extern __shared__ __align__(1024) uint8_t smem[];
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // MMA configurations: the ring starts on a 1024-byte boundary (the
+    // swizzle pattern of a tile follows its shared-memory address).
+    uint8_t* smem = smem_raw + (C::MMA ? ((1024 - (smem_addr(smem_raw) & 1023)) & 1023) : 0);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     Bars B;
     B.full = bars;
@@ -1221,20 +1526,40 @@ __global__ void __launch_bounds__(Cfg<D, G, EB>::THREADS, 1) decode_kernel(const
         griddep_wait();
         // Test hook: no descriptor is ever published, so the other warps
         // leave through their bounded waits; nothing is in flight.
-        if (!P.stall) run_producer<D, G, EB, FUSED>(P, smem, B, abort_flag, lane);
+        if (!P.stall) run_producer<D, G, EB, FUSED>(P, &tm_k, &tm_v, smem, B, abort_flag, lane);
     } else if (warp == C::MERGER_WARP) {
         prefetch_first_blocks<D, G, EB>(P, lane, C::STAGES);
         griddep_wait();
         run_merger<D, G, EB>(P, smem, B, abort_flag, lane);
     } else {
         prefetch_inputs<D, FUSED>(P, threadIdx.x, C::W * 32);
-        run_consumer<D, G, EB, FUSED>(P, smem, B, abort_flag, warp, lane);
+        if constexpr (C::MMA) {
+            run_consumer_mma<D, G, EB, FUSED>(P, smem, B, abort_flag, warp, lane);
+        } else {
+            run_consumer<D, G, EB, FUSED>(P, smem, B, abort_flag, warp, lane);
+        }
     }
 }
 
 template <int D, int G, int EB, bool FUSED>
 cudaError_t launch_one(const DecodeParams& P, int grid, cudaStream_t stream) {
     using C = Cfg<D, G, EB>;
+    // MMA configurations read the pools through tiled tensor maps (rows of
+    // D * EB = 128 bytes, 16-row boxes, 128-byte swizzle); the others get
+    // unused zero maps.
+    CUtensorMap tk, tv;
+    std::memset(&tk, 0, sizeof(tk));
+    std::memset(&tv, 0, sizeof(tv));
+    if constexpr (C::MMA) {
+        const cuuint64_t rows = static_cast<cuuint64_t>(P.num_blocks) * P.hkv * kBlockSize;
+        if (rows > static_cast<cuuint64_t>(INT32_MAX)) return cudaErrorInvalidValue;
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), rows > 0 ? rows : 1};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * EB};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / EB), kBlockSize};
+        const CUtensorMapDataType dt = EB == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        if (!make_tile_map(&tk, dt, P.k_pool, 2, dims, strides, box)) return cudaErrorInvalidValue;
+        if (!make_tile_map(&tv, dt, P.v_pool, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    }
     static bool configured[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -1244,7 +1569,8 @@ cudaError_t launch_one(const DecodeParams& P, int grid, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    return launch_overlapped(decode_kernel<D, G, EB, FUSED>, dim3(grid), dim3(C::THREADS), C::SMEM, stream, P);
+    return launch_overlapped(decode_kernel<D, G, EB, FUSED>, dim3(grid), dim3(C::THREADS), C::SMEM, stream, tk, tv,
+                             P);
 }
 
 template <int D, int EB, bool FUSED>

@@ -73,7 +73,9 @@ int32_t shared_prefix_chunks(int32_t num_seqs, int32_t num_q_heads, int32_t num_
 // launch it right before launch_decode(a) on the same stream.
 cudaError_t launch_shared_prefix(const DecodeArgs& a, cudaStream_t stream);
 
-// A tiled tensor map of bf16 elements with the 128-byte swizzle.
+// A tiled tensor map with the 128-byte swizzle (element type dtype, or bf16).
+bool make_tile_map(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, cuuint32_t rank,
+                   const cuuint64_t* dims, const cuuint64_t* strides_bytes, const cuuint32_t* box);
 bool make_bf16_map(CUtensorMap* map, const void* base, cuuint32_t rank, const cuuint64_t* dims,
                    const cuuint64_t* strides_bytes, const cuuint32_t* box);
 

@@ -670,16 +670,21 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-bool make_bf16_map(CUtensorMap* map, const void* base, cuuint32_t rank, const cuuint64_t* dims,
-                   const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+bool make_tile_map(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, cuuint32_t rank,
+                   const cuuint64_t* dims, const cuuint64_t* strides_bytes, const cuuint32_t* box) {
     auto fn = encode_fn();
     if (fn == nullptr) return false;
     const cuuint32_t elem_strides[3] = {1, 1, 1};
     std::memset(map, 0, sizeof(*map));
-    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides_bytes,
-                          box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const CUresult r = fn(map, dtype, rank, const_cast<void*>(base), dims, strides_bytes, box, elem_strides,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+bool make_bf16_map(CUtensorMap* map, const void* base, cuuint32_t rank, const cuuint64_t* dims,
+                   const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+    return make_tile_map(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, rank, dims, strides_bytes, box);
 }
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {

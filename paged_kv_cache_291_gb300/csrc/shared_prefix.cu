@@ -18,9 +18,11 @@
 //    [c J / C, (c + 1) J / C)) for one kv head and 64 query rows (row r =
 //    sequence r / G, q head g G + r % G).
 //  * Warp 8 streams the chunk's K and V slabs with tiled TMA copies (one
-//    16-row box per 64-dim panel, 128-byte swizzle) into a ring of stages.
+//    16-row box per 64-dim panel, 128-byte swizzle) into a ring of stages;
+//    it reads the chunk's table entries 32 at a time.
 //  * Warps 0..7 form two groups of four; group j takes the chunk's blocks
-//    j, j + 2, ... (two warps per scheduler hide each other's MMA latency).
+//    j, j + 2, ...: a block's time is set by the latency of its MMA and
+//    softmax chains, so two blocks are in flight per CTA.
 //    A warp holds 16 query rows as MMA operands (mma.sync m16n8k16, bf16
 //    operands, fp32 accumulators) and per block computes
 //        S = Q K^T  (16 rows x 16 keys),
@@ -37,10 +39,11 @@
 //    different 16-byte bank groups of the swizzled slab.
 //  * Each group leaves every row's state of its blocks -- m (the log2-
 //    domain reference maximum), l = sum 2^(x - m) and the unnormalised o --
-//    in shared memory; after a cluster barrier CTA c merges rows
-//    [64 c / C, 64 (c + 1) / C) over all 2 C states of the cluster (read
-//    through distributed shared memory, log-sum-exp rule) and writes one
-//    state per (sequence, q head) for the decode kernel.
+//    in shared memory, and the CTA merges its groups' states (log-sum-exp
+//    rule).  After a cluster barrier CTA c merges rows [64 c / C,
+//    64 (c + 1) / C) over the C states of the cluster (read through
+//    distributed shared memory) and writes one state per (sequence, q head)
+//    for the decode kernel.
 //  * The shared blocks are taken from sequence 0's table.  Every CTA checks
 //    that its sequences' tables hold the same ids over its chunk and that
 //    their contexts extend past the prefix; a mismatch is reported as
@@ -61,14 +64,20 @@ namespace pkv {
 
 namespace {
 
-constexpr int kRowsPerCta = 64;
-constexpr int kGroups = 2;                       // warp groups splitting a chunk's blocks
+#ifndef PKV_PREFIX_ROWS
+#define PKV_PREFIX_ROWS 64
+#endif
+#ifndef PKV_PREFIX_STAGES
+#define PKV_PREFIX_STAGES 8
+#endif
+constexpr int kRowsPerCta = PKV_PREFIX_ROWS;     // query rows per CTA (32 or 64)
+constexpr int kGroups = 128 / kRowsPerCta;       // warp groups splitting a chunk's blocks (8 warps in all)
 constexpr int kWarpsPerGroup = kRowsPerCta / 16;  // one warp per 16 query rows
 constexpr int kConsumerWarps = kGroups * kWarpsPerGroup;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
-constexpr int kStages = 8;
+constexpr int kStages = PKV_PREFIX_STAGES;
 constexpr int kPanelBytes = kBlockSize * 128;  // 16 rows x 64 bf16
-constexpr int kMaxChunks = 8;                  // CTAs of one cluster (portable cluster size)
+constexpr int kMaxChunks = 8;                  // CTAs of one cluster (the portable cluster size)
 constexpr int kTargetCtas = 152;               // CTAs a launch aims at (chunks x kv heads x tiles)
 constexpr int kMinChunkBlocks = 4;             // fewest shared blocks per chunk
 constexpr float kLog2e = 1.4426950408889634f;
@@ -92,15 +101,18 @@ struct PCfg {
     static constexpr int STAGE = 2 * SLAB;
     static constexpr int RING = kStages * STAGE;
     // After the block loop the ring's bytes hold the groups' states:
-    // o [kGroups][64][D] fp32, then (m, l) [kGroups][64].
+    // o [kGroups][kRowsPerCta][D] fp32, then (m, l) [kGroups][kRowsPerCta],
+    // then the CTA's merged (m, l) [kRowsPerCta] (its o is merged in place
+    // into group 0's rows).
     static constexpr int OFF_MO = 0;
     static constexpr int OFF_MML = kGroups * kRowsPerCta * D * 4;
-    static constexpr int MERGE = OFF_MML + kGroups * kRowsPerCta * 8;
+    static constexpr int OFF_CML = OFF_MML + kGroups * kRowsPerCta * 8;
+    static constexpr int MERGE = OFF_CML + kRowsPerCta * 8;
     static constexpr int OFF_BAR = RING > MERGE ? RING : MERGE;
     static constexpr int SMEM_USED = OFF_BAR + 2 * kStages * 8 + 16;
     static constexpr int SMEM = SMEM_USED + 1024;  // slack to align the base to 1024 B
     static_assert(STAGE % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
-    static_assert(OFF_MML % 16 == 0 && OFF_BAR % 8 == 0, "aligned regions");
+    static_assert(OFF_MML % 16 == 0 && OFF_CML % 8 == 0 && OFF_BAR % 8 == 0, "aligned regions");
     static_assert(kStages % kGroups == 0, "a group's blocks keep to its own stages");
 };
 
@@ -162,9 +174,11 @@ __device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
     return r;
 }
 
+// Loads from another CTA's shared memory, issued back to back (they only
+// run between the two cluster barriers, which order them).
 __device__ __forceinline__ float2 ld_cluster_f2(uint32_t a) {
     float2 v;
-    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a) : "memory");
+    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a));
     return v;
 }
 
@@ -172,59 +186,83 @@ __device__ __forceinline__ float4 ld_cluster_f4(uint32_t a) {
     float4 v;
     asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
                  : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(a)
-                 : "memory");
+                 : "r"(a));
     return v;
 }
 
+// The producer warp: the chunk's table entries (sequence 0's row) are read
+// 32 at a time by the whole warp, the next batch requested before this
+// one's copies; lane 0 issues each block's copies once its stage is free.
 template <int D>
 __device__ void produce(const CUtensorMap* tk, const CUtensorMap* tv, const PrefixParams& P, uint8_t* smem,
-                        uint64_t* full, uint64_t* empty, volatile int* abort_flag, int g, int j0, int nblk) {
+                        uint64_t* full, uint64_t* empty, volatile int* abort_flag, int g, int j0, int nblk,
+                        int lane) {
     using C = PCfg<D>;
+    const unsigned FULL = 0xffffffffu;
+    const int32_t* row0 = P.block_tables + j0;
     int k = 0;
     bool bad = false;
-    for (; k < nblk; ++k) {
-        const int st = k % kStages;
-        if (*abort_flag || !mbar_wait(&empty[st], ((k / kStages) & 1) ^ 1)) {
-            bad = true;
-            break;
-        }
-        int phys = __ldg(P.block_tables + j0 + k);  // sequence 0's row
-        if (phys < 0 || phys >= P.num_blocks) {
-            record_error(P.err, kErrRange, 0u);
-            phys = 0;  // never address an invalid id
-        }
-        const int y = (phys * P.hkv + g) * kBlockSize;  // first row of the slab in the pool's row space
-        uint8_t* dst = smem + st * C::STAGE;
-        mbar_arrive_expect_tx(&full[st], C::STAGE);
+    int e = (lane < nblk) ? __ldg(row0 + lane) : 0;
+    for (int base = 0; base < nblk && !bad; base += 32) {
+        const int e_next = (base + 32 + lane < nblk) ? __ldg(row0 + base + 32 + lane) : 0;
+        const int cnt = min(32, nblk - base);
+        for (int i = 0; i < cnt; ++i) {
+            k = base + i;
+            const int st = k % kStages;
+            int phys = __shfl_sync(FULL, e, i);
+            int ok = 1;
+            if (lane == 0) {
+                if (*abort_flag || !mbar_wait(&empty[st], ((k / kStages) & 1) ^ 1)) {
+                    ok = 0;
+                } else {
+                    if (phys < 0 || phys >= P.num_blocks) {
+                        record_error(P.err, kErrRange, 0u);
+                        phys = 0;  // never address an invalid id
+                    }
+                    const int y = (phys * P.hkv + g) * kBlockSize;  // the slab's first row in the pool's row space
+                    uint8_t* dst = smem + st * C::STAGE;
+                    mbar_arrive_expect_tx(&full[st], C::STAGE);
 #pragma unroll
-        for (int p = 0; p < C::PANELS; ++p) {
-            tc::tma_load_2d(dst + p * kPanelBytes, tk, p * 64, y, &full[st]);
-            tc::tma_load_2d(dst + C::SLAB + p * kPanelBytes, tv, p * 64, y, &full[st]);
+                    for (int p = 0; p < C::PANELS; ++p) {
+                        tc::tma_load_2d(dst + p * kPanelBytes, tk, p * 64, y, &full[st]);
+                        tc::tma_load_2d(dst + C::SLAB + p * kPanelBytes, tv, p * 64, y, &full[st]);
+                    }
+                }
+            }
+            if (!__shfl_sync(FULL, ok, 0)) {
+                bad = true;
+                break;
+            }
         }
+        e = e_next;
     }
-    if (bad) {
+    if (bad && lane == 0) {
         *abort_flag = 1;
         record_error(P.err, kErrTimeout, 4u);
-        // Only the last use of each stage can still be in flight.
+        // Blocks 0 .. k-1 were issued; only the last use of each stage can
+        // still be in flight.
         for (int kk = max(0, k - kStages); kk < k; ++kk) mbar_wait(&full[kk % kStages], (kk / kStages) & 1);
     }
+    __syncwarp();
 }
 
-// The tables of this CTA's sequences hold sequence 0's ids over the chunk,
-// and their contexts reach past the shared prefix (one CTA per tile checks
-// the lengths).
+// The tables of this tile's sequences hold sequence 0's ids over the chunk,
+// and their contexts reach past the shared prefix.  The kv heads' CTAs of a
+// (chunk, tile) share the work: CTA g checks the sequences s = g mod Hkv
+// (the chunk's first CTA also their lengths).  It runs after the CTA's
+// blocks, off the path to the first MMA.
 __device__ void check_shared(const PrefixParams& P, int G, int j0, int nblk, int tid, int nthreads) {
     const int s_lo = blockIdx.z * kRowsPerCta / G;
     const int s_hi = min(P.num_seqs, ((blockIdx.z + 1) * kRowsPerCta + G - 1) / G);
     const int per = nblk + 1;
-    const long long total = static_cast<long long>(s_hi - s_lo) * per;
-    const bool lens = blockIdx.x == 0 && blockIdx.y == 0;
+    const int first = s_lo + (static_cast<int>(blockIdx.y) - s_lo % P.hkv + P.hkv) % P.hkv;
+    const int mine = first < s_hi ? (s_hi - 1 - first) / P.hkv + 1 : 0;
+    const long long total = static_cast<long long>(mine) * per;
     for (long long x = tid; x < total; x += nthreads) {
-        const int s = s_lo + static_cast<int>(x / per);
+        const int s = first + static_cast<int>(x / per) * P.hkv;
         const int k = static_cast<int>(x % per);
         if (k == nblk) {
-            if (lens && __ldg(P.context_lens + s) < P.shared_blocks * kBlockSize)
+            if (blockIdx.x == 0 && __ldg(P.context_lens + s) < P.shared_blocks * kBlockSize)
                 record_error(P.err, kErrRange, static_cast<uint32_t>(s));
         } else if (__ldg(P.block_tables + static_cast<size_t>(s) * P.max_blocks + j0 + k) !=
                    __ldg(P.block_tables + j0 + k)) {
@@ -283,18 +321,26 @@ __device__ void consume(const PrefixParams& P, uint8_t* smem, uint64_t* full, ui
         const uint8_t* vst = kst + C::SLAB;
         // ---- S = Q K^T: key tile nt holds keys 8 nt .. 8 nt + 7 (B operand
         // column g8 = key 8 nt + g8).
-        float s[2][4];
+        // Two accumulator sets per key tile (even and odd k-steps) halve the
+        // dependent MMA chain.
+        float s[2][4], s2[2][4];
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) s[nt][j] = s2[nt][j] = 0.f;
 #pragma unroll
         for (int i = 0; i < D / 32; ++i) {
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
                 const uint4 u = lds128(kst + swz(nt * 8 + g8, kchunk(t, i)));
                 mma_bf16(s[nt], qa[2 * i], u.x, u.y);
-                mma_bf16(s[nt], qa[2 * i + 1], u.z, u.w);
+                mma_bf16(s2[nt], qa[2 * i + 1], u.z, u.w);
             }
         }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) s[nt][j] += s2[nt][j];
         // ---- online softmax (log2 domain); s[nt] = rows (g8, g8+8) x keys
         // (8 nt + 2t, + 1); a row's 16 keys sit in the 4 lanes of its quad.
         float x[2][4];
@@ -395,44 +441,79 @@ __device__ void consume(const PrefixParams& P, uint8_t* smem, uint64_t* full, ui
             }
         }
     }
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+    // ---- the CTA's state: the groups' states merged (log-sum-exp), o in
+    // place over group 0's rows (each float4 by one thread), (m, l) apart.
+    constexpr int C4 = D / 4;
+    const float2* gml = reinterpret_cast<const float2*>(smem + C::OFF_MML);
+    float4* o4 = reinterpret_cast<float4*>(smem + C::OFF_MO);
+    float2* cml = reinterpret_cast<float2*>(smem + C::OFF_CML);
+    for (int it = warp * 32 + lane; it < kRowsPerCta * C4; it += kConsumerWarps * 32) {
+        const int row = it / C4, c4 = it % C4;
+        float2 e[kGroups];
+        float M = -INFINITY;
+#pragma unroll
+        for (int gr = 0; gr < kGroups; ++gr) {
+            e[gr] = gml[gr * kRowsPerCta + row];
+            M = fmaxf(M, e[gr].x);
+        }
+        float L = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int gr = 0; gr < kGroups; ++gr) {
+            const float w = (e[gr].x == -INFINITY) ? 0.f : fast_exp2(e[gr].x - M);
+            const float4 v = o4[(gr * kRowsPerCta + row) * C4 + c4];
+            L = fmaf(e[gr].y, w, L);
+            acc.x = fmaf(v.x, w, acc.x);
+            acc.y = fmaf(v.y, w, acc.y);
+            acc.z = fmaf(v.z, w, acc.z);
+            acc.w = fmaf(v.w, w, acc.w);
+        }
+        o4[row * C4 + c4] = acc;
+        if (c4 == 0) cml[row] = make_float2(M, L);
+    }
 }
 
 // After the cluster barrier: this CTA's share of the tile's live rows,
-// merged over the kGroups states of every CTA of the cluster, to global.
+// merged over the states of every CTA of the cluster (distributed shared
+// memory; each source's loads issued together), to global.
 template <int D>
 __device__ void merge_rows(const PrefixParams& P, const uint8_t* smem, int G, int g, int tid, int nthreads) {
     using C = PCfg<D>;
     constexpr int C4 = D / 4;
-    const int chunks = gridDim.x;  // = the cluster size
+    const int chunks = gridDim.x;  // = the cluster size, at most kMaxChunks
     const int rank = blockIdx.x;
     const int live = min(kRowsPerCta, P.num_seqs * G - static_cast<int>(blockIdx.z) * kRowsPerCta);
     const int r_lo = rank * kRowsPerCta / chunks;
     const int r_hi = min(live, (rank + 1) * kRowsPerCta / chunks);
-    const float* mo = reinterpret_cast<const float*>(smem + C::OFF_MO);
-    const float2* mml = reinterpret_cast<const float2*>(smem + C::OFF_MML);
+    const float4* o4 = reinterpret_cast<const float4*>(smem + C::OFF_MO);
+    const float2* cml = reinterpret_cast<const float2*>(smem + C::OFF_CML);
     for (int it = tid; it < (r_hi - r_lo) * C4; it += nthreads) {
         const int row = r_lo + it / C4;
         const int c4 = it % C4;
+        float2 e[kMaxChunks];
+        float4 v[kMaxChunks];
         float M = -INFINITY;
-        for (int src = 0; src < chunks; ++src) {
 #pragma unroll
-            for (int gr = 0; gr < kGroups; ++gr)
-                M = fmaxf(M, ld_cluster_f2(cluster_addr(mml + gr * kRowsPerCta + row, src)).x);
+        for (int src = 0; src < kMaxChunks; ++src) {
+            e[src] = make_float2(-INFINITY, 0.f);
+            v[src] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (src < chunks) {
+                e[src] = ld_cluster_f2(cluster_addr(cml + row, src));
+                v[src] = ld_cluster_f4(cluster_addr(o4 + row * C4 + c4, src));
+            }
+            M = fmaxf(M, e[src].x);
         }
         float L = 0.f;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int src = 0; src < chunks; ++src) {
 #pragma unroll
-            for (int gr = 0; gr < kGroups; ++gr) {
-                const float2 e = ld_cluster_f2(cluster_addr(mml + gr * kRowsPerCta + row, src));
-                const float4 v = ld_cluster_f4(cluster_addr(mo + (gr * kRowsPerCta + row) * D + 4 * c4, src));
-                const float w = (e.x == -INFINITY) ? 0.f : fast_exp2(e.x - M);
-                L = fmaf(e.y, w, L);
-                acc.x = fmaf(v.x, w, acc.x);
-                acc.y = fmaf(v.y, w, acc.y);
-                acc.z = fmaf(v.z, w, acc.z);
-                acc.w = fmaf(v.w, w, acc.w);
-            }
+        for (int src = 0; src < kMaxChunks; ++src) {
+            const float w = (e[src].x == -INFINITY) ? 0.f : fast_exp2(e[src].x - M);
+            L = fmaf(e[src].y, w, L);
+            acc.x = fmaf(v[src].x, w, acc.x);
+            acc.y = fmaf(v[src].y, w, acc.y);
+            acc.z = fmaf(v[src].z, w, acc.z);
+            acc.w = fmaf(v[src].w, w, acc.w);
         }
         const int r = static_cast<int>(blockIdx.z) * kRowsPerCta + row;
         const size_t idx = static_cast<size_t>(r / G) * P.hq + static_cast<size_t>(g) * G + r % G;
@@ -460,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], kWarpsPerGroup);  // the 4 warps of the group that takes the stage's block
+            mbar_init(&empty[i], kWarpsPerGroup);  // the warps of the group that takes the stage's block
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -473,11 +554,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::prefetch_tensormap(&tm_v);
         }
         griddep_wait();
-        if (lane == 0) produce<D>(&tm_k, &tm_v, P, smem, full, empty, abort_flag, g, j0, j1 - j0);
-        __syncwarp();
+        produce<D>(&tm_k, &tm_v, P, smem, full, empty, abort_flag, g, j0, j1 - j0, lane);
+        check_shared(P, G, j0, j1 - j0, lane, 32);
     } else {
         griddep_wait();
-        check_shared(P, G, j0, j1 - j0, threadIdx.x, kConsumerWarps * 32);
         consume<D>(P, smem, full, empty, abort_flag, G, g, j1 - j0, warp, lane);
     }
     // Every thread of the cluster passes both barriers: the states are
@@ -525,8 +605,6 @@ cudaError_t launch_t(const DecodeArgs& a, const DecodeWsLayout& L, cudaStream_t 
     const int G = a.num_q_heads / a.num_kv_heads;
     const int tiles = static_cast<int>((static_cast<int64_t>(a.num_seqs) * G + kRowsPerCta - 1) / kRowsPerCta);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(a.prefix_chunks), static_cast<unsigned>(a.num_kv_heads),
-                       static_cast<unsigned>(tiles));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = stream;
@@ -535,6 +613,8 @@ cudaError_t launch_t(const DecodeArgs& a, const DecodeWsLayout& L, cudaStream_t 
     attr[0].val.clusterDim.x = static_cast<unsigned>(a.prefix_chunks);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(a.prefix_chunks), static_cast<unsigned>(a.num_kv_heads),
+                       static_cast<unsigned>(tiles));
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
