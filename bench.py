@@ -53,11 +53,15 @@ L2_ROTATE_BYTES = 512 << 20
 # sources it was taken on; reported only while the sources still match.
 # Keys: (kernel entry, config).
 NCU_TRAFFIC = {
-    ("decode_step", 2): {"bytes": 91886080, "sources_sha": "d71b593ebff90b04"},
-    ("decode", 4): {"bytes": 18808320, "sources_sha": "d71b593ebff90b04"},
+    ("decode_step", 2): {"bytes": 91859712, "sources_sha": "63123afe5795a653"},
+    ("decode", 4): {"bytes": 18807296, "sources_sha": "63123afe5795a653"},
+    ("fp8_decode", 2): {"bytes": 44811520, "sources_sha": "63123afe5795a653"},
+    # both kernels of the shared-prefix decode (shared_prefix_kernel, then decode_kernel)
+    ("shared_prefix", 4): {"bytes": 19249920, "sources_sha": "63123afe5795a653"},
 }
 KERNEL_SOURCES = ["paged_kv_cache_291_gb300/csrc/decode_kernel.cuh", "paged_kv_cache_291_gb300/csrc/decode.cu",
-                  "paged_kv_cache_291_gb300/csrc/decode_fused.cu", "paged_kv_cache_291_gb300/csrc/pkv_device.cuh"]
+                  "paged_kv_cache_291_gb300/csrc/decode_fused.cu", "paged_kv_cache_291_gb300/csrc/pkv_device.cuh",
+                  "paged_kv_cache_291_gb300/csrc/shared_prefix.cu"]
 
 
 def sources_sha() -> str:
@@ -1046,7 +1050,7 @@ def config_entry(run, hbm, hbm_kind, tpeak, tkind, clocks=None, cpu=True, cpu_bu
             entry["decode_per_sequence"] = decode_entry(w, dec_t, hbm, hbm_kind,
                                                         traffic=ncu_traffic("decode", run.config))
             entry["decode"] = decode_entry(w, run.kernel_alone(dec, shared=run.shared_blocks), hbm, hbm_kind,
-                                           shared=run.shared_blocks)
+                                           traffic=ncu_traffic("shared_prefix", run.config), shared=run.shared_blocks)
         else:
             entry["decode"] = decode_entry(w, dec_t, hbm, hbm_kind, traffic=ncu_traffic("decode", run.config))
     if len(pre):
