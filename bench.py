@@ -1130,11 +1130,14 @@ def run_ours(args):
 
     # End to end through the public API with pinned host buffers: every step
     # copies all its inputs (one staging buffer, one copy) to the device,
-    # runs the calls and reads the output back.  As a serving loop does, the
-    # step (its input copy from pinned memory, the calls, the output copy
-    # back) is captured through the same public calls in CUDA graphs and
-    # replayed: one graph per cycle over the replicas, and one per replica
-    # for the remainder.
+    # runs the calls and reads the output back.  The copies are pkv_copy
+    # launches (the GPU reads and writes the pinned host buffers directly),
+    # which chain with the step's kernels where copy-engine transfers would
+    # cost an engine switch on each side (about 10 us a step on this machine).
+    # As a serving loop does, the step (its input copy from pinned memory,
+    # the calls, the output copy back) is captured through the same public
+    # calls in CUDA graphs and replayed: one graph per cycle over the
+    # replicas, and one per replica for the remainder.
     e2e_steps = min(args.steps, args.e2e_steps)
     host_stage = torch.from_numpy(run.stage_np).pin_memory()
     host_out = torch.empty((Tq, w.num_q_heads, w.head_dim), dtype=torch.float32).pin_memory()
@@ -1142,9 +1145,9 @@ def run_ours(args):
     d2h = host_out.numel() * host_out.element_size()
 
     def e2e_step(r):
-        r["stage"].copy_(host_stage, non_blocking=True)
+        pkv.copy(r["stage"], host_stage, stream=stream)
         run.step(r)
-        host_out.copy_(r["out"], non_blocking=True)
+        pkv.copy(host_out, r["out"], stream=stream)
 
     with torch.cuda.stream(stream):
         for i in range(3):

@@ -164,6 +164,23 @@ pkv_status pkv_swap_blocks(const pkv_cache_t* cache, int32_t direction, const in
                            int32_t n, void* host, int64_t num_host_slots, void* stream);
 
 /*
+ * pkv_copy -- copy `bytes` bytes from src to dst with a kernel, for moving a
+ * step's inputs in from host memory and its output back without the copy
+ * engine: on a Grace system the GPU reads and writes page-locked host memory
+ * directly over the host link, and a kernel chains with the launches around
+ * it (programmatic serialization) where a copy-engine transfer cannot.
+ * Not on the pages: the transfer helper of the end-to-end step.
+ *
+ *   dst, src   each device memory or page-locked host memory mapped for the
+ *              device (cudaHostAlloc, or cudaHostRegister with the mapped
+ *              flag); 16-byte aligned; they must not overlap
+ *   bytes      a multiple of 16 (else PKV_ERR_SHAPE); 0 does nothing
+ *   Returns PKV_ERR_HOST_MEMORY, launching nothing, for any other memory
+ *   (pageable host memory).  Asynchronous on `stream`, like every call.
+ */
+pkv_status pkv_copy(void* dst, const void* src, size_t bytes, void* stream);
+
+/*
  * pkv_decode_workspace_size -- bytes of workspace pkv_decode_attention needs
  * (a 256-byte header, one arrival counter per (sequence, kv head) and the
  * split-KV partial results).  Depends on the current device's SM count.

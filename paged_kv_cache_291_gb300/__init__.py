@@ -89,6 +89,7 @@ def load():
         "pkv_decode_attention_shared_prefix": ([CP, P, i32, P, i32, P, i32, i32, i32, f32, P, P, sz, P],
                                                ctypes.c_int),
         "pkv_common_prefix_blocks": ([P, i32, P, i32], i32),
+        "pkv_copy": ([P, P, sz, P], ctypes.c_int),
         "pkv_prefill_workspace_size": ([i32, i32, i32, i32, i32, i32], sz),
         "pkv_chunked_prefill_attention": ([CP, P, i32, i32, P, P, P, i32, P, i32, i32, f32, P, P, sz, P],
                                           ctypes.c_int),
@@ -298,6 +299,21 @@ def decode_step(k_pool, v_pool, k_new, v_new, slot_mapping, q, block_tables, con
                              _stream_handle(stream))
     _check(st, "pkv_decode_step")
     return out
+
+
+def copy(dst, src, stream=None) -> None:
+    """Copy the bytes of tensor ``src`` into tensor ``dst`` (same byte size,
+    contiguous) with a kernel; either may be on the device or in page-locked
+    host memory (``pin_memory()``), which the GPU then reads or writes
+    directly (pkv_copy)."""
+    if not (dst.is_contiguous() and src.is_contiguous()):
+        raise ValueError("copy needs contiguous tensors")
+    nbytes = dst.numel() * dst.element_size()
+    if nbytes != src.numel() * src.element_size():
+        raise ValueError("copy needs tensors of the same byte size")
+    st = load().pkv_copy(ctypes.c_void_p(dst.data_ptr()), ctypes.c_void_p(src.data_ptr()), nbytes,
+                         _stream_handle(stream))
+    _check(st, "pkv_copy")
 
 
 def common_prefix_blocks(block_tables_host, context_lens_host) -> int:

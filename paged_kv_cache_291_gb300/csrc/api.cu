@@ -372,6 +372,46 @@ PKV_API pkv_status pkv_swap_blocks(const pkv_cache_t* cache, int32_t direction, 
     return e == cudaSuccess ? PKV_OK : cuda_fail(e);
 }
 
+namespace {
+
+// The address a kernel uses for p: device memory as it is, page-locked host
+// memory mapped for the device through the pointer the runtime reports for
+// it; anything else (pageable host memory) is refused.
+pkv_status device_address(const void* p, const void** out) {
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+        cudaGetLastError();
+        return PKV_ERR_HOST_MEMORY;
+    }
+    if (attr.type == cudaMemoryTypeDevice || attr.type == cudaMemoryTypeManaged) {
+        *out = p;
+        return PKV_OK;
+    }
+    if (attr.type == cudaMemoryTypeHost && attr.devicePointer != nullptr) {
+        *out = attr.devicePointer;
+        return PKV_OK;
+    }
+    return PKV_ERR_HOST_MEMORY;
+}
+
+}  // namespace
+
+PKV_API pkv_status pkv_copy(void* dst, const void* src, size_t bytes, void* stream) {
+    if (bytes == 0) return PKV_OK;
+    if (dst == nullptr || src == nullptr) return PKV_ERR_NULL;
+    if (bytes % 16 != 0 || bytes > (static_cast<size_t>(1) << 40)) return PKV_ERR_SHAPE;
+    if (!aligned16(dst) || !aligned16(src)) return PKV_ERR_ALIGN;
+    DeviceState* dev = nullptr;
+    pkv_status st = current_device(&dev);
+    if (st != PKV_OK) return st;
+    const void *d = nullptr, *s = nullptr;
+    if ((st = device_address(dst, &d)) != PKV_OK) return st;
+    if ((st = device_address(src, &s)) != PKV_OK) return st;
+    cudaError_t e = pkv::launch_copy16(const_cast<void*>(d), s, static_cast<int64_t>(bytes / 16), dev->num_sms,
+                                       static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e);
+}
+
 PKV_API size_t pkv_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                          int32_t head_dim, int32_t max_context_len, int32_t partition_blocks) {
     if (check_heads(num_q_heads, num_kv_heads) != PKV_OK) return 0;

@@ -146,7 +146,28 @@ __global__ void __launch_bounds__(256) swap_blocks_kernel(int32_t direction, con
     }
 }
 
+// A plain copy of n 16-byte chunks by the SMs: either side may be device
+// memory or page-locked host memory that the device reaches directly (the
+// host link of a Grace system), so a transfer needs no copy engine and
+// chains with the kernels around it like any other launch.
+__global__ void __launch_bounds__(256) copy16_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                                     int64_t n) {
+    griddep_launch_dependents();
+    griddep_wait();
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
+        dst[i] = src[i];
+}
+
 }  // namespace
+
+cudaError_t launch_copy16(void* dst, const void* src, int64_t chunks, int num_sms, cudaStream_t stream) {
+    const int threads = 256;
+    int64_t blocks = (chunks + threads - 1) / threads;
+    blocks = blocks < 1 ? 1 : (blocks > 4 * num_sms ? 4 * num_sms : blocks);
+    return launch_overlapped(copy16_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, stream,
+                             static_cast<const uint4*>(src), static_cast<uint4*>(dst), chunks);
+}
 
 cudaError_t launch_swap_blocks(int32_t direction, const int32_t* blocks, const int32_t* slots, int32_t n,
                                void* host, int64_t num_slots, void* k_pool, void* v_pool, int32_t num_blocks,

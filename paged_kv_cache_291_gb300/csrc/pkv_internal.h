@@ -103,6 +103,10 @@ cudaError_t launch_copy_blocks(const int32_t* src, const int32_t* dst, int32_t n
                                void* v_pool, int32_t num_blocks, int32_t num_kv_heads, int32_t head_dim,
                                int32_t elem_bytes, unsigned long long* err, cudaStream_t stream);
 
+// Copy `chunks` 16-byte chunks from src to dst (device addresses) with a
+// kernel.
+cudaError_t launch_copy16(void* dst, const void* src, int64_t chunks, int num_sms, cudaStream_t stream);
+
 cudaError_t launch_swap_blocks(int32_t direction, const int32_t* blocks, const int32_t* slots, int32_t n,
                                void* host, int64_t num_slots, void* k_pool, void* v_pool, int32_t num_blocks,
                                int32_t num_kv_heads, int32_t head_dim, int32_t elem_bytes, unsigned long long* err,

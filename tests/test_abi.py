@@ -134,3 +134,20 @@ def test_e4m3_descriptor_checks_without_gpu(lib):
     for bad in (0.0, -0.5, float("inf"), float("nan"), 1e-45):
         assert write(pkv.PKV_KV_E4M3, bad, 1.0) == 16
         assert write(pkv.PKV_KV_E4M3, 1.0, bad) == 16
+
+
+def test_copy_argument_checks_without_gpu(lib):
+    """pkv_copy checks its arguments before touching a device: 0 bytes is a
+    no-op, NULL pointers give PKV_ERR_NULL (1), a size that is not a multiple
+    of 16 PKV_ERR_SHAPE (2), unaligned pointers PKV_ERR_ALIGN."""
+    import paged_kv_cache_291_gb300 as pkv
+    lib.pkv_copy.restype = ctypes.c_int
+    lib.pkv_copy.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    a, b = 1 << 20, 2 << 20                 # aligned, never dereferenced
+    names = {v: k for k, v in pkv.STATUS_NAMES.items()}
+    assert lib.pkv_copy(a, b, 0, None) == 0
+    assert lib.pkv_copy(None, b, 16, None) == 1
+    assert lib.pkv_copy(a, None, 16, None) == 1
+    assert lib.pkv_copy(a, b, 24, None) == 2
+    assert lib.pkv_copy(a + 8, b, 16, None) == names["PKV_ERR_ALIGN"]
+    assert lib.pkv_copy(a, b + 4, 16, None) == names["PKV_ERR_ALIGN"]

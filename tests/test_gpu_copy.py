@@ -1,0 +1,81 @@
+"""GPU checks of pkv_copy (a kernel copy between device memory and page-locked
+host memory that the GPU reaches directly): bit-exact in every direction,
+refused for pageable host memory, and the end-to-end step pattern (inputs in
+from pinned host memory, the decode step, the output back) captured in a CUDA
+graph gives the direct calls' result."""
+import numpy as np
+import pytest
+import torch
+
+import pkv_workloads as W
+from gpu_helpers import DeviceStep
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    import paged_kv_cache_291_gb300 as p
+    p.load()
+    return p
+
+
+@pytest.mark.parametrize("nbytes", [16, 4096, 284928, 3 << 20])
+def test_copy_directions_bit_exact(pkv, nbytes):
+    rng = np.random.default_rng(nbytes)
+    data = torch.from_numpy(rng.integers(0, 256, size=nbytes, dtype=np.uint8))
+    host_in = data.pin_memory()
+    dev = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    dev2 = torch.empty_like(dev)
+    host_out = torch.zeros(nbytes, dtype=torch.uint8).pin_memory()
+    pkv.copy(dev, host_in)
+    pkv.copy(dev2, dev)
+    pkv.copy(host_out, dev2)
+    torch.cuda.synchronize()
+    assert torch.equal(dev.cpu(), data) and torch.equal(host_out, data)
+
+
+def test_copy_refuses_pageable_host_memory(pkv):
+    dev = torch.empty(64, dtype=torch.uint8, device="cuda")
+    pageable = torch.zeros(64, dtype=torch.uint8)
+    with pytest.raises(pkv.PKVError) as e:
+        pkv.copy(dev, pageable)
+    assert pkv.STATUS_NAMES[e.value.status] == "PKV_ERR_HOST_MEMORY"
+
+
+def test_step_with_host_io_in_a_graph(pkv):
+    """The bench's end-to-end step: one staging copy in, the fused decode
+    step, the output copy out, captured and replayed, equals the direct
+    call on device inputs."""
+    w = W.build_config(2)
+    ds = DeviceStep(w)
+    k0, v0 = ds.k.clone(), ds.v.clone()
+    ref = pkv.decode_step(ds.k, ds.v, ds.k_new, ds.v_new, ds.slots, ds.q, ds.tables, ds.ctx, w.max_context_len,
+                          w.scale).clone()
+    # The same step from host buffers: q staged through pinned memory.
+    host_q = ds.q.cpu().pin_memory()
+    dev_q = torch.empty_like(ds.q)
+    out = torch.empty_like(ref)
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    ws = pkv.new_workspace(pkv.decode_workspace_size(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                                     w.max_context_len))
+    stream = torch.cuda.Stream()
+    k, v = k0.clone(), v0.clone()
+    torch.cuda.synchronize()
+
+    def step():
+        pkv.copy(dev_q, host_q, stream=stream)
+        pkv.decode_step(k, v, ds.k_new, ds.v_new, ds.slots, dev_q, ds.tables, ds.ctx, w.max_context_len, w.scale,
+                        out=out, workspace=ws, stream=stream)
+        pkv.copy(host_out, out, stream=stream)
+    with torch.cuda.stream(stream):
+        step()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        step()
+    host_out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert pkv.get_error() == (0, 0)
+    assert torch.equal(host_out, ref.cpu())
