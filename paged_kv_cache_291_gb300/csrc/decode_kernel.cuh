@@ -85,8 +85,9 @@ constexpr bool use_mma() {
 
 // Consumer warps per CTA: 12 for head groups of 1 or 2 (their per-lane state
 // is small, and a fourth warp per scheduler hides more of the latency of the
-// dependent shuffle and FMA chains), 8 for groups of 4 and 8 (which need
-// more than the 128 registers a thread that 14 warps leave).  e4m3 pools
+// dependent shuffle and FMA chains), 8 for groups of 4 (which need more than
+// the 128 registers a thread that 14 warps leave), 6 for groups of 8 (about
+// 220 registers a thread, no spills).  e4m3 pools
 // (EB = 1) with groups of 1 or 2 on CUDA cores take 16: their blocks cost
 // more issue (the widening) and half the ring bytes, so the same ring still
 // gives each warp 3 stages.  A build can force one count for every group
@@ -96,7 +97,7 @@ constexpr int consumer_warps() {
 #ifdef PKV_DECODE_CONSUMER_WARPS
     return PKV_DECODE_CONSUMER_WARPS;
 #else
-    return use_mma<D, G, EB>() ? (G <= 2 ? 12 : 8) : (G <= 2 ? (EB == 1 ? 16 : 12) : 8);
+    return use_mma<D, G, EB>() ? (G <= 2 ? 12 : 8) : (G <= 2 ? (EB == 1 ? 16 : 12) : (G == 4 ? 8 : 6));
 #endif
 }
 constexpr int kItemRing = 8;
