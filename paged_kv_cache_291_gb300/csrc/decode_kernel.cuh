@@ -271,6 +271,21 @@ __device__ __noinline__ void store_new_row_e4m3(const DecodeParams& P, size_t of
     fence_proxy_async_shared();
 }
 
+// Units per range when the caller lets the kernel choose: the total over
+// the grid, at least kMinRangeUnits.  When every pair has the same number
+// of units u (a batch of equal contexts), a range of whole pairs -- u times
+// the pairs it then holds -- is taken instead if it costs at most 15% more
+// units: no pair is split, so no part waits for another's partial result
+// (Qwen3-1.7B, 34 x 640: 80 units on 136 CTAs beat 72 on 152).
+__device__ __forceinline__ long long auto_range_units(long long T, unsigned grid, int umin, int umax) {
+    long long RU = max(static_cast<long long>(kMinRangeUnits), (T + grid - 1) / grid);
+    if (umin == umax && umin > 0) {
+        const long long whole = static_cast<long long>(umin) * ((RU + umin - 1) / umin);
+        if (whole * 20 <= RU * 23) RU = whole;
+    }
+    return RU;
+}
+
 // Units of work of one kv head of sequence s: one per 16-token block of its
 // context past the shared prefix (at least one, so that an empty context
 // still yields its output row), 0 for rows that are not decode rows.  The
@@ -499,16 +514,26 @@ __device__ void run_producer(const DecodeParams& P, const CUtensorMap* tmk, cons
     Win win{0, 0, 0, 0, 0};
     load_window(win, blockIdx.x == 0);
     long long per_head = __shfl_sync(FULL, win.incl, 31);
+    // Smallest and largest units of a decode row's pair (rows with none
+    // excluded): equal for a batch whose contexts span the same blocks.
+    int umin = win.u > 0 ? win.u : INT32_MAX, umax = win.u;
     for (int s0 = 32; s0 < P.num_seqs; s0 += 32) {
         int n, u = 0;
         if (s0 + lane < P.num_seqs) u = seq_units(P, s0 + lane, n, blockIdx.x == 0);
+        umin = min(umin, u > 0 ? u : INT32_MAX);
+        umax = max(umax, u);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) u += __shfl_xor_sync(FULL, u, o);
         per_head += u;
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        umin = min(umin, __shfl_xor_sync(FULL, umin, o));
+        umax = max(umax, __shfl_xor_sync(FULL, umax, o));
+    }
     const long long T = per_head * P.hkv;
     long long RU = P.range_units;
-    if (RU <= 0) RU = max(static_cast<long long>(kMinRangeUnits), (T + gridDim.x - 1) / gridDim.x);
+    if (RU <= 0) RU = auto_range_units(T, gridDim.x, umin, umax);
     const long long shift_max = max(8LL, RU / 8);  // largest move of a range boundary (see snap)
     long long R = (T + RU - 1) / RU;
     if (R > P.max_ranges) {  // cannot happen with a workspace sized by the library
@@ -1450,9 +1475,20 @@ __device__ void prefetch_first_blocks(const DecodeParams& P, int lane, int max_u
         }
         per_head += __shfl_sync(FULL, incl[w], 31);
     }
+    int umin = INT32_MAX, umax = 0;
+#pragma unroll
+    for (int w = 0; w < kSpecWindows; ++w) {
+        umin = min(umin, u[w] > 0 ? u[w] : INT32_MAX);
+        umax = max(umax, u[w]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        umin = min(umin, __shfl_xor_sync(FULL, umin, o));
+        umax = max(umax, __shfl_xor_sync(FULL, umax, o));
+    }
     const long long T = per_head * P.hkv;
     long long RU = P.range_units;
-    if (RU <= 0) RU = max(static_cast<long long>(kMinRangeUnits), (T + gridDim.x - 1) / gridDim.x);
+    if (RU <= 0) RU = auto_range_units(T, gridDim.x, umin, umax);
     long long x = static_cast<long long>(blockIdx.x) * RU;
     const long long hi = min(T, x + min(RU, static_cast<long long>(max_units)));
     // Walk the pairs from x: find the sequence (window w, lane j) holding x.

@@ -73,6 +73,15 @@ def test_head_shapes(pkv, hq, hkv, d):
     run_and_check(pkv, w)
 
 
+@pytest.mark.parametrize("B,n", [(34, 640), (20, 640), (50, 320), (7, 2000), (300, 48), (152, 17)])
+def test_equal_contexts(pkv, B, n):
+    """Batches whose pairs all span the same blocks: the automatic plan then
+    takes ranges of whole pairs when that costs at most 15% more units per
+    range (no pair split), else the usual cut."""
+    w = W.make_paged("equal", 4000 + B + n, 16, 8, 128, [n] * B, [1] * B)
+    run_and_check(pkv, w)
+
+
 def test_many_sequences_ragged(pkv):
     """More than one 32-sequence window in the work decoder, random lengths."""
     ctx = W.randint_inclusive(5, 7, 300, 1, 700)
