@@ -64,18 +64,12 @@ namespace pkv {
 
 namespace {
 
-#ifndef PKV_PREFIX_ROWS
-#define PKV_PREFIX_ROWS 64
-#endif
-#ifndef PKV_PREFIX_STAGES
-#define PKV_PREFIX_STAGES 8
-#endif
-constexpr int kRowsPerCta = PKV_PREFIX_ROWS;     // query rows per CTA (32 or 64)
-constexpr int kGroups = 128 / kRowsPerCta;       // warp groups splitting a chunk's blocks (8 warps in all)
+constexpr int kRowsPerCta = 64;                  // query rows per CTA
+constexpr int kGroups = 2;                       // warp groups splitting a chunk's blocks
 constexpr int kWarpsPerGroup = kRowsPerCta / 16;  // one warp per 16 query rows
 constexpr int kConsumerWarps = kGroups * kWarpsPerGroup;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
-constexpr int kStages = PKV_PREFIX_STAGES;
+constexpr int kStages = 8;
 constexpr int kPanelBytes = kBlockSize * 128;  // 16 rows x 64 bf16
 constexpr int kMaxChunks = 8;                  // CTAs of one cluster (the portable cluster size)
 constexpr int kTargetCtas = 152;               // CTAs a launch aims at (chunks x kv heads x tiles)
