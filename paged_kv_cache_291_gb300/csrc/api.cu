@@ -486,7 +486,15 @@ pkv_status decode_common(const pkv_cache_t* cache, const void* q, int32_t num_q_
         a.skip_blocks = shared_blocks;
         a.prefix_chunks = chunks;
         cudaError_t e = pkv::launch_shared_prefix(a, static_cast<cudaStream_t>(stream));
-        if (e != cudaSuccess) return cuda_fail(e);
+        if (e == cudaErrorInvalidClusterSize) {
+            // A device that cannot place the kernel's clusters: every
+            // sequence attends the shared blocks itself (the same result).
+            cudaGetLastError();
+            a.skip_blocks = 0;
+            a.prefix_chunks = 0;
+        } else if (e != cudaSuccess) {
+            return cuda_fail(e);
+        }
     }
     cudaError_t e = pkv::launch_decode(a, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PKV_OK : cuda_fail(e);
