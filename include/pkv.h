@@ -295,9 +295,10 @@ pkv_status pkv_decode_step(const pkv_cache_t* cache, const void* k_new, const vo
  *   The promise is checked on the device: a sequence whose table differs in
  *   the shared part, or whose context is shorter than it, raises
  *   PKV_ERR_RANGE (detail: the sequence), and the call's results are then
- *   not valid.  e4m3 pools (and pools of more than 2^31 rows of 16 tokens x
- *   kv heads) attend the shared blocks per sequence, as
- *   pkv_decode_attention does; the promise is then not checked.
+ *   not valid.  e4m3 pools, pools of more than 2^31 rows of 16 tokens x kv
+ *   heads, and devices that refuse the kernel's 8-CTA clusters attend the
+ *   shared blocks per sequence, as pkv_decode_attention does; the promise is
+ *   then not checked.
  */
 size_t pkv_decode_shared_prefix_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                                int32_t head_dim, int32_t max_context_len, int32_t shared_blocks);
