@@ -209,7 +209,10 @@ size_t pkv_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t 
  *                  max_blocks_per_seq*16 or max_context_len is clamped and
  *                  raises PKV_ERR_RANGE
  *   max_context_len host-side upper bound of context_lens (sizes the split)
- *   out            fp32 [num_seqs][num_q_heads][head_dim]
+ *   out            fp32 [num_seqs][num_q_heads][head_dim]: device memory,
+ *                  or page-locked host memory mapped for the device (the
+ *                  kernel then writes the rows there directly, with no copy
+ *                  after it); other host memory gives PKV_ERR_HOST_MEMORY
  *   workspace      device buffer of >= pkv_decode_workspace_size() bytes,
  *                  256-byte aligned, ZERO-FILLED BEFORE ITS FIRST USE.  Its
  *                  first part (a 256-byte header and one arrival counter per
@@ -341,7 +344,9 @@ size_t pkv_prefill_workspace_size(int32_t num_seqs, int32_t num_tokens, int32_t 
  *   query_start_loc       int32 [num_seqs+1], device
  *   query_start_loc_host  the same values on the host (plans the launch)
  *   context_lens          int32 [num_seqs], device, including this step's rows
- *   out                   fp32 [num_tokens][num_q_heads][head_dim]
+ *   out                   fp32 [num_tokens][num_q_heads][head_dim], device
+ *                         memory or page-locked host memory mapped for the
+ *                         device (as for pkv_decode_attention)
  *   workspace             >= pkv_prefill_workspace_size() bytes, 256-byte
  *                         aligned, zero-filled before first use; used as the
  *                         decode workspace for the decode rows (its counters

@@ -152,6 +152,19 @@ def _dev(t, name, elem_size=None, dtype=None):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _out(t, name="out"):
+    """An fp32 output tensor on the device or in page-locked host memory
+    (``pin_memory()``), which the kernels then write directly."""
+    torch = _torch()
+    if isinstance(t, torch.Tensor) and not t.is_cuda:
+        if not t.is_pinned():
+            raise ValueError(f"{name} must be a CUDA tensor or page-locked host memory")
+        if not t.is_contiguous() or t.dtype != torch.float32:
+            raise ValueError(f"{name} must be contiguous float32")
+        return ctypes.c_void_p(t.data_ptr())
+    return _dev(t, name, dtype=torch.float32)
+
+
 def _cache(k_pool, v_pool, k_scale=None, v_scale=None, need_scales=False) -> Cache:
     """Descriptor of a pool pair: 2-byte elements are bf16, 1-byte elements
     (uint8 or float8_e4m3fn) e4m3 codes with one scale per pool."""
@@ -262,7 +275,7 @@ def decode_attention(k_pool, v_pool, q, block_tables, context_lens, max_context_
     st = lib.pkv_decode_attention(ctypes.byref(c), _dev(q, "q", 2), hq,
                                   _dev(block_tables, "block_tables", dtype=torch.int32), int(block_tables.shape[1]),
                                   _dev(context_lens, "context_lens", dtype=torch.int32), B, int(max_context_len),
-                                  float(scale), _dev(out, "out", dtype=torch.float32),
+                                  float(scale), _out(out),
                                   _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
                                   int(partition_blocks), _stream_handle(stream))
     _check(st, "pkv_decode_attention")
@@ -294,7 +307,7 @@ def decode_step(k_pool, v_pool, k_new, v_new, slot_mapping, q, block_tables, con
                              _dev(slot_mapping, "slot_mapping", dtype=torch.int32), _dev(q, "q", 2), hq,
                              _dev(block_tables, "block_tables", dtype=torch.int32), int(block_tables.shape[1]),
                              _dev(context_lens, "context_lens", dtype=torch.int32), B, int(max_context_len),
-                             float(scale), _dev(out, "out", dtype=torch.float32), _dev(workspace, "workspace"),
+                             float(scale), _out(out), _dev(workspace, "workspace"),
                              workspace.numel() * workspace.element_size(), int(partition_blocks),
                              _stream_handle(stream))
     _check(st, "pkv_decode_step")
@@ -362,7 +375,7 @@ def decode_attention_shared_prefix(k_pool, v_pool, q, block_tables, context_lens
     st = lib.pkv_decode_attention_shared_prefix(
         ctypes.byref(c), _dev(q, "q", 2), hq, _dev(block_tables, "block_tables", dtype=torch.int32),
         int(block_tables.shape[1]), _dev(context_lens, "context_lens", dtype=torch.int32), B, int(max_context_len),
-        int(shared_blocks), float(scale), _dev(out, "out", dtype=torch.float32), _dev(workspace, "workspace"),
+        int(shared_blocks), float(scale), _out(out), _dev(workspace, "workspace"),
         workspace.numel() * workspace.element_size(), _stream_handle(stream))
     _check(st, "pkv_decode_attention_shared_prefix")
     return out
@@ -400,7 +413,7 @@ def chunked_prefill_attention(k_pool, v_pool, q, query_start_loc, context_lens, 
         ctypes.byref(c), _dev(q, "q", 2), hq, T, _dev(query_start_loc, "query_start_loc", dtype=torch.int32), qhp,
         _dev(context_lens, "context_lens", dtype=torch.int32), S,
         _dev(block_tables, "block_tables", dtype=torch.int32), int(block_tables.shape[1]), int(max_context_len),
-        float(scale), _dev(out, "out", dtype=torch.float32), _dev(workspace, "workspace"),
+        float(scale), _out(out), _dev(workspace, "workspace"),
         workspace.numel() * workspace.element_size(), _stream_handle(stream))
     _check(st, "pkv_chunked_prefill_attention")
     return out

@@ -98,6 +98,26 @@ pkv_status check_cache(const pkv_cache_t* c) {
 
 int32_t elem_bytes(const pkv_cache_t* c) { return c->kv_dtype == PKV_KV_E4M3 ? 1 : 2; }
 
+// The address a kernel uses for p: device memory as it is, page-locked host
+// memory mapped for the device through the pointer the runtime reports for
+// it; anything else (pageable host memory) is refused.
+pkv_status device_address(const void* p, const void** out) {
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+        cudaGetLastError();
+        return PKV_ERR_HOST_MEMORY;
+    }
+    if (attr.type == cudaMemoryTypeDevice || attr.type == cudaMemoryTypeManaged) {
+        *out = p;
+        return PKV_OK;
+    }
+    if (attr.type == cudaMemoryTypeHost && attr.devicePointer != nullptr) {
+        *out = attr.devicePointer;
+        return PKV_OK;
+    }
+    return PKV_ERR_HOST_MEMORY;
+}
+
 pkv_status check_heads(int32_t hq, int32_t hkv) {
     if (hq < 1 || hkv < 1 || hq % hkv != 0) return PKV_ERR_HEADS;
     const int32_t g = hq / hkv;
@@ -372,30 +392,6 @@ PKV_API pkv_status pkv_swap_blocks(const pkv_cache_t* cache, int32_t direction, 
     return e == cudaSuccess ? PKV_OK : cuda_fail(e);
 }
 
-namespace {
-
-// The address a kernel uses for p: device memory as it is, page-locked host
-// memory mapped for the device through the pointer the runtime reports for
-// it; anything else (pageable host memory) is refused.
-pkv_status device_address(const void* p, const void** out) {
-    cudaPointerAttributes attr;
-    if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
-        cudaGetLastError();
-        return PKV_ERR_HOST_MEMORY;
-    }
-    if (attr.type == cudaMemoryTypeDevice || attr.type == cudaMemoryTypeManaged) {
-        *out = p;
-        return PKV_OK;
-    }
-    if (attr.type == cudaMemoryTypeHost && attr.devicePointer != nullptr) {
-        *out = attr.devicePointer;
-        return PKV_OK;
-    }
-    return PKV_ERR_HOST_MEMORY;
-}
-
-}  // namespace
-
 PKV_API pkv_status pkv_copy(void* dst, const void* src, size_t bytes, void* stream) {
     if (bytes == 0) return PKV_OK;
     if (dst == nullptr || src == nullptr) return PKV_ERR_NULL;
@@ -444,6 +440,11 @@ pkv_status decode_common(const pkv_cache_t* cache, const void* q, int32_t num_q_
     if (!aligned16(q) || !aligned16(out)) return PKV_ERR_ALIGN;
     DeviceState* dev = nullptr;
     if ((st = current_device(&dev)) != PKV_OK) return st;
+    // out may be page-locked host memory: the kernel then writes the rows
+    // there directly.
+    const void* out_dev = nullptr;
+    if ((st = device_address(out, &out_dev)) != PKV_OK) return st;
+    out = static_cast<float*>(const_cast<void*>(out_dev));
     // A shared prefix is read once for all sequences on bf16 pools whose rows
     // a tensor map can address; otherwise every sequence reads it (the same
     // result).  The workspace is sized for the shared-prefix states either way.
@@ -609,6 +610,9 @@ PKV_API pkv_status pkv_chunked_prefill_attention(const pkv_cache_t* cache, const
     }
     DeviceState* dev = nullptr;
     if ((st = current_device(&dev)) != PKV_OK) return st;
+    const void* out_dev = nullptr;
+    if ((st = device_address(out, &out_dev)) != PKV_OK) return st;
+    out = static_cast<float*>(const_cast<void*>(out_dev));
     if (decode_rows > 0) {
         st = decode_common(cache, q, num_q_heads, block_tables, max_blocks_per_seq, context_lens, query_start_loc,
                            num_seqs, max_context_len, scale, out, workspace, workspace_bytes, 0, stream);

@@ -79,3 +79,50 @@ def test_step_with_host_io_in_a_graph(pkv):
     torch.cuda.synchronize()
     assert pkv.get_error() == (0, 0)
     assert torch.equal(host_out, ref.cpu())
+
+
+def test_outputs_written_to_page_locked_host_memory(pkv):
+    """An fp32 output in page-locked host memory is written by the kernels
+    directly: the decode step, decode attention, the shared-prefix call and
+    the mixed batch give the same rows as with device outputs."""
+    w = W.build_config(2)
+    ds = DeviceStep(w)
+    ref = pkv.decode_step(ds.k.clone(), ds.v.clone(), ds.k_new, ds.v_new, ds.slots, ds.q, ds.tables, ds.ctx,
+                          w.max_context_len, w.scale)
+    host = torch.zeros(tuple(ref.shape), dtype=torch.float32).pin_memory()
+    pkv.decode_step(ds.k.clone(), ds.v.clone(), ds.k_new, ds.v_new, ds.slots, ds.q, ds.tables, ds.ctx,
+                    w.max_context_len, w.scale, out=host)
+    torch.cuda.synchronize()
+    assert torch.equal(host, ref.cpu())
+    host.zero_()
+    dev = pkv.decode_attention(ds.k, ds.v, ds.q, ds.tables, ds.ctx, w.max_context_len, w.scale)
+    pkv.decode_attention(ds.k, ds.v, ds.q, ds.tables, ds.ctx, w.max_context_len, w.scale, out=host)
+    torch.cuda.synchronize()
+    assert torch.equal(host, dev.cpu())
+    # shared prefix
+    J = 10
+    ws = W.make_paged("host-out-shared", 5005, 16, 8, 128, [16 * J + 3, 16 * J + 70, 16 * J + 200], [1] * 3,
+                      share_prefix_blocks=J)
+    d2 = DeviceStep(ws)
+    pkv.cache_write(d2.k, d2.v, d2.k_new, d2.v_new, d2.slots)
+    dev = pkv.decode_attention_shared_prefix(d2.k, d2.v, d2.q, d2.tables, d2.ctx, ws.max_context_len, J, ws.scale)
+    host2 = torch.zeros(tuple(dev.shape), dtype=torch.float32).pin_memory()
+    pkv.decode_attention_shared_prefix(d2.k, d2.v, d2.q, d2.tables, d2.ctx, ws.max_context_len, J, ws.scale,
+                                       out=host2)
+    torch.cuda.synchronize()
+    assert torch.equal(host2, dev.cpu())
+    # mixed batch (prefill tiles and decode rows)
+    wm = W.build_config(5)
+    d3 = DeviceStep(wm)
+    pkv.cache_write(d3.k, d3.v, d3.k_new, d3.v_new, d3.slots)
+    dev = pkv.chunked_prefill_attention(d3.k, d3.v, d3.q, d3.qsl, d3.ctx, d3.tables, wm.max_context_len, wm.scale,
+                                        query_start_loc_host=wm.query_start_loc)
+    host3 = torch.zeros(tuple(dev.shape), dtype=torch.float32).pin_memory()
+    pkv.chunked_prefill_attention(d3.k, d3.v, d3.q, d3.qsl, d3.ctx, d3.tables, wm.max_context_len, wm.scale,
+                                  out=host3, query_start_loc_host=wm.query_start_loc)
+    torch.cuda.synchronize()
+    assert pkv.get_error() == (0, 0)
+    assert torch.equal(host3, dev.cpu())
+    with pytest.raises(ValueError):
+        pkv.decode_attention(ds.k, ds.v, ds.q, ds.tables, ds.ctx, w.max_context_len, w.scale,
+                             out=torch.zeros(tuple(ref.shape), dtype=torch.float32))
