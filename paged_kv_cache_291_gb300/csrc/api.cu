@@ -637,6 +637,24 @@ PKV_API pkv_status pkv_chunked_prefill_attention(const pkv_cache_t* cache, const
         a.max_blocks_per_seq = max_blocks_per_seq;
         a.max_context_len = max_context_len;
         a.num_tiles = tiles;
+        // The longest row tiles of each sequence (its last ones: they hold
+        // the most keys) go to two one-head CTAs each, as many of them as
+        // keep the whole grid within one CTA per SM.
+        a.split_last = 0;
+        a.split_tiles = 0;
+        const int64_t pairs = (num_q_heads / cache->num_kv_heads) % 2 == 0 ? num_q_heads / 2 : 0;
+        for (int32_t k = 1; pairs > 0; ++k) {
+            int64_t extra = 0, longest = 0;
+            for (int32_t s = 0; s < num_seqs; ++s) {
+                const int32_t ql = query_start_loc_host[s + 1] - query_start_loc_host[s];
+                const int64_t nt = ql > 1 ? (ql + 127) / 128 : 0;
+                extra += std::min<int64_t>(k, nt);
+                longest = std::max(longest, nt);
+            }
+            if (k > longest || (tiles + extra) * pairs > dev->num_sms) break;
+            a.split_last = k;
+            a.split_tiles = static_cast<int32_t>(extra);
+        }
         a.scale = scale;
         cudaError_t e = pkv::launch_prefill(a, static_cast<cudaStream_t>(stream));
         if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;

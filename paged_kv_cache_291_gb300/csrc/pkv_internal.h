@@ -125,6 +125,8 @@ struct PrefillArgs {
     int32_t num_blocks, num_kv_heads, num_q_heads, head_dim;
     int32_t num_seqs, num_tokens, max_blocks_per_seq, max_context_len;
     int32_t num_tiles;                // query tiles of the prefill sequences
+    int32_t split_last;               // last row tiles of each sequence split by head (two-head CTAs only)
+    int32_t split_tiles;              // tiles so split over all sequences (extra CTAs per head pair)
     float scale;
 };
 

@@ -106,6 +106,10 @@ struct PrefillParams {
     float* out;
     unsigned long long* err;
     int32_t num_blocks, hkv, hq, num_seqs, max_blocks, ctx_cap, num_tokens, units;
+    // The last split_last row tiles of each prefill sequence (its longest:
+    // they hold the most keys) run as two one-head CTAs instead of one
+    // two-head CTA (units == 2 only), so that more SMs share them.
+    int32_t split_last;
     float scale_log2;
 };
 
@@ -123,7 +127,7 @@ enum {
 };
 
 // Tile info slots (written by warp 0 before the CTA-wide sync).
-enum { I_S = 0, I_ROW0, I_ROWS, I_PMIN, I_PMAX, I_NT, I_KLAST, I_BAD, I_CTX, I_VMAX };
+enum { I_S = 0, I_ROW0, I_ROWS, I_PMIN, I_PMAX, I_NT, I_KLAST, I_BAD, I_CTX, I_VMAX, I_UNITS, I_H0 };
 
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
@@ -239,9 +243,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_TMEM);
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-    const int units = P.units;
-    const int h0 = blockIdx.y * units;           // q head of unit 0 (unit 1 is h0 + 1)
-    const int g = h0 / (P.hq / P.hkv);           // the kv head both units read
     const unsigned FULL = 0xffffffffu;
 
     // ---------------------------------------------------------- setup
@@ -250,10 +251,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     griddep_launch_dependents();
     if (warp == 0) {
         griddep_wait();
-        // Find the sequence and row tile of this CTA: tiles are numbered over
-        // the prefill sequences (query_len > 1) in order, ceil(qlen/128) each.
+        // Find the sequence and row tile of this CTA: entries are numbered
+        // over the prefill sequences (query_len > 1) in order, one per row
+        // tile of 128 rows (ceil(qlen/128) tiles), and two for each of the
+        // last split_last tiles (one per q head).
         const int tile = blockIdx.x;
-        int base = 0, found = -1, tloc = 0;
+        const int split = P.units == 2 ? P.split_last : 0;
+        int base = 0, found = -1, e = 0, nt_s = 0;
         for (int s0 = 0; s0 < P.num_seqs && found < 0; s0 += 32) {
             const int s = s0 + lane;
             int nt = 0;
@@ -261,7 +265,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int ql = __ldg(P.qsl + s + 1) - __ldg(P.qsl + s);
                 nt = ql > 1 ? (ql + kTileM - 1) / kTileM : 0;
             }
-            int incl = nt;
+            const int ne = nt + min(split, nt);
+            int incl = ne;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const int t = __shfl_up_sync(FULL, incl, o);
@@ -271,12 +276,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (hit) {
                 const int j = __ffs(hit) - 1;
                 found = s0 + j;
-                tloc = tile - (base + __shfl_sync(FULL, incl - nt, j));
+                e = tile - (base + __shfl_sync(FULL, incl - ne, j));
+                nt_s = __shfl_sync(FULL, nt, j);
             } else {
                 base += __shfl_sync(FULL, incl, 31);
             }
         }
+        // Entry e of the sequence: row tile e while e < nt - sl (both
+        // heads), then tile nt - sl + (e - (nt - sl)) / 2, one head each.
+        const int sl = min(split, nt_s);
+        int tloc = e, cta_units = P.units, cta_h0 = blockIdx.y * P.units;
+        if (sl > 0 && e >= nt_s - sl) {
+            const int k = e - (nt_s - sl);
+            tloc = nt_s - sl + k / 2;
+            cta_units = 1;
+            cta_h0 += k % 2;
+        }
         if (lane == 0) {
+            info[I_UNITS] = cta_units;
+            info[I_H0] = cta_h0;
             int bad = 0, s = found, row0 = 0, rows = 0, pmin = 0, pmax = 0, nt = 0, klast = 0, ctx = 0;
             if (s < 0) {
                 bad = 1;
@@ -328,6 +346,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
+    const int units = info[I_UNITS];
+    const int h0 = info[I_H0];                   // q head of unit 0 (unit 1 is h0 + 1)
+    const int g = h0 / (P.hq / P.hkv);           // the kv head both units read
     const int s = info[I_S];
     const int row0 = info[I_ROW0];
     const int rows = info[I_ROWS];
@@ -726,6 +747,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
     P.num_tokens = a.num_tokens;
     // Two q heads per CTA when a GQA group holds an even number of them.
     P.units = ((a.num_q_heads / a.num_kv_heads) % 2 == 0) ? 2 : 1;
+    P.split_last = P.units == 2 ? a.split_last : 0;
     P.scale_log2 = a.scale * kLog2e;
     auto kernel = a.head_dim == 64 ? prefill_kernel<64> : prefill_kernel<kMaxHeadDim>;
     static bool configured[2][64] = {};
@@ -737,7 +759,8 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         configured[which][dev] = true;
     }
-    dim3 grid(static_cast<unsigned>(a.num_tiles), static_cast<unsigned>(a.num_q_heads / P.units));
+    dim3 grid(static_cast<unsigned>(a.num_tiles + (P.units == 2 ? a.split_tiles : 0)),
+              static_cast<unsigned>(a.num_q_heads / P.units));
     return launch_overlapped(kernel, grid, dim3(kThreads), SMEM_BYTES, stream, tq, tk, tv, P);
 }
 
