@@ -12,12 +12,12 @@
 //
 //  * A CTA owns 128 query rows of the two q heads of a GQA group ("units";
 //    one unit when Hq/Hkv is odd).  Both units read the same K/V tiles, so a
-//    tile is loaded once for two heads.  Warp 8 loads the two Q tiles and
+//    tile is loaded once for two heads.  Warp 16 loads the two Q tiles and
 //    the K/V key tiles (128 keys = 8 paged blocks, each block a 16-row TMA
 //    box with 128-byte swizzle) into rings of 2 (K) and 3 (V) stages.
-//    Warp 9 issues tcgen05.mma.  Warps 0-3 and 4-7 are the softmax
-//    warpgroups of units 0 and 1 (TMEM lane = query row), so one unit's
-//    softmax overlaps the other unit's MMAs.
+//    Warp 17 issues tcgen05.mma.  Warps 0-7 and 8-15 run the softmax of
+//    units 0 and 1 (TMEM lane = query row; two warps per lane quarter, 16
+//    rows each), so one unit's softmax overlaps the other unit's MMAs.
 //  * Per unit, TMEM holds S (128 fp32 columns) and O (128 columns).  S =
 //    Q K^T is written there; the softmax reads it, then writes P into the
 //    first 64 of the same columns as fp16 pairs, and O += P V takes P
@@ -25,9 +25,9 @@
 //    memory (MN-major operand).
 //  * P V runs in fp16: P (in [0, 256]) is rounded to fp16, 2^-11 relative,
 //    where a bf16 P (2^-9) can miss a 2e-3 absolute bound when a few keys
-//    carry all the weight.  The MMA needs V in the same type, so warps 0-7
-//    rewrite each V tile in shared memory from bf16 to fp16 in place, an
-//    eighth each, between their softmax passes (exact for 2^-14 <= |v| <=
+//    carry all the weight.  The MMA needs V in the same type, so warps 0-15
+//    rewrite each V tile in shared memory from bf16 to fp16 in place, a
+//    sixteenth each, between their softmax passes (exact for 2^-14 <= |v| <=
 //    65504, absolute error at most 2^-25 below).  l sums P in fp32.
 //  * A CTA whose visible V values leave that range (some |v| above 65504,
 //    which became inf, or every |v| below 2^-12, mostly fp16 subnormals)
@@ -82,11 +82,11 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget (227 KB)");
 // of the SM's 228 KB of shared memory rules a second CTA out.
 static_assert(2 * SMEM_BYTES > 228 * 1024, "the 512-column TMEM allocation needs one CTA per SM");
 
-constexpr int kSoftmaxWarps = 4;                     // per unit
-constexpr int kLoadWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kThreads = 32 * 10;
-constexpr int kConvWarps = kSoftmaxWarps * kUnits;   // warps 0-7 also convert V tiles
+constexpr int kSoftmaxWarps = 8;                     // per unit: two per TMEM lane quarter
+constexpr int kLoadWarp = 16;
+constexpr int kMmaWarp = 17;
+constexpr int kThreads = 32 * 18;
+constexpr int kConvWarps = kSoftmaxWarps * kUnits;   // warps 0-15 also convert V tiles
 
 constexpr uint32_t kTmemCols = 512;
 // Unit u: S/P at columns [256u, 256u + 128), O at [256u + 128, 256u + 256).
@@ -224,10 +224,6 @@ __device__ __noinline__ void redo_rows_exact(const PrefillParams& P, int s, int 
 #pragma unroll
         for (int i = 0; i < DPL; ++i) orow[i] = (o[i] + oc[i]) / lt;
     }
-}
-
-__device__ __forceinline__ uint32_t tmem_lane_addr(uint32_t base, int warp, uint32_t col) {
-    return base + (static_cast<uint32_t>((warp & 3) * 32) << 16) + col;
 }
 
 template <int D>
@@ -486,15 +482,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp < kConvWarps) {
         // ------------------------------------------------------ V to fp16
-        // Warps 0-7 convert each V tile in place, an eighth (256 16-byte
-        // chunks, contiguous) each; the map is elementwise, so the 128-byte
-        // swizzle is irrelevant.  On the last tile, rows of keys past the last
-        // visible position (unused slots of the last block, blocks never
-        // loaded) are zeroed instead: a 0 weight times a NaN would poison
-        // the MMA.  A softmax warp converts tile j right before it waits for
-        // S of tile j, while the MMAs run.  Spread over eight warps (all four
-        // SM sub-partitions), the work stays off the softmax's critical
-        // path; two dedicated warps on two sub-partitions slowed it down.
+        // Warps 0-15 convert each V tile in place, a sixteenth (128 16-byte
+        // chunks at head_dim 128, contiguous) each; the map is elementwise,
+        // so the 128-byte swizzle is irrelevant.  On the last tile, rows of
+        // keys past the last visible position (unused slots of the last
+        // block, blocks never loaded) are zeroed instead: a 0 weight times a
+        // NaN would poison the MMA.  A softmax warp converts tile j right
+        // before it waits for S of tile j, while the MMAs run.  Spread over
+        // all sixteen warps (all four SM sub-partitions), the work stays off
+        // the softmax's critical path; two dedicated warps on two
+        // sub-partitions slowed it down.
         float vmax = 0.f;
         auto convert_v = [&](int j) -> bool {
             const int sv = j % kVStages;
@@ -526,101 +523,132 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < nt && ok; ++j) ok = convert_v(j);
         } else {
         // ------------------------------------------------------ softmax rows
-        const int m = (warp % kSoftmaxWarps) * 32 + lane;
+        // Eight warps per unit: warps w and w + 4 share TMEM lane quarter
+        // w % 4 and take its first and second 16 lanes (16-lane shapes).
+        // Thread t holds rows ra = t/4 and ra + 8 of those 16 and columns
+        // 8g + 2(t%4) and + 1 of every group g of 8, so a row is spread over
+        // the 4 threads of a quad: its maximum and sum take two shuffles,
+        // and its P pairs land in the layout of the 16x128b store (P column
+        // 4g + t%4 holds keys 8g + 2(t%4) and + 1).
+        const int hh = (warp >> 2) & 1;
+        const int ma = 32 * (warp & 3) + 16 * hh + lane / 4;  // tile rows ma and ma + 8
+        const int mb = ma + 8;
+        const int tq = lane & 3;
+        const uint32_t tlane = static_cast<uint32_t>(32 * (warp & 3) + 16 * hh) << 16;
         const int h = h0 + u;
-        const int pos = (m < rows) ? pmin + m : pmax;
-        float m_used = -INFINITY;
-        float2 l2[4];  // row sum of P (8 interleaved partial sums)
-#pragma unroll
-        for (int k = 0; k < 4; ++k) l2[k] = make_float2(0.f, 0.f);
+        const int pos_a = (ma < rows) ? pmin + ma : pmax;
+        const int pos_b = (mb < rows) ? pmin + mb : pmax;
+        float mua = -INFINITY, mub = -INFINITY;  // reference maxima of the two rows
+        float2 la = make_float2(0.f, 0.f), lb = make_float2(0.f, 0.f);  // row sums of P
         for (int j = 0; j < nt && ok; ++j) {
             // V tile j first (unit 1 gets here while unit 0 still works on
             // tile j), then S of tile j.
             if (!convert_v(j) || !warp_wait(&bar[B_SFULL + u], j & 1)) { ok = false; break; }
             tc::fence_after_sync();
             const int kbase = j * kTileN;
-            // Rows grow down the warp, so the tile is fully visible to the
+            // Rows grow with the lane, so the tile is fully visible to the
             // warp when its last key is visible to the warp's first row.
-            const bool full = kbase + kTileN - 1 <= __shfl_sync(FULL, pos, 0);
-            // The row's 128 scores, loaded once behind a single wait and kept
-            // in registers for both passes.
-            uint32_t sr[kTileN];
-#pragma unroll
-            for (int c = 0; c < kTileN / 32; ++c)
-                tc::tmem_ld32(tmem_lane_addr(tmem, warp, col_s(u) + 32 * c),
-                              *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
+            const bool full = kbase + kTileN - 1 <= __shfl_sync(FULL, pos_a, 0);
+            uint32_t sr[64];  // groups 0-7, then 8-15
+            tc::tmem_ld16x256b_x8(tmem + tlane + col_s(u), *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+            tc::tmem_ld16x256b_x8(tmem + tlane + col_s(u) + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
             tc::tmem_wait_ld();
-            // Pass 1: the tile's row maximum (of the raw scores; the scale is
-            // positive, so it is applied afterwards), as 8 independent
-            // partial maxima.
-            float mp[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) mp[k] = -INFINITY;
+            // Pass 1: each row's maximum over the tile (raw scores; the scale
+            // is positive, so it is applied afterwards).
+            float xa0 = -INFINITY, xa1 = -INFINITY, xb0 = -INFINITY, xb1 = -INFINITY;
             if (full) {
 #pragma unroll
-                for (int i = 0; i < kTileN; i += 2)
-                    mp[(i / 2) % 8] = fmax3(mp[(i / 2) % 8], __uint_as_float(sr[i]), __uint_as_float(sr[i + 1]));
+                for (int g = 0; g < 16; g += 2) {
+                    xa0 = fmax3(xa0, __uint_as_float(sr[4 * g]), __uint_as_float(sr[4 * g + 1]));
+                    xa1 = fmax3(xa1, __uint_as_float(sr[4 * g + 4]), __uint_as_float(sr[4 * g + 5]));
+                    xb0 = fmax3(xb0, __uint_as_float(sr[4 * g + 2]), __uint_as_float(sr[4 * g + 3]));
+                    xb1 = fmax3(xb1, __uint_as_float(sr[4 * g + 6]), __uint_as_float(sr[4 * g + 7]));
+                }
             } else {
 #pragma unroll
-                for (int i = 0; i < kTileN; ++i)
-                    if (kbase + i <= pos) mp[i % 8] = fmaxf(mp[i % 8], __uint_as_float(sr[i]));
+                for (int g = 0; g < 16; ++g) {
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        const int key = kbase + 8 * g + 2 * tq + c;
+                        if (key <= pos_a) xa0 = fmaxf(xa0, __uint_as_float(sr[4 * g + c]));
+                        if (key <= pos_b) xb0 = fmaxf(xb0, __uint_as_float(sr[4 * g + 2 + c]));
+                    }
+                }
             }
-            const float mraw = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                                     fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
-            const float mt = mraw * P.scale_log2;
+            float mxa = fmaxf(xa0, xa1), mxb = fmaxf(xb0, xb1);
+            mxa = fmaxf(mxa, __shfl_xor_sync(FULL, mxa, 1));
+            mxb = fmaxf(mxb, __shfl_xor_sync(FULL, mxb, 1));
+            mxa = fmaxf(mxa, __shfl_xor_sync(FULL, mxa, 2));
+            mxb = fmaxf(mxb, __shfl_xor_sync(FULL, mxb, 2));
+            const float mta = mxa * P.scale_log2, mtb = mxb * P.scale_log2;
             // A new reference only when the maximum grew by more than 2^8;
             // O is then rescaled by alpha after pass 2 (before P is handed
             // to the MMA warp), l now.
-            float alpha = 1.f;
+            float alpha_a = 1.f, alpha_b = 1.f;
             bool rescale = false;
             if (j == 0) {
-                m_used = mt;
+                mua = mta;
+                mub = mtb;
             } else {
-                const bool need = mt > m_used + kRescaleThreshold;
-                rescale = __any_sync(FULL, need);
-                if (need) {
-                    alpha = fast_exp2(m_used - mt);
-                    m_used = mt;
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        l2[k].x *= alpha;
-                        l2[k].y *= alpha;
-                    }
+                const bool need_a = mta > mua + kRescaleThreshold, need_b = mtb > mub + kRescaleThreshold;
+                rescale = __any_sync(FULL, need_a || need_b);
+                if (need_a) {
+                    alpha_a = fast_exp2(mua - mta);
+                    mua = mta;
+                    la.x *= alpha_a;
+                    la.y *= alpha_a;
+                }
+                if (need_b) {
+                    alpha_b = fast_exp2(mub - mtb);
+                    mub = mtb;
+                    lb.x *= alpha_b;
+                    lb.y *= alpha_b;
                 }
             }
-            // Pass 2: P = exp2(scale * s - m_used) as fp16, written over the
-            // S columns: keys 2i, 2i+1 of the tile in column i.  The row sum
-            // goes to 4 independent fp32x2 accumulators.
+            // Pass 2: P = exp2(scale * s - reference) as fp16 pairs, written
+            // over the first 64 S columns; the row sums in fp32.
             const float2 sc2 = make_float2(P.scale_log2, P.scale_log2);
-            const float2 nm2 = make_float2(-m_used, -m_used);
+            const float2 nma = make_float2(-mua, -mua), nmb = make_float2(-mub, -mub);
 #pragma unroll
-            for (int c = 0; c < kTileN / 64; ++c) {
-                uint32_t w[32];
+            for (int hf = 0; hf < 2; ++hf) {
+            uint32_t w[16];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int k0 = 64 * c + 2 * i;
-                    const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[k0]), __uint_as_float(sr[k0 + 1])),
-                                                sc2, nm2);
-                    float2 p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-                    if (!full) {  // keys past the row's position (NaN in unused slots included)
-                        if (kbase + k0 > pos) p.x = 0.f;
-                        if (kbase + k0 + 1 > pos) p.y = 0.f;
-                    }
-                    w[i] = tc::pack_f16x2(p.x, p.y);
-                    l2[i % 4] = __fadd2_rn(l2[i % 4], p);
+            for (int g = 8 * hf; g < 8 * hf + 8; ++g) {
+                const float2 xa = __ffma2_rn(make_float2(__uint_as_float(sr[4 * g]), __uint_as_float(sr[4 * g + 1])),
+                                             sc2, nma);
+                const float2 xb = __ffma2_rn(
+                    make_float2(__uint_as_float(sr[4 * g + 2]), __uint_as_float(sr[4 * g + 3])), sc2, nmb);
+                float2 pa = make_float2(fast_exp2(xa.x), fast_exp2(xa.y));
+                float2 pb = make_float2(fast_exp2(xb.x), fast_exp2(xb.y));
+                if (!full) {  // keys past the row's position (NaN in unused slots included)
+                    const int key = kbase + 8 * g + 2 * tq;
+                    if (key > pos_a) pa.x = 0.f;
+                    if (key + 1 > pos_a) pa.y = 0.f;
+                    if (key > pos_b) pb.x = 0.f;
+                    if (key + 1 > pos_b) pb.y = 0.f;
                 }
-                tc::tmem_st32(tmem_lane_addr(tmem, warp, col_s(u) + 32 * c), w);
+                w[2 * (g - 8 * hf)] = tc::pack_f16x2(pa.x, pa.y);
+                w[2 * (g - 8 * hf) + 1] = tc::pack_f16x2(pb.x, pb.y);
+                la = __fadd2_rn(la, pa);
+                lb = __fadd2_rn(lb, pb);
+            }
+            tc::tmem_st16x128b_x8(tmem + tlane + col_s(u) + 32 * hf, w);
             }
             if (rescale) {
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
+                for (int c = 0; c < D / 64; ++c) {
                     uint32_t r[32];
-                    const uint32_t ta = tmem_lane_addr(tmem, warp, col_o(u) + 32 * c);
-                    tc::tmem_ld32(ta, r);
+                    const uint32_t ta = tmem + tlane + col_o(u) + 64 * c;
+                    tc::tmem_ld16x256b_x8(ta, r);
                     tc::tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                    tc::tmem_st32(ta, r);
+                    for (int g = 0; g < 8; ++g) {
+                        r[4 * g] = __float_as_uint(__uint_as_float(r[4 * g]) * alpha_a);
+                        r[4 * g + 1] = __float_as_uint(__uint_as_float(r[4 * g + 1]) * alpha_a);
+                        r[4 * g + 2] = __float_as_uint(__uint_as_float(r[4 * g + 2]) * alpha_b);
+                        r[4 * g + 3] = __float_as_uint(__uint_as_float(r[4 * g + 3]) * alpha_b);
+                    }
+                    tc::tmem_st16x256b_x8(ta, r);
                 }
             }
             tc::tmem_wait_st();
@@ -633,26 +661,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = false;
             } else {
                 tc::fence_after_sync();
-                const float inv = 1.f / (((l2[0].x + l2[0].y) + (l2[1].x + l2[1].y)) +
-                                         ((l2[2].x + l2[2].y) + (l2[3].x + l2[3].y)));
-                float* orow = P.out + (static_cast<size_t>(row0 + m) * P.hq + h) * D;
+                float sa = la.x + la.y, sb = lb.x + lb.y;
+                sa += __shfl_xor_sync(FULL, sa, 1);
+                sb += __shfl_xor_sync(FULL, sb, 1);
+                sa += __shfl_xor_sync(FULL, sa, 2);
+                sb += __shfl_xor_sync(FULL, sb, 2);
+                const float inva = 1.f / sa, invb = 1.f / sb;
+                float* oa = P.out + (static_cast<size_t>(row0 + ma) * P.hq + h) * D;
+                float* ob = P.out + (static_cast<size_t>(row0 + mb) * P.hq + h) * D;
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
+                for (int c = 0; c < D / 64; ++c) {
                     uint32_t r[32];
-                    tc::tmem_ld32(tmem_lane_addr(tmem, warp, col_o(u) + 32 * c), r);
+                    tc::tmem_ld16x256b_x8(tmem + tlane + col_o(u) + 64 * c, r);
                     tc::tmem_wait_ld();
-                    if (m < rows) {
 #pragma unroll
-                        for (int i = 0; i < 32; i += 4)
-                            *reinterpret_cast<float4*>(orow + 32 * c + i) =
-                                make_float4(__uint_as_float(r[i]) * inv, __uint_as_float(r[i + 1]) * inv,
-                                            __uint_as_float(r[i + 2]) * inv, __uint_as_float(r[i + 3]) * inv);
+                    for (int g = 0; g < 8; ++g) {
+                        const int col = 64 * c + 8 * g + 2 * tq;
+                        if (ma < rows)
+                            *reinterpret_cast<float2*>(oa + col) =
+                                make_float2(__uint_as_float(r[4 * g]) * inva, __uint_as_float(r[4 * g + 1]) * inva);
+                        if (mb < rows)
+                            *reinterpret_cast<float2*>(ob + col) = make_float2(__uint_as_float(r[4 * g + 2]) * invb,
+                                                                               __uint_as_float(r[4 * g + 3]) * invb);
                     }
                 }
             }
-        } else if (bad && s >= 0 && m < rows) {
-            float* orow = P.out + (static_cast<size_t>(row0 + m) * P.hq + h) * D;
-            for (int c = 0; c < D; c += 4) *reinterpret_cast<float4*>(orow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+        } else if (bad && s >= 0) {
+            // Zero rows for a sequence whose arguments were out of range.
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int m = e ? mb : ma;
+                if (m < rows) {
+                    float* orow = P.out + (static_cast<size_t>(row0 + m) * P.hq + h) * D;
+                    for (int c = 2 * tq; c < D; c += 8)
+                        *reinterpret_cast<float2*>(orow + c) = make_float2(0.f, 0.f);
+                }
+            }
         }
         }
         // The CTA's largest visible |v|, for the range check after the loop.
