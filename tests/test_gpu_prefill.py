@@ -60,6 +60,17 @@ def test_mixed_order_and_many_sequences(pkv):
     run_and_check(pkv, w)
 
 
+def test_prefill_grid_of_several_waves(pkv):
+    """Enough row tiles that the grid needs more than one CTA per SM: no
+    row tile is split into one-head CTAs and the CTAs run in several waves
+    (the batches above are small enough that their longest tiles are
+    split)."""
+    ctx = [400 + 37 * i for i in range(14)]
+    ql = [400 - 13 * i for i in range(14)]
+    w = W.make_paged("waves", 515, 16, 8, 128, ctx, ql)
+    run_and_check(pkv, w)
+
+
 def test_chunked_equals_one_shot_on_gpu(pkv):
     """A prompt processed in consecutive slices (each over the cached
     prefix) gives the rows of one-shot causal prefill."""
