@@ -49,24 +49,30 @@ NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal (the measured copy bandwidth is
 L2_ROTATE_BYTES = 512 << 20
 
 # DRAM traffic of one launch of a kernel on a workload from an ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum), with the hash of the kernel
-# sources it was taken on; reported only while the sources still match.
+# (dram__bytes_read.sum + dram__bytes_write.sum), with the hash of the
+# kernel's sources it was taken on; reported only while they still match.
 # Keys: (kernel entry, config).
 NCU_TRAFFIC = {
-    ("decode_step", 2): {"bytes": 91660800, "sources_sha": "2943c4f1c245ef84"},
-    ("decode", 4): {"bytes": 18811392, "sources_sha": "2943c4f1c245ef84"},
-    ("fp8_decode", 2): {"bytes": 44804608, "sources_sha": "2943c4f1c245ef84"},
+    ("decode_step", 2): {"bytes": 91660800, "sources": "decode", "sources_sha": "2943c4f1c245ef84"},
+    ("decode", 4): {"bytes": 18811392, "sources": "decode", "sources_sha": "2943c4f1c245ef84"},
+    ("fp8_decode", 2): {"bytes": 44804608, "sources": "decode", "sources_sha": "2943c4f1c245ef84"},
     # both kernels of the shared-prefix decode (shared_prefix_kernel, then decode_kernel)
-    ("shared_prefix", 4): {"bytes": 19252480, "sources_sha": "2943c4f1c245ef84"},
+    ("shared_prefix", 4): {"bytes": 19252480, "sources": "decode", "sources_sha": "2943c4f1c245ef84"},
+    # prefill tiles of the mixed batch (the K and V tiles are read by every row-tile CTA of a kv head)
+    ("prefill", 5): {"bytes": 25325824, "sources": "prefill", "sources_sha": "334b56d190920b05"},
 }
-KERNEL_SOURCES = ["paged_kv_cache_291_gb300/csrc/decode_kernel.cuh", "paged_kv_cache_291_gb300/csrc/decode.cu",
-                  "paged_kv_cache_291_gb300/csrc/decode_fused.cu", "paged_kv_cache_291_gb300/csrc/pkv_device.cuh",
-                  "paged_kv_cache_291_gb300/csrc/shared_prefix.cu"]
+KERNEL_SOURCES = {
+    "decode": ["paged_kv_cache_291_gb300/csrc/decode_kernel.cuh", "paged_kv_cache_291_gb300/csrc/decode.cu",
+               "paged_kv_cache_291_gb300/csrc/decode_fused.cu", "paged_kv_cache_291_gb300/csrc/pkv_device.cuh",
+               "paged_kv_cache_291_gb300/csrc/shared_prefix.cu"],
+    "prefill": ["paged_kv_cache_291_gb300/csrc/prefill.cu", "paged_kv_cache_291_gb300/csrc/tcgen05.cuh",
+                "paged_kv_cache_291_gb300/csrc/pkv_device.cuh"],
+}
 
 
-def sources_sha() -> str:
+def sources_sha(group: str = "decode") -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[group]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -74,7 +80,7 @@ def sources_sha() -> str:
 
 def ncu_traffic(kernel, config):
     rec = NCU_TRAFFIC.get((kernel, config))
-    return rec["bytes"] if rec is not None and rec["sources_sha"] == sources_sha() else None
+    return rec["bytes"] if rec is not None and rec["sources_sha"] == sources_sha(rec["sources"]) else None
 
 
 # ----------------------------------------------------------- multi-rank host logic
@@ -845,11 +851,11 @@ def decode_entry(w, t, hbm, hbm_kind, kv_elem_bytes=2, traffic=None, fused=False
     return rec
 
 
-def prefill_entry(w, t, peak, kind):
+def prefill_entry(w, t, peak, kind, traffic=None):
     fl = prefill_flops(w)
     achieved = fl / (t["mean_us"] * 1e-6) / 1e12
     return {"bound": "tensor", "kernel": "prefill_kernel", "achieved": achieved, "peak": peak, "peak_kind": kind,
-            "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None, "algorithmic_flops": fl,
+            "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic, "algorithmic_flops": fl,
             "avg_launch_us": t["mean_us"], "median_us": t["median_us"], "min_us": t["min_us"],
             "warm_us": t["warm_us"], "launches": t["launches"], "replicas": t["replicas"],
             "tokens_per_s": int(sum(int(w.query_lens[s]) for s in prefill_rows(w))) / (t["mean_us"] * 1e-6)}
@@ -1054,7 +1060,8 @@ def config_entry(run, hbm, hbm_kind, tpeak, tkind, clocks=None, cpu=True, cpu_bu
         else:
             entry["decode"] = decode_entry(w, dec_t, hbm, hbm_kind, traffic=ncu_traffic("decode", run.config))
     if len(pre):
-        entry["prefill"] = prefill_entry(w, run.kernel_alone(pre), tpeak, tkind)
+        entry["prefill"] = prefill_entry(w, run.kernel_alone(pre), tpeak, tkind,
+                                         traffic=ncu_traffic("prefill", run.config))
     if len(dec):
         t8 = run.kernel_alone(dec, kv_e4m3=True)
         e8 = decode_entry(w, t8, hbm, hbm_kind, kv_elem_bytes=1, traffic=ncu_traffic("fp8_decode", run.config))
