@@ -126,3 +126,43 @@ def test_outputs_written_to_page_locked_host_memory(pkv):
     with pytest.raises(ValueError):
         pkv.decode_attention(ds.k, ds.v, ds.q, ds.tables, ds.ctx, w.max_context_len, w.scale,
                              out=torch.zeros(tuple(ref.shape), dtype=torch.float32))
+
+
+def test_page_locked_output_for_e4m3_pools_and_the_static_entry_point(pkv):
+    """The page-locked output also serves e4m3 pools (the tensor-core block
+    math writes it) and pkv_decode_attention_static: the same rows as with a
+    device output."""
+    import ctypes
+    w = W.build_config(2)
+    ds = DeviceStep(w)
+    pkv.cache_write(ds.k, ds.v, ds.k_new, ds.v_new, ds.slots)
+    nb, hkv, _, d = w.k_pool.shape
+    k8 = torch.empty((nb, hkv, 16, d), dtype=torch.uint8, device="cuda")
+    v8 = torch.empty_like(k8)
+    slots = torch.arange(nb * 16, dtype=torch.int32, device="cuda")
+    rk = ds.k.permute(0, 2, 1, 3).reshape(nb * 16, hkv, d).contiguous()
+    rv = ds.v.permute(0, 2, 1, 3).reshape(nb * 16, hkv, d).contiguous()
+    pkv.cache_write(k8, v8, rk, rv, slots, k_scale=1 / 64, v_scale=1 / 64)
+    args = (ds.q, ds.tables, ds.ctx, w.max_context_len, w.scale)
+    dev = pkv.decode_attention(k8, v8, *args, k_scale=1 / 64, v_scale=1 / 64)
+    host = torch.zeros(tuple(dev.shape), dtype=torch.float32).pin_memory()
+    pkv.decode_attention(k8, v8, *args, out=host, k_scale=1 / 64, v_scale=1 / 64)
+    torch.cuda.synchronize()
+    assert pkv.get_error() == (0, 0)
+    assert torch.equal(host, dev.cpu())
+    # the allocation-free entry point, bf16 pools
+    lib = pkv.load()
+    P, i32, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float
+    lib.pkv_decode_attention_static.argtypes = [ctypes.POINTER(pkv.Cache), P, i32, P, i32, P, i32, i32, f32, P, P]
+    lib.pkv_decode_attention_static.restype = ctypes.c_int
+    dev = pkv.decode_attention(ds.k, ds.v, *args)
+    host.zero_()
+    cache = pkv._cache(ds.k, ds.v, None, None)
+    st = lib.pkv_decode_attention_static(ctypes.byref(cache), ctypes.c_void_p(ds.q.data_ptr()), w.num_q_heads,
+                                         ctypes.c_void_p(ds.tables.data_ptr()), int(ds.tables.shape[1]),
+                                         ctypes.c_void_p(ds.ctx.data_ptr()), w.num_seqs, w.max_context_len,
+                                         ctypes.c_float(w.scale), ctypes.c_void_p(host.data_ptr()), None)
+    assert st == 0, pkv.status_string(st)
+    torch.cuda.synchronize()
+    assert pkv.get_error() == (0, 0)
+    assert torch.equal(host, dev.cpu())
