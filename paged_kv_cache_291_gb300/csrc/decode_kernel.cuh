@@ -101,7 +101,11 @@ constexpr int consumer_warps() {
 #endif
 }
 constexpr int kItemRing = 8;
-constexpr int kMinRangeUnits = 8;  // smallest automatic range (blocks per CTA)
+// Smallest automatic range (blocks per CTA).  It sets the grid of small
+// batches: Llama-3.2-1B (4 sequences, 336 units) ran in 12.2 us with 4,
+// 12.6 with 6, 14.6 with 8 and 16.9 with 2 or 3 (split pairs' merges then
+// cost more than the extra CTAs bring).
+constexpr int kMinRangeUnits = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
