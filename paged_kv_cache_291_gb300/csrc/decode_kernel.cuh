@@ -83,9 +83,11 @@ constexpr bool use_mma() {
 #endif
 }
 
-// Consumer warps per CTA: 12 for head groups of 1 or 2 (their per-lane state
-// is small, and a fourth warp per scheduler hides more of the latency of the
-// dependent shuffle and FMA chains), 8 for groups of 4 (which need more than
+// Consumer warps per CTA: 12 for head groups of 1, 11 for bf16 groups of 2
+// (their per-lane state is small, and a third or fourth warp per scheduler
+// hides more of the latency of the dependent shuffle and FMA chains; for
+// groups of 2, timed at 9-12 and 16 warps, 11 ran the Qwen3-1.7B step in
+// 20.5 us against 20.9 with 12, 20.7 with 10), 8 for groups of 4 (which need more than
 // the 128 registers a thread that 14 warps leave), 6 for groups of 8 (about
 // 220 registers a thread, no spills).  e4m3 pools
 // (EB = 1) with groups of 1 or 2 on CUDA cores take 16: their blocks cost
@@ -97,7 +99,8 @@ constexpr int consumer_warps() {
 #ifdef PKV_DECODE_CONSUMER_WARPS
     return PKV_DECODE_CONSUMER_WARPS;
 #else
-    return use_mma<D, G, EB>() ? (G <= 2 ? 12 : 8) : (G <= 2 ? (EB == 1 ? 16 : 12) : (G == 4 ? 8 : 6));
+    return use_mma<D, G, EB>() ? (G <= 2 ? 12 : 8)
+                               : (G <= 2 ? (EB == 1 ? 16 : (G == 2 ? 11 : 12)) : (G == 4 ? 8 : 6));
 #endif
 }
 constexpr int kItemRing = 8;
