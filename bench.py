@@ -53,11 +53,11 @@ L2_ROTATE_BYTES = 512 << 20
 # kernel's sources it was taken on; reported only while they still match.
 # Keys: (kernel entry, config).
 NCU_TRAFFIC = {
-    ("decode_step", 2): {"bytes": 91233536, "sources": "decode", "sources_sha": "f9fc4ba4e32da658"},
-    ("decode", 4): {"bytes": 18811648, "sources": "decode", "sources_sha": "f9fc4ba4e32da658"},
-    ("fp8_decode", 2): {"bytes": 44803584, "sources": "decode", "sources_sha": "f9fc4ba4e32da658"},
+    ("decode_step", 2): {"bytes": 91181824, "sources": "decode", "sources_sha": "9924469a8935d603"},
+    ("decode", 4): {"bytes": 18811392, "sources": "decode", "sources_sha": "9924469a8935d603"},
+    ("fp8_decode", 2): {"bytes": 44804608, "sources": "decode", "sources_sha": "9924469a8935d603"},
     # both kernels of the shared-prefix decode (shared_prefix_kernel, then decode_kernel)
-    ("shared_prefix", 4): {"bytes": 19253248, "sources": "decode", "sources_sha": "f9fc4ba4e32da658"},
+    ("shared_prefix", 4): {"bytes": 19253248, "sources": "decode", "sources_sha": "9924469a8935d603"},
     # prefill tiles of the mixed batch (the K and V tiles are read by every row-tile CTA of a kv head)
     ("prefill", 5): {"bytes": 25325824, "sources": "prefill", "sources_sha": "334b56d190920b05"},
 }

@@ -92,14 +92,16 @@ constexpr bool use_mma() {
 // 220 registers a thread, no spills).  e4m3 pools
 // (EB = 1) with groups of 1 or 2 on CUDA cores take 16: their blocks cost
 // more issue (the widening) and half the ring bytes, so the same ring still
-// gives each warp 3 stages.  A build can force one count for every group
-// with PKV_DECODE_CONSUMER_WARPS.
+// gives each warp 3 stages.  The tensor-core block math (e4m3, d = 128,
+// groups of 2) takes 10: 15.0 us on Qwen3-1.7B against 15.2 with 12, 8 or
+// 11 and 15.5 with 14.  A build can force one count for every group with
+// PKV_DECODE_CONSUMER_WARPS.
 template <int D, int G, int EB>
 constexpr int consumer_warps() {
 #ifdef PKV_DECODE_CONSUMER_WARPS
     return PKV_DECODE_CONSUMER_WARPS;
 #else
-    return use_mma<D, G, EB>() ? (G <= 2 ? 12 : 8)
+    return use_mma<D, G, EB>() ? (G <= 2 ? 10 : 8)
                                : (G <= 2 ? (EB == 1 ? 16 : (G == 2 ? 11 : 12)) : (G == 4 ? 8 : 6));
 #endif
 }
