@@ -199,6 +199,23 @@ def test_a_reused_prompt_takes_its_cached_blocks_and_allocation_follows_lru():
     assert slots.tolist() == list(range(3 * B, 3 * B + 8))
 
 
+def test_match_stops_at_the_first_key_not_cached():
+    """A key stands for its whole prefix (section 4 of the serving-engine KV
+    blog), so a row's cached blocks are a leading run: with the second key
+    unknown, the third block is not taken even though its key is cached."""
+    st = bm.BlockState(6, 2, 4)
+    prompt = np.arange(48)
+    bm.append(st, [0, 48])                                       # blocks 0, 1, 2
+    ks = keys_of(prompt, 3)
+    bm.register(st, [ks], [3])
+    bm.release(st, [0])                                          # queue: 3, 4, 5, 2, 1, 0
+    other = keys_of(np.arange(1000, 1016), 1)[0]
+    status, m = bm.match(st, [[ks[0], other, ks[2]]], [3])
+    assert status == bm.OK and m.tolist() == [1]
+    assert st.tables[0].tolist() == [0, -1, -1, -1] and st.context_lens[0] == 16
+    assert st.free_queue() == [3, 4, 5, 2, 1]
+
+
 def test_reusing_a_freed_block_drops_its_key():
     st = bm.BlockState(3, 3, 4)
     prompt = np.arange(32)

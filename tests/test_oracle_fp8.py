@@ -51,6 +51,19 @@ def test_quantize_rounds_the_fp32_product_first():
     assert np.array_equal(fp8.quantize_bf16_rows(bits, inv), fp8.encode((f * inv).astype(np.float32)))
 
 
+def test_fp32_product_decides_a_tie():
+    """x = 1.0078125 (bf16 0x3F81) times inv_scale = 1.0542635917663574 (an
+    fp32 value) is 1.0625 + 2.6e-8 exactly, but rounds in fp32 to 1.0625, the
+    midpoint of the e4m3 values 1.0 (code 0x38, even mantissa) and 1.125
+    (0x39).  Rounding the fp32 product gives the even code; rounding the exact
+    product would give 0x39.  The same with the sign bit set."""
+    inv = np.float32(1.0542635917663574)
+    x = np.float32(1.0078125)
+    assert np.float32(x * inv) == np.float32(1.0625) and float(x) * float(inv) > 1.0625   # the premise
+    codes = fp8.quantize_bf16_rows(np.array([0x3F81, 0xBF81], dtype=np.uint16), inv)
+    assert codes.tolist() == [0x38, 0xB8]
+
+
 @pytest.mark.parametrize("hq,hkv,d", [(16, 8, 128), (32, 8, 64)])
 def test_fp8_attention_equals_the_c_oracle_on_bf16_exact_values(hq, hkv, d):
     """With power-of-two scales every dequantised value is exactly bf16, so
