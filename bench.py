@@ -53,9 +53,19 @@ L2_ROTATE_BYTES = 512 << 20
 # kernel's sources it was taken on; reported only while they still match.
 # Keys: (kernel entry, config).
 NCU_TRAFFIC = {
+    ("decode_step", 1): {"bytes": 1511680, "sources": "decode", "sources_sha": "9924469a8935d603"},
     ("decode_step", 2): {"bytes": 91181824, "sources": "decode", "sources_sha": "9924469a8935d603"},
+    ("decode_step", 3): {"bytes": 4063371264, "sources": "decode", "sources_sha": "9924469a8935d603"},
+    ("decode", 1): {"bytes": 1498880, "sources": "decode", "sources_sha": "9924469a8935d603"},
+    ("decode", 2): {"bytes": 91179008, "sources": "decode", "sources_sha": "9924469a8935d603"},
+    ("decode", 3): {"bytes": 4073321216, "sources": "decode", "sources_sha": "9924469a8935d603"},
     ("decode", 4): {"bytes": 18811392, "sources": "decode", "sources_sha": "9924469a8935d603"},
+    ("decode", 5): {"bytes": 306025728, "sources": "decode", "sources_sha": "9924469a8935d603"},
+    ("fp8_decode", 1): {"bytes": 814336, "sources": "decode", "sources_sha": "9924469a8935d603"},
     ("fp8_decode", 2): {"bytes": 44804608, "sources": "decode", "sources_sha": "9924469a8935d603"},
+    ("fp8_decode", 3): {"bytes": 2038387456, "sources": "decode", "sources_sha": "9924469a8935d603"},
+    ("fp8_decode", 4): {"bytes": 9532416, "sources": "decode", "sources_sha": "9924469a8935d603"},
+    ("fp8_decode", 5): {"bytes": 154604544, "sources": "decode", "sources_sha": "9924469a8935d603"},
     # both kernels of the shared-prefix decode (shared_prefix_kernel, then decode_kernel)
     ("shared_prefix", 4): {"bytes": 19253248, "sources": "decode", "sources_sha": "9924469a8935d603"},
     # prefill tiles of the mixed batch (the K and V tiles are read by every row-tile CTA of a kv head)
